@@ -1,0 +1,353 @@
+"""Benchmark: dgrad useful-MAC TFLOP/s on one GB300, printed as one JSON line.
+
+Default workload: the page-3 dgrad shape (bf16 NHWC, N=16, Hi=1, Wi=512,
+C=K=2048, 1x2 filter, stride (1, 2), pad 0 -> dy 16x1x256x2048), seeded
+synthetic inputs N(0,1)*0.02 rounded to bf16.  A "step" is one
+conv_bwd_data_run (every kernel of the path) with dy and w resident in HBM;
+L2 is flushed (a 512 MiB write) before every step, outside the step's events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg3]
+  python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
+
+Under torchrun (N > 1) every rank runs an independent replica of the same
+workload on its own GPU (the op needs no exchange); the time is the max over
+ranks and the value the work of all ranks divided by it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dgrad useful-MAC TFLOP/s and % of GB300 bf16 dense peak, 1 GPU"
+# Pages' number for this workload: IREE "BOO" lowering, 551 us on an AMD GPU
+# whose model the page does not name (6.872e10 useful FLOP -> 124.7 TFLOP/s).
+PAGE_TFLOPS = 124.7
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+# DRAM traffic of the tensor-core kernel per launch on this workload, from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), valid only for
+# the kernel source whose sha256 is recorded with it.
+TRAFFIC = {}
+
+
+def kernel_sha() -> str:
+    p = os.path.join(ROOT, "conv2d_backward_implicit_bwd_gb300", "csrc", "tc_sm103.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            out = {"source": "measured"}
+            for k in ("bf16_tflops", "bf16_tflops_sustained", "hbm_gbs"):
+                if k in d:
+                    out[k] = float(d[k])
+            if "bf16_tflops" in out and "hbm_gbs" in out:
+                return out
+        except Exception:
+            pass
+    return {"source": "fallback", **FALLBACK_PEAKS}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def make_inputs(case, plan):
+    from conv2d_backward_implicit_bwd_gb300 import workloads as wl
+    dy_s, w_s, dx_s = plan.shapes()
+    dy, w = wl.draw(case, dy_s, w_s)
+    return dy, w, dx_s
+
+
+def oracle_sample(case, dy, w, step: int, max_channels: int = 256):
+    """One bounded oracle sample: image (step mod N), a block of up to 256
+    input channels of every group starting at a step-dependent offset.
+    Returns (seconds, fraction of the workload, threads that had work)."""
+    import oracle
+    from conv2d_backward_implicit_bwd_gb300 import workloads as wl
+    g = oracle.geom(case.N, case.C, case.K, case.Hi, case.Wi, case.Y, case.X, case.pad, case.stride, case.dil,
+                    case.groups)
+    lay = oracle.LAYOUT_NCHW if case.layout == wl.NCHW else oracle.LAYOUT_NHWC
+    Cg = case.C // case.groups
+    cb = min(max_channels, Cg)
+    nblk = max(1, Cg // cb)
+    c0 = (step % nblk) * cb
+    n0 = step % case.N
+    t0 = time.perf_counter()
+    oracle.dgrad(g, lay, dy, w, n_range=(n0, n0 + 1), c_range=(c0, c0 + cb), with_absdot=False)
+    dt = time.perf_counter() - t0
+    items = case.groups * ((cb + 15) // 16)  # the oracle's OpenMP work items (16-channel blocks)
+    return dt, cb / Cg / case.N, min(oracle.num_threads(), items)
+
+
+def run_reference(args, case):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from conv2d_backward_implicit_bwd_gb300 import workloads as wl
+    g = oracle.geom(case.N, case.C, case.K, case.Hi, case.Wi, case.Y, case.X, case.pad, case.stride, case.dil,
+                    case.groups)
+    lay = oracle.LAYOUT_NCHW if case.layout == wl.NCHW else oracle.LAYOUT_NHWC
+    dy_s, w_s, _ = oracle.shapes(g, lay)
+    dy, w = wl.draw(case, dy_s, w_s)
+    useful = useful_flop_bruteforce(case, g)
+    # keep the whole run to a few minutes: shrink the per-step sample for long runs
+    mc = max(16, min(256, (256 * 300 // max(1, args.steps + args.warmup)) // 16 * 16))
+    for s in range(args.warmup):
+        oracle_sample(case, dy, w, s, mc)
+    times, fracs = [], []
+    threads = 1
+    for s in range(args.steps):
+        dt, frac, threads = oracle_sample(case, dy, w, args.warmup + s, mc)
+        times.append(dt)
+        fracs.append(frac)
+    total_t = sum(times)
+    value = useful * sum(fracs) / total_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; identical inputs to the GPU arm)",
+        "config": {"workload": case.name, "sample_per_step": f"one image x {mc} input channels of every group"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: one image x {mc} input channels of every group (scatter loop, fp64)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def useful_flop_bruteforce(case, g):
+    def taps(In, Out, F, s, d, p):
+        return sum(1 for o in range(Out) for f in range(F) if 0 <= o * s - p + f * d < In)
+    th = taps(case.Hi, g.Ho, case.Y, case.stride[0], case.dil[0], case.pad[0])
+    tw = taps(case.Wi, g.Wo, case.X, case.stride[1], case.dil[1], case.pad[1])
+    return 2.0 * case.N * case.K * (case.C // case.groups) * th * tw
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="cfg3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from conv2d_backward_implicit_bwd_gb300 import workloads as wl
+    case = wl.case(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, case)
+
+    import numpy as np
+    import torch
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from conv2d_backward_implicit_bwd_gb300 import build as cbuild
+    cbuild.build()
+    from conv2d_backward_implicit_bwd_gb300 import binding as B
+
+    plan = B.Plan.from_case(case)
+    path, launches = plan.path()
+    useful, algo_bytes = plan.work()
+    dy, w, dx_s = make_inputs(case, plan)
+    tdt = torch.bfloat16 if case.dtype == wl.BF16 else torch.float32
+    if case.dtype == wl.BF16:
+        dy_h = torch.from_numpy(dy.view(np.int16)).view(torch.bfloat16)
+        w_h = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16)
+    else:
+        dy_h, w_h = torch.from_numpy(dy), torch.from_numpy(w)
+    dy_d, w_d = dy_h.cuda(), w_h.cuda()
+    dx_d = torch.empty(dx_s, dtype=tdt, device="cuda")
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    plan.set_timing(True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        plan.run(dy_d, w_d, dx_d, stream)
+    st, det = plan.status(stream)
+    if st != B.OK:
+        raise RuntimeError(f"device status {B.status_string(st)} {det:#x}")
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.2)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kern_ms, fill_ms = [], []
+    barrier()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        plan.run(dy_d, w_d, dx_d, stream)
+        evs[i][1].record(stream)
+        f, m = plan.last_timing()
+        fill_ms.append(f)
+        kern_ms.append(m)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    st, det = plan.status(stream)
+    if st != B.OK:
+        raise RuntimeError(f"device status {B.status_string(st)} {det:#x}")
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    mean_ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([mean_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_ms = float(t.item())
+    value = useful * world / (mean_ms * 1e-3) / 1e12
+
+    # end-to-end through the host-buffer entry point (pinned host memory)
+    dy_p, w_p = dy_h.pin_memory(), w_h.pin_memory()
+    dx_p = torch.empty(dx_s, dtype=tdt).pin_memory()
+    e2e_ms = []
+    for i in range(args.e2e_steps + 2):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        plan.run_host(dy_p, w_p, dx_p, dy_d, w_d, dx_d, stream)
+        b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_mean = sum(e2e_ms) / len(e2e_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_mean], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_mean = float(t.item())
+    esz = 2 if case.dtype == wl.BF16 else 4
+
+    peaks = load_peaks()
+    kmean = sum(kern_ms) / len(kern_ms)
+    if path == "tcgen05":
+        achieved = useful / (kmean * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": peaks["source"] + " (bf16 dense, burst)", "kernel": "tc_dgrad_kernel",
+                "kernel_ms": kmean}
+    else:
+        achieved = algo_bytes / (kmean * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": peaks["source"], "kernel": "simt_dgrad_kernel", "kernel_ms": kmean}
+    tr = TRAFFIC.get(case.name)
+    roof["traffic"] = tr["bytes"] if tr and tr.get("sha") == kernel_sha() else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / PAGE_TFLOPS if case.name.startswith("cfg3") else None,
+        "dtype": case.dtype, "data": f"synthetic (seeded {case.dist}, sigma {case.sigma}, {case.dtype} RNE)",
+        "config": {"workload": case.name, "N": case.N, "C": case.C, "K": case.K, "Hi": case.Hi, "Wi": case.Wi,
+                   "Y": case.Y, "X": case.X, "pad": list(case.pad), "stride": list(case.stride),
+                   "dil": list(case.dil), "groups": case.groups, "layout": case.layout,
+                   "l2": "flushed before every step (512 MiB write, outside the step events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "kernel_path": path, "useful_flop_per_step": useful, "algo_bytes_per_step": algo_bytes},
+        "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+        "roofline": roof,
+        "e2e": {"value": useful * world / (e2e_mean * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(dy_h.numel() + w_h.numel()) * esz,
+                "d2h_bytes_per_step": int(np.prod(dx_s)) * esz, "ms_per_step": e2e_mean},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # bounded oracle sample on the host cores (a reported baseline only)
+        dts, fr, thr = [], 0.0, 1
+        s = 0
+        t_start = time.perf_counter()
+        while time.perf_counter() - t_start < 10.0 and s < 256:
+            dt, f, thr = oracle_sample(case, dy, w, s)
+            dts.append(dt)
+            fr += f
+            s += 1
+        line["cpu_baseline"] = {"value": useful * fr / sum(dts) / 1e12, "unit": "TFLOP/s", "cores": thr,
+                                "kind": "oracle",
+                                "sample": f"{s} oracle calls of one image x 256 input channels "
+                                          f"({100 * fr:.2f}% of the workload, {sum(dts):.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,509 @@
+// capi.cpp -- host planner and C ABI (include/conv_bwd_data.h).
+//
+// Planner: the v4r1 backward-data multi-kernel decomposition (pages
+// "Backward data", rocMLIR pull request 246, and "[igemm_dynamic] v4r1 bwd
+// dynamic kernel", MIOpen pull request 272).  Problem -> plan -> run mirrors
+// the library workflow described in "Re: MIOpen package LFS files" (Problem,
+// Find solution, Load kernel, Run on GPU), with a single solution per
+// problem and ahead-of-time compiled kernels: one compiled kernel serves every
+// shape, which receives the shape at run time (the "dynamic kernel" idea of
+// MIOpen pull request 272).
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/conv_bwd_data.h"
+#include "internal.h"
+
+using namespace cbd;
+
+struct conv_bwd_plan_s {
+    conv_bwd_desc desc;
+    Geom g;
+    Strides st;
+    int32_t path = CONV_BWD_PATH_SIMT;
+    int32_t bn = 64;                      // tensor-core tile width (N_gemm)
+    std::vector<ClassDesc> classes;       // gemm_id order
+    std::vector<int> sched;               // launch order (indices into classes)
+    std::vector<uint8_t> row_cov, col_cov;
+    uint64_t cov_h = 0, cov_w = 0;
+    bool any_uncovered = false;
+    double useful_flop = 0, algo_bytes = 0;
+    // device side
+    bool has_device = false;
+    int device = -1;
+    int num_sms = 0;
+    int32_t *d_status = nullptr;
+    int64_t wait_budget = 0;
+    bool timing = false;
+    bool fill_ran = false;
+    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+    // TMA descriptor cache (keyed by the filter pointer)
+    const void *tmap_w_ptr = nullptr;
+    CUtensorMap tmap_w;
+    std::mutex mu;
+};
+
+namespace {
+
+int64_t floor_div(int64_t a, int64_t b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+int64_t ceil_div_s(int64_t a, int64_t b) { return -floor_div(-a, b); }
+
+struct DimClass {
+    int t, taps, lo, cnt;
+};
+
+// Residue classes of one spatial dim.  Returns T (tilde factor) and D (dy
+// step per tap index); fills the per-class taps and row ranges, the coverage
+// residue mask (bit r: indices i with i % s == r are written), the per-index
+// coverage, and the count of (o, f) pairs whose tap lands inside [0, In).
+void plan_dim(int64_t In, int64_t Out, int64_t F, int64_t s, int64_t d, int64_t p, int &T, int &D,
+              std::vector<DimClass> &cls, uint64_t &mask, std::vector<uint8_t> &cov, int64_t &useful) {
+    int64_t g = std::gcd(s, d);
+    T = (int)(s / g);
+    D = (int)(d / g);
+    cls.clear();
+    mask = 0;
+    cov.assign((size_t)In, 0);
+    for (int t = 0; t < T; ++t) {
+        int taps = t < F ? (int)((F - t + T - 1) / T) : 0;
+        int64_t lo = ceil_div_s(p - (int64_t)t * d, s);
+        int64_t hi = floor_div(In - 1 + p - (int64_t)t * d, s);
+        int64_t cnt = std::max<int64_t>(0, hi - lo + 1);
+        cls.push_back({t, taps, (int)lo, (int)cnt});
+        if (taps > 0 && cnt > 0) {
+            int64_t r = ((int64_t)t * d - p) % s;
+            if (r < 0) r += s;
+            mask |= 1ull << r;
+            for (int64_t q = lo; q < lo + cnt; ++q) cov[(size_t)(q * s + (int64_t)t * d - p)] = 1;
+        }
+    }
+    useful = 0;
+    for (int64_t o = 0; o < Out; ++o)
+        for (int64_t f = 0; f < F; ++f) {
+            int64_t i = o * s - p + f * d;
+            if (i >= 0 && i < In) ++useful;
+        }
+}
+
+bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
+    uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + nb && y < x + na;
+}
+
+size_t elem_size(int32_t dt) { return dt == CONV_BWD_BF16 ? 2 : 4; }
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                     CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                     CUtensorMapFloatOOBfill);
+
+PFN_encodeTiled get_encode_tiled() {
+    static PFN_encodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_encodeTiled)p;
+    });
+    return fn;
+}
+
+// w (KYXC, bf16) as a 5-D tensor {Cg, X, Y, Kg, G}: a box {64, 1, 1, 64, 1}
+// is a 64(k) x 64(c) slice of one filter tap, c contiguous (128 bytes per k
+// row, 128-byte swizzle).  Coordinates past Cg or past Kg (the next group's
+// rows) read as zero.
+bool encode_w_map(conv_bwd_plan_s *p, const void *w) {
+    PFN_encodeTiled enc = get_encode_tiled();
+    if (!enc) return false;
+    const Geom &g = p->g;
+    cuuint64_t dims[5] = {(cuuint64_t)g.Cg, (cuuint64_t)g.X, (cuuint64_t)g.Y, (cuuint64_t)g.Kg, (cuuint64_t)g.G};
+    cuuint64_t strides[4] = {(cuuint64_t)g.Cg * 2, (cuuint64_t)g.X * g.Cg * 2, (cuuint64_t)g.Y * g.X * g.Cg * 2,
+                             (cuuint64_t)g.Kg * g.Y * g.X * g.Cg * 2};
+    cuuint32_t box[5] = {64, 1, 1, 64, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(&p->tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(w), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+const char *env(const char *k) {
+    const char *v = std::getenv(k);
+    return (v && *v) ? v : nullptr;
+}
+
+conv_bwd_status validate(const conv_bwd_desc *d) {
+    if (!d) return CONV_BWD_ERR_INVALID_ARG;
+    if (d->N < 1 || d->C < 1 || d->K < 1 || d->Hi < 1 || d->Wi < 1 || d->Y < 1 || d->X < 1)
+        return CONV_BWD_ERR_INVALID_ARG;
+    if (d->pad_h < 0 || d->pad_w < 0 || d->stride_h < 1 || d->stride_w < 1 || d->dil_h < 1 || d->dil_w < 1 ||
+        d->groups < 1)
+        return CONV_BWD_ERR_INVALID_ARG;
+    if (d->C % d->groups || d->K % d->groups) return CONV_BWD_ERR_INVALID_ARG;
+    if (d->layout != CONV_BWD_NCHW_GKCYX && d->layout != CONV_BWD_NHWC_KYXC) return CONV_BWD_ERR_INVALID_ARG;
+    if (d->dtype != CONV_BWD_F32 && d->dtype != CONV_BWD_BF16) return CONV_BWD_ERR_INVALID_ARG;
+    int64_t eh = d->Hi + 2LL * d->pad_h - (int64_t)d->dil_h * (d->Y - 1) - 1;
+    int64_t ew = d->Wi + 2LL * d->pad_w - (int64_t)d->dil_w * (d->X - 1) - 1;
+    if (eh < 0 || ew < 0) return CONV_BWD_ERR_INVALID_ARG;
+    if (d->stride_h > 64 || d->stride_w > 64) return CONV_BWD_ERR_UNSUPPORTED;
+    return CONV_BWD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t conv_bwd_data_version(void) { return 100; }
+
+const char *conv_bwd_status_string(conv_bwd_status s) {
+    switch (s) {
+    case CONV_BWD_OK: return "CONV_BWD_OK";
+    case CONV_BWD_ERR_INVALID_ARG: return "CONV_BWD_ERR_INVALID_ARG";
+    case CONV_BWD_ERR_UNSUPPORTED: return "CONV_BWD_ERR_UNSUPPORTED";
+    case CONV_BWD_ERR_MISALIGNED: return "CONV_BWD_ERR_MISALIGNED";
+    case CONV_BWD_ERR_CUDA: return "CONV_BWD_ERR_CUDA";
+    case CONV_BWD_ERR_DEVICE_TIMEOUT: return "CONV_BWD_ERR_DEVICE_TIMEOUT";
+    case CONV_BWD_ERR_DEVICE_FAULT: return "CONV_BWD_ERR_DEVICE_FAULT";
+    }
+    return "CONV_BWD_UNKNOWN_STATUS";
+}
+
+conv_bwd_status conv_bwd_data_create(const conv_bwd_desc *desc, conv_bwd_plan *out) {
+    if (!out) return CONV_BWD_ERR_INVALID_ARG;
+    *out = nullptr;
+    conv_bwd_status st = validate(desc);
+    if (st != CONV_BWD_OK) return st;
+    const conv_bwd_desc &d = *desc;
+    int64_t Ho = (d.Hi + 2LL * d.pad_h - (int64_t)d.dil_h * (d.Y - 1) - 1) / d.stride_h + 1;
+    int64_t Wo = (d.Wi + 2LL * d.pad_w - (int64_t)d.dil_w * (d.X - 1) - 1) / d.stride_w + 1;
+    const int64_t lim = 0x7fffffffLL;
+    if (d.N * d.C * d.Hi * d.Wi > lim || d.N * d.K * Ho * Wo > lim || d.K * (d.C / d.groups) * d.Y * d.X > lim)
+        return CONV_BWD_ERR_UNSUPPORTED;
+
+    conv_bwd_plan_s *p = new (std::nothrow) conv_bwd_plan_s();
+    if (!p) return CONV_BWD_ERR_CUDA;
+    p->desc = d;
+    Geom &g = p->g;
+    g.N = (int)d.N; g.C = (int)d.C; g.K = (int)d.K; g.Hi = (int)d.Hi; g.Wi = (int)d.Wi;
+    g.Ho = (int)Ho; g.Wo = (int)Wo; g.Y = (int)d.Y; g.X = (int)d.X;
+    g.ph = d.pad_h; g.pw = d.pad_w; g.sh = d.stride_h; g.sw = d.stride_w; g.dh = d.dil_h; g.dw = d.dil_w;
+    g.G = d.groups; g.Cg = (int)(d.C / d.groups); g.Kg = (int)(d.K / d.groups);
+
+    std::vector<DimClass> ch, cw;
+    int64_t uh, uw;
+    plan_dim(d.Hi, Ho, d.Y, d.stride_h, d.dil_h, d.pad_h, g.YT, g.DH, ch, p->cov_h, p->row_cov, uh);
+    plan_dim(d.Wi, Wo, d.X, d.stride_w, d.dil_w, d.pad_w, g.XT, g.DW, cw, p->cov_w, p->col_cov, uw);
+    p->useful_flop = 2.0 * (double)d.N * (double)d.K * (double)g.Cg * (double)uh * (double)uw;
+    size_t es = elem_size(d.dtype);
+    p->algo_bytes = (double)es * ((double)d.N * d.K * Ho * Wo + (double)d.K * g.Cg * d.Y * d.X +
+                                  (double)d.N * d.C * d.Hi * d.Wi);
+    for (uint8_t v : p->row_cov) p->any_uncovered |= (v == 0);
+    for (uint8_t v : p->col_cov) p->any_uncovered |= (v == 0);
+
+    // Non-empty sub-GEMMs, consecutive gemmIds (row class major).
+    for (const DimClass &a : ch)
+        for (const DimClass &b : cw) {
+            if (a.taps == 0 || b.taps == 0 || a.cnt == 0 || b.cnt == 0) continue;
+            ClassDesc c{};
+            c.ty = a.t; c.tx = b.t; c.taps_y = a.taps; c.taps_x = b.taps;
+            c.ht_lo = a.lo; c.HT = a.cnt; c.wt_lo = b.lo; c.WT = b.cnt;
+            int64_t M = d.N * (int64_t)a.cnt * b.cnt;
+            c.M = (int)M;
+            c.gemm_id = (int)p->classes.size();
+            p->classes.push_back(c);
+        }
+    if ((int)p->classes.size() > kMaxClasses) {
+        delete p;
+        return CONV_BWD_ERR_UNSUPPORTED;
+    }
+
+    // Strides of the logical orders dy[n][k][h][w], w[k][c][y][x], dx[n][c][h][w].
+    Strides &s = p->st;
+    if (d.layout == CONV_BWD_NCHW_GKCYX) {
+        s.dy_w = 1; s.dy_h = Wo; s.dy_k = Ho * Wo; s.dy_n = d.K * Ho * Wo;
+        s.w_x = 1; s.w_y = d.X; s.w_c = d.Y * d.X; s.w_k = g.Cg * d.Y * d.X;
+        s.dx_w = 1; s.dx_h = d.Wi; s.dx_c = d.Hi * d.Wi; s.dx_n = d.C * d.Hi * d.Wi;
+    } else {
+        s.dy_k = 1; s.dy_w = d.K; s.dy_h = Wo * d.K; s.dy_n = Ho * Wo * d.K;
+        s.w_c = 1; s.w_x = g.Cg; s.w_y = d.X * g.Cg; s.w_k = d.Y * d.X * g.Cg;
+        s.dx_c = 1; s.dx_w = d.C; s.dx_h = d.Wi * d.C; s.dx_n = d.Hi * d.Wi * d.C;
+    }
+
+    // Kernel path.
+    bool tc_ok = d.dtype == CONV_BWD_BF16 && d.layout == CONV_BWD_NHWC_KYXC && g.Cg % 8 == 0 && g.Kg % 8 == 0 &&
+                 d.K % 8 == 0 && d.C % 8 == 0 && g.Cg >= 64;
+    p->path = tc_ok ? CONV_BWD_PATH_TCGEN05 : CONV_BWD_PATH_SIMT;
+    if (const char *f = env("CONVBWD_DEBUG_PATH")) {
+        if (!std::strcmp(f, "simt")) p->path = CONV_BWD_PATH_SIMT;
+    }
+    p->bn = (p->path == CONV_BWD_PATH_TCGEN05) ? (g.Cg >= 256 ? 256 : 128) : 64;
+
+    // Schedule: classes with the longest reduction first (LPT), tiles of one
+    // class contiguous; BM = 128 rows for the tensor-core path, 64 for SIMT.
+    const int bm = p->path == CONV_BWD_PATH_TCGEN05 ? 128 : 64;
+    const int n_tiles = (g.Cg + p->bn - 1) / p->bn;
+    p->sched.resize(p->classes.size());
+    std::iota(p->sched.begin(), p->sched.end(), 0);
+    std::stable_sort(p->sched.begin(), p->sched.end(), [&](int a, int b) {
+        return p->classes[a].taps_y * p->classes[a].taps_x > p->classes[b].taps_y * p->classes[b].taps_x;
+    });
+    int64_t tiles = 0;
+    for (int idx : p->sched) {
+        ClassDesc &c = p->classes[idx];
+        c.m_tiles = (c.M + bm - 1) / bm;
+        c.tile_begin = (int)tiles;
+        tiles += (int64_t)g.G * c.m_tiles * n_tiles;
+    }
+    if (tiles > lim) {
+        delete p;
+        return CONV_BWD_ERR_UNSUPPORTED;
+    }
+
+    // Device resources (optional: planning works without a GPU).
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0) {
+        cudaGetDevice(&p->device);
+        cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+        int clk_khz = 0;
+        cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, p->device);
+        if (clk_khz <= 0) clk_khz = 2000000;
+        double secs = 2.0;
+        if (const char *b = env("CONVBWD_DEBUG_WAIT_SECONDS")) secs = std::atof(b);
+        p->wait_budget = (int64_t)(secs * clk_khz * 1000.0);
+        if (cudaMalloc(&p->d_status, 16) != cudaSuccess || cudaMemset(p->d_status, 0, 16) != cudaSuccess) {
+            cudaGetLastError();
+            delete p;
+            return CONV_BWD_ERR_CUDA;
+        }
+        p->has_device = true;
+    } else {
+        cudaGetLastError();  // clear "no device"
+    }
+    *out = p;
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_destroy(conv_bwd_plan p) {
+    if (!p) return CONV_BWD_OK;
+    if (p->has_device) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (cur != p->device) cudaSetDevice(p->device);
+        cudaFree(p->d_status);
+        for (auto &e : p->ev)
+            if (e) cudaEventDestroy(e);
+        if (cur != p->device && cur >= 0) cudaSetDevice(cur);
+    }
+    delete p;
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_out_dims(const conv_bwd_plan p, int64_t *Ho, int64_t *Wo) {
+    if (!p) return CONV_BWD_ERR_INVALID_ARG;
+    if (Ho) *Ho = p->g.Ho;
+    if (Wo) *Wo = p->g.Wo;
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_num_subgemms(const conv_bwd_plan p, int32_t *n) {
+    if (!p || !n) return CONV_BWD_ERR_INVALID_ARG;
+    *n = (int32_t)p->classes.size();
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_subgemm_info(const conv_bwd_plan p, int32_t id, int32_t *ty, int32_t *tx, int64_t *M,
+                                           int64_t *N, int64_t *K, int32_t *taps_y, int32_t *taps_x) {
+    if (!p || id < 0 || id >= (int32_t)p->classes.size()) return CONV_BWD_ERR_INVALID_ARG;
+    const ClassDesc &c = p->classes[(size_t)id];
+    if (ty) *ty = c.ty;
+    if (tx) *tx = c.tx;
+    if (M) *M = c.M;
+    if (N) *N = p->g.Cg;
+    if (K) *K = (int64_t)p->g.Kg * c.taps_y * c.taps_x;
+    if (taps_y) *taps_y = c.taps_y;
+    if (taps_x) *taps_x = c.taps_x;
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_coverage(const conv_bwd_plan p, uint8_t *row_mask, uint8_t *col_mask) {
+    if (!p) return CONV_BWD_ERR_INVALID_ARG;
+    if (row_mask) std::memcpy(row_mask, p->row_cov.data(), p->row_cov.size());
+    if (col_mask) std::memcpy(col_mask, p->col_cov.data(), p->col_cov.size());
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t *launches) {
+    if (!p) return CONV_BWD_ERR_INVALID_ARG;
+    if (path) *path = p->path;
+    if (launches) *launches = (p->any_uncovered ? 1 : 0) + (p->classes.empty() ? 0 : 1);
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_work(const conv_bwd_plan p, double *flop, double *bytes) {
+    if (!p) return CONV_BWD_ERR_INVALID_ARG;
+    if (flop) *flop = p->useful_flop;
+    if (bytes) *bytes = p->algo_bytes;
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w, void *dx, void *stream) {
+    if (!p || !dy || !w || !dx) return CONV_BWD_ERR_INVALID_ARG;
+    if (!p->has_device) return CONV_BWD_ERR_CUDA;
+    const conv_bwd_desc &d = p->desc;
+    const Geom &g = p->g;
+    size_t es = elem_size(d.dtype);
+    size_t ndy = (size_t)d.N * d.K * g.Ho * g.Wo * es, nw = (size_t)d.K * g.Cg * d.Y * d.X * es,
+           ndx = (size_t)d.N * d.C * d.Hi * d.Wi * es;
+    if (ranges_overlap(dy, ndy, dx, ndx) || ranges_overlap(w, nw, dx, ndx)) return CONV_BWD_ERR_INVALID_ARG;
+    if (((uintptr_t)dy | (uintptr_t)w | (uintptr_t)dx) % es) return CONV_BWD_ERR_MISALIGNED;
+    // Every alignment rule is checked before anything is launched.
+    if (p->path == CONV_BWD_PATH_TCGEN05 && ((uintptr_t)dy | (uintptr_t)w | (uintptr_t)dx) % 16)
+        return CONV_BWD_ERR_MISALIGNED;
+    cudaStream_t s = (cudaStream_t)stream;
+    std::lock_guard<std::mutex> lock(p->mu);
+
+    if (p->timing) {
+        for (auto &e : p->ev)
+            if (!e && cudaEventCreate(&e) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+    }
+    p->fill_ran = false;
+    if (p->any_uncovered) {
+        FillParams fp{};
+        fp.dx = dx; fp.esize = (int)es; fp.layout = d.layout;
+        fp.N = g.N; fp.C = g.C; fp.Hi = g.Hi; fp.Wi = g.Wi; fp.sh = g.sh; fp.sw = g.sw;
+        fp.cov_h = p->cov_h; fp.cov_w = p->cov_w;
+        fp.vec16 = (d.layout == CONV_BWD_NHWC_KYXC && ((int64_t)d.C * (int64_t)es) % 16 == 0 &&
+                    (uintptr_t)dx % 16 == 0) ? 1 : 0;
+        if (p->timing) cudaEventRecord(p->ev[0], s);
+        if (launch_fill(fp, p->num_sms, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        if (p->timing) cudaEventRecord(p->ev[1], s);
+        p->fill_ran = true;
+    }
+    if (p->classes.empty()) return CONV_BWD_OK;
+
+    if (p->path == CONV_BWD_PATH_TCGEN05) {
+        TcParams tp;
+        std::memset(&tp, 0, sizeof(tp));
+        if (p->tmap_w_ptr != w) {
+            if (!encode_w_map(p, w)) return CONV_BWD_ERR_CUDA;
+            p->tmap_w_ptr = w;
+        }
+        tp.tmap_w = p->tmap_w;
+        tp.dy = dy; tp.dx = dx; tp.status = p->d_status; tp.wait_budget = p->wait_budget;
+        tp.g = g;
+        tp.num_classes = (int)p->sched.size();
+        tp.n_tiles = (g.Cg + p->bn - 1) / p->bn;
+        tp.kb_per_tap = (g.Kg + 63) / 64;
+        int64_t total = 0;
+        for (size_t i = 0; i < p->sched.size(); ++i) {
+            tp.cls[i] = p->classes[(size_t)p->sched[i]];
+            total += (int64_t)g.G * tp.cls[i].m_tiles * tp.n_tiles;
+        }
+        tp.total_tiles = (int)total;
+        int grid = (int)std::min<int64_t>(total, p->num_sms);
+        if (p->timing) cudaEventRecord(p->ev[2], s);
+        if (launch_tc(tp, p->bn, grid, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        if (p->timing) cudaEventRecord(p->ev[3], s);
+        return CONV_BWD_OK;
+    }
+
+    SimtParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.g = g; sp.st = p->st; sp.dy = dy; sp.w = w; sp.dx = dx;
+    sp.num_classes = (int)p->sched.size();
+    sp.n_tiles = (g.Cg + 63) / 64;
+    int64_t total = 0;
+    for (size_t i = 0; i < p->sched.size(); ++i) {
+        sp.cls[i] = p->classes[(size_t)p->sched[i]];
+        total += (int64_t)g.G * sp.cls[i].m_tiles * sp.n_tiles;
+    }
+    sp.total_tiles = (int)total;
+    if (p->timing) cudaEventRecord(p->ev[2], s);
+    if (launch_simt(sp, d.dtype, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+    if (p->timing) cudaEventRecord(p->ev[3], s);
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_run_host(conv_bwd_plan p, const void *dy_h, const void *w_h, void *dx_h, void *dy_d,
+                                       void *w_d, void *dx_d, void *stream) {
+    if (!p || !dy_h || !w_h || !dx_h || !dy_d || !w_d || !dx_d) return CONV_BWD_ERR_INVALID_ARG;
+    if (!p->has_device) return CONV_BWD_ERR_CUDA;
+    const conv_bwd_desc &d = p->desc;
+    size_t es = elem_size(d.dtype);
+    size_t ndy = (size_t)d.N * d.K * p->g.Ho * p->g.Wo * es, nw = (size_t)d.K * p->g.Cg * d.Y * d.X * es,
+           ndx = (size_t)d.N * d.C * d.Hi * d.Wi * es;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(dy_d, dy_h, ndy, cudaMemcpyHostToDevice, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+    if (cudaMemcpyAsync(w_d, w_h, nw, cudaMemcpyHostToDevice, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+    conv_bwd_status st = conv_bwd_data_run(p, dy_d, w_d, dx_d, stream);
+    if (st != CONV_BWD_OK) return st;
+    if (cudaMemcpyAsync(dx_h, dx_d, ndx, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_get_status(conv_bwd_plan p, void *stream, int32_t *detail) {
+    if (!p) return CONV_BWD_ERR_INVALID_ARG;
+    if (detail) *detail = 0;
+    if (!p->has_device) return CONV_BWD_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t h = 0;
+    if (cudaMemcpyAsync(&h, p->d_status, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+    if (h == 0) return CONV_BWD_OK;
+    if (detail) *detail = h;
+    cudaMemsetAsync(p->d_status, 0, 16, s);
+    cudaStreamSynchronize(s);
+    return (h & 0xF00) == 0x200 ? CONV_BWD_ERR_DEVICE_FAULT : CONV_BWD_ERR_DEVICE_TIMEOUT;
+}
+
+conv_bwd_status conv_bwd_data_set_timing(conv_bwd_plan p, int32_t enable) {
+    if (!p) return CONV_BWD_ERR_INVALID_ARG;
+    p->timing = enable != 0;
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_last_timing(conv_bwd_plan p, float *fill_ms, float *gemm_ms) {
+    if (!p || !p->timing || !p->ev[3]) return CONV_BWD_ERR_INVALID_ARG;
+    float f = 0.f, m = 0.f;
+    if (p->fill_ran) {
+        if (cudaEventSynchronize(p->ev[1]) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        cudaEventElapsedTime(&f, p->ev[0], p->ev[1]);
+    }
+    if (!p->classes.empty()) {
+        if (cudaEventSynchronize(p->ev[3]) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        cudaEventElapsedTime(&m, p->ev[2], p->ev[3]);
+    }
+    if (fill_ms) *fill_ms = f;
+    if (gemm_ms) *gemm_ms = m;
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_selftest_wait_timeout(void *stream, int64_t budget_cycles, int32_t *observed) {
+    if (!observed || budget_cycles <= 0) return CONV_BWD_ERR_INVALID_ARG;
+    int32_t *d = nullptr;
+    if (cudaMalloc(&d, 16) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    conv_bwd_status st = CONV_BWD_OK;
+    int32_t h = -1;
+    if (cudaMemsetAsync(d, 0, 16, s) != cudaSuccess || launch_selftest_wait(d, budget_cycles, s) != cudaSuccess ||
+        cudaMemcpyAsync(&h, d, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        st = CONV_BWD_ERR_CUDA;
+    cudaFree(d);
+    if (st != CONV_BWD_OK) return st;
+    *observed = (h == kDevTimeoutSelftest) ? CONV_BWD_ERR_DEVICE_TIMEOUT : (h == 0 ? CONV_BWD_OK : CONV_BWD_ERR_DEVICE_FAULT);
+    return CONV_BWD_OK;
+}
+
+}  // extern "C"

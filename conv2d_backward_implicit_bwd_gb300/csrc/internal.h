@@ -1,0 +1,100 @@
+// internal.h -- types shared by the host planner, the C ABI and the kernels.
+//
+// The decomposition (pages "Backward data" / "[igemm_dynamic] v4r1 bwd
+// dynamic kernel", the v4r1 backward-data gridwise-GEMM strategy): per
+// spatial dim with stride s, dilation d, pad p and filter length F,
+//   g = gcd(s, d), T = s / g (YTilde / XTilde), D = d / g;
+//   class t in [0, T) owns taps y = t + T*j, j < ceil((F - t) / T);
+//   it writes dx rows hi = ht*s + t*d - p for ht in [ht_lo, ht_lo + HT) (all
+//   such rows inside [0, Hi)), and tap j of row ht reads dy row ho = ht - j*D
+//   (zero when ho is outside [0, Ho)).
+// One sub-GEMM per pair of non-empty row/column classes:
+//   M = N * HT * WT rows (n, ht, wt), N_gemm = C/G, K_gemm = K/G * taps.
+#pragma once
+#include <stdint.h>
+#include <cuda.h>           // CUtensorMap (header-only use)
+#include <cuda_runtime.h>
+
+namespace cbd {
+
+constexpr int kMaxClasses = 64;   // stride_h * stride_w classes at most (each stride <= 64 handled via this cap)
+
+struct ClassDesc {
+    int32_t ty, tx;          // row / column residue class
+    int32_t taps_y, taps_x;  // taps of each class (>= 1 for a non-empty sub-GEMM)
+    int32_t ht_lo, HT;       // first class row index and count
+    int32_t wt_lo, WT;       // first class column index and count
+    int32_t M;               // N * HT * WT
+    int32_t m_tiles;         // ceil(M / BM) for the kernel that runs this class
+    int32_t tile_begin;      // first tile of this class in the launch's schedule
+    int32_t gemm_id;         // consecutive id of the sub-GEMM
+};
+
+struct Geom {
+    int32_t N, C, K, Hi, Wi, Ho, Wo, Y, X;
+    int32_t ph, pw, sh, sw, dh, dw, G, Cg, Kg;
+    int32_t YT, XT, DH, DW;
+};
+
+// Element strides of the logical index orders dy[n][k][ho][wo],
+// w[k][c][y][x] (c within the group) and dx[n][c][hi][wi] for either layout.
+struct Strides {
+    int64_t dy_n, dy_k, dy_h, dy_w;
+    int64_t w_k, w_c, w_y, w_x;
+    int64_t dx_n, dx_c, dx_h, dx_w;
+};
+
+struct SimtParams {
+    Geom g;
+    Strides st;
+    const void *dy;
+    const void *w;
+    void *dx;
+    int32_t num_classes;
+    int32_t n_tiles;      // ceil(Cg / 64)
+    int32_t total_tiles;  // sum over classes of G * m_tiles * n_tiles
+    ClassDesc cls[kMaxClasses];
+};
+
+struct FillParams {
+    void *dx;
+    int32_t esize;        // bytes per element
+    int32_t layout;       // 0 NCHW, 1 NHWC
+    int32_t vec16;        // 1: NHWC, C*esize % 16 == 0 and dx 16-byte aligned -> 16-byte stores
+    int32_t N, C, Hi, Wi;
+    int32_t sh, sw;
+    uint64_t cov_h, cov_w; // bit r set: rows/cols with index % s == r are written by a sub-GEMM
+};
+
+// Tensor-core (tcgen05) kernel parameters.
+struct TcParams {  // 128-byte aligned through CUtensorMap
+    CUtensorMap tmap_w;   // w viewed as 5-D {Cg, X, Y, Kg, G}, box {64, 1, 1, 64, 1}, 128B swizzle
+    const void *dy;
+    void *dx;
+    int32_t *status;      // device status word (0 = ok)
+    int64_t wait_budget;  // SM clock cycles a blocking wait may spin before giving up
+    Geom g;
+    int32_t num_classes;
+    int32_t n_tiles;      // ceil(Cg / BN)
+    int32_t kb_per_tap;   // ceil(Kg / 64)
+    int32_t total_tiles;
+    ClassDesc cls[kMaxClasses];
+};
+
+// Status codes written by kernels (first writer wins).
+enum : int32_t {
+    kDevOk = 0,
+    kDevTimeoutProducer = 0x101,
+    kDevTimeoutMma = 0x102,
+    kDevTimeoutEpilogue = 0x103,
+    kDevTimeoutSelftest = 0x1FF,
+    kDevFaultIndex = 0x201,
+};
+
+cudaError_t launch_fill(const FillParams &p, int num_sms, cudaStream_t s);
+cudaError_t launch_simt(const SimtParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_tc(const TcParams &p, int bn, int grid, cudaStream_t s);
+cudaError_t launch_selftest_wait(int32_t *status, int64_t budget, cudaStream_t s);
+size_t tc_smem_bytes(int bn);
+
+}  // namespace cbd

@@ -1,0 +1,235 @@
+// simt.cu -- CUDA-core kernels: the dx fill, the tiled SIMT implicit GEMM
+// (fp32 path, and the bf16 fallback for shapes the tensor-core kernel does
+// not take), and the bounded-wait self-test.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "device_util.cuh"
+#include "internal.h"
+
+namespace cbd {
+
+// ---------------------------------------------------------------------------
+// Fill: dx := +0 at every pixel that no sub-GEMM writes.  A pixel is written
+// iff its row residue (hi % sh) and column residue (wi % sw) both belong to a
+// class with at least one tap; the planner encodes those residues as bit
+// masks.  The pages never state the zero-initialisation; it follows from dx
+// being fully overwritten (torch-IR `torch.overwrite.tensor.contents` on page
+// "Non-unit stride input backward different input and dispatches between BOO
+// and Fusilli").  NHWC: one 16-byte store per 8 bf16 / 4 fp32 channels of an
+// uncovered pixel (consecutive threads -> consecutive chunks).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) fill_kernel(const FillParams p) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (p.vec16) {
+        const int64_t cpp = (int64_t)p.C * p.esize / 16;
+        const int64_t total = (int64_t)p.N * p.Hi * p.Wi * cpp;
+        uint4 *out = reinterpret_cast<uint4 *>(p.dx);
+        for (int64_t u = first; u < total; u += stride) {
+            int64_t pix = u / cpp;
+            int wi = (int)(pix % p.Wi);
+            int hi = (int)((pix / p.Wi) % p.Hi);
+            bool cov = ((p.cov_h >> (hi % p.sh)) & 1ull) && ((p.cov_w >> (wi % p.sw)) & 1ull);
+            if (!cov) out[u] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        return;
+    }
+    const int64_t total = (int64_t)p.N * p.C * p.Hi * p.Wi;
+    for (int64_t e = first; e < total; e += stride) {
+        int hi, wi;
+        if (p.layout == 0) {
+            wi = (int)(e % p.Wi);
+            hi = (int)((e / p.Wi) % p.Hi);
+        } else {
+            int64_t pix = e / p.C;
+            wi = (int)(pix % p.Wi);
+            hi = (int)((pix / p.Wi) % p.Hi);
+        }
+        bool cov = ((p.cov_h >> (hi % p.sh)) & 1ull) && ((p.cov_w >> (wi % p.sw)) & 1ull);
+        if (!cov) {
+            if (p.esize == 4)
+                reinterpret_cast<float *>(p.dx)[e] = 0.f;
+            else
+                reinterpret_cast<uint16_t *>(p.dx)[e] = 0;
+        }
+    }
+}
+
+cudaError_t launch_fill(const FillParams &p, int num_sms, cudaStream_t s) {
+    int64_t units = (int64_t)p.N * p.C * p.Hi * p.Wi;
+    if (p.vec16) units = units * p.esize / 16;
+    int64_t blocks = (units + 255) / 256;
+    int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 148) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    fill_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// SIMT implicit GEMM over all sub-GEMMs in one launch.  One 64x64 output tile
+// per block: rows are the class's (n, ht, wt) positions, columns the input
+// channels of one group.  The reduction runs over (tap, k) with
+//   A[m, (tap, k)] = dy[n, gi*Kg + k, ht - j*DH, wt - i*DW]   (0 outside dy)
+//   B[(tap, k), c] = w[gi*Kg + k, c, ty + YT*j, tx + XT*i]
+// and the result goes to dx[n, gi*Cg + c, ht*sh + ty*dh - ph, wt*sw + tx*dw - pw].
+// fp32 accumulation; each thread owns a 4x4 micro-tile.
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ float ld_as_float(const T *p, int64_t i);
+template <>
+__device__ __forceinline__ float ld_as_float<float>(const float *p, int64_t i) {
+    return __ldg(p + i);
+}
+template <>
+__device__ __forceinline__ float ld_as_float<__nv_bfloat16>(const __nv_bfloat16 *p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+template <typename T>
+__device__ __forceinline__ void st_from_float(T *p, int64_t i, float v);
+template <>
+__device__ __forceinline__ void st_from_float<float>(float *p, int64_t i, float v) {
+    p[i] = v;
+}
+template <>
+__device__ __forceinline__ void st_from_float<__nv_bfloat16>(__nv_bfloat16 *p, int64_t i, float v) {
+    p[i] = __float2bfloat16_rn(v);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) simt_dgrad_kernel(const __grid_constant__ SimtParams p) {
+    constexpr int BM = 64, BN = 64, BK = 16;
+    __shared__ float As[BK][BM + 4];
+    __shared__ float Bs[BK][BN + 4];
+    const Geom &g = p.g;
+    const Strides &st = p.st;
+    const T *dy = static_cast<const T *>(p.dy);
+    const T *w = static_cast<const T *>(p.w);
+    T *dx = static_cast<T *>(p.dx);
+
+    const int tile = blockIdx.x;
+    int ci = 0;
+    for (int i = 1; i < p.num_classes; ++i)
+        if (tile >= p.cls[i].tile_begin) ci = i;
+    const ClassDesc &c = p.cls[ci];
+    const int local = tile - c.tile_begin;
+    const int nb = local % p.n_tiles;
+    const int rest = local / p.n_tiles;
+    const int mb = rest % c.m_tiles;
+    const int gi = rest / c.m_tiles;
+
+    const int tid = threadIdx.x;
+    const int HTWT = c.HT * c.WT;
+    const int Kred = c.taps_y * c.taps_x * g.Kg;
+
+    // the A row this thread loads
+    const int arow = tid % BM;
+    const int am = mb * BM + arow;
+    int an = -1, aht = 0, awt = 0;
+    if (am < c.M) {
+        an = am / HTWT;
+        int rem = am - an * HTWT;
+        aht = c.ht_lo + rem / c.WT;
+        awt = c.wt_lo + rem % c.WT;
+    }
+    // the B column this thread loads
+    const int bcol = tid % BN;
+    const int bc = nb * BN + bcol;
+
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+    const int tr = tid / 16, tc = tid % 16;
+    for (int r0 = 0; r0 < Kred; r0 += BK) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int kk = tid / BM + 4 * q;
+            const int r = r0 + kk;
+            float va = 0.f, vb = 0.f;
+            if (r < Kred) {
+                const int tap = r / g.Kg, k = r - tap * g.Kg;
+                const int j = tap / c.taps_x, i = tap - j * c.taps_x;
+                if (an >= 0) {
+                    const int ho = aht - j * g.DH, wo = awt - i * g.DW;
+                    if (ho >= 0 && ho < g.Ho && wo >= 0 && wo < g.Wo)
+                        va = ld_as_float<T>(dy, an * st.dy_n + (int64_t)(gi * g.Kg + k) * st.dy_k + ho * st.dy_h +
+                                                    wo * st.dy_w);
+                }
+                if (bc < g.Cg) {
+                    const int y = c.ty + g.YT * j, x = c.tx + g.XT * i;
+                    vb = ld_as_float<T>(w, (int64_t)(gi * g.Kg + k) * st.w_k + bc * st.w_c + y * st.w_y + x * st.w_x);
+                }
+            }
+            As[kk][arow] = va;
+            Bs[kk][bcol] = vb;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[kk][tr * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tc * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = mb * BM + tr * 4 + i;
+        if (m >= c.M) continue;
+        const int n = m / HTWT;
+        const int rem = m - n * HTWT;
+        const int hi = (c.ht_lo + rem / c.WT) * g.sh + c.ty * g.dh - g.ph;
+        const int wi = (c.wt_lo + rem % c.WT) * g.sw + c.tx * g.dw - g.pw;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int cc = nb * BN + tc * 4 + j;
+            if (cc >= g.Cg) continue;
+            st_from_float<T>(dx, n * st.dx_n + (int64_t)(gi * g.Cg + cc) * st.dx_c + hi * st.dx_h + wi * st.dx_w,
+                             acc[i][j]);
+        }
+    }
+}
+
+cudaError_t launch_simt(const SimtParams &p, int dtype, cudaStream_t s) {
+    if (p.total_tiles <= 0) return cudaSuccess;
+    if (dtype == 1)
+        simt_dgrad_kernel<__nv_bfloat16><<<p.total_tiles, 256, 0, s>>>(p);
+    else
+        simt_dgrad_kernel<float><<<p.total_tiles, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded wait: a barrier that nothing arrives on.
+// ---------------------------------------------------------------------------
+__global__ void selftest_wait_kernel(int32_t *status, int64_t budget) {
+    __shared__ alignas(8) uint64_t bar;
+    __shared__ int32_t abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        (void)mbar_wait_bounded(smem_u32(&bar), 0, budget, &abort_flag, status, kDevTimeoutSelftest);
+    }
+}
+
+cudaError_t launch_selftest_wait(int32_t *status, int64_t budget, cudaStream_t s) {
+    selftest_wait_kernel<<<1, 32, 0, s>>>(status, budget);
+    return cudaGetLastError();
+}
+
+}  // namespace cbd

@@ -1,0 +1,396 @@
+// tc_sm103.cu -- bf16 NHWC/KYXC dgrad on the 5th-generation tensor cores
+// (tcgen05 + TMEM), all sub-GEMMs of a plan in one persistent launch.
+//
+// Per residue class (ty, tx) and group gi the sub-GEMM is
+//   D[m, c] = sum over taps (j, i) and k < Kg of A[m, (j, i, k)] * B[(j, i, k), c]
+//   A[m, (j, i, k)] = dy[n, ht - j*DH, wt - i*DW, gi*Kg + k]     (zero outside dy)
+//   B[(j, i, k), c] = w[gi*Kg + k, ty + YT*j, tx + XT*i, c]
+//   dx[n, ht*sh + ty*dh - ph, wt*sw + tx*dw - pw, gi*Cg + c] = bf16_rne(D[m, c])
+// with m enumerating the class's (n, ht, wt) positions.  This is the v4r1
+// backward-data multi-kernel split (pages "Backward data" and "[igemm_dynamic]
+// v4r1 bwd dynamic kernel"): stride > 1 needs no zero insertion, and the
+// filter flip of the BOO IR (`1 - x` index, page "Non-unit stride input
+// backward different input and dispatches between BOO and Fusilli") becomes
+// the decreasing dy row ho = ht - j*DH.  Out-of-range dy rows read as zero
+// (the "OOB dims in getGemmA" point of the rocMLIR review); the epilogue
+// writes only rows of the class that exist in dx (the "OOB write" point).
+//
+// Tile: 128 (m) x BN (c) with BN in {128, 256}, K step 64 (one 128-byte
+// swizzled row per operand row).  Roles (288 threads, one CTA per SM):
+//   warps 0-3  epilogue: tcgen05.ld of the fp32 accumulator (warp q reads TMEM
+//              lanes 32q..32q+31 = tile rows), RNE to bf16, 16-byte stores to
+//              the class's strided dx pixels;
+//   warps 4-7  producers: A rows gathered with 16-byte cp.async (zero-fill for
+//              rows outside dy or past Kg) into the 128-byte-swizzled K-major
+//              layout; one thread also issues the TMA loads of B (w is
+//              c-contiguous, so B is MN-major: BN/64 boxes of 64 k x 64 c);
+//   warp 8     TMEM allocation and the single-thread tcgen05.mma issue
+//              (M=128, N=BN, K=16, bf16 x bf16 -> fp32), committing each stage
+//              back to its producer barrier and each finished tile to the
+//              epilogue.  The accumulator is double-buffered in TMEM (2*BN
+//              columns) so the epilogue of tile t overlaps the MMAs of t+1.
+// Every barrier wait is bounded (device_util.cuh); on a timeout the kernel
+// records the status word, drains what it started and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "device_util.cuh"
+#include "internal.h"
+
+namespace cbd {
+
+template <int BN>
+struct TcCfg {
+    static constexpr int BM = 128;
+    static constexpr int BK = 64;
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int LAG = STAGES - 1;  // cp.async groups kept in flight per producer thread
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + BAR_BYTES;
+    static constexpr int THREADS = 288;
+};
+
+// --- PTX wrappers ----------------------------------------------------------
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;  // descriptor version for tcgen05
+    d |= 2ull << 61;  // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
+// B MN-major (c contiguous), M = 128, N = BN.
+template <int BN>
+__device__ __forceinline__ constexpr uint32_t idesc_bf16() {
+    return (1u << 4)                  // D format: f32
+           | (1u << 7)                // A format: bf16
+           | (1u << 10)               // B format: bf16
+           | (0u << 15)               // A major: K
+           | (1u << 16)               // B major: MN
+           | ((uint32_t)(BN >> 3) << 17)
+           | ((uint32_t)(128 >> 4) << 24);
+}
+
+struct TileCoord {
+    int ci, mb, nb, gi;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const TcParams &p, int t) {
+    int ci = 0;
+    for (int i = 1; i < p.num_classes; ++i)
+        if (t >= p.cls[i].tile_begin) ci = i;
+    const ClassDesc &c = p.cls[ci];
+    int local = t - c.tile_begin;
+    TileCoord r;
+    r.ci = ci;
+    r.nb = local % p.n_tiles;
+    int rest = local / p.n_tiles;
+    r.mb = rest % c.m_tiles;
+    r.gi = rest / c.m_tiles;
+    return r;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1) tc_dgrad_kernel(const __grid_constant__ TcParams p) {
+    using Cfg = TcCfg<BN>;
+    constexpr int S = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + S * Cfg::A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S * Cfg::B_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
+
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+    const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const Geom &g = p.g;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 128);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);
+            mbar_init(tempty0 + 8 * b, 128);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async_smem();
+    }
+    if (warp == 8) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tc_fence_before();
+    }
+    if (warp == 4 && lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_w)) : "memory");
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ producers
+        const int pt = threadIdx.x - 128;
+        const int chunk = pt & 7, rsub = pt >> 3;
+        const uint32_t swz = (uint32_t)((chunk ^ (rsub & 7)) << 4);
+        const __nv_bfloat16 *dy = static_cast<const __nv_bfloat16 *>(p.dy);
+        uint32_t it = 0;
+        bool ok = true;
+        bool issued_tma = false;
+        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            const TileCoord tcd = decode_tile(p, t);
+            const ClassDesc &c = p.cls[tcd.ci];
+            const int HTWT = c.HT * c.WT;
+            int rn[8], rht[8], rwt[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int m = tcd.mb * 128 + rsub + 16 * q;
+                rn[q] = -1;
+                rht[q] = 0;
+                rwt[q] = 0;
+                if (m < c.M) {
+                    const int n = m / HTWT;
+                    const int rem = m - n * HTWT;
+                    rn[q] = n;
+                    rht[q] = c.ht_lo + rem / c.WT;
+                    rwt[q] = c.wt_lo + rem % c.WT;
+                }
+            }
+            const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
+            for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                const int tap = kb / p.kb_per_tap;
+                const int k0 = (kb - tap * p.kb_per_tap) * 64;
+                const int j = tap / c.taps_x, i = tap - j * c.taps_x;
+                const uint32_t s = it % S, ph = (it / S) & 1;
+                if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, p.wait_budget, abort_flag, p.status,
+                                       kDevTimeoutProducer)) {
+                    ok = false;
+                    break;
+                }
+                if (pt == 0) {
+                    mbar_expect_tx(full0 + 8 * s, (uint32_t)Cfg::B_BYTES);
+                    const uint32_t bdst = smem_u32(sB + s * Cfg::B_BYTES);
+#pragma unroll
+                    for (int cb = 0; cb < BN / 64; ++cb)
+                        tma_load_5d(bdst + cb * 8192, &p.tmap_w, full0 + 8 * s, tcd.nb * BN + cb * 64,
+                                    c.tx + g.XT * i, c.ty + g.YT * j, k0, tcd.gi);
+                    issued_tma = true;
+                }
+                const int kch = k0 + chunk * 8;
+                const bool kval = kch < g.Kg;
+                const uint32_t abase = smem_u32(sA + s * Cfg::A_BYTES) + swz;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int ho = rht[q] - j * g.DH, wo = rwt[q] - i * g.DW;
+                    const bool v = rn[q] >= 0 && kval && ho >= 0 && ho < g.Ho && wo >= 0 && wo < g.Wo;
+                    const __nv_bfloat16 *src =
+                        v ? dy + ((((int64_t)rn[q] * g.Ho + ho) * g.Wo + wo) * g.K + (int64_t)tcd.gi * g.Kg + kch) : dy;
+                    cp_async_16(abase + (uint32_t)(rsub + 16 * q) * 128u, src, v ? 16u : 0u);
+                }
+                cp_async_commit();
+                if (it >= (uint32_t)Cfg::LAG) {
+                    cp_async_wait<Cfg::LAG>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(full0 + 8 * ((it - Cfg::LAG) % S));
+                }
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        if (ok) {
+            const uint32_t first = it >= (uint32_t)Cfg::LAG ? it - Cfg::LAG : 0u;
+            for (uint32_t u = first; u < it; ++u) mbar_arrive(full0 + 8 * (u % S));
+        } else if (issued_tma) {
+            // let TMA loads already in flight land before the block exits
+            for (int q = 0; q < 100; ++q) __nanosleep(1000);
+        }
+    } else if (warp == 8) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16<BN>();
+            uint32_t it = 0, tc = 0;
+            bool ok = true, issued = false;
+            for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++tc) {
+                const TileCoord tcd = decode_tile(p, t);
+                const ClassDesc &c = p.cls[tcd.ci];
+                const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
+                const uint32_t b = tc & 1, tph = (tc >> 1) & 1;
+                if (!mbar_wait_bounded(tempty0 + 8 * b, tph ^ 1, p.wait_budget, abort_flag, p.status,
+                                       kDevTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + b * BN;
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                    const uint32_t s = it % S, ph = (it / S) & 1;
+                    if (!mbar_wait_bounded(full0 + 8 * s, ph, p.wait_budget, abort_flag, p.status, kDevTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + s * Cfg::A_BYTES);
+                    const uint32_t b_addr = smem_u32(sB + s * Cfg::B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
+                        tc_mma(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    tc_commit(empty0 + 8 * s);
+                }
+                if (!ok) break;
+                tc_commit(tfull0 + 8 * b);
+            }
+            if (!ok && issued) {
+                for (int q = 0; q < 100; ++q) __nanosleep(1000);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int row = warp * 32 + lane;  // TMEM lane = tile row
+        __nv_bfloat16 *dx = static_cast<__nv_bfloat16 *>(p.dx);
+        uint32_t tc = 0;
+        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++tc) {
+            const TileCoord tcd = decode_tile(p, t);
+            const ClassDesc &c = p.cls[tcd.ci];
+            const uint32_t b = tc & 1, tph = (tc >> 1) & 1;
+            bool ok = mbar_wait_bounded(tfull0 + 8 * b, tph, p.wait_budget, abort_flag, p.status, kDevTimeoutEpilogue);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const int m = tcd.mb * 128 + row;
+            const bool rvalid = m < c.M;
+            int64_t off = 0;
+            if (rvalid) {
+                const int HTWT = c.HT * c.WT;
+                const int n = m / HTWT;
+                const int rem = m - n * HTWT;
+                const int hi = (c.ht_lo + rem / c.WT) * g.sh + c.ty * g.dh - g.ph;
+                const int wi = (c.wt_lo + rem % c.WT) * g.sw + c.tx * g.dw - g.pw;
+                off = (((int64_t)n * g.Hi + hi) * g.Wi + wi) * g.C + (int64_t)tcd.gi * g.Cg + (int64_t)tcd.nb * BN;
+            }
+            const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + b * BN;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld32(tbase + cc * 32, v);
+                const int col0 = tcd.nb * BN + cc * 32;
+                if (rvalid && col0 < g.Cg) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                        pk[e] = *reinterpret_cast<uint32_t *>(&h2);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(dx + off + cc * 32);
+#pragma unroll
+                    for (int piece = 0; piece < 4; ++piece)
+                        if (col0 + piece * 8 < g.Cg)
+                            dst[piece] = make_uint4(pk[4 * piece], pk[4 * piece + 1], pk[4 * piece + 2], pk[4 * piece + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty0 + 8 * b);
+        }
+    }
+
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+size_t tc_smem_bytes(int bn) { return bn == 256 ? TcCfg<256>::SMEM : TcCfg<128>::SMEM; }
+
+template <int BN>
+static cudaError_t launch_tc_bn(const TcParams &p, int grid, cudaStream_t s) {
+    static bool attr_set = false;  // per process; the attribute is per function and device-independent here
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(tc_dgrad_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             TcCfg<BN>::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    tc_dgrad_kernel<BN><<<grid, TcCfg<BN>::THREADS, TcCfg<BN>::SMEM, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc(const TcParams &p, int bn, int grid, cudaStream_t s) {
+    if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
+    return bn == 256 ? launch_tc_bn<256>(p, grid, s) : launch_tc_bn<128>(p, grid, s);
+}
+
+}  // namespace cbd

@@ -1,0 +1,189 @@
+/*
+ * conv_bwd_data.h -- C ABI of the GB300 (sm_103a) convolution backward-data
+ * library: dx = dgrad(dy, w) as a stride-decomposed implicit GEMM.
+ *
+ * What the library computes.  The gradient of a forward 2-D
+ * cross-correlation with respect to its input: the grad_input result of
+ * `torch.aten.convolution_backward` with output_mask [true, false, false]
+ * (page "Non-unit stride input backward different input and dispatches
+ * between BOO and Fusilli", torch-IR input):
+ *
+ *   dx[n, c, hi, wi] = sum over k in group(c), y < Y, x < X, ho, wo with
+ *                      ho*sh - ph + y*dh == hi and wo*sw - pw + x*dw == wi
+ *                      of dy[n, k, ho, wo] * w[k, c mod (C/G), y, x]
+ *
+ * dx is fully overwritten; pixels that no filter tap reaches become +0
+ * (the same torch-IR overwrites the destination tensor's contents).
+ *
+ * How.  For stride > 1 the problem is split into one sub-GEMM per filter-tap
+ * residue class instead of zero-inserting dy into a dilated tensor: the
+ * "v4r1 backward_data" multi-kernel strategy (pages "Backward data", rocMLIR
+ * pull request 246, and "[igemm_dynamic] v4r1 bwd dynamic kernel", MIOpen
+ * pull request 272).  Per spatial dim with stride s, dilation d, pad p:
+ * g = gcd(s, d), YTilde = s / g, and class t in [0, YTilde) owns taps
+ * y = t + YTilde*j.  Non-empty classes get consecutive gemmIds 0..n-1 (the
+ * review of pull request 246 asks for consecutive gemmId).  The caller never
+ * passes kernel ids: the library rebuilds every per-class argument itself
+ * (same review), and one run() launches all classes.
+ *
+ * Memory ownership.  The caller owns dy, w, dx and the stream (any
+ * allocator; PyTorch in the bundled binding).  The library owns the plan
+ * (host memory) and one 16-byte device status word per plan, allocated by
+ * conv_bwd_data_create when a CUDA device is present.  conv_bwd_data_run
+ * allocates nothing, never synchronises and is ordered on the given stream.
+ *
+ * Layouts (all tensors dense, row-major in the order written):
+ *   CONV_BWD_NCHW_GKCYX: dy [N][K][Ho][Wo], w [K][C/G][Y][X] (= [G][K/G][C/G][Y][X]),
+ *                        dx [N][C][Hi][Wi]
+ *   CONV_BWD_NHWC_KYXC:  dy [N][Ho][Wo][K], w [K][Y][X][C/G], dx [N][Hi][Wi][C]
+ * Group gi owns input channels [gi*C/G, (gi+1)*C/G) and output channels
+ * [gi*K/G, (gi+1)*K/G).  Ho = (Hi + 2*ph - dh*(Y-1) - 1)/sh + 1, likewise Wo.
+ * Padding is symmetric per dimension.
+ *
+ * Numerics.  fp32 tensors: fp32 FFMA on CUDA cores (no TF32).  bf16 tensors:
+ * bf16 x bf16 products accumulated in fp32 (tensor cores for the NHWC path),
+ * one round-to-nearest-even conversion to bf16 at the end (the `arith.extf`,
+ * `arith.mulf`/`arith.addf` in f32 and `arith.truncf` ops of the BOO IR on
+ * the page above).  The summation order is unspecified.
+ *
+ * Errors.  Every call returns a conv_bwd_status; nothing throws across the
+ * ABI.  Device-side problems (a bounded wait that ran out, an index check
+ * that failed) are recorded in the plan's status word and reported by
+ * conv_bwd_data_get_status; kernels never trap.
+ */
+#ifndef CONV_BWD_DATA_H
+#define CONV_BWD_DATA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CONV_BWD_OK = 0,
+    CONV_BWD_ERR_INVALID_ARG = 1,   /* bad descriptor value, null or overlapping pointer */
+    CONV_BWD_ERR_UNSUPPORTED = 2,   /* valid problem outside what this library implements */
+    CONV_BWD_ERR_MISALIGNED = 3,    /* pointer or channel stride breaks a 16-byte rule of the path */
+    CONV_BWD_ERR_CUDA = 4,          /* a CUDA runtime call failed (or no device) */
+    CONV_BWD_ERR_DEVICE_TIMEOUT = 5,/* a bounded device-side wait ran out */
+    CONV_BWD_ERR_DEVICE_FAULT = 6   /* a device-side index/consistency check failed */
+} conv_bwd_status;
+
+typedef enum { CONV_BWD_F32 = 0, CONV_BWD_BF16 = 1 } conv_bwd_dtype;
+typedef enum { CONV_BWD_NCHW_GKCYX = 0, CONV_BWD_NHWC_KYXC = 1 } conv_bwd_layout;
+
+/* Problem descriptor; the fields mirror the driver flags of the tested
+ * command lines in "Backward data" (-batchsize -in_channels -out_channels
+ * -in_h -in_w -fil_h -fil_w --padding_* --conv_stride_* --dilation_*
+ * --groupsize and the layouts).  C and K are totals over all groups. */
+typedef struct {
+    int64_t N, C, K, Hi, Wi, Y, X;
+    int32_t pad_h, pad_w, stride_h, stride_w, dil_h, dil_w, groups;
+    int32_t layout; /* conv_bwd_layout */
+    int32_t dtype;  /* conv_bwd_dtype */
+} conv_bwd_desc;
+
+typedef struct conv_bwd_plan_s *conv_bwd_plan;
+
+/* Which kernel family runs the sub-GEMMs of a plan. */
+typedef enum {
+    CONV_BWD_PATH_TCGEN05 = 0, /* bf16 NHWC: persistent tcgen05/TMEM implicit GEMM */
+    CONV_BWD_PATH_SIMT = 1,    /* fp32 (or bf16 fallback): CUDA-core tiled implicit GEMM */
+    CONV_BWD_PATH_GROUPED = 2  /* bf16 NHWC with <= 32 channels per group: direct per-pixel kernel */
+} conv_bwd_path;
+
+/* Validate the descriptor and plan on the host: forward output size, tilde
+ * factors, non-empty sub-GEMM list (consecutive gemmIds), coverage of dx,
+ * kernel path and tile schedule.  If a CUDA device is visible, also
+ * allocates the plan's device status word on the current device (run() must
+ * then be called with that device current).  Without a device the plan is
+ * still created (so the planner can be queried) and run() returns
+ * CONV_BWD_ERR_CUDA.  *out is set to NULL on failure.
+ * Errors: INVALID_ARG (non-positive sizes, pad < 0, stride/dilation < 1,
+ * C or K not divisible by groups, empty forward output, unknown enum),
+ * UNSUPPORTED (stride > 64, more than 2^31-1 elements in a tensor, bf16 in a
+ * layout/shape no kernel covers), CUDA (device allocation failed). */
+conv_bwd_status conv_bwd_data_create(const conv_bwd_desc *desc, conv_bwd_plan *out);
+
+/* Free the plan and its device status word.  NULL is accepted. */
+conv_bwd_status conv_bwd_data_destroy(conv_bwd_plan plan);
+
+/* Forward output size (the spatial extent of dy). */
+conv_bwd_status conv_bwd_data_out_dims(const conv_bwd_plan plan, int64_t *Ho, int64_t *Wo);
+
+/* Number of non-empty sub-GEMMs; their gemmIds are 0..n-1. */
+conv_bwd_status conv_bwd_data_num_subgemms(const conv_bwd_plan plan, int32_t *n);
+
+/* Sub-GEMM `id`: its residue classes (ty, tx), its GEMM sizes per group
+ * (M = N * rows of the class, N = C/G, K = K/G * taps) and its tap counts.
+ * Any output pointer may be NULL.  INVALID_ARG for an id out of range. */
+conv_bwd_status conv_bwd_data_subgemm_info(const conv_bwd_plan plan, int32_t id, int32_t *ty, int32_t *tx,
+                                           int64_t *M, int64_t *N, int64_t *K, int32_t *taps_y,
+                                           int32_t *taps_x);
+
+/* Coverage of dx: row_mask[hi] (Hi bytes) and col_mask[wi] (Wi bytes) are
+ * set to 1 where some sub-GEMM writes that row/column, else 0.  A pixel is
+ * written by a sub-GEMM iff both its row and its column are covered; every
+ * other pixel is zeroed by the fill kernel.  Either pointer may be NULL. */
+conv_bwd_status conv_bwd_data_coverage(const conv_bwd_plan plan, uint8_t *row_mask, uint8_t *col_mask);
+
+/* Kernel path chosen by the planner (conv_bwd_path) and the number of
+ * kernel launches one run() makes (fill + sub-GEMM kernel). */
+conv_bwd_status conv_bwd_data_path(const conv_bwd_plan plan, int32_t *path, int32_t *launches_per_run);
+
+/* Useful work: 2 * N * K * (C/G) * Th * Tw floating-point operations, where
+ * Th = #{(ho, y): 0 <= ho*sh - ph + y*dh < Hi} counts only taps that land
+ * inside dx (likewise Tw).  Also the algorithmic bytes: dy, w and dx each
+ * moved once. */
+conv_bwd_status conv_bwd_data_work(const conv_bwd_plan plan, double *useful_flop, double *algo_bytes);
+
+/* Compute dx from dy and w on `stream` (a cudaStream_t; NULL = legacy
+ * default stream).  dy, w, dx are device pointers in the plan's layout and
+ * dtype; they must not overlap.  Asynchronous: returns after enqueueing the
+ * fill kernel (only if some pixel is uncovered) and one sub-GEMM kernel.
+ * Errors: INVALID_ARG (null or overlapping pointers), MISALIGNED (bf16 NHWC
+ * tensor-core path needs 16-byte aligned dy, w, dx), CUDA (launch failure or
+ * plan created without a device). */
+conv_bwd_status conv_bwd_data_run(conv_bwd_plan plan, const void *dy, const void *w, void *dx, void *stream);
+
+/* End-to-end variant with host buffers: copies dy_host/w_host into the
+ * caller's device buffers dy_dev/w_dev, runs, and copies dx_dev back into
+ * dx_host, all ordered on `stream` (use pinned host memory for async
+ * copies).  Returns after enqueueing; synchronise the stream before reading
+ * dx_host.  Same errors as conv_bwd_data_run. */
+conv_bwd_status conv_bwd_data_run_host(conv_bwd_plan plan, const void *dy_host, const void *w_host, void *dx_host,
+                                       void *dy_dev, void *w_dev, void *dx_dev, void *stream);
+
+/* Synchronise `stream`, read and clear the plan's device status word.
+ * Returns OK, DEVICE_TIMEOUT or DEVICE_FAULT (with *detail, if not NULL, set
+ * to the device-side location code), or CUDA if the stream reported an
+ * error. */
+conv_bwd_status conv_bwd_data_get_status(conv_bwd_plan plan, void *stream, int32_t *detail);
+
+/* Per-kernel timing.  When enabled, run() records CUDA events around each
+ * kernel it launches on the stream; conv_bwd_data_last_timing synchronises
+ * on those events and returns the device time of the last run's fill kernel
+ * (0 if it was skipped) and sub-GEMM kernel in milliseconds. */
+conv_bwd_status conv_bwd_data_set_timing(conv_bwd_plan plan, int32_t enable);
+conv_bwd_status conv_bwd_data_last_timing(conv_bwd_plan plan, float *fill_ms, float *gemm_ms);
+
+/* Device self-test of the bounded-wait mechanism every pipelined kernel
+ * uses: a one-thread kernel waits on a shared-memory barrier that nothing
+ * ever arrives on, with a budget of `budget_cycles` SM clocks, and must give
+ * up and record a timeout.  *observed receives the recorded status code
+ * (CONV_BWD_ERR_DEVICE_TIMEOUT when the mechanism works).  Faults nothing,
+ * hangs nothing; synchronises the stream. */
+conv_bwd_status conv_bwd_data_selftest_wait_timeout(void *stream, int64_t budget_cycles, int32_t *observed);
+
+/* Human-readable status name (static storage). */
+const char *conv_bwd_status_string(conv_bwd_status s);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t conv_bwd_data_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV_BWD_DATA_H */

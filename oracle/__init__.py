@@ -74,7 +74,7 @@ def _load():
         i64 = ctypes.c_int64
         lib.oracle_out_dims.argtypes = [g]
         lib.oracle_out_dims.restype = ctypes.c_int
-        lib.oracle_dgrad_scatter.argtypes = [g, ctypes.c_int, d, d, d, d, i64, i64]
+        lib.oracle_dgrad_scatter.argtypes = [g, ctypes.c_int, d, d, d, d, i64, i64, i64, i64]
         lib.oracle_dgrad_scatter.restype = None
         lib.oracle_dgrad_point.argtypes = [g, ctypes.c_int, d, d, i64, i64, i64, i64, d, d]
         lib.oracle_dgrad_point.restype = None
@@ -120,11 +120,13 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
-def dgrad(g: Geom, layout: int, dy, w, n_range=None, with_absdot=True):
+def dgrad(g: Geom, layout: int, dy, w, n_range=None, c_range=None, with_absdot=True):
     """Scatter-loop dgrad.  Returns (dx, absdot) as float64 arrays in dx's shape.
 
-    ``n_range=(a, b)`` restricts the work to images a..b-1; the other images of
-    the returned arrays are left at zero.
+    ``n_range=(a, b)`` restricts the work to images a..b-1 and
+    ``c_range=(u, v)`` to channels u..v-1 within every group; entries outside
+    the selection are left at zero.  Used for bounded samples of large
+    problems.
     """
     dy_s, w_s, dx_s = shapes(g, layout)
     dy64 = widen(dy).reshape(dy_s)
@@ -132,8 +134,11 @@ def dgrad(g: Geom, layout: int, dy, w, n_range=None, with_absdot=True):
     dx = np.zeros(dx_s, dtype=np.float64)
     ab = np.zeros(dx_s, dtype=np.float64) if with_absdot else None
     a, b = (0, g.N) if n_range is None else n_range
+    u, v = (0, g.C // g.groups) if c_range is None else c_range
+    if not (0 <= a <= b <= g.N and 0 <= u <= v <= g.C // g.groups):
+        raise ValueError("sample range outside the problem")
     _load().oracle_dgrad_scatter(ctypes.byref(g), layout, _ptr(dy64), _ptr(w64), _ptr(dx),
-                                 _ptr(ab) if ab is not None else None, a, b)
+                                 _ptr(ab) if ab is not None else None, a, b, u, v)
     return dx, ab
 
 

@@ -23,7 +23,8 @@
  *   oracle_out_dims       forward output size Ho, Wo
  *   oracle_dgrad_scatter  the definition above as a scatter loop, plus the
  *                         per-element magnitude sum  sum |dy*w|  used for
- *                         tolerances; optional batch range for sampling
+ *                         tolerances; optional image / channel ranges for
+ *                         bounded samples
  *   oracle_dgrad_point    the same definition gathered at one dx element
  *   oracle_dgrad_zero_insert  second formulation: zero-insert dy with the
  *                         stride, pad, then correlate with the flipped filter
@@ -79,21 +80,25 @@ int oracle_out_dims(oracle_geom *g) {
     return 0;
 }
 
-/* The definition as a scatter loop.  Only images n in [n_begin, n_end) are
- * computed (their dx / absdot slices are zeroed first); the rest of dx is not
- * touched.  absdot may be NULL.  Work items are (image, group, channel block):
+/* The definition as a scatter loop.  Only images n in [n_begin, n_end) and
+ * channels c with c mod Cg in [cg_begin, cg_end) are computed (those dx /
+ * absdot entries are zeroed first); the rest of dx is not touched, which is
+ * how bounded samples of a large problem are taken.  absdot may be NULL.  Work items are (image, group, channel block):
  * each owns a disjoint slice of dx, so the OpenMP split needs no atomics. */
 void oracle_dgrad_scatter(const oracle_geom *g, int layout, const double *dy, const double *w,
-                          double *dx, double *absdot, int64_t n_begin, int64_t n_end) {
-    const int64_t G = g->groups, Cg = g->C / G, Kg = g->K / G;
-    const int64_t CB = 64; /* channel block per work item */
-    const int64_t ncb = (Cg + CB - 1) / CB;
+                          double *dx, double *absdot, int64_t n_begin, int64_t n_end,
+                          int64_t cg_begin, int64_t cg_end) {
+    const int64_t G = g->groups, Kg = g->K / G;
+    const int64_t CB = 16; /* channel block per work item (the OpenMP grain) */
+    const int64_t cspan = cg_end - cg_begin;
+    const int64_t ncb = (cspan + CB - 1) / CB;
     const int64_t items = (n_end - n_begin) * G * ncb;
     #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t it = 0; it < items; ++it) {
         int64_t n = n_begin + it / (G * ncb);
         int64_t gi = (it / ncb) % G;
-        int64_t c0 = (it % ncb) * CB, c1 = c0 + CB < Cg ? c0 + CB : Cg;
+        int64_t c0 = cg_begin + (it % ncb) * CB, c1 = c0 + CB < cg_end ? c0 + CB : cg_end;
+        const int64_t Cg = g->C / G;
         /* zero this item's slice */
         for (int64_t hi = 0; hi < g->Hi; ++hi)
             for (int64_t wi = 0; wi < g->Wi; ++wi)

@@ -1,0 +1,177 @@
+"""Host-side tests of the C ABI (no GPU): the library loads and exports every
+declared symbol, and the planner's decomposition (residue classes, gemmIds,
+coverage, useful work) agrees with brute-force enumeration of the forward
+windows.  The brute force here is written from the forward index relation
+hi = ho*sh - ph + y*dh, independently of the planner's closed forms."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conv2d_backward_implicit_bwd_gb300 import build as cbuild
+from conv2d_backward_implicit_bwd_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    cbuild.build()
+    from conv2d_backward_implicit_bwd_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(conv_bwd_[a-z0-9_]+)\s*\(", txt,
+                                re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(B):
+    names = declared_functions()
+    assert len(names) >= 15
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(B.EXPORTED) <= set(names)
+
+
+def brute(c):
+    """Per dim: which dx indices some tap reaches, and the useful tap count."""
+    def dim(In, Out, F, s, d, p):
+        hit = np.zeros(In, dtype=bool)
+        useful = 0
+        for o in range(Out):
+            for f in range(F):
+                i = o * s - p + f * d
+                if 0 <= i < In:
+                    hit[i] = True
+                    useful += 1
+        return hit, useful
+    Ho = (c.Hi + 2 * c.pad[0] - c.dil[0] * (c.Y - 1) - 1) // c.stride[0] + 1
+    Wo = (c.Wi + 2 * c.pad[1] - c.dil[1] * (c.X - 1) - 1) // c.stride[1] + 1
+    rh, uh = dim(c.Hi, Ho, c.Y, c.stride[0], c.dil[0], c.pad[0])
+    rw, uw = dim(c.Wi, Wo, c.X, c.stride[1], c.dil[1], c.pad[1])
+    return Ho, Wo, rh, rw, uh, uw
+
+
+def _ok(c):
+    return (c.Hi + 2 * c.pad[0] - c.dil[0] * (c.Y - 1) - 1 >= 0 and
+            c.Wi + 2 * c.pad[1] - c.dil[1] * (c.X - 1) - 1 >= 0)
+
+
+PLAN_CASES = wl.CASES + wl.random_tiny_cases(150, seed=21, accept=_ok)
+
+
+@pytest.mark.parametrize("c", PLAN_CASES, ids=lambda c: c.name)
+def test_planner_against_brute_force(B, c):
+    p = B.Plan.from_case(c)
+    Ho, Wo, rh, rw, uh, uw = brute(c)
+    assert (p.Ho, p.Wo) == (Ho, Wo)
+    rows, cols = p.coverage()
+    # a sub-GEMM writes exactly the rows/columns some tap reaches (classes are
+    # not trimmed, so a written row may still receive only zeros: it is then
+    # reached by a tap whose dy row is out of range -- never the case for a
+    # row that no tap reaches at all)
+    np.testing.assert_array_equal(rows, rh | _class_rows(c, 0))
+    np.testing.assert_array_equal(cols, rw | _class_rows(c, 1))
+    n = p.num_subgemms()
+    infos = [p.subgemm(i) for i in range(n)]
+    # consecutive gemmIds, distinct classes
+    assert len({(s["ty"], s["tx"]) for s in infos}) == n
+    # every written pixel is written by exactly one class: sum of M = N*rows*cols
+    assert sum(s["M"] for s in infos) == c.N * int(rows.sum()) * int(cols.sum())
+    g = math.gcd(c.stride[0], c.dil[0])
+    YT = c.stride[0] // g
+    g2 = math.gcd(c.stride[1], c.dil[1])
+    XT = c.stride[1] // g2
+    assert n <= YT * XT
+    # the class's taps are y = ty + YT*j: all of them, and together every tap once
+    assert sum(s["taps_y"] * s["taps_x"] for s in infos) <= c.Y * c.X
+    for s in infos:
+        assert s["taps_y"] == len(range(s["ty"], c.Y, YT))
+        assert s["taps_x"] == len(range(s["tx"], c.X, XT))
+        assert s["N"] == c.C // c.groups
+        assert s["K"] == (c.K // c.groups) * s["taps_y"] * s["taps_x"]
+    flop, nbytes = p.work()
+    assert flop == 2.0 * c.N * c.K * (c.C // c.groups) * uh * uw
+    es = 2 if c.dtype == wl.BF16 else 4
+    assert nbytes == es * (c.N * c.K * Ho * Wo + c.K * (c.C // c.groups) * c.Y * c.X + c.N * c.C * c.Hi * c.Wi)
+
+
+def _class_rows(c, dim):
+    """Rows (dim 0) / columns (dim 1) of every residue class that has >= 1 tap,
+    enumerated from hi = ht*s + t*d - p directly."""
+    In, F, s, d, p = ((c.Hi, c.Y, c.stride[0], c.dil[0], c.pad[0]) if dim == 0 else
+                      (c.Wi, c.X, c.stride[1], c.dil[1], c.pad[1]))
+    T = s // math.gcd(s, d)
+    out = np.zeros(In, dtype=bool)
+    for t in range(min(T, F)):
+        for ht in range(-In - p - t * d, In + p + 1):
+            i = ht * s + t * d - p
+            if 0 <= i < In:
+                out[i] = True
+    return out
+
+
+def test_survey_table_cfg1(B):
+    p = B.Plan.from_case(wl.case("cfg1"))
+    got = [(s["ty"], s["tx"], s["taps_y"] * s["taps_x"], s["M"]) for s in map(p.subgemm, range(p.num_subgemms()))]
+    assert got == [(0, 0, 4, 98), (0, 1, 2, 112), (1, 0, 2, 112), (1, 1, 1, 128)]
+
+
+def test_cfg5_class_structure(B):
+    a = B.Plan.from_case(wl.case("cfg5a"))   # stride 2, dilation 2: one class, 9 taps, 1/4 of dx written
+    assert a.num_subgemms() == 1 and a.subgemm(0)["taps_y"] * a.subgemm(0)["taps_x"] == 9
+    rows, cols = a.coverage()
+    assert rows.sum() == 14 and cols.sum() == 14
+    b = B.Plan.from_case(wl.case("cfg5b"))   # 1x1 stride 2: one class of four non-empty
+    assert b.num_subgemms() == 1 and b.subgemm(0)["M"] == 32 * 7 * 7
+    c = B.Plan.from_case(wl.case("cfg5c"))   # 5x5 stride 3: nine classes
+    taps = sorted(s["taps_y"] * s["taps_x"] for s in map(c.subgemm, range(c.num_subgemms())))
+    assert taps == sorted([4, 4, 2, 4, 4, 2, 2, 2, 1])
+
+
+def test_paths(B):
+    assert B.Plan.from_case(wl.case("cfg3")).path()[0] == "tcgen05"
+    assert B.Plan.from_case(wl.case("cfg5a")).path()[0] == "tcgen05"
+    assert B.Plan.from_case(wl.case("cfg1")).path()[0] == "simt"
+    # launches per run: fill only where some pixel is uncovered
+    assert B.Plan.from_case(wl.case("cfg3")).path()[1] == 1
+    assert B.Plan.from_case(wl.case("cfg5a")).path()[1] == 2
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(N=0), 1), (dict(C=3, groups=2), 1), (dict(Y=40), 1), (dict(stride=(0, 1)), 1),
+    (dict(pad=(-1, 0)), 1), (dict(dil=(1, 0)), 1), (dict(stride=(65, 1)), 2), (dict(layout=7), 1),
+    (dict(dtype=9), 1),
+])
+def test_invalid_descriptors(B, kw, status):
+    args = dict(N=1, C=4, K=4, Hi=8, Wi=8, Y=3, X=3, pad=(1, 1), stride=(1, 1), dil=(1, 1), groups=1,
+                layout="nchw", dtype="f32")
+    args.update(kw)
+    with pytest.raises(B.ConvBwdError) as e:
+        B.Plan(**args)
+    assert e.value.status == status
+
+
+def test_run_argument_errors_without_device(B):
+    p = B.Plan(1, 4, 4, 8, 8, 3, 3, (1, 1))
+    assert p.run_ptr(0, 0, 0) == B.ERR_INVALID_ARG
+    import torch
+    if not torch.cuda.is_available():
+        # a plan made without a device cannot run
+        assert p.run_ptr(4096, 8192, 1 << 20) == B.ERR_CUDA
+
+
+def test_status_strings(B):
+    for s in range(7):
+        assert B.status_string(s).startswith("CONV_BWD_")
+    assert B.lib().conv_bwd_data_version() >= 100

@@ -1,0 +1,251 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Tolerances per element (ref = oracle value, S = sum over taps of |dy*w|):
+  fp32 output: |err| <= 1e-5 * S
+  bf16 output: |err| <= 2^-8 * |ref| + 1e-4 * S
+Inputs come from the seeded generators shared with the oracle (byte-identical
+bf16/fp32 values).  dx is pre-filled with NaN so that a pixel the library
+forgets to write shows up as a failure.  Large problems are compared on a
+batch slice computed in full by the oracle plus random sample points from
+every image; everything else is compared element by element.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conv2d_backward_implicit_bwd_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from conv2d_backward_implicit_bwd_gb300 import build as cbuild
+    cbuild.build()
+    from conv2d_backward_implicit_bwd_gb300 import binding
+    return binding
+
+
+def _geom(c):
+    return oracle.geom(c.N, c.C, c.K, c.Hi, c.Wi, c.Y, c.X, c.pad, c.stride, c.dil, c.groups)
+
+
+def _lay(c):
+    return oracle.LAYOUT_NCHW if c.layout == wl.NCHW else oracle.LAYOUT_NHWC
+
+
+def to_dev(a, dtype):
+    if dtype == wl.BF16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def gpu_dgrad(B, c, dy, w, stream=None, prefill=float("nan")):
+    plan = B.Plan.from_case(c)
+    _, _, dx_s = plan.shapes()
+    tdt = torch.bfloat16 if c.dtype == wl.BF16 else torch.float32
+    dyd, wd = to_dev(dy, c.dtype), to_dev(w, c.dtype)
+    dx = torch.full(dx_s, prefill, dtype=tdt, device="cuda")
+    plan.run(dyd, wd, dx, stream)
+    st, det = plan.status(stream)
+    assert st == B.OK, (B.status_string(st), hex(det))
+    return dx.float().cpu().numpy().astype(np.float64), plan
+
+
+def inputs(c):
+    g = _geom(c)
+    dy_s, w_s, _ = oracle.shapes(g, _lay(c))
+    dy, w = wl.draw(c, dy_s, w_s)
+    return g, dy, w
+
+
+def check_full(c, got, g, dy, w, n_range=None):
+    ref, ab = oracle.dgrad(g, _lay(c), dy, w, n_range=n_range)
+    if n_range is not None:
+        sl = slice(*n_range)
+        got, ref, ab = got[sl], ref[sl], ab[sl]
+    assert np.all(np.isfinite(got)), "unwritten (NaN) outputs"
+    bound = oracle.tolerance(ref, ab, c.dtype)
+    err = np.abs(got - ref)
+    worst = float(np.max(err - bound))
+    assert worst <= 0.0, f"max excess {worst:.3e}; max err {err.max():.3e}"
+    return float(np.max(err / np.maximum(bound, 1e-300)))
+
+
+def check_points(c, got, g, dy, w, count=1500, seed=0):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    pts = [(int(rng.integers(c.N)), int(rng.integers(c.C)), int(rng.integers(c.Hi)), int(rng.integers(c.Wi)))
+           for _ in range(count)]
+    vals, abss = oracle.dgrad_points(g, _lay(c), dy, w, pts)
+    idx = [(n, ch, h, x) if c.layout == wl.NCHW else (n, h, x, ch) for (n, ch, h, x) in pts]
+    gv = np.array([got[i] for i in idx])
+    bound = oracle.tolerance(vals, abss, c.dtype)
+    assert np.all(np.abs(gv - vals) <= bound)
+
+
+SMALL = [c for c in wl.CASES if c.tags[0] in ("cfg1", "cfg2")]
+
+
+@pytest.mark.parametrize("c", SMALL, ids=lambda c: c.name)
+def test_small_configs_full(B, c):
+    g, dy, w = inputs(c)
+    got, plan = gpu_dgrad(B, c, dy, w)
+    assert plan.path()[0] == "simt"
+    check_full(c, got, g, dy, w)
+
+
+LARGE = {"cfg3": (0, 1), "cfg4": None, "cfg5a": (0, 2), "cfg5b": (0, 4), "cfg5c": (0, 3)}
+
+
+@pytest.mark.parametrize("name", list(LARGE))
+def test_large_configs(B, name):
+    c = wl.case(name)
+    g, dy, w = inputs(c)
+    got, plan = gpu_dgrad(B, c, dy, w)
+    assert np.all(np.isfinite(got)), "unwritten (NaN) outputs"
+    check_full(c, got, g, dy, w, n_range=LARGE[name])
+    check_points(c, got, g, dy, w, seed=zlib.crc32(name.encode()) % 1000)
+    if name != "cfg4":
+        assert plan.path()[0] == "tcgen05"
+
+
+def _mk(name, **kw):
+    base = dict(dtype=wl.BF16, layout=wl.NHWC, dist="normal", sigma=0.5, seed=zlib.crc32(name.encode()) % 100000)
+    base.update(kw)
+    return wl.Case(name=name, **base)
+
+
+# Tensor-core path: several tiles, ragged M / N / K tails, groups, classes whose
+# taps all fall outside dy, uncovered rows/columns, asymmetric geometry.
+TC_CASES = [
+    _mk("tc_ragged_3x3s2", N=3, C=192, K=136, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2)),
+    _mk("tc_1x1s2", N=2, C=256, K=64, Hi=9, Wi=17, Y=1, X=1, stride=(2, 2)),
+    _mk("tc_groups2", N=2, C=128, K=128, Hi=10, Wi=10, Y=3, X=3, pad=(1, 1), groups=2),
+    _mk("tc_groups4_kg72", N=2, C=256, K=288, Hi=7, Wi=8, Y=3, X=2, pad=(1, 0), stride=(2, 1), groups=4),
+    _mk("tc_asym", N=4, C=320, K=96, Hi=7, Wi=9, Y=5, X=3, pad=(2, 1), stride=(3, 2), dil=(1, 2)),
+    _mk("tc_filter_gt_input", N=2, C=64, K=64, Hi=3, Wi=3, Y=5, X=5, pad=(2, 2)),
+    _mk("tc_stride4_uncovered", N=2, C=128, K=64, Hi=15, Wi=14, Y=3, X=3, pad=(1, 1), stride=(4, 4)),
+    _mk("tc_m1", N=1, C=512, K=512, Hi=1, Wi=1, Y=1, X=1),
+    _mk("tc_page3_small", N=2, C=256, K=256, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)),
+    _mk("tc_dil2_s2", N=2, C=128, K=128, Hi=12, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)),
+    _mk("tc_mixed", N=2, C=200, K=40, Hi=11, Wi=6, Y=2, X=4, pad=(0, 3), stride=(3, 1), dil=(2, 3)),
+    _mk("tc_bn256_ragged", N=3, C=264, K=64, Hi=6, Wi=7, Y=3, X=3, pad=(1, 1), stride=(1, 1)),
+    _mk("tc_deep_k", N=1, C=64, K=1024, Hi=5, Wi=6, Y=2, X=2, pad=(1, 1), stride=(2, 2)),
+]
+
+
+@pytest.mark.parametrize("c", TC_CASES, ids=lambda c: c.name)
+def test_tensor_core_path_full(B, c):
+    g, dy, w = inputs(c)
+    got, plan = gpu_dgrad(B, c, dy, w)
+    assert plan.path()[0] == "tcgen05", plan.path()
+    check_full(c, got, g, dy, w)
+
+
+# CUDA-core path: fp32 in both layouts, bf16 fallbacks (small channel
+# counts, NCHW bf16), and random tiny geometries.
+def _ok(c):
+    return (c.Hi + 2 * c.pad[0] - c.dil[0] * (c.Y - 1) - 1 >= 0 and
+            c.Wi + 2 * c.pad[1] - c.dil[1] * (c.X - 1) - 1 >= 0)
+
+
+SIMT_CASES = (wl.random_tiny_cases(40, seed=31, accept=_ok) +
+              wl.random_tiny_cases(20, seed=32, layout=wl.NHWC, accept=_ok) +
+              wl.random_tiny_cases(20, seed=33, dtype=wl.BF16, layout=wl.NHWC, accept=_ok) +
+              wl.random_tiny_cases(10, seed=34, dtype=wl.BF16, layout=wl.NCHW, accept=_ok) + [
+                  _mk("simt_bf16_cg24", N=2, C=48, K=32, Hi=9, Wi=9, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=2),
+                  _mk("simt_f32_nhwc", N=2, C=96, K=80, Hi=8, Wi=7, Y=3, X=3, pad=(1, 1), stride=(2, 2),
+                      dtype=wl.F32, dist="uniform"),
+                  _mk("simt_f32_wide", N=1, C=130, K=70, Hi=6, Wi=5, Y=2, X=3, pad=(1, 1), stride=(1, 2),
+                      dtype=wl.F32, layout=wl.NCHW, dist="uniform"),
+              ])
+
+
+@pytest.mark.parametrize("c", SIMT_CASES, ids=lambda c: c.name + "_" + c.dtype + "_" + c.layout)
+def test_cuda_core_path_full(B, c):
+    g, dy, w = inputs(c)
+    got, plan = gpu_dgrad(B, c, dy, w)
+    check_full(c, got, g, dy, w)
+
+
+def test_forced_simt_matches_tensor_core_path(B, monkeypatch):
+    """The tensor-core kernel and the CUDA-core kernel agree on a bf16 case
+    (both compared with the oracle too)."""
+    c = TC_CASES[0]
+    g, dy, w = inputs(c)
+    tc, _ = gpu_dgrad(B, c, dy, w)
+    monkeypatch.setenv("CONVBWD_DEBUG_PATH", "simt")
+    simt, plan = gpu_dgrad(B, c, dy, w)
+    assert plan.path()[0] == "simt"
+    check_full(c, simt, g, dy, w)
+    check_full(c, tc, g, dy, w)
+
+
+def test_deterministic_and_stream_ordered(B):
+    c = TC_CASES[4]
+    g, dy, w = inputs(c)
+    s = torch.cuda.Stream()
+    a, _ = gpu_dgrad(B, c, dy, w, stream=s)
+    b, _ = gpu_dgrad(B, c, dy, w)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_run_host_end_to_end(B):
+    c = TC_CASES[0]
+    g, dy, w = inputs(c)
+    plan = B.Plan.from_case(c)
+    dy_s, w_s, dx_s = plan.shapes()
+    dy_h = torch.from_numpy(dy.view(np.int16)).view(torch.bfloat16).pin_memory()
+    w_h = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).pin_memory()
+    dx_h = torch.empty(dx_s, dtype=torch.bfloat16).pin_memory()
+    dy_d = torch.empty(dy_s, dtype=torch.bfloat16, device="cuda")
+    w_d = torch.empty(w_s, dtype=torch.bfloat16, device="cuda")
+    dx_d = torch.empty(dx_s, dtype=torch.bfloat16, device="cuda")
+    plan.run_host(dy_h, w_h, dx_h, dy_d, w_d, dx_d)
+    torch.cuda.synchronize()
+    check_full(c, dx_h.float().numpy().astype(np.float64), g, dy, w)
+
+
+def test_overlap_and_alignment_errors(B):
+    c = TC_CASES[1]
+    plan = B.Plan.from_case(c)
+    dy_s, w_s, dx_s = plan.shapes()
+    buf = torch.zeros(int(np.prod(dx_s)) + int(np.prod(dy_s)) + 64, dtype=torch.bfloat16, device="cuda")
+    base = buf.data_ptr()
+    # dx overlapping dy
+    assert plan.run_ptr(base, base + 4096, base + 2) == B.ERR_INVALID_ARG
+    w = torch.zeros(w_s, dtype=torch.bfloat16, device="cuda")
+    dxo = torch.zeros(int(np.prod(dx_s)) + 8, dtype=torch.bfloat16, device="cuda")
+    # bf16 tensor-core path needs 16-byte aligned tensors
+    dyt = torch.zeros(dy_s, dtype=torch.bfloat16, device="cuda")
+    assert plan.run_ptr(dyt.data_ptr(), w.data_ptr(), dxo.data_ptr() + 2) == B.ERR_MISALIGNED
+    torch.cuda.synchronize()
+
+
+def test_bounded_wait_gives_up_and_context_survives(B):
+    """A kernel waiting on a barrier that nothing arrives on gives up after its
+    budget (~1 ms of SM clocks), records a timeout, and the device keeps
+    working afterwards."""
+    assert B.selftest_wait_timeout(2_000_000) == B.ERR_DEVICE_TIMEOUT
+    c = TC_CASES[5]
+    g, dy, w = inputs(c)
+    got, _ = gpu_dgrad(B, c, dy, w)
+    check_full(c, got, g, dy, w)
+
+
+def test_per_kernel_timing(B):
+    c = wl.case("cfg5a")
+    plan = B.Plan.from_case(c)
+    dy_s, w_s, dx_s = plan.shapes()
+    dy = torch.zeros(dy_s, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(w_s, dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty(dx_s, dtype=torch.bfloat16, device="cuda")
+    plan.set_timing(True)
+    plan.run(dy, w, dx)
+    f, m = plan.last_timing()
+    assert f > 0 and m > 0

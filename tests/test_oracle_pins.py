@@ -210,6 +210,16 @@ def test_batch_range_sampling_is_a_slice():
     np.testing.assert_array_equal(part[1], full[1])
     np.testing.assert_array_equal(pab[1], fab[1])
     assert np.all(part[0] == 0)
+    part2, _ = oracle.dgrad(g, oracle.LAYOUT_NCHW, dy, w, n_range=(0, 2), c_range=(3, 11))
+    np.testing.assert_array_equal(part2[:, 3:11], full[:, 3:11])
+    assert np.all(part2[:, :3] == 0) and np.all(part2[:, 11:] == 0)
+    c2 = wl.random_tiny_cases(1, seed=5, accept=_valid)[0]
+    c2 = wl.Case(**{**c2.__dict__, "C": 3 * 4, "groups": 3, "name": "grp"})
+    g2, dy2, w2 = _inputs(c2)
+    f2, _ = oracle.dgrad(g2, oracle.LAYOUT_NCHW, dy2, w2)
+    p2, _ = oracle.dgrad(g2, oracle.LAYOUT_NCHW, dy2, w2, c_range=(1, 3))
+    for gi in range(3):
+        np.testing.assert_array_equal(p2[:, gi * 4 + 1:gi * 4 + 3], f2[:, gi * 4 + 1:gi * 4 + 3])
 
 
 def test_bf16_rounding_is_nearest_even():
