@@ -24,7 +24,7 @@ EXPORTED = [
     "conv_bwd_data_subgemm_info", "conv_bwd_data_coverage", "conv_bwd_data_path", "conv_bwd_data_work",
     "conv_bwd_data_run", "conv_bwd_data_run_host", "conv_bwd_data_get_status", "conv_bwd_data_set_timing",
     "conv_bwd_data_last_timing", "conv_bwd_data_selftest_wait_timeout", "conv_bwd_status_string",
-    "conv_bwd_data_version",
+    "conv_bwd_data_version", "conv_bwd_data_run_noalloc",
 ]
 
 
@@ -63,6 +63,7 @@ def _load():
         "conv_bwd_data_set_timing": [vp, i32],
         "conv_bwd_data_last_timing": [vp, P(ctypes.c_float), P(ctypes.c_float)],
         "conv_bwd_data_selftest_wait_timeout": [vp, i64, P(i32)],
+        "conv_bwd_data_run_noalloc": [P(Desc), vp, vp, vp, vp, P(i32)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -199,6 +200,17 @@ class Plan:
         f, g = ctypes.c_float(), ctypes.c_float()
         _check(_lib.conv_bwd_data_last_timing(self._h, ctypes.byref(f), ctypes.byref(g)), "last_timing")
         return f.value, g.value
+
+
+def run_noalloc(desc: Desc, dy, w, dx, stream=None, sync: bool = False):
+    """conv_bwd_data_run_noalloc: tensor-core dgrad without any device
+    allocation (status word in the library's static device scratch).
+    Returns (status, device_status)."""
+    det = ctypes.c_int32(0)
+    st = _lib.conv_bwd_data_run_noalloc(ctypes.byref(desc), ctypes.c_void_p(dy.data_ptr()),
+                                        ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(dx.data_ptr()),
+                                        _stream_handle(stream), ctypes.byref(det) if sync else None)
+    return st, det.value
 
 
 def selftest_wait_timeout(budget_cycles: int, stream=None) -> int:

@@ -42,6 +42,7 @@ struct conv_bwd_plan_s {
     int device = -1;
     int num_sms = 0;
     int32_t *d_status = nullptr;
+    bool owns_status = true;              // false: the status word is borrowed (no-allocation entry point)
     int64_t wait_budget = 0;
     bool timing = false;
     bool fill_ran = false;
@@ -180,7 +181,7 @@ const char *conv_bwd_status_string(conv_bwd_status s) {
     return "CONV_BWD_UNKNOWN_STATUS";
 }
 
-conv_bwd_status conv_bwd_data_create(const conv_bwd_desc *desc, conv_bwd_plan *out) {
+static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out, bool alloc_status) {
     if (!out) return CONV_BWD_ERR_INVALID_ARG;
     *out = nullptr;
     conv_bwd_status st = validate(desc);
@@ -282,17 +283,25 @@ conv_bwd_status conv_bwd_data_create(const conv_bwd_desc *desc, conv_bwd_plan *o
         double secs = 2.0;
         if (const char *b = env("CONVBWD_DEBUG_WAIT_SECONDS")) secs = std::atof(b);
         p->wait_budget = (int64_t)(secs * clk_khz * 1000.0);
-        if (cudaMalloc(&p->d_status, 16) != cudaSuccess || cudaMemset(p->d_status, 0, 16) != cudaSuccess) {
-            cudaGetLastError();
-            delete p;
-            return CONV_BWD_ERR_CUDA;
+        if (alloc_status) {
+            if (cudaMalloc(&p->d_status, 16) != cudaSuccess || cudaMemset(p->d_status, 0, 16) != cudaSuccess) {
+                cudaGetLastError();
+                delete p;
+                return CONV_BWD_ERR_CUDA;
+            }
+            p->has_device = true;
+        } else {
+            p->owns_status = false;  // run() becomes possible once a status word is attached
         }
-        p->has_device = true;
     } else {
         cudaGetLastError();  // clear "no device"
     }
     *out = p;
     return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_create(const conv_bwd_desc *desc, conv_bwd_plan *out) {
+    return create_impl(desc, out, true);
 }
 
 conv_bwd_status conv_bwd_data_destroy(conv_bwd_plan p) {
@@ -301,7 +310,7 @@ conv_bwd_status conv_bwd_data_destroy(conv_bwd_plan p) {
         int cur = -1;
         cudaGetDevice(&cur);
         if (cur != p->device) cudaSetDevice(p->device);
-        cudaFree(p->d_status);
+        if (p->owns_status) cudaFree(p->d_status);
         for (auto &e : p->ev)
             if (e) cudaEventDestroy(e);
         if (cur != p->device && cur >= 0) cudaSetDevice(cur);
@@ -507,3 +516,28 @@ conv_bwd_status conv_bwd_data_selftest_wait_timeout(void *stream, int64_t budget
 }
 
 }  // extern "C"
+
+namespace cbd {
+
+// Host-only plan (no device allocation) whose kernels will record their
+// status in `status`, device memory the caller keeps alive.  Used by the
+// no-allocation entry point; the plan is freed with conv_bwd_data_destroy,
+// which then leaves `status` alone.
+conv_bwd_status plan_create_borrowed_status(const conv_bwd_desc *desc, int32_t *status, conv_bwd_plan *out) {
+    conv_bwd_status st = create_impl(desc, out, false);
+    if (st != CONV_BWD_OK) return st;
+    conv_bwd_plan p = *out;
+    if (p->device < 0) {
+        conv_bwd_data_destroy(p);
+        *out = nullptr;
+        return CONV_BWD_ERR_CUDA;
+    }
+    p->d_status = status;
+    p->owns_status = false;
+    p->has_device = true;
+    return CONV_BWD_OK;
+}
+
+int32_t plan_path_of(conv_bwd_plan p) { return p ? p->path : -1; }
+
+}  // namespace cbd

@@ -176,6 +176,29 @@ conv_bwd_status conv_bwd_data_last_timing(conv_bwd_plan plan, float *fill_ms, fl
  * hangs nothing; synchronises the stream. */
 conv_bwd_status conv_bwd_data_selftest_wait_timeout(void *stream, int64_t budget_cycles, int32_t *observed);
 
+/* No-allocation variant of conv_bwd_data_run for the bf16 NHWC/KYXC
+ * tensor-core path (C/G >= 64, C/G and K/G multiples of 8).  The pages have
+ * no counterpart to this call; it exists for callers that cannot allocate
+ * device memory (a host framework that owns all device memory through its own
+ * pool, or a loop that must not call cudaMalloc because it can synchronise
+ * the device or fail mid-run).  It plans on the host from `desc` on every
+ * call and allocates no device memory: the kernel's only scratch, its 4-byte
+ * status word, lives in a 256-byte file-scope __device__ array that every GPU
+ * loading the library holds until the process exits.  The first call on a
+ * device looks up that array's device address (once per device, with the
+ * device current); make that first call before any stream capture.  Every
+ * call shares the array and clears its status word on `stream` before
+ * launching; calls whose kernels overlap on the GPU race on it.
+ * Arguments: as conv_bwd_data_run, plus `device_status`: NULL for a fully
+ * asynchronous call, or a host int that receives the device status code
+ * after the call synchronises `stream`.
+ * Errors: INVALID_ARG, MISALIGNED and CUDA as conv_bwd_data_run;
+ * UNSUPPORTED if the descriptor is not on the tensor-core path or its scratch
+ * would exceed the 256-byte maximum; DEVICE_TIMEOUT / DEVICE_FAULT (only
+ * with device_status != NULL) as conv_bwd_data_get_status. */
+conv_bwd_status conv_bwd_data_run_noalloc(const conv_bwd_desc *desc, const void *dy, const void *w, void *dx,
+                                          void *stream, int32_t *device_status);
+
 /* Human-readable status name (static storage). */
 const char *conv_bwd_status_string(conv_bwd_status s);
 
