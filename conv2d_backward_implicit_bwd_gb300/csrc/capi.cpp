@@ -244,7 +244,7 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
 
     // Kernel path.
     bool tc_ok = d.dtype == CONV_BWD_BF16 && d.layout == CONV_BWD_NHWC_KYXC && g.Cg % 8 == 0 && g.Kg % 8 == 0 &&
-                 d.K % 8 == 0 && d.C % 8 == 0 && g.Cg >= 64;
+                 d.K % 8 == 0 && d.C % 8 == 0 && g.Cg >= 64 && d.Hi < 16384 && d.Wi < 16384;
     p->path = tc_ok ? CONV_BWD_PATH_TCGEN05 : CONV_BWD_PATH_SIMT;
     if (const char *f = env("CONVBWD_DEBUG_PATH")) {
         if (!std::strcmp(f, "simt")) p->path = CONV_BWD_PATH_SIMT;

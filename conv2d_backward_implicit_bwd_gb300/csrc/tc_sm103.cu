@@ -16,19 +16,25 @@
 // writes only rows of the class that exist in dx (the "OOB write" point).
 //
 // Tile: 128 (m) x BN (c) with BN in {128, 256}, K step 64 (one 128-byte
-// swizzled row per operand row).  Roles (288 threads, one CTA per SM):
-//   warps 0-3  epilogue: tcgen05.ld of the fp32 accumulator (warp q reads TMEM
-//              lanes 32q..32q+31 = tile rows), RNE to bf16, 16-byte stores to
-//              the class's strided dx pixels;
-//   warps 4-7  producers: A rows gathered with 16-byte cp.async (zero-fill for
-//              rows outside dy or past Kg) into the 128-byte-swizzled K-major
-//              layout; one thread also issues the TMA loads of B (w is
-//              c-contiguous, so B is MN-major: BN/64 boxes of 64 k x 64 c);
-//   warp 8     TMEM allocation and the single-thread tcgen05.mma issue
-//              (M=128, N=BN, K=16, bf16 x bf16 -> fp32), committing each stage
-//              back to its producer barrier and each finished tile to the
-//              epilogue.  The accumulator is double-buffered in TMEM (2*BN
-//              columns) so the epilogue of tile t overlaps the MMAs of t+1.
+// swizzled row per operand row), S pipeline slots.  Roles (one CTA per SM):
+//   warps 0-3      epilogue: tcgen05.ld of the fp32 accumulator (warp q reads
+//                  TMEM lanes 32q..32q+31 = tile rows), RNE to bf16, 16-byte
+//                  stores to the class's strided dx pixels;
+//   warps 4..4+S-1 producers, one per pipeline slot: producer warp s loads
+//                  every stage that lands in slot s.  The A rows are gathered
+//                  with 16-byte cp.async (zero-fill for rows outside dy or
+//                  past Kg; 4 rows x 128 B per instruction, coalesced) into
+//                  the 128-byte-swizzled K-major layout, then the warp waits
+//                  for its own copies, fences them to the async proxy and
+//                  arrives on the slot's barrier.  Lane 0 also issues the TMA
+//                  loads of B (w is c-contiguous, so B is MN-major: BN/64
+//                  boxes of 64 k x 64 c).  Slots fill independently, so S
+//                  stages are in flight at once;
+//   warp 4+S       TMEM allocation and the single-thread tcgen05.mma issue
+//                  (M=128, N=BN, K=16, bf16 x bf16 -> fp32), committing each
+//                  stage back to its slot and each finished tile to the
+//                  epilogue.  The accumulator is double-buffered in TMEM (2*BN
+//                  columns) so the epilogue of tile t overlaps the MMAs of t+1.
 // Every barrier wait is bounded (device_util.cuh); on a timeout the kernel
 // records the status word, drains what it started and returns.
 #include <cuda.h>
@@ -44,14 +50,15 @@ template <int BN>
 struct TcCfg {
     static constexpr int BM = 128;
     static constexpr int BK = 64;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
-    static constexpr int LAG = STAGES - 1;  // cp.async groups kept in flight per producer thread
+    static constexpr int STAGES = BN == 256 ? 4 : 6;   // = producer warps
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int ROWTAB_BYTES = STAGES * BM * 8;  // per producer warp: 128 x {pixel, ht|wt}
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + BAR_BYTES;
-    static constexpr int THREADS = 288;
+    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + ROWTAB_BYTES + BAR_BYTES;
+    static constexpr int MMA_WARP = 4 + STAGES;
+    static constexpr int THREADS = 32 * (MMA_WARP + 1);
 };
 
 // --- PTX wrappers ----------------------------------------------------------
@@ -167,7 +174,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1) tc_dgrad_kernel(const _
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + S * Cfg::A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S * Cfg::B_BYTES);
+    int2 *rowtab = reinterpret_cast<int2 *>(sB + S * Cfg::B_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S * Cfg::B_BYTES + Cfg::ROWTAB_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
 
@@ -178,7 +186,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1) tc_dgrad_kernel(const _
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8 * s, 128);
+            mbar_init(full0 + 8 * s, 32);  // the 32 lanes of the slot's producer warp
             mbar_init(empty0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -189,7 +197,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1) tc_dgrad_kernel(const _
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async_smem();
     }
-    if (warp == 8) {
+    if (warp == Cfg::MMA_WARP) {
         tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
         tc_fence_before();
     }
@@ -198,83 +206,95 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1) tc_dgrad_kernel(const _
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp >= 4 && warp < 8) {
+    if (warp >= 4 && warp < Cfg::MMA_WARP) {
         // ------------------------------------------------------------ producers
-        const int pt = threadIdx.x - 128;
-        const int chunk = pt & 7, rsub = pt >> 3;
-        const uint32_t swz = (uint32_t)((chunk ^ (rsub & 7)) << 4);
+        const int pw = warp - 4;                 // this warp owns pipeline slot pw
+        const int chunk = lane & 7;              // 16-byte chunk of the 128-byte k row
+        const int rsub = lane >> 3;              // rows rsub + 4*q, q < 32
         const __nv_bfloat16 *dy = static_cast<const __nv_bfloat16 *>(p.dy);
-        uint32_t it = 0;
-        bool ok = true;
-        bool issued_tma = false;
+        int2 *tab = rowtab + pw * 128;
+        const uint32_t full_s = full0 + 8 * pw, empty_s = empty0 + 8 * pw;
+        const uint32_t a_slot = smem_u32(sA + pw * Cfg::A_BYTES);
+        const uint32_t b_slot = smem_u32(sB + pw * Cfg::B_BYTES);
+        uint32_t it = 0;   // global stage counter of this CTA (all slots)
+        bool ok = true, issued_tma = false;
         for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
             const TileCoord tcd = decode_tile(p, t);
             const ClassDesc &c = p.cls[tcd.ci];
-            const int HTWT = c.HT * c.WT;
-            int rn[8], rht[8], rwt[8];
+            const uint32_t num_kb = (uint32_t)(c.taps_y * c.taps_x * p.kb_per_tap);
+            // first stage of this tile that lands in my slot
+            uint32_t mine = it + (uint32_t)((pw - (int)(it % S) + S) % S);
+            if (mine < it + num_kb) {
+                // row table of the tile: pixel index of tap (0,0) and (ht, wt) as two
+                // signed 16-bit halves (class rows may start at a negative ht); rows
+                // past M get ht = -32768, which no tap brings back inside dy
+                const int HTWT = c.HT * c.WT;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int m = tcd.mb * 128 + rsub + 16 * q;
-                rn[q] = -1;
-                rht[q] = 0;
-                rwt[q] = 0;
-                if (m < c.M) {
-                    const int n = m / HTWT;
-                    const int rem = m - n * HTWT;
-                    rn[q] = n;
-                    rht[q] = c.ht_lo + rem / c.WT;
-                    rwt[q] = c.wt_lo + rem % c.WT;
+                for (int q = 0; q < 4; ++q) {
+                    const int r = lane + 32 * q;
+                    const int m = tcd.mb * 128 + r;
+                    int2 e = make_int2(0, (int)0x80000000u);
+                    if (m < c.M) {
+                        const int n = m / HTWT;
+                        const int rem = m - n * HTWT;
+                        const int ht = c.ht_lo + rem / c.WT, wt = c.wt_lo + rem % c.WT;
+                        e = make_int2((n * g.Ho + ht) * g.Wo + wt, (int)(((uint32_t)ht << 16) | ((uint32_t)wt & 0xFFFFu)));
+                    }
+                    tab[r] = e;
                 }
+                __syncwarp();
             }
-            const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
-            for (int kb = 0; kb < num_kb; ++kb, ++it) {
+            int2 rinfo[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) rinfo[q] = tab[rsub + 4 * q];
+            __syncwarp();
+            for (; mine < it + num_kb; mine += S) {
+                const int kb = (int)(mine - it);
                 const int tap = kb / p.kb_per_tap;
                 const int k0 = (kb - tap * p.kb_per_tap) * 64;
                 const int j = tap / c.taps_x, i = tap - j * c.taps_x;
-                const uint32_t s = it % S, ph = (it / S) & 1;
-                if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, p.wait_budget, abort_flag, p.status,
+                const uint32_t use = mine / S;
+                if (!mbar_wait_bounded(empty_s, (use & 1) ^ 1, p.wait_budget, abort_flag, p.status,
                                        kDevTimeoutProducer)) {
                     ok = false;
                     break;
                 }
-                if (pt == 0) {
-                    mbar_expect_tx(full0 + 8 * s, (uint32_t)Cfg::B_BYTES);
-                    const uint32_t bdst = smem_u32(sB + s * Cfg::B_BYTES);
+                if (lane == 0) {
+                    mbar_expect_tx(full_s, (uint32_t)Cfg::B_BYTES);
 #pragma unroll
                     for (int cb = 0; cb < BN / 64; ++cb)
-                        tma_load_5d(bdst + cb * 8192, &p.tmap_w, full0 + 8 * s, tcd.nb * BN + cb * 64,
-                                    c.tx + g.XT * i, c.ty + g.YT * j, k0, tcd.gi);
+                        tma_load_5d(b_slot + cb * 8192, &p.tmap_w, full_s, tcd.nb * BN + cb * 64, c.tx + g.XT * i,
+                                    c.ty + g.YT * j, k0, tcd.gi);
                     issued_tma = true;
                 }
+                const int dh = j * g.DH, dw = i * g.DW;
+                const int dpix = dh * g.Wo + dw;
                 const int kch = k0 + chunk * 8;
                 const bool kval = kch < g.Kg;
-                const uint32_t abase = smem_u32(sA + s * Cfg::A_BYTES) + swz;
+                const int64_t kofs = (int64_t)tcd.gi * g.Kg + kch;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int ho = rht[q] - j * g.DH, wo = rwt[q] - i * g.DW;
-                    const bool v = rn[q] >= 0 && kval && ho >= 0 && ho < g.Ho && wo >= 0 && wo < g.Wo;
-                    const __nv_bfloat16 *src =
-                        v ? dy + ((((int64_t)rn[q] * g.Ho + ho) * g.Wo + wo) * g.K + (int64_t)tcd.gi * g.Kg + kch) : dy;
-                    cp_async_16(abase + (uint32_t)(rsub + 16 * q) * 128u, src, v ? 16u : 0u);
+                for (int q = 0; q < 32; ++q) {
+                    const int ht = rinfo[q].y >> 16, wt = (int)(short)(rinfo[q].y & 0xFFFF);
+                    const int ho = ht - dh, wo = wt - dw;
+                    const bool v = kval && ho >= 0 && ho < g.Ho && wo >= 0 && wo < g.Wo;
+                    const __nv_bfloat16 *src = v ? dy + ((int64_t)(rinfo[q].x - dpix) * g.K + kofs) : dy;
+                    // row r = rsub + 4q: (r & 7) == (rsub & 7) ^ (4 * (q & 1)) since rsub < 4
+                    const uint32_t sw = (uint32_t)((chunk ^ ((rsub + 4 * q) & 7)) << 4);
+                    cp_async_16(a_slot + (uint32_t)(rsub + 4 * q) * 128u + sw, src, v ? 16u : 0u);
                 }
                 cp_async_commit();
-                if (it >= (uint32_t)Cfg::LAG) {
-                    cp_async_wait<Cfg::LAG>();
-                    fence_proxy_async_smem();
-                    mbar_arrive(full0 + 8 * ((it - Cfg::LAG) % S));
-                }
+                cp_async_wait<0>();
+                fence_proxy_async_smem();
+                mbar_arrive(full_s);
             }
+            it += num_kb;
         }
         cp_async_wait<0>();
-        fence_proxy_async_smem();
-        if (ok) {
-            const uint32_t first = it >= (uint32_t)Cfg::LAG ? it - Cfg::LAG : 0u;
-            for (uint32_t u = first; u < it; ++u) mbar_arrive(full0 + 8 * (u % S));
-        } else if (issued_tma) {
+        if (!ok && issued_tma) {
             // let TMA loads already in flight land before the block exits
             for (int q = 0; q < 100; ++q) __nanosleep(1000);
         }
-    } else if (warp == 8) {
+    } else if (warp == Cfg::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16<BN>();
@@ -367,7 +387,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1) tc_dgrad_kernel(const _
     }
 
     __syncthreads();
-    if (warp == 8) {
+    if (warp == Cfg::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
