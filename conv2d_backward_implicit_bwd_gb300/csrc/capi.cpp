@@ -50,6 +50,9 @@ struct conv_bwd_plan_s {
     // TMA descriptor cache (keyed by the filter pointer)
     const void *tmap_w_ptr = nullptr;
     CUtensorMap tmap_w;
+    const void *tmap_a_ptr = nullptr;     // dy pointer the per-class im2col maps were encoded for
+    std::vector<CUtensorMap> tmap_a;      // per class (gemm_id order)
+    bool im2col = false;                  // A rows by TMA im2col loads (else cp.async gather)
     std::mutex mu;
 };
 
@@ -138,6 +141,56 @@ bool encode_w_map(conv_bwd_plan_s *p, const void *w) {
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+typedef CUresult (*PFN_encodeIm2col)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                      const cuuint64_t *, const int *, const int *, cuuint32_t, cuuint32_t,
+                                      const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                      CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+PFN_encodeIm2col get_encode_im2col() {
+    static PFN_encodeIm2col fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_encodeIm2col)p;
+    });
+    return fn;
+}
+
+// Bounding-box corners of class c's im2col map over dy {K, Wo, Ho, N}: the
+// base pixel of tap (taps-1) walks ht - (taps_y-1)*DH over the class rows, so
+// the box spans [lo, dim - 1 + hi] with lo/hi below (index 0 = W, 1 = H).
+void im2col_corners(const Geom &g, const ClassDesc &c, int lo[2], int hi[2]) {
+    lo[0] = c.wt_lo - (c.taps_x - 1) * g.DW;
+    lo[1] = c.ht_lo - (c.taps_y - 1) * g.DH;
+    hi[0] = lo[0] + c.WT - g.Wo;
+    hi[1] = lo[1] + c.HT - g.Ho;
+}
+
+// One im2col map per class: 64 channels x 128 pixels per load, 128-byte
+// swizzle, pixels outside dy read as zero.
+bool encode_a_maps(conv_bwd_plan_s *p, const void *dy) {
+    PFN_encodeIm2col enc = get_encode_im2col();
+    if (!enc) return false;
+    const Geom &g = p->g;
+    p->tmap_a.resize(p->classes.size());
+    cuuint64_t dims[4] = {(cuuint64_t)g.K, (cuuint64_t)g.Wo, (cuuint64_t)g.Ho, (cuuint64_t)g.N};
+    cuuint64_t strides[3] = {(cuuint64_t)g.K * 2, (cuuint64_t)g.Wo * g.K * 2, (cuuint64_t)g.Ho * g.Wo * g.K * 2};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    for (size_t i = 0; i < p->classes.size(); ++i) {
+        int lo[2], hi[2];
+        im2col_corners(g, p->classes[i], lo, hi);
+        CUresult r = enc(&p->tmap_a[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(dy), dims, strides, lo,
+                         hi, 64, 128, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return false;
+    }
+    return true;
 }
 
 const char *env(const char *k) {
@@ -250,6 +303,17 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
         if (!std::strcmp(f, "simt")) p->path = CONV_BWD_PATH_SIMT;
     }
     p->bn = (p->path == CONV_BWD_PATH_TCGEN05) ? (g.Cg >= 256 ? 256 : 128) : 64;
+    // im2col loads read 64 channels past k0 of dy's flat K axis, exact only
+    // when no 64-block crosses a group boundary; rank-4 im2col corners must
+    // lie in [-128, 127].  Otherwise the cp.async gather producer runs.
+    p->im2col = p->path == CONV_BWD_PATH_TCGEN05 && (g.G == 1 || g.Kg % 64 == 0);
+    for (const ClassDesc &c : p->classes) {
+        int lo[2], hi[2];
+        im2col_corners(g, c, lo, hi);
+        for (int q = 0; q < 2; ++q)
+            if (lo[q] < -128 || lo[q] > 127 || hi[q] < -128 || hi[q] > 127) p->im2col = false;
+    }
+    if (const char *f = env("CONVBWD_DEBUG_NOIM2COL")) p->im2col = p->im2col && f[0] == '0';
 
     // Schedule: classes with the longest reduction first (LPT), tiles of one
     // class contiguous; BM = 128 rows for the tensor-core path, 64 for SIMT.
@@ -356,7 +420,9 @@ conv_bwd_status conv_bwd_data_coverage(const conv_bwd_plan p, uint8_t *row_mask,
 conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t *launches) {
     if (!p) return CONV_BWD_ERR_INVALID_ARG;
     if (path) *path = p->path;
-    if (launches) *launches = (p->any_uncovered ? 1 : 0) + (p->classes.empty() ? 0 : 1);
+    int gemm_launches = p->classes.empty() ? 0 : 1;
+    if (p->path == CONV_BWD_PATH_TCGEN05) gemm_launches = (int)((p->classes.size() + kMaxTcClasses - 1) / kMaxTcClasses);
+    if (launches) *launches = (p->any_uncovered ? 1 : 0) + gemm_launches;
     return CONV_BWD_OK;
 }
 
@@ -403,27 +469,39 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
     if (p->classes.empty()) return CONV_BWD_OK;
 
     if (p->path == CONV_BWD_PATH_TCGEN05) {
-        TcParams tp;
-        std::memset(&tp, 0, sizeof(tp));
         if (p->tmap_w_ptr != w) {
             if (!encode_w_map(p, w)) return CONV_BWD_ERR_CUDA;
             p->tmap_w_ptr = w;
         }
-        tp.tmap_w = p->tmap_w;
-        tp.dy = dy; tp.dx = dx; tp.status = p->d_status; tp.wait_budget = p->wait_budget;
-        tp.g = g;
-        tp.num_classes = (int)p->sched.size();
-        tp.n_tiles = (g.Cg + p->bn - 1) / p->bn;
-        tp.kb_per_tap = (g.Kg + 63) / 64;
-        int64_t total = 0;
-        for (size_t i = 0; i < p->sched.size(); ++i) {
-            tp.cls[i] = p->classes[(size_t)p->sched[i]];
-            total += (int64_t)g.G * tp.cls[i].m_tiles * tp.n_tiles;
+        if (p->im2col && p->tmap_a_ptr != dy) {
+            if (!encode_a_maps(p, dy)) return CONV_BWD_ERR_CUDA;
+            p->tmap_a_ptr = dy;
         }
-        tp.total_tiles = (int)total;
-        int grid = (int)std::min<int64_t>(total, p->num_sms);
         if (p->timing) cudaEventRecord(p->ev[2], s);
-        if (launch_tc(tp, p->bn, grid, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        // at most kMaxTcClasses sub-GEMMs per launch (their maps travel as kernel parameters)
+        for (size_t c0 = 0; c0 < p->sched.size(); c0 += kMaxTcClasses) {
+            TcParams tp;
+            std::memset(&tp, 0, sizeof(tp));
+            tp.tmap_w = p->tmap_w;
+            tp.dy = dy; tp.dx = dx; tp.status = p->d_status; tp.wait_budget = p->wait_budget;
+            tp.g = g;
+            tp.n_tiles = (g.Cg + p->bn - 1) / p->bn;
+            tp.kb_per_tap = (g.Kg + 63) / 64;
+            tp.im2col = p->im2col ? 1 : 0;
+            const size_t nc = std::min<size_t>(kMaxTcClasses, p->sched.size() - c0);
+            tp.num_classes = (int)nc;
+            int64_t total = 0;
+            for (size_t i = 0; i < nc; ++i) {
+                const int idx = p->sched[c0 + i];
+                tp.cls[i] = p->classes[(size_t)idx];
+                tp.cls[i].tile_begin = (int)total;
+                total += (int64_t)g.G * tp.cls[i].m_tiles * tp.n_tiles;
+                if (p->im2col) tp.tmap_a[i] = p->tmap_a[(size_t)idx];
+            }
+            tp.total_tiles = (int)total;
+            const int grid = (int)std::min<int64_t>(total, p->num_sms);
+            if (launch_tc(tp, p->bn, grid, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        }
         if (p->timing) cudaEventRecord(p->ev[3], s);
         return CONV_BWD_OK;
     }

@@ -17,7 +17,8 @@
 
 namespace cbd {
 
-constexpr int kMaxClasses = 64;   // stride_h * stride_w classes at most (each stride <= 64 handled via this cap)
+constexpr int kMaxClasses = 64;   // non-empty sub-GEMMs per plan
+constexpr int kMaxTcClasses = 16; // sub-GEMMs per tensor-core launch (more classes -> several launches)
 
 struct ClassDesc {
     int32_t ty, tx;          // row / column residue class
@@ -69,6 +70,7 @@ struct FillParams {
 // Tensor-core (tcgen05) kernel parameters.
 struct TcParams {  // 128-byte aligned through CUtensorMap
     CUtensorMap tmap_w;   // w viewed as 5-D {Cg, X, Y, Kg, G}, box {64, 1, 1, 64, 1}, 128B swizzle
+    CUtensorMap tmap_a[kMaxTcClasses];  // per class: dy as im2col {K, Wo, Ho, N}, 64 ch x 128 px, 128B swizzle
     const void *dy;
     void *dx;
     int32_t *status;      // device status word (0 = ok)
@@ -78,7 +80,8 @@ struct TcParams {  // 128-byte aligned through CUtensorMap
     int32_t n_tiles;      // ceil(Cg / BN)
     int32_t kb_per_tap;   // ceil(Kg / 64)
     int32_t total_tiles;
-    ClassDesc cls[kMaxClasses];
+    int32_t im2col;       // 1: A rows by TMA im2col loads (tmap_a), 0: cp.async gather
+    ClassDesc cls[kMaxTcClasses];
 };
 
 // Status codes written by kernels (first writer wins).
@@ -95,6 +98,6 @@ cudaError_t launch_fill(const FillParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_simt(const SimtParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_tc(const TcParams &p, int bn, int grid, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t *status, int64_t budget, cudaStream_t s);
-size_t tc_smem_bytes(int bn);
+size_t tc_smem_bytes(int bn, bool im2col);
 
 }  // namespace cbd

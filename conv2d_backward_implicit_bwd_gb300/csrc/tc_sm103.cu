@@ -20,17 +20,23 @@
 //   warps 0-3      epilogue: tcgen05.ld of the fp32 accumulator (warp q reads
 //                  TMEM lanes 32q..32q+31 = tile rows), RNE to bf16, 16-byte
 //                  stores to the class's strided dx pixels;
-//   warps 4..4+S-1 producers, one per pipeline slot: producer warp s loads
-//                  every stage that lands in slot s.  The A rows are gathered
-//                  with 16-byte cp.async (zero-fill for rows outside dy or
-//                  past Kg; 4 rows x 128 B per instruction, coalesced) into
-//                  the 128-byte-swizzled K-major layout, then the warp waits
-//                  for its own copies, fences them to the async proxy and
-//                  arrives on the slot's barrier.  Lane 0 also issues the TMA
-//                  loads of B (w is c-contiguous, so B is MN-major: BN/64
-//                  boxes of 64 k x 64 c).  Slots fill independently, so S
-//                  stages are in flight at once;
-//   warp 4+S       TMEM allocation and the single-thread tcgen05.mma issue
+//   warp 4         producer (im2col mode, the default): one lane issues, per
+//                  stage, a single TMA im2col load of the 128 A rows -- each
+//                  class has its own rank-4 map over dy whose bounding box is
+//                  the class's (ht, wt) range shifted to tap (taps-1), so the
+//                  map walks the class rows in (n, ht, wt) order and the tap
+//                  (j, i) is the im2col offset; rows outside dy (padding,
+//                  borders, the flip's out-of-range taps, the M tail) read as
+//                  zero -- plus the BN/64 TMA boxes of B (w is c-contiguous, so
+//                  B is MN-major: 64 k x 64 c per box);
+//   warps 4..4+S-1 producers (cp.async mode, where a 64-channel block may cross
+//                  a group boundary or a bounding box exceeds the im2col corner
+//                  range): producer warp s loads every stage of slot s,
+//                  gathering A rows with 16-byte cp.async (zero-fill outside dy
+//                  or past Kg; 4 rows x 128 B per instruction), waits for its
+//                  own copies, fences them to the async proxy and arrives;
+//                  lane 0 issues the B boxes;
+//   last warp      TMEM allocation and the single-thread tcgen05.mma issue
 //                  (M=128, N=BN, K=16, bf16 x bf16 -> fp32), committing each
 //                  stage back to its slot and each finished tile to the
 //                  epilogue.  The accumulator is double-buffered in TMEM (2*BN
@@ -46,18 +52,19 @@
 
 namespace cbd {
 
-template <int BN>
+template <int BN, bool IM2COL>
 struct TcCfg {
     static constexpr int BM = 128;
     static constexpr int BK = 64;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;   // = producer warps
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int PRODUCER_WARPS = IM2COL ? 1 : STAGES;  // cp.async: one warp per slot; im2col: one
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int ROWTAB_BYTES = STAGES * BM * 8;  // per producer warp: 128 x {pixel, ht|wt}
+    static constexpr int ROWTAB_BYTES = IM2COL ? 0 : STAGES * BM * 8;  // per producer warp: 128 x {pixel, ht|wt}
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + ROWTAB_BYTES + BAR_BYTES;
-    static constexpr int MMA_WARP = 4 + STAGES;
+    static constexpr int MMA_WARP = 4 + PRODUCER_WARPS;
     static constexpr int THREADS = 32 * (MMA_WARP + 1);
 };
 
@@ -81,6 +88,23 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
         : "memory");
+}
+
+// im2col-mode load of a rank-4 map {C, W, H, N}: 128 consecutive pixels of
+// the map's bounding box (raster order W, H, N) starting at base pixel
+// (w, h, n), each shifted by (ow, oh), 64 channels from c; pixels outside the
+// tensor read as zero.  Lands as 128 rows of 128 bytes, 128-byte swizzled.
+__device__ __forceinline__ void tma_load_im2col(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c, int w,
+                                                int h, int n, uint16_t ow, uint16_t oh) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8};" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar), "h"(ow), "h"(oh)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
@@ -166,9 +190,9 @@ __device__ __forceinline__ TileCoord decode_tile(const TcParams &p, int t) {
     return r;
 }
 
-template <int BN>
-__global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1) tc_dgrad_kernel(const __grid_constant__ TcParams p) {
-    using Cfg = TcCfg<BN>;
+template <int BN, bool IM2COL>
+__global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel(const __grid_constant__ TcParams p) {
+    using Cfg = TcCfg<BN, IM2COL>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -186,7 +210,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1) tc_dgrad_kernel(const _
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8 * s, 32);  // the 32 lanes of the slot's producer warp
+            // im2col: one arrive.expect_tx per stage; cp.async: the 32 lanes of the slot's warp
+            mbar_init(full0 + 8 * s, IM2COL ? 1 : 32);
             mbar_init(empty0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -201,13 +226,64 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1) tc_dgrad_kernel(const _
         tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
         tc_fence_before();
     }
-    if (warp == 4 && lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_w)) : "memory");
+    if (warp == 4 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_w)) : "memory");
+        if (IM2COL)
+            for (int ci = 0; ci < p.num_classes; ++ci)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_a[ci])) : "memory");
+    }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp >= 4 && warp < Cfg::MMA_WARP) {
-        // ------------------------------------------------------------ producers
+    if (IM2COL && warp == 4) {
+        // ------------------------------------------------------------ producer (TMA)
+        // One lane issues every load: per stage one im2col load of the 128 A
+        // rows (the class's map walks its (n, ht, wt) rows in order; the tap
+        // is the im2col offset) and the BN/64 boxes of B.
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true, issued = false;
+            for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+                const TileCoord tcd = decode_tile(p, t);
+                const ClassDesc &c = p.cls[tcd.ci];
+                const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
+                // first row of the tile -> base pixel of tap (taps_y-1, taps_x-1)
+                const int HTWT = c.HT * c.WT;
+                const int m0 = tcd.mb * 128;
+                const int n0 = m0 / HTWT, rem = m0 - n0 * HTWT;
+                const int bh = c.ht_lo + rem / c.WT - (c.taps_y - 1) * g.DH;
+                const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
+                const CUtensorMap *amap = &p.tmap_a[tcd.ci];
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                    const int tap = kb / p.kb_per_tap;
+                    const int k0 = (kb - tap * p.kb_per_tap) * 64;
+                    const int j = tap / c.taps_x, i = tap - j * c.taps_x;
+                    const uint32_t s = it % S, ph = (it / S) & 1;
+                    if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, p.wait_budget, abort_flag, p.status,
+                                           kDevTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_s = full0 + 8 * s;
+                    mbar_arrive_expect_tx(full_s, (uint32_t)(Cfg::A_BYTES + Cfg::B_BYTES));
+                    tma_load_im2col(smem_u32(sA + s * Cfg::A_BYTES), amap, full_s, tcd.gi * g.Kg + k0, bw, bh, n0,
+                                    (uint16_t)((c.taps_x - 1 - i) * g.DW), (uint16_t)((c.taps_y - 1 - j) * g.DH));
+                    const uint32_t bdst = smem_u32(sB + s * Cfg::B_BYTES);
+#pragma unroll
+                    for (int cb = 0; cb < BN / 64; ++cb)
+                        tma_load_5d(bdst + cb * 8192, &p.tmap_w, full_s, tcd.nb * BN + cb * 64, c.tx + g.XT * i,
+                                    c.ty + g.YT * j, k0, tcd.gi);
+                    issued = true;
+                }
+            }
+            if (!ok && issued) {
+                for (int q = 0; q < 100; ++q) __nanosleep(1000);
+            }
+        }
+        __syncwarp();
+    } else if (!IM2COL && warp >= 4 && warp < Cfg::MMA_WARP) {
+        // ------------------------------------------------------------ producers (cp.async)
         const int pw = warp - 4;                 // this warp owns pipeline slot pw
         const int chunk = lane & 7;              // 16-byte chunk of the 128-byte k row
         const int rsub = lane >> 3;              // rows rsub + 4*q, q < 32
@@ -393,24 +469,32 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1) tc_dgrad_kernel(const _
     }
 }
 
-size_t tc_smem_bytes(int bn) { return bn == 256 ? TcCfg<256>::SMEM : TcCfg<128>::SMEM; }
+size_t tc_smem_bytes(int bn, bool im2col) {
+    if (bn == 256) return im2col ? TcCfg<256, true>::SMEM : TcCfg<256, false>::SMEM;
+    return im2col ? TcCfg<128, true>::SMEM : TcCfg<128, false>::SMEM;
+}
 
-template <int BN>
-static cudaError_t launch_tc_bn(const TcParams &p, int grid, cudaStream_t s) {
-    static bool attr_set = false;  // per process; the attribute is per function and device-independent here
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_dgrad_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             TcCfg<BN>::SMEM);
+template <int BN, bool IM2COL>
+static cudaError_t launch_tc_cfg(const TcParams &p, int grid, cudaStream_t s) {
+    using Cfg = TcCfg<BN, IM2COL>;
+    // the dynamic shared-memory opt-in is per device: set it for the current one
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_dgrad_kernel<BN, IM2COL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg::SMEM);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    tc_dgrad_kernel<BN><<<grid, TcCfg<BN>::THREADS, TcCfg<BN>::SMEM, s>>>(p);
+    tc_dgrad_kernel<BN, IM2COL><<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_tc(const TcParams &p, int bn, int grid, cudaStream_t s) {
     if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
-    return bn == 256 ? launch_tc_bn<256>(p, grid, s) : launch_tc_bn<128>(p, grid, s);
+    if (bn == 256) return p.im2col ? launch_tc_cfg<256, true>(p, grid, s) : launch_tc_cfg<256, false>(p, grid, s);
+    return p.im2col ? launch_tc_cfg<128, true>(p, grid, s) : launch_tc_cfg<128, false>(p, grid, s);
 }
 
 }  // namespace cbd

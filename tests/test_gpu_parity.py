@@ -136,6 +136,8 @@ TC_CASES = [
     _mk("tc_mixed", N=2, C=200, K=40, Hi=11, Wi=6, Y=2, X=4, pad=(0, 3), stride=(3, 1), dil=(2, 3)),
     _mk("tc_bn256_ragged", N=3, C=264, K=64, Hi=6, Wi=7, Y=3, X=3, pad=(1, 1), stride=(1, 1)),
     _mk("tc_deep_k", N=1, C=64, K=1024, Hi=5, Wi=6, Y=2, X=2, pad=(1, 1), stride=(2, 2)),
+    _mk("tc_25_classes", N=1, C=64, K=64, Hi=20, Wi=20, Y=5, X=5, pad=(2, 2), stride=(5, 5)),
+    _mk("tc_groups2_kg96", N=2, C=128, K=192, Hi=9, Wi=9, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=2),
 ]
 
 
@@ -184,6 +186,19 @@ def test_forced_simt_matches_tensor_core_path(B, monkeypatch):
     assert plan.path()[0] == "simt"
     check_full(c, simt, g, dy, w)
     check_full(c, tc, g, dy, w)
+
+
+@pytest.mark.parametrize("idx", [0, 4, 8, 10])
+def test_cp_async_producer_variant(B, monkeypatch, idx):
+    """The cp.async A producer (used where a 64-channel block may cross a
+    group boundary, or im2col corners fall outside their range) on shapes
+    that normally take the TMA im2col producer."""
+    c = TC_CASES[idx]
+    g, dy, w = inputs(c)
+    monkeypatch.setenv("CONVBWD_DEBUG_NOIM2COL", "1")
+    got, plan = gpu_dgrad(B, c, dy, w)
+    assert plan.path()[0] == "tcgen05"
+    check_full(c, got, g, dy, w)
 
 
 def test_deterministic_and_stream_ordered(B):
