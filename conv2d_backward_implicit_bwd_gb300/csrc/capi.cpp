@@ -303,6 +303,8 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
         if (!std::strcmp(f, "simt")) p->path = CONV_BWD_PATH_SIMT;
     }
     p->bn = (p->path == CONV_BWD_PATH_TCGEN05) ? (g.Cg >= 256 ? 256 : 128) : 64;
+    if (const char *f = env("CONVBWD_DEBUG_BN"))
+        if (p->path == CONV_BWD_PATH_TCGEN05 && (!std::strcmp(f, "128") || !std::strcmp(f, "256"))) p->bn = std::atoi(f);
     // im2col loads read 64 channels past k0 of dy's flat K axis, exact only
     // when no 64-block crosses a group boundary; rank-4 im2col corners must
     // lie in [-128, 127].  Otherwise the cp.async gather producer runs.
@@ -499,7 +501,8 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
                 if (p->im2col) tp.tmap_a[i] = p->tmap_a[(size_t)idx];
             }
             tp.total_tiles = (int)total;
-            const int grid = (int)std::min<int64_t>(total, p->num_sms);
+            int grid = (int)std::min<int64_t>(total, p->num_sms);
+            if (const char *f = env("CONVBWD_DEBUG_GRID")) grid = std::max(1, std::min(grid, std::atoi(f)));
             if (launch_tc(tp, p->bn, grid, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
         }
         if (p->timing) cudaEventRecord(p->ev[3], s);
