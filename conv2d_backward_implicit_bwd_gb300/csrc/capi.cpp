@@ -53,6 +53,7 @@ struct conv_bwd_plan_s {
     const void *tmap_a_ptr = nullptr;     // dy pointer the per-class im2col maps were encoded for
     std::vector<CUtensorMap> tmap_a;      // per class (gemm_id order)
     bool im2col = false;                  // A rows by TMA im2col loads (else cp.async gather)
+    bool two_sm = false;                  // 256x256 tiles on SM pairs (cta_group::2)
     std::mutex mu;
 };
 
@@ -316,10 +317,15 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
             if (lo[q] < -128 || lo[q] > 127 || hi[q] < -128 || hi[q] > 127) p->im2col = false;
     }
     if (const char *f = env("CONVBWD_DEBUG_NOIM2COL")) p->im2col = p->im2col && f[0] == '0';
+    // 256 x 256 tiles on SM pairs (tcgen05 cta_group::2) where the tile is wide
+    // enough: each SM then loads only half of B.
+    p->two_sm = p->path == CONV_BWD_PATH_TCGEN05 && p->im2col && p->bn == 256;
+    if (const char *f = env("CONVBWD_DEBUG_NO2SM")) p->two_sm = p->two_sm && f[0] == '0';
 
     // Schedule: classes with the longest reduction first (LPT), tiles of one
-    // class contiguous; BM = 128 rows for the tensor-core path, 64 for SIMT.
-    const int bm = p->path == CONV_BWD_PATH_TCGEN05 ? 128 : 64;
+    // class contiguous; BM = 256 rows on SM pairs, 128 for the 1-SM
+    // tensor-core kernel, 64 for SIMT.
+    const int bm = p->path == CONV_BWD_PATH_TCGEN05 ? (p->two_sm ? 256 : 128) : 64;
     const int n_tiles = (g.Cg + p->bn - 1) / p->bn;
     p->sched.resize(p->classes.size());
     std::iota(p->sched.begin(), p->sched.end(), 0);
@@ -501,6 +507,11 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
                 if (p->im2col) tp.tmap_a[i] = p->tmap_a[(size_t)idx];
             }
             tp.total_tiles = (int)total;
+            if (p->two_sm) {
+                const int pairs = (int)std::min<int64_t>(total, tc2_max_pairs(p->num_sms));
+                if (launch_tc2(tp, 2 * pairs, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+                continue;
+            }
             int grid = (int)std::min<int64_t>(total, p->num_sms);
             if (const char *f = env("CONVBWD_DEBUG_GRID")) grid = std::max(1, std::min(grid, std::atoi(f)));
             if (launch_tc(tp, p->bn, grid, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;

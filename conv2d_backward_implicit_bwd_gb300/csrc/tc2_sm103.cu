@@ -1,0 +1,348 @@
+// tc2_sm103.cu -- bf16 NHWC/KYXC dgrad on pairs of SMs (tcgen05 cta_group::2).
+//
+// Same sub-GEMMs as tc_sm103.cu (one per filter-tap residue class and group,
+// the v4r1 backward-data split of pages "Backward data" and "[igemm_dynamic]
+// v4r1 bwd dynamic kernel"), but each output tile is 256 (m) x 256 (c) and is
+// computed by a cluster of two CTAs on two SMs:
+//   * CTA rank r of the pair loads the tile's A rows [128r, 128r+128) (TMA
+//     im2col, one map per class, exactly as in the 1-SM kernel) and the B
+//     columns [128r, 128r+128) (two TMA boxes of 64 k x 64 c) into its own
+//     shared memory.  Both CTAs' loads complete on the leader's (rank 0)
+//     stage barrier (`.cta_group::2` TMA), which expects the bytes of both.
+//   * The leader's single MMA thread issues M=256, N=256, K=16
+//     `tcgen05.mma.cta_group::2` instructions that read A and B from both
+//     CTAs' shared memory and accumulate rows [128r, 128r+128) in CTA r's
+//     TMEM; each stage is committed back to both CTAs' empty barriers and each
+//     finished tile to both CTAs' accumulator-full barriers (multicast).
+//   * Each CTA's four epilogue warps drain their own TMEM rows (RNE to bf16,
+//     16-byte stores to the class's strided dx pixels) and release the
+//     leader's accumulator-empty barrier (remote arrive from the peer).
+// Per SM and per 128x256x64 step this moves 32 KB of operands into shared
+// memory instead of 48 KB (each SM loads only half of B), and six stages fit.
+// Every barrier wait is bounded; both CTAs meet in a cluster barrier before
+// deallocating TMEM and exiting.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "device_util.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace cbd {
+
+struct Tc2Cfg {
+    static constexpr int BN = 256;          // tile width of the pair (= MMA N)
+    static constexpr int BNH = 128;         // columns of B held by each CTA
+    static constexpr int STAGES = 6;
+    static constexpr int A_BYTES = 128 * 64 * 2;
+    static constexpr int B_BYTES = BNH * 64 * 2;
+    static constexpr int TMEM_COLS = 2 * BN;  // double-buffered 256-column accumulator
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + BAR_BYTES;
+    static constexpr int MMA_WARP = 5;
+    static constexpr int THREADS = 192;
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t slot, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+__device__ __forceinline__ void tc_mma2(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive (once) on the barrier at this shared-memory offset in every CTA of
+// `mask` when all prior tcgen05 operations of this thread have completed.
+__device__ __forceinline__ void tc_commit2_mc(uint32_t bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+                 "h"(mask)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_im2col_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c, int w,
+                                                     int h, int n, uint16_t ow, uint16_t oh) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8};" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar), "h"(ow), "h"(oh)
+        : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
+    tc2_dgrad_kernel(const __grid_constant__ TcParams p) {
+    using Cfg = Tc2Cfg;
+    constexpr int S = Cfg::STAGES;
+    constexpr int BN = Cfg::BN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + S * Cfg::A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S * Cfg::B_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
+
+    const uint32_t rank = cluster_ctarank();  // 0 = leader of the pair
+    const bool leader = rank == 0;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+    const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const Geom &g = p.g;
+    const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);   // leader: one arrive.expect_tx for both CTAs' bytes
+            mbar_init(empty0 + 8 * s, 1);  // one multicast commit per stage
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);   // one multicast commit per tile
+            mbar_init(tempty0 + 8 * b, 8);  // leader: 4 epilogue warps of each CTA
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async_smem();
+    }
+    if (warp == Cfg::MMA_WARP) {
+        tmem_alloc2(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tc_fence_before();
+    }
+    if (warp == 4 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_w)) : "memory");
+        for (int ci = 0; ci < p.num_classes; ++ci)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_a[ci])) : "memory");
+    }
+    // barriers of both CTAs initialised and TMEM allocated before any remote operation
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0 && !leader) {
+        // the pair's MMAs write this CTA's rows at the leader's TMEM address
+        if (ld_shared_cluster_u32(mapa_shared(smem_u32(tmem_slot), 0)) != tmem_base)
+            record_status(p.status, kDevFaultIndex);
+    }
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint32_t full_leader0 = mapa_shared(full0, 0);
+            uint32_t it = 0;
+            bool ok = true, issued = false;
+            for (int t = pair; t < p.total_tiles && ok; t += npairs) {
+                const TileCoord tcd = decode_tile(p, t);
+                const ClassDesc &c = p.cls[tcd.ci];
+                const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
+                const int HTWT = c.HT * c.WT;
+                const int m0 = tcd.mb * 256 + (int)rank * 128;
+                const int n0 = m0 / HTWT, rem = m0 - n0 * HTWT;
+                const int bh = c.ht_lo + rem / c.WT - (c.taps_y - 1) * g.DH;
+                const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
+                const CUtensorMap *amap = &p.tmap_a[tcd.ci];
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                    const int tap = kb / p.kb_per_tap;
+                    const int k0 = (kb - tap * p.kb_per_tap) * 64;
+                    const int j = tap / c.taps_x, i = tap - j * c.taps_x;
+                    const uint32_t s = it % S, ph = (it / S) & 1;
+                    if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, p.wait_budget, abort_flag, p.status,
+                                           kDevTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = full_leader0 + 8 * s;
+                    if (leader) mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(2 * (Cfg::A_BYTES + Cfg::B_BYTES)));
+                    tma_load_im2col_pair(smem_u32(sA + s * Cfg::A_BYTES), amap, bar, tcd.gi * g.Kg + k0, bw, bh, n0,
+                                         (uint16_t)((c.taps_x - 1 - i) * g.DW), (uint16_t)((c.taps_y - 1 - j) * g.DH));
+                    const uint32_t bdst = smem_u32(sB + s * Cfg::B_BYTES);
+#pragma unroll
+                    for (int cb = 0; cb < Cfg::BNH / 64; ++cb)
+                        tma_load_5d_pair(bdst + cb * 8192, &p.tmap_w, bar, tcd.nb * BN + (int)rank * Cfg::BNH + cb * 64,
+                                         c.tx + g.XT * i, c.ty + g.YT * j, k0, tcd.gi);
+                    issued = true;
+                }
+            }
+            if (!ok && issued) {
+                for (int q = 0; q < 100; ++q) __nanosleep(1000);
+            }
+        }
+        __syncwarp();
+    } else if (warp == Cfg::MMA_WARP) {
+        // ------------------------------------------------------------ MMA (leader only)
+        if (leader && lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16<BN, 256>();
+            uint32_t it = 0, tc = 0;
+            bool ok = true, issued = false;
+            for (int t = pair; t < p.total_tiles && ok; t += npairs, ++tc) {
+                const TileCoord tcd = decode_tile(p, t);
+                const ClassDesc &c = p.cls[tcd.ci];
+                const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
+                const uint32_t b = tc & 1, tph = (tc >> 1) & 1;
+                if (!mbar_wait_bounded(tempty0 + 8 * b, tph ^ 1, p.wait_budget, abort_flag, p.status,
+                                       kDevTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + b * BN;
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                    const uint32_t s = it % S, ph = (it / S) & 1;
+                    if (!mbar_wait_bounded(full0 + 8 * s, ph, p.wait_budget, abort_flag, p.status, kDevTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + s * Cfg::A_BYTES);
+                    const uint32_t b_addr = smem_u32(sB + s * Cfg::B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
+                        tc_mma2(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    tc_commit2_mc(empty0 + 8 * s, (uint16_t)0x3);
+                }
+                if (!ok) break;
+                tc_commit2_mc(tfull0 + 8 * b, (uint16_t)0x3);
+            }
+            if (!ok && issued) {
+                for (int q = 0; q < 100; ++q) __nanosleep(1000);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int row = warp * 32 + lane;  // TMEM lane = this CTA's tile row
+        __nv_bfloat16 *dx = static_cast<__nv_bfloat16 *>(p.dx);
+        const uint32_t tempty_leader0 = mapa_shared(tempty0, 0);
+        uint32_t tc = 0;
+        for (int t = pair; t < p.total_tiles; t += npairs, ++tc) {
+            const TileCoord tcd = decode_tile(p, t);
+            const ClassDesc &c = p.cls[tcd.ci];
+            const uint32_t b = tc & 1, tph = (tc >> 1) & 1;
+            bool ok = mbar_wait_bounded(tfull0 + 8 * b, tph, p.wait_budget, abort_flag, p.status, kDevTimeoutEpilogue);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const int m = tcd.mb * 256 + (int)rank * 128 + row;
+            const bool rvalid = m < c.M;
+            int64_t off = 0;
+            if (rvalid) {
+                const int HTWT = c.HT * c.WT;
+                const int n = m / HTWT;
+                const int rem = m - n * HTWT;
+                const int hi = (c.ht_lo + rem / c.WT) * g.sh + c.ty * g.dh - g.ph;
+                const int wi = (c.wt_lo + rem % c.WT) * g.sw + c.tx * g.dw - g.pw;
+                off = (((int64_t)n * g.Hi + hi) * g.Wi + wi) * g.C + (int64_t)tcd.gi * g.Cg + (int64_t)tcd.nb * BN;
+            }
+            const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + b * BN;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld32(tbase + cc * 32, v);
+                const int col0 = tcd.nb * BN + cc * 32;
+                if (rvalid && col0 < g.Cg) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        __nv_bfloat162 h2 =
+                            __floats2bfloat162_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                        pk[e] = *reinterpret_cast<uint32_t *>(&h2);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(dx + off + cc * 32);
+#pragma unroll
+                    for (int piece = 0; piece < 4; ++piece)
+                        if (col0 + piece * 8 < g.Cg)
+                            dst[piece] = make_uint4(pk[4 * piece], pk[4 * piece + 1], pk[4 * piece + 2], pk[4 * piece + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);
+        }
+    }
+
+    // no remote arrive or MMA may target a CTA that has left
+    cluster_sync_all();
+    if (warp == Cfg::MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc2(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+cudaError_t launch_tc2(const TcParams &p, int grid, cudaStream_t s) {
+    if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc2_dgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Cfg::SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    tc2_dgrad_kernel<<<grid, Tc2Cfg::THREADS, Tc2Cfg::SMEM, s>>>(p);
+    return cudaGetLastError();
+}
+
+int tc2_max_pairs(int num_sms) {
+    static int cached[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+    cudaFuncSetAttribute(tc2_dgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Cfg::SMEM);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
+    cfg.blockDim = dim3(Tc2Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Tc2Cfg::SMEM;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, tc2_dgrad_kernel, &cfg) != cudaSuccess || clusters <= 0) {
+        cudaGetLastError();
+        clusters = num_sms / 2;
+    }
+    if (dev >= 0 && dev < 64) cached[dev] = clusters;
+    return clusters;
+}
+
+}  // namespace cbd
