@@ -106,6 +106,17 @@ bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
 
 size_t elem_size(int32_t dt) { return dt == CONV_BWD_BF16 ? 2 : 4; }
 
+const char *env(const char *k);
+
+// L2 sector promotion of the TMA maps (256 B by default).
+CUtensorMapL2promotion l2_promotion() {
+    if (const char *f = env("CONVBWD_DEBUG_L2PROMO")) {
+        if (f[0] == '0') return CU_TENSOR_MAP_L2_PROMOTION_NONE;
+        if (f[0] == '1') return CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+    }
+    return CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+}
+
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                      const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
                                      CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
@@ -140,7 +151,7 @@ bool encode_w_map(conv_bwd_plan_s *p, const void *w) {
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(&p->tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(w), dims, strides, box,
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     l2_promotion(), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -188,7 +199,7 @@ bool encode_a_maps(conv_bwd_plan_s *p, const void *dy) {
         im2col_corners(g, p->classes[i], lo, hi);
         CUresult r = enc(&p->tmap_a[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(dy), dims, strides, lo,
                          hi, 64, 128, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         l2_promotion(), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return false;
     }
     return true;
@@ -467,6 +478,7 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
         fp.dx = dx; fp.esize = (int)es; fp.layout = d.layout;
         fp.N = g.N; fp.C = g.C; fp.Hi = g.Hi; fp.Wi = g.Wi; fp.sh = g.sh; fp.sw = g.sw;
         fp.cov_h = p->cov_h; fp.cov_w = p->cov_w;
+        if (fp.cov_w == (g.sw >= 64 ? ~0ull : ((1ull << g.sw) - 1))) fp.cov_w = ~0ull;  // every column written
         fp.vec16 = (d.layout == CONV_BWD_NHWC_KYXC && ((int64_t)d.C * (int64_t)es) % 16 == 0 &&
                     (uintptr_t)dx % 16 == 0) ? 1 : 0;
         if (p->timing) cudaEventRecord(p->ev[0], s);

@@ -20,21 +20,31 @@ namespace cbd {
 // uncovered pixel (consecutive threads -> consecutive chunks).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) fill_kernel(const FillParams p) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (p.vec16) {
-        const int64_t cpp = (int64_t)p.C * p.esize / 16;
-        const int64_t total = (int64_t)p.N * p.Hi * p.Wi * cpp;
+        // one block per dx row (n, hi): a row no class writes is one contiguous
+        // run of Wi*C elements; in a written row only the uncovered columns
+        // (C elements each) are zeroed
+        const uint32_t cpp = (uint32_t)((int64_t)p.C * p.esize / 16);  // 16-byte chunks per pixel
+        const uint32_t cpr = cpp * (uint32_t)p.Wi;                     // chunks per row
         uint4 *out = reinterpret_cast<uint4 *>(p.dx);
-        for (int64_t u = first; u < total; u += stride) {
-            int64_t pix = u / cpp;
-            int wi = (int)(pix % p.Wi);
-            int hi = (int)((pix / p.Wi) % p.Hi);
-            bool cov = ((p.cov_h >> (hi % p.sh)) & 1ull) && ((p.cov_w >> (wi % p.sw)) & 1ull);
-            if (!cov) out[u] = make_uint4(0u, 0u, 0u, 0u);
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t rows = (uint32_t)p.N * (uint32_t)p.Hi;
+        for (uint32_t r = blockIdx.x; r < rows; r += gridDim.x) {
+            const uint32_t hi = r % (uint32_t)p.Hi;
+            uint4 *row = out + (size_t)r * cpr;
+            if (!((p.cov_h >> (hi % (uint32_t)p.sh)) & 1ull)) {
+                for (uint32_t u = threadIdx.x; u < cpr; u += blockDim.x) row[u] = z;
+            } else if (p.cov_w != ~0ull) {
+                for (uint32_t u = threadIdx.x; u < cpr; u += blockDim.x) {
+                    const uint32_t wi = u / cpp;
+                    if (!((p.cov_w >> (wi % (uint32_t)p.sw)) & 1ull)) row[u] = z;
+                }
+            }
         }
         return;
     }
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = (int64_t)p.N * p.C * p.Hi * p.Wi;
     for (int64_t e = first; e < total; e += stride) {
         int hi, wi;
@@ -57,10 +67,13 @@ __global__ void __launch_bounds__(256) fill_kernel(const FillParams p) {
 }
 
 cudaError_t launch_fill(const FillParams &p, int num_sms, cudaStream_t s) {
-    int64_t units = (int64_t)p.N * p.C * p.Hi * p.Wi;
-    if (p.vec16) units = units * p.esize / 16;
-    int64_t blocks = (units + 255) / 256;
-    int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 148) * 8;
+    int64_t blocks;
+    if (p.vec16) {
+        blocks = (int64_t)p.N * p.Hi;  // one block per dx row
+    } else {
+        blocks = ((int64_t)p.N * p.C * p.Hi * p.Wi + 255) / 256;
+    }
+    int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 148) * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     fill_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);

@@ -35,76 +35,16 @@ struct Tc2Cfg {
     static constexpr int BN = 256;          // tile width of the pair (= MMA N)
     static constexpr int BNH = 128;         // columns of B held by each CTA
     static constexpr int STAGES = 6;
+    static constexpr bool STAGED_EPILOGUE = true;  // coalesce dx stores through shared memory
     static constexpr int A_BYTES = 128 * 64 * 2;
     static constexpr int B_BYTES = BNH * 64 * 2;
     static constexpr int TMEM_COLS = 2 * BN;  // double-buffered 256-column accumulator
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + BAR_BYTES;
+    static constexpr int STAGE_OUT_BYTES = STAGED_EPILOGUE ? 4 * 32 * 128 : 0;  // 4 warps x 32 rows x 128 B
+    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + STAGE_OUT_BYTES + BAR_BYTES;
     static constexpr int MMA_WARP = 5;
     static constexpr int THREADS = 192;
 };
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ void tmem_alloc2(uint32_t slot, uint32_t cols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(cols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t cols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
-}
-__device__ __forceinline__ void tc_mma2(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive (once) on the barrier at this shared-memory offset in every CTA of
-// `mask` when all prior tcgen05 operations of this thread have completed.
-__device__ __forceinline__ void tc_commit2_mc(uint32_t bar, uint16_t mask) {
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-                 "h"(mask)
-                 : "memory");
-}
-__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
-                                                 int c2, int c3, int c4) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_im2col_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c, int w,
-                                                     int h, int n, uint16_t ow, uint16_t oh) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8};" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar), "h"(ow), "h"(oh)
-        : "memory");
-}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
     tc2_dgrad_kernel(const __grid_constant__ TcParams p) {
@@ -115,7 +55,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + S * Cfg::A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S * Cfg::B_BYTES);
+    uint8_t *stage = sB + S * Cfg::B_BYTES;  // epilogue staging (1024-aligned)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stage + Cfg::STAGE_OUT_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
 
@@ -271,26 +212,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
                 off = (((int64_t)n * g.Hi + hi) * g.Wi + wi) * g.C + (int64_t)tcd.gi * g.Cg + (int64_t)tcd.nb * BN;
             }
             const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + b * BN;
-#pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld32(tbase + cc * 32, v);
-                const int col0 = tcd.nb * BN + cc * 32;
-                if (rvalid && col0 < g.Cg) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        __nv_bfloat162 h2 =
-                            __floats2bfloat162_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-                        pk[e] = *reinterpret_cast<uint32_t *>(&h2);
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(dx + off + cc * 32);
-#pragma unroll
-                    for (int piece = 0; piece < 4; ++piece)
-                        if (col0 + piece * 8 < g.Cg)
-                            dst[piece] = make_uint4(pk[4 * piece], pk[4 * piece + 1], pk[4 * piece + 2], pk[4 * piece + 3]);
-                }
-            }
+            if (Cfg::STAGED_EPILOGUE)
+                epilogue_rows<BN>(tbase, stage + warp * 4096, lane, rvalid, off, tcd.nb * BN, g.Cg, dx);
+            else
+                epilogue_rows_direct<BN>(tbase, lane, rvalid, off, tcd.nb * BN, g.Cg, dx);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);

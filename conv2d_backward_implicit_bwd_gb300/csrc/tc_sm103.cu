@@ -64,7 +64,8 @@ struct TcCfg {
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int ROWTAB_BYTES = IM2COL ? 0 : STAGES * BM * 8;  // per producer warp: 128 x {pixel, ht|wt}
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + ROWTAB_BYTES + BAR_BYTES;
+    static constexpr int STAGE_OUT_BYTES = 4 * 32 * 128;  // epilogue staging: 4 warps x 32 rows x 128 B
+    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + ROWTAB_BYTES + STAGE_OUT_BYTES + BAR_BYTES;
     static constexpr int MMA_WARP = 4 + PRODUCER_WARPS;
     static constexpr int THREADS = 32 * (MMA_WARP + 1);
 };
@@ -77,8 +78,9 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + S * Cfg::A_BYTES;
-    int2 *rowtab = reinterpret_cast<int2 *>(sB + S * Cfg::B_BYTES);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S * Cfg::B_BYTES + Cfg::ROWTAB_BYTES);
+    uint8_t *stage = sB + S * Cfg::B_BYTES;  // epilogue staging (1024-aligned)
+    int2 *rowtab = reinterpret_cast<int2 *>(stage + Cfg::STAGE_OUT_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stage + Cfg::STAGE_OUT_BYTES + Cfg::ROWTAB_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
 
@@ -317,25 +319,7 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
                 off = (((int64_t)n * g.Hi + hi) * g.Wi + wi) * g.C + (int64_t)tcd.gi * g.Cg + (int64_t)tcd.nb * BN;
             }
             const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + b * BN;
-#pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld32(tbase + cc * 32, v);
-                const int col0 = tcd.nb * BN + cc * 32;
-                if (rvalid && col0 < g.Cg) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-                        pk[e] = *reinterpret_cast<uint32_t *>(&h2);
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(dx + off + cc * 32);
-#pragma unroll
-                    for (int piece = 0; piece < 4; ++piece)
-                        if (col0 + piece * 8 < g.Cg)
-                            dst[piece] = make_uint4(pk[4 * piece], pk[4 * piece + 1], pk[4 * piece + 2], pk[4 * piece + 3]);
-                }
-            }
+            epilogue_rows<BN>(tbase, stage + warp * 4096, lane, rvalid, off, tcd.nb * BN, g.Cg, dx);
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * b);
         }
