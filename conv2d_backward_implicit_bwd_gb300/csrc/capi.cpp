@@ -310,7 +310,12 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
     // Kernel path.
     bool tc_ok = d.dtype == CONV_BWD_BF16 && d.layout == CONV_BWD_NHWC_KYXC && g.Cg % 8 == 0 && g.Kg % 8 == 0 &&
                  d.K % 8 == 0 && d.C % 8 == 0 && g.Cg >= 64 && d.Hi < 16384 && d.Wi < 16384;
-    p->path = tc_ok ? CONV_BWD_PATH_TCGEN05 : CONV_BWD_PATH_SIMT;
+    // narrow groups: memory-bound direct kernel (w staged in shared memory)
+    bool grouped_ok = d.dtype == CONV_BWD_BF16 && d.layout == CONV_BWD_NHWC_KYXC && g.Cg == g.Kg &&
+                      (g.Cg == 8 || g.Cg == 16) && g.G % 8 == 0 &&
+                      (int64_t)d.K * d.Y * d.X * g.Cg * 4 <= 160 * 1024 && d.Y * d.X <= 16 &&
+                      d.N * d.Hi * d.stride_w * (d.K / 8) < (1LL << 30);
+    p->path = tc_ok ? CONV_BWD_PATH_TCGEN05 : (grouped_ok ? CONV_BWD_PATH_GROUPED : CONV_BWD_PATH_SIMT);
     if (const char *f = env("CONVBWD_DEBUG_PATH")) {
         if (!std::strcmp(f, "simt")) p->path = CONV_BWD_PATH_SIMT;
     }
@@ -441,7 +446,9 @@ conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t
     if (path) *path = p->path;
     int gemm_launches = p->classes.empty() ? 0 : 1;
     if (p->path == CONV_BWD_PATH_TCGEN05) gemm_launches = (int)((p->classes.size() + kMaxTcClasses - 1) / kMaxTcClasses);
-    if (launches) *launches = (p->any_uncovered ? 1 : 0) + gemm_launches;
+    const bool fill = p->any_uncovered && p->path != CONV_BWD_PATH_GROUPED;  // the grouped kernel writes every pixel
+    if (p->path == CONV_BWD_PATH_GROUPED) gemm_launches = 1;
+    if (launches) *launches = (fill ? 1 : 0) + gemm_launches;
     return CONV_BWD_OK;
 }
 
@@ -463,7 +470,8 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
     if (ranges_overlap(dy, ndy, dx, ndx) || ranges_overlap(w, nw, dx, ndx)) return CONV_BWD_ERR_INVALID_ARG;
     if (((uintptr_t)dy | (uintptr_t)w | (uintptr_t)dx) % es) return CONV_BWD_ERR_MISALIGNED;
     // Every alignment rule is checked before anything is launched.
-    if (p->path == CONV_BWD_PATH_TCGEN05 && ((uintptr_t)dy | (uintptr_t)w | (uintptr_t)dx) % 16)
+    if ((p->path == CONV_BWD_PATH_TCGEN05 || p->path == CONV_BWD_PATH_GROUPED) &&
+        ((uintptr_t)dy | (uintptr_t)w | (uintptr_t)dx) % 16)
         return CONV_BWD_ERR_MISALIGNED;
     cudaStream_t s = (cudaStream_t)stream;
     std::lock_guard<std::mutex> lock(p->mu);
@@ -473,6 +481,29 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             if (!e && cudaEventCreate(&e) != cudaSuccess) return CONV_BWD_ERR_CUDA;
     }
     p->fill_ran = false;
+    if (p->path == CONV_BWD_PATH_GROUPED) {
+        GroupedParams gp;
+        std::memset(&gp, 0, sizeof(gp));
+        gp.dy = dy; gp.w = w; gp.dx = dx; gp.g = g;
+        gp.gblocks = g.G / 8;
+        // class of each row / column residue: the class t with t*d == (i + p) mod s
+        for (int q = 0; q < g.sh; ++q) gp.row_class[q] = 0;
+        for (int q = 0; q < g.sw; ++q) gp.col_class[q] = 0;
+        for (int t = 0; t < g.YT; ++t) {
+            const int taps = t < g.Y ? (g.Y - t + g.YT - 1) / g.YT : 0;
+            const int res = (int)((((int64_t)t * g.dh - g.ph) % g.sh + g.sh) % g.sh);
+            gp.row_class[res] = (taps << 16) | t;
+        }
+        for (int t = 0; t < g.XT; ++t) {
+            const int taps = t < g.X ? (g.X - t + g.XT - 1) / g.XT : 0;
+            const int res = (int)((((int64_t)t * g.dw - g.pw) % g.sw + g.sw) % g.sw);
+            gp.col_class[res] = (taps << 16) | t;
+        }
+        if (p->timing) cudaEventRecord(p->ev[2], s);
+        if (launch_grouped(gp, p->num_sms, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        if (p->timing) cudaEventRecord(p->ev[3], s);
+        return CONV_BWD_OK;
+    }
     if (p->any_uncovered) {
         FillParams fp{};
         fp.dx = dx; fp.esize = (int)es; fp.layout = d.layout;

@@ -84,6 +84,17 @@ struct TcParams {  // 128-byte aligned through CUtensorMap
     ClassDesc cls[kMaxTcClasses];
 };
 
+// Narrow-group kernel parameters (C/G = K/G in {8, 16}, G % 8 == 0).
+struct GroupedParams {
+    const void *dy;
+    const void *w;
+    void *dx;
+    Geom g;
+    int32_t gblocks;         // G / 8
+    int32_t row_class[64];   // per row residue hi % sh: (taps_y << 16) | ty (taps 0: no class writes it)
+    int32_t col_class[64];   // per column residue wi % sw: (taps_x << 16) | tx
+};
+
 // Status codes written by kernels (first writer wins).
 enum : int32_t {
     kDevOk = 0,
@@ -96,6 +107,7 @@ enum : int32_t {
 
 cudaError_t launch_fill(const FillParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_simt(const SimtParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_grouped(const GroupedParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_tc(const TcParams &p, int bn, int grid, cudaStream_t s);
 cudaError_t launch_tc2(const TcParams &p, int grid, cudaStream_t s);
 int tc2_max_pairs(int num_sms);

@@ -90,7 +90,7 @@ typedef struct conv_bwd_plan_s *conv_bwd_plan;
 typedef enum {
     CONV_BWD_PATH_TCGEN05 = 0, /* bf16 NHWC: persistent tcgen05/TMEM implicit GEMM */
     CONV_BWD_PATH_SIMT = 1,    /* fp32 (or bf16 fallback): CUDA-core tiled implicit GEMM */
-    CONV_BWD_PATH_GROUPED = 2  /* bf16 NHWC with <= 32 channels per group: direct per-pixel kernel */
+    CONV_BWD_PATH_GROUPED = 2  /* bf16 NHWC, C/G = K/G in {8, 16}, G % 8 == 0: memory-bound direct kernel */
 } conv_bwd_path;
 
 /* Validate the descriptor and plan on the host: forward output size, tilde

@@ -143,6 +143,7 @@ def test_paths(B):
     assert B.Plan.from_case(wl.case("cfg3")).path()[0] == "tcgen05"
     assert B.Plan.from_case(wl.case("cfg5a")).path()[0] == "tcgen05"
     assert B.Plan.from_case(wl.case("cfg1")).path()[0] == "simt"
+    assert B.Plan.from_case(wl.case("cfg4")).path() == ("grouped", 1)  # writes every pixel itself
     # launches per run: fill only where some pixel is uncovered
     assert B.Plan.from_case(wl.case("cfg3")).path()[1] == 1
     assert B.Plan.from_case(wl.case("cfg5a")).path()[1] == 2

@@ -110,8 +110,7 @@ def test_large_configs(B, name):
     assert np.all(np.isfinite(got)), "unwritten (NaN) outputs"
     check_full(c, got, g, dy, w, n_range=LARGE[name])
     check_points(c, got, g, dy, w, seed=zlib.crc32(name.encode()) % 1000)
-    if name != "cfg4":
-        assert plan.path()[0] == "tcgen05"
+    assert plan.path()[0] == ("grouped" if name == "cfg4" else "tcgen05")
 
 
 def _mk(name, **kw):
@@ -146,6 +145,29 @@ def test_tensor_core_path_full(B, c):
     g, dy, w = inputs(c)
     got, plan = gpu_dgrad(B, c, dy, w)
     assert plan.path()[0] == "tcgen05", plan.path()
+    check_full(c, got, g, dy, w)
+
+
+# Narrow-group path (C/G = K/G in {8, 16}, G % 32 == 0): every pixel written by
+# the kernel itself, including ones no tap reaches.
+GROUPED_CASES = [
+    _mk("grp_g32_cg8_3x3s2", N=2, C=256, K=256, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=32),
+    _mk("grp_g32_cg8_s3_uncov", N=1, C=256, K=256, Hi=10, Wi=9, Y=2, X=2, pad=(0, 1), stride=(3, 3), groups=32),
+    _mk("grp_g32_cg8_dil2", N=2, C=256, K=256, Hi=9, Wi=12, Y=3, X=3, pad=(2, 2), stride=(2, 2), dil=(2, 2), groups=32),
+    _mk("grp_g64_cg8_1x1", N=3, C=512, K=512, Hi=7, Wi=5, Y=1, X=1, stride=(1, 1), groups=64),
+    _mk("grp_g32_cg16_2x2s2", N=2, C=512, K=512, Hi=6, Wi=7, Y=2, X=2, pad=(1, 1), stride=(2, 2), groups=32),
+    _mk("grp_g32_cg8_wide_row", N=1, C=256, K=256, Hi=3, Wi=37, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=32),
+    _mk("grp_g8_cg8", N=2, C=64, K=64, Hi=9, Wi=10, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=8),
+    _mk("grp_g16_cg16_s4", N=2, C=256, K=256, Hi=11, Wi=9, Y=3, X=3, pad=(1, 1), stride=(4, 4), groups=16),
+    _mk("grp_g32_cg8_5x3_s1x2", N=1, C=256, K=256, Hi=8, Wi=13, Y=5, X=3, pad=(2, 1), stride=(1, 2), groups=32),
+]
+
+
+@pytest.mark.parametrize("c", GROUPED_CASES, ids=lambda c: c.name)
+def test_grouped_path_full(B, c):
+    g, dy, w = inputs(c)
+    got, plan = gpu_dgrad(B, c, dy, w)
+    assert plan.path() == ("grouped", 1)
     check_full(c, got, g, dy, w)
 
 
