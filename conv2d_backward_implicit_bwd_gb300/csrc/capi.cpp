@@ -446,7 +446,8 @@ conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t
     if (path) *path = p->path;
     int gemm_launches = p->classes.empty() ? 0 : 1;
     if (p->path == CONV_BWD_PATH_TCGEN05) gemm_launches = (int)((p->classes.size() + kMaxTcClasses - 1) / kMaxTcClasses);
-    const bool fill = p->any_uncovered && p->path != CONV_BWD_PATH_GROUPED;  // the grouped kernel writes every pixel
+    // the grouped kernel writes every pixel; the tensor-core kernels zero uncovered pixels themselves
+    const bool fill = p->any_uncovered && (p->path == CONV_BWD_PATH_SIMT || p->classes.empty());
     if (p->path == CONV_BWD_PATH_GROUPED) gemm_launches = 1;
     if (launches) *launches = (fill ? 1 : 0) + gemm_launches;
     return CONV_BWD_OK;
@@ -481,6 +482,7 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             if (!e && cudaEventCreate(&e) != cudaSuccess) return CONV_BWD_ERR_CUDA;
     }
     p->fill_ran = false;
+    const uint64_t all_w = g.sw >= 64 ? ~0ull : ((1ull << g.sw) - 1);
     if (p->path == CONV_BWD_PATH_GROUPED) {
         GroupedParams gp;
         std::memset(&gp, 0, sizeof(gp));
@@ -504,7 +506,9 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
         if (p->timing) cudaEventRecord(p->ev[3], s);
         return CONV_BWD_OK;
     }
-    if (p->any_uncovered) {
+    // the tensor-core kernels zero uncovered pixels themselves (epilogue warps,
+    // during the first tile's main loop); other paths use the fill kernel
+    if (p->any_uncovered && (p->path != CONV_BWD_PATH_TCGEN05 || p->classes.empty())) {
         FillParams fp{};
         fp.dx = dx; fp.esize = (int)es; fp.layout = d.layout;
         fp.N = g.N; fp.C = g.C; fp.Hi = g.Hi; fp.Wi = g.Wi; fp.sh = g.sh; fp.sw = g.sw;
@@ -539,6 +543,9 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             tp.n_tiles = (g.Cg + p->bn - 1) / p->bn;
             tp.kb_per_tap = (g.Kg + 63) / 64;
             tp.im2col = p->im2col ? 1 : 0;
+            tp.fill = (c0 == 0 && p->any_uncovered) ? 1 : 0;  // first launch zeroes the uncovered pixels
+            tp.cov_h = p->cov_h;
+            tp.cov_w = p->cov_w == all_w ? ~0ull : p->cov_w;
             const size_t nc = std::min<size_t>(kMaxTcClasses, p->sched.size() - c0);
             tp.num_classes = (int)nc;
             int64_t total = 0;

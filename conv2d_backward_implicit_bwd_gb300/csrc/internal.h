@@ -81,6 +81,8 @@ struct TcParams {  // 128-byte aligned through CUtensorMap
     int32_t kb_per_tap;   // ceil(Kg / 64)
     int32_t total_tiles;
     int32_t im2col;       // 1: A rows by TMA im2col loads (tmap_a), 0: cp.async gather
+    int32_t fill;         // 1: the epilogue warps also zero the dx pixels no class writes
+    uint64_t cov_h, cov_w;  // residues of rows / columns some class writes (as in FillParams)
     ClassDesc cls[kMaxTcClasses];
 };
 

@@ -193,6 +193,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
         __nv_bfloat16 *dx = static_cast<__nv_bfloat16 *>(p.dx);
         const uint32_t tempty_leader0 = mapa_shared(tempty0, 0);
         uint32_t tc = 0;
+        if (p.fill) fill_uncovered(p, threadIdx.x, 128);  // threads 0..127 are the epilogue warps
         for (int t = pair; t < p.total_tiles; t += npairs, ++tc) {
             const TileCoord tcd = decode_tile(p, t);
             const ClassDesc &c = p.cls[tcd.ci];

@@ -299,6 +299,33 @@ __device__ __forceinline__ void tma_load_5d_mc(uint32_t dst, const CUtensorMap *
         : "memory");
 }
 
+// Zero the dx pixels that no residue class writes (bf16 NHWC, 16-byte
+// stores), spread over the CTAs of the launch: CTA b takes dx rows b,
+// b + gridDim.x, ...; a row no class writes is one contiguous run, a written
+// row is zeroed only at its uncovered columns.  Run by a CTA's epilogue warps
+// while the first tile's main loop is still in flight.
+__device__ __forceinline__ void fill_uncovered(const TcParams &p, int tid, int nthreads) {
+    const Geom &g = p.g;
+    const uint32_t cpp = (uint32_t)g.C / 8;     // 16-byte chunks per pixel
+    const uint32_t cpr = cpp * (uint32_t)g.Wi;  // per row
+    uint4 *out = static_cast<uint4 *>(p.dx);
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t rows = (uint32_t)g.N * (uint32_t)g.Hi;
+    const bool all_cols = p.cov_w == ~0ull;
+    for (uint32_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const uint32_t hi = r % (uint32_t)g.Hi;
+        uint4 *row = out + (size_t)r * cpr;
+        if (!((p.cov_h >> (hi % (uint32_t)g.sh)) & 1ull)) {
+            for (uint32_t u = tid; u < cpr; u += nthreads) row[u] = z;
+        } else if (!all_cols) {
+            for (uint32_t u = tid; u < cpr; u += nthreads) {
+                const uint32_t wi = u / cpp;
+                if (!((p.cov_w >> (wi % (uint32_t)g.sw)) & 1ull)) row[u] = z;
+            }
+        }
+    }
+}
+
 struct TileCoord {
     int ci, mb, nb, gi;
 };

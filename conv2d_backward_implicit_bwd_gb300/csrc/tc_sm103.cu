@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
         const int row = warp * 32 + lane;  // TMEM lane = tile row
         __nv_bfloat16 *dx = static_cast<__nv_bfloat16 *>(p.dx);
         uint32_t tc = 0;
+        if (p.fill) fill_uncovered(p, threadIdx.x, 128);  // threads 0..127 are the epilogue warps
         for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++tc) {
             const TileCoord tcd = decode_tile(p, t);
             const ClassDesc &c = p.cls[tcd.ci];

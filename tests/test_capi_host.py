@@ -144,9 +144,11 @@ def test_paths(B):
     assert B.Plan.from_case(wl.case("cfg5a")).path()[0] == "tcgen05"
     assert B.Plan.from_case(wl.case("cfg1")).path()[0] == "simt"
     assert B.Plan.from_case(wl.case("cfg4")).path() == ("grouped", 1)  # writes every pixel itself
-    # launches per run: fill only where some pixel is uncovered
+    # launches per run: the tensor-core kernel zeroes uncovered pixels itself
     assert B.Plan.from_case(wl.case("cfg3")).path()[1] == 1
-    assert B.Plan.from_case(wl.case("cfg5a")).path()[1] == 2
+    assert B.Plan.from_case(wl.case("cfg5a")).path()[1] == 1
+    # the CUDA-core path launches the fill kernel where some pixel is uncovered
+    assert B.Plan(1, 4, 4, 9, 9, 1, 1, stride=(2, 2)).path() == ("simt", 2)
 
 
 @pytest.mark.parametrize("kw,status", [

@@ -276,6 +276,7 @@ def test_bounded_wait_gives_up_and_context_survives(B):
 
 
 def test_per_kernel_timing(B):
+    # tensor-core path: one launch (uncovered pixels are zeroed inside it)
     c = wl.case("cfg5a")
     plan = B.Plan.from_case(c)
     dy_s, w_s, dx_s = plan.shapes()
@@ -285,4 +286,12 @@ def test_per_kernel_timing(B):
     plan.set_timing(True)
     plan.run(dy, w, dx)
     f, m = plan.last_timing()
+    assert f == 0 and m > 0
+    # CUDA-core path with uncovered pixels: fill kernel + sub-GEMM kernel
+    p2 = B.Plan(2, 16, 16, 15, 15, 1, 1, stride=(2, 2))
+    assert p2.path() == ("simt", 2)
+    dy_s, w_s, dx_s = p2.shapes()
+    p2.set_timing(True)
+    p2.run(torch.zeros(dy_s, device="cuda"), torch.zeros(w_s, device="cuda"), torch.empty(dx_s, device="cuda"))
+    f, m = p2.last_timing()
     assert f > 0 and m > 0
