@@ -54,6 +54,10 @@ struct conv_bwd_plan_s {
     std::vector<CUtensorMap> tmap_a;      // per class (gemm_id order)
     bool im2col = false;                  // A rows by TMA im2col loads (else cp.async gather)
     bool two_sm = false;                  // 256x256 tiles on SM pairs (cta_group::2)
+    int max_pairs = 0;                    // co-resident SM pairs of the 2-SM kernel
+    float4 *d_partials = nullptr;         // stream-K workspace: per pair and CTA, one 128x256 fp32 tile
+    int32_t *d_flags = nullptr;           // stream-K flags, tagged with the launch epoch
+    int32_t epoch = 0;
     std::mutex mu;
 };
 
@@ -378,6 +382,20 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                 return CONV_BWD_ERR_CUDA;
             }
             p->has_device = true;
+            if (p->two_sm) {
+                // stream-K workspace (used when whole tiles would leave SM pairs idle)
+                p->max_pairs = tc2_max_pairs(p->num_sms);
+                const size_t slots = (size_t)p->max_pairs * 2;
+                if (cudaMalloc(&p->d_partials, slots * 128 * 64 * sizeof(float4)) != cudaSuccess ||
+                    cudaMalloc(&p->d_flags, slots * sizeof(int32_t)) != cudaSuccess ||
+                    cudaMemset(p->d_flags, 0, slots * sizeof(int32_t)) != cudaSuccess) {
+                    cudaGetLastError();
+                    cudaFree(p->d_partials);
+                    cudaFree(p->d_flags);
+                    p->d_partials = nullptr;
+                    p->d_flags = nullptr;
+                }
+            }
         } else {
             p->owns_status = false;  // run() becomes possible once a status word is attached
         }
@@ -399,6 +417,8 @@ conv_bwd_status conv_bwd_data_destroy(conv_bwd_plan p) {
         cudaGetDevice(&cur);
         if (cur != p->device) cudaSetDevice(p->device);
         if (p->owns_status) cudaFree(p->d_status);
+        cudaFree(p->d_partials);
+        cudaFree(p->d_flags);
         for (auto &e : p->ev)
             if (e) cudaEventDestroy(e);
         if (cur != p->device && cur >= 0) cudaSetDevice(cur);
@@ -544,21 +564,44 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             tp.kb_per_tap = (g.Kg + 63) / 64;
             tp.im2col = p->im2col ? 1 : 0;
             tp.fill = (c0 == 0 && p->any_uncovered) ? 1 : 0;  // first launch zeroes the uncovered pixels
+            if (const char *f = env("CONVBWD_DEBUG_RASTER_M")) tp.raster_m = f[0] == '1' ? 1 : 0;
             tp.cov_h = p->cov_h;
             tp.cov_w = p->cov_w == all_w ? ~0ull : p->cov_w;
             const size_t nc = std::min<size_t>(kMaxTcClasses, p->sched.size() - c0);
             tp.num_classes = (int)nc;
             int64_t total = 0;
+            int64_t units = 0;
             for (size_t i = 0; i < nc; ++i) {
                 const int idx = p->sched[c0 + i];
                 tp.cls[i] = p->classes[(size_t)idx];
                 tp.cls[i].tile_begin = (int)total;
-                total += (int64_t)g.G * tp.cls[i].m_tiles * tp.n_tiles;
+                tp.cls[i].unit_begin = (int)units;
+                const int64_t tiles_c = (int64_t)g.G * tp.cls[i].m_tiles * tp.n_tiles;
+                total += tiles_c;
+                units += tiles_c * tp.cls[i].taps_y * tp.cls[i].taps_x * tp.kb_per_tap;
                 if (p->im2col) tp.tmap_a[i] = p->tmap_a[(size_t)idx];
             }
             tp.total_tiles = (int)total;
+            tp.units_total = (int)std::min<int64_t>(units, 0x7fffffff);
             if (p->two_sm) {
-                const int pairs = (int)std::min<int64_t>(total, tc2_max_pairs(p->num_sms));
+                const int maxp = tc2_max_pairs(p->num_sms);
+                int pairs = (int)std::min<int64_t>(total, maxp);
+                // Stream-K (equal unit ranges per pair, partial tiles through the
+                // workspace) is opt-in: on GB300 the partial-tile traffic costs about
+                // what the better balance saves on the shapes measured here.
+                bool sk = false;
+                if (const char *f = env("CONVBWD_DEBUG_STREAMK"))
+                    sk = p->d_partials && f[0] == '1' && units < 0x7fffffff && maxp <= p->max_pairs;
+                if (sk) {
+                    // every worker gets at least one unit: a worker without units would
+                    // never raise the flag its tile's owner waits for
+                    pairs = (int)std::min<int64_t>(maxp, units);
+                    tp.streamk = 1;
+                    tp.partials = p->d_partials;
+                    tp.flags = p->d_flags;
+                    p->epoch = p->epoch >= 0x7ffffffe ? 1 : p->epoch + 1;
+                    tp.epoch = p->epoch;
+                }
                 if (launch_tc2(tp, 2 * pairs, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
                 continue;
             }

@@ -29,6 +29,7 @@ struct ClassDesc {
     int32_t m_tiles;         // ceil(M / BM) for the kernel that runs this class
     int32_t tile_begin;      // first tile of this class in the launch's schedule
     int32_t gemm_id;         // consecutive id of the sub-GEMM
+    int32_t unit_begin;      // first (tile, k-block) unit of this class in the launch (stream-K)
 };
 
 struct Geom {
@@ -82,6 +83,12 @@ struct TcParams {  // 128-byte aligned through CUtensorMap
     int32_t total_tiles;
     int32_t im2col;       // 1: A rows by TMA im2col loads (tmap_a), 0: cp.async gather
     int32_t fill;         // 1: the epilogue warps also zero the dx pixels no class writes
+    int32_t raster_m;     // 1: consecutive tiles walk m-blocks first (else n-blocks first)
+    int32_t streamk;      // 1: workers take equal ranges of (tile, k-block) units (2-SM kernel)
+    int32_t units_total;  // sum over tiles of their k-blocks
+    int32_t epoch;        // tag of this launch's partial-tile flags (never 0)
+    float4 *partials;     // stream-K: per worker and CTA rank, one 128 x 256 fp32 partial tile
+    int32_t *flags;       // stream-K: per worker and CTA rank, == epoch once its partial is written
     uint64_t cov_h, cov_w;  // residues of rows / columns some class writes (as in FillParams)
     ClassDesc cls[kMaxTcClasses];
 };
@@ -104,6 +111,7 @@ enum : int32_t {
     kDevTimeoutMma = 0x102,
     kDevTimeoutEpilogue = 0x103,
     kDevTimeoutSelftest = 0x1FF,
+    kDevTimeoutPartial = 0x104,
     kDevFaultIndex = 0x201,
 };
 

@@ -35,12 +35,11 @@ struct Tc2Cfg {
     static constexpr int BN = 256;          // tile width of the pair (= MMA N)
     static constexpr int BNH = 128;         // columns of B held by each CTA
     static constexpr int STAGES = 6;
-    static constexpr bool STAGED_EPILOGUE = true;  // coalesce dx stores through shared memory
     static constexpr int A_BYTES = 128 * 64 * 2;
     static constexpr int B_BYTES = BNH * 64 * 2;
     static constexpr int TMEM_COLS = 2 * BN;  // double-buffered 256-column accumulator
     static constexpr int BAR_BYTES = 256;
-    static constexpr int STAGE_OUT_BYTES = STAGED_EPILOGUE ? 4 * 32 * 128 : 0;  // 4 warps x 32 rows x 128 B
+    static constexpr int STAGE_OUT_BYTES = 4 * 32 * 128;  // epilogue staging: 4 warps x 32 rows x 128 B
     static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + STAGE_OUT_BYTES + BAR_BYTES;
     static constexpr int MMA_WARP = 5;
     static constexpr int THREADS = 192;
@@ -106,17 +105,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
             const uint32_t full_leader0 = mapa_shared(full0, 0);
             uint32_t it = 0;
             bool ok = true, issued = false;
-            for (int t = pair; t < p.total_tiles && ok; t += npairs) {
-                const TileCoord tcd = decode_tile(p, t);
+            SegmentIter segs(p, pair, npairs);
+            Segment sg;
+            while (ok && segs.next(p, sg)) {
+                const TileCoord tcd = decode_tile(p, sg.t);
                 const ClassDesc &c = p.cls[tcd.ci];
-                const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
                 const int HTWT = c.HT * c.WT;
                 const int m0 = tcd.mb * 256 + (int)rank * 128;
                 const int n0 = m0 / HTWT, rem = m0 - n0 * HTWT;
                 const int bh = c.ht_lo + rem / c.WT - (c.taps_y - 1) * g.DH;
                 const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
                 const CUtensorMap *amap = &p.tmap_a[tcd.ci];
-                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const int tap = kb / p.kb_per_tap;
                     const int k0 = (kb - tap * p.kb_per_tap) * 64;
                     const int j = tap / c.taps_x, i = tap - j * c.taps_x;
@@ -149,10 +149,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
             constexpr uint32_t idesc = idesc_bf16<BN, 256>();
             uint32_t it = 0, tc = 0;
             bool ok = true, issued = false;
-            for (int t = pair; t < p.total_tiles && ok; t += npairs, ++tc) {
-                const TileCoord tcd = decode_tile(p, t);
-                const ClassDesc &c = p.cls[tcd.ci];
-                const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
+            SegmentIter segs(p, pair, npairs);
+            Segment sg;
+            for (; ok && segs.next(p, sg); ++tc) {
                 const uint32_t b = tc & 1, tph = (tc >> 1) & 1;
                 if (!mbar_wait_bounded(tempty0 + 8 * b, tph ^ 1, p.wait_budget, abort_flag, p.status,
                                        kDevTimeoutMma)) {
@@ -161,7 +160,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * BN;
-                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const uint32_t s = it % S, ph = (it / S) & 1;
                     if (!mbar_wait_bounded(full0 + 8 * s, ph, p.wait_budget, abort_flag, p.status, kDevTimeoutMma)) {
                         ok = false;
@@ -174,7 +173,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
                         const uint64_t bd = smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
-                        tc_mma2(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma2(d_tmem, ad, bd, idesc, (kb != sg.kb0 || kk != 0) ? 1u : 0u);
                     }
                     issued = true;
                     tc_commit2_mc(empty0 + 8 * s, (uint16_t)0x3);
@@ -194,13 +193,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
         const uint32_t tempty_leader0 = mapa_shared(tempty0, 0);
         uint32_t tc = 0;
         if (p.fill) fill_uncovered(p, threadIdx.x, 128);  // threads 0..127 are the epilogue warps
-        for (int t = pair; t < p.total_tiles; t += npairs, ++tc) {
-            const TileCoord tcd = decode_tile(p, t);
+        SegmentIter segs(p, pair, npairs);
+        Segment sg;
+        const size_t slot_f4 = (size_t)(BN / 4) * 128;  // one CTA's 128 x BN fp32 partial, in float4
+        for (; segs.next(p, sg); ++tc) {
+            const TileCoord tcd = decode_tile(p, sg.t);
             const ClassDesc &c = p.cls[tcd.ci];
             const uint32_t b = tc & 1, tph = (tc >> 1) & 1;
             bool ok = mbar_wait_bounded(tfull0 + 8 * b, tph, p.wait_budget, abort_flag, p.status, kDevTimeoutEpilogue);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + b * BN;
+            if (!sg.owner) {
+                // stream-K contributor: park the fp32 partial, then raise this CTA's flag
+                store_partial_rows<BN>(tbase, row, p.partials + (size_t)(pair * 2 + rank) * slot_f4);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);
+                __threadfence();
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (threadIdx.x == 0) st_release_gpu(p.flags + pair * 2 + rank, p.epoch);
+                continue;
+            }
             const int m = tcd.mb * 256 + (int)rank * 128 + row;
             const bool rvalid = m < c.M;
             int64_t off = 0;
@@ -212,11 +226,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
                 const int wi = (c.wt_lo + rem % c.WT) * g.sw + c.tx * g.dw - g.pw;
                 off = (((int64_t)n * g.Hi + hi) * g.Wi + wi) * g.C + (int64_t)tcd.gi * g.Cg + (int64_t)tcd.nb * BN;
             }
-            const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + b * BN;
-            if (Cfg::STAGED_EPILOGUE)
-                epilogue_rows<BN>(tbase, stage + warp * 4096, lane, rvalid, off, tcd.nb * BN, g.Cg, dx);
-            else
-                epilogue_rows_direct<BN>(tbase, lane, rvalid, off, tcd.nb * BN, g.Cg, dx);
+            const int nparts = pair - sg.q_first;
+            if (nparts > 0) {
+                // partials of the earlier stretches of this tile (bounded wait per worker)
+                for (int q = sg.q_first; q < pair; ++q) {
+                    const int32_t *f = p.flags + q * 2 + rank;
+                    const long long t0 = clock64();
+                    while (ld_acquire_gpu(f) != p.epoch) {
+                        if (clock64() - t0 > p.wait_budget) {
+                            record_status(p.status, kDevTimeoutPartial);
+                            break;
+                        }
+                    }
+                }
+            }
+            const float4 *parts = nparts > 0 ? p.partials + (size_t)(sg.q_first * 2 + rank) * slot_f4 : nullptr;
+            epilogue_rows<BN>(tbase, stage + warp * 4096, lane, rvalid, off, tcd.nb * BN, g.Cg, dx, parts, nparts,
+                              2 * slot_f4, row);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);

@@ -147,9 +147,13 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64]) {
 // 128-byte row segments instead of 32 scattered 16-byte pieces.  `off` is the
 // dx element offset of this thread's row at the tile's first channel, `col0`
 // that channel's index within the group; channels >= Cg are not written.
+// With `parts` set, the fp32 partial tiles of `nparts` stream-K workers
+// (slots `pstride` float4 apart, layout [64 column chunks of 4][128 rows],
+// this thread's row `prow`) are added before rounding.
 template <int BN>
 __device__ __forceinline__ void epilogue_rows(uint32_t taddr, uint8_t *stage, int lane, bool rvalid, int64_t off,
-                                              int col0, int Cg, __nv_bfloat16 *dx) {
+                                              int col0, int Cg, __nv_bfloat16 *dx, const float4 *parts = nullptr,
+                                              int nparts = 0, size_t pstride = 0, int prow = 0) {
     const uint32_t sbase = smem_u32(stage);
     int64_t roff[8];
     bool rok[8];
@@ -166,6 +170,17 @@ __device__ __forceinline__ void epilogue_rows(uint32_t taddr, uint8_t *stage, in
     for (int cc = 0; cc < BN / 64; ++cc) {
         uint32_t v[64];
         tmem_ld64(taddr + cc * 64, v);
+        for (int w = 0; w < nparts; ++w) {
+            const float4 *pp = parts + (size_t)w * pstride + (size_t)(cc * 16) * 128 + prow;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 a = pp[(size_t)i * 128];
+                v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + a.x);
+                v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + a.y);
+                v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + a.z);
+                v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + a.w);
+            }
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             uint32_t pk[4];
@@ -197,31 +212,29 @@ __device__ __forceinline__ void epilogue_rows(uint32_t taddr, uint8_t *stage, in
     }
 }
 
-// Same as epilogue_rows without shared-memory staging: each thread stores
-// its own row, 16 bytes at a time.
+// Stream-K contributor: this thread's accumulator row -> fp32 partial slot
+// (layout [64 column chunks of 4][128 rows]: a warp writes 512 contiguous bytes).
 template <int BN>
-__device__ __forceinline__ void epilogue_rows_direct(uint32_t taddr, int lane, bool rvalid, int64_t off, int col0,
-                                                     int Cg, __nv_bfloat16 *dx) {
-    (void)lane;
+__device__ __forceinline__ void store_partial_rows(uint32_t taddr, int prow, float4 *slot) {
 #pragma unroll 1
     for (int cc = 0; cc < BN / 64; ++cc) {
         uint32_t v[64];
         tmem_ld64(taddr + cc * 64, v);
-        if (!rvalid) continue;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int col = col0 + cc * 64 + q * 8;
-            if (col >= Cg) break;
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]),
-                                                          __uint_as_float(v[8 * q + 2 * e + 1]));
-                pk[e] = *reinterpret_cast<uint32_t *>(&h2);
-            }
-            *reinterpret_cast<uint4 *>(dx + off + cc * 64 + q * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
+        for (int i = 0; i < 16; ++i)
+            slot[(size_t)(cc * 16 + i) * 128 + prow] =
+                make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                            __uint_as_float(v[4 * i + 3]));
     }
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int32_t *p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ---- clusters and SM pairs (tcgen05 cta_group::2) -------------------------
@@ -326,6 +339,70 @@ __device__ __forceinline__ void fill_uncovered(const TcParams &p, int tid, int n
     }
 }
 
+// A stretch [kb0, kb1) of the k-blocks of tile t handled by one worker (CTA or
+// SM pair).  `owner`: the stretch ends the tile, so this worker stores the
+// tile, first adding the partial tiles of workers q_first .. self-1 (stream-K).
+struct Segment {
+    int t, kb0, kb1;
+    bool owner;
+    int q_first;
+};
+
+__device__ __forceinline__ int class_of_tile(const TcParams &p, int t) {
+    int ci = 0;
+    for (int i = 1; i < p.num_classes; ++i)
+        if (t >= p.cls[i].tile_begin) ci = i;
+    return ci;
+}
+
+// Work of worker w of nw.  Static schedule: whole tiles w, w + nw, ...
+// Stream-K: the units [w*U/nw, (w+1)*U/nw) of the (tile, k-block) sequence,
+// visited from the last stretch to the first, so a worker's only partial
+// stretch (the one that does not reach its tile's end) comes first and the
+// stretch it owns after earlier workers' partials comes last.
+struct SegmentIter {
+    int w, nw, next_t, u, u_lo;
+    __device__ __forceinline__ SegmentIter(const TcParams &p, int w_, int nw_) : w(w_), nw(nw_), next_t(w_) {
+        u_lo = (int)((int64_t)w * p.units_total / nw);
+        u = (int)((int64_t)(w + 1) * p.units_total / nw);
+    }
+    __device__ __forceinline__ int nkb(const TcParams &p, int ci) const {
+        return p.cls[ci].taps_y * p.cls[ci].taps_x * p.kb_per_tap;
+    }
+    __device__ __forceinline__ bool next(const TcParams &p, Segment &sg) {
+        if (!p.streamk) {
+            if (next_t >= p.total_tiles) return false;
+            sg.t = next_t;
+            sg.kb0 = 0;
+            sg.kb1 = nkb(p, class_of_tile(p, next_t));
+            sg.owner = true;
+            sg.q_first = w;
+            next_t += nw;
+            return true;
+        }
+        if (u <= u_lo) return false;
+        const int last = u - 1;
+        int ci = 0;
+        for (int i = 1; i < p.num_classes; ++i)
+            if (last >= p.cls[i].unit_begin) ci = i;
+        const ClassDesc &c = p.cls[ci];
+        const int n = nkb(p, ci);
+        const int tl = (last - c.unit_begin) / n;
+        const int ts = c.unit_begin + tl * n, te = ts + n;
+        const int s0 = u_lo > ts ? u_lo : ts;
+        sg.t = c.tile_begin + tl;
+        sg.kb0 = s0 - ts;
+        sg.kb1 = u - ts;
+        sg.owner = u == te;
+        int q = w;
+        if (sg.owner && s0 > ts)
+            while (q > 0 && (int)((int64_t)q * p.units_total / nw) > ts) --q;  // u_hi(q-1) > ts
+        sg.q_first = q;
+        u = s0;
+        return true;
+    }
+};
+
 struct TileCoord {
     int ci, mb, nb, gi;
 };
@@ -338,10 +415,17 @@ __device__ __forceinline__ TileCoord decode_tile(const TcParams &p, int t) {
     int local = t - c.tile_begin;
     TileCoord r;
     r.ci = ci;
-    r.nb = local % p.n_tiles;
-    int rest = local / p.n_tiles;
-    r.mb = rest % c.m_tiles;
-    r.gi = rest / c.m_tiles;
+    if (p.raster_m) {
+        r.mb = local % c.m_tiles;
+        int rest = local / c.m_tiles;
+        r.nb = rest % p.n_tiles;
+        r.gi = rest / p.n_tiles;
+    } else {
+        r.nb = local % p.n_tiles;
+        int rest = local / p.n_tiles;
+        r.mb = rest % c.m_tiles;
+        r.gi = rest / c.m_tiles;
+    }
     return r;
 }
 

@@ -28,7 +28,9 @@
  *
  * Memory ownership.  The caller owns dy, w, dx and the stream (any
  * allocator; PyTorch in the bundled binding).  The library owns the plan
- * (host memory) and one 16-byte device status word per plan, allocated by
+ * (host memory), one 16-byte device status word per plan and, for bf16
+ * problems that run on SM pairs, a stream-K scratch of 256 KB per pair (fp32
+ * partial tiles and flags, ~19 MB on 152 SMs), all allocated by
  * conv_bwd_data_create when a CUDA device is present.  conv_bwd_data_run
  * allocates nothing, never synchronises and is ordered on the given stream.
  *
@@ -140,8 +142,11 @@ conv_bwd_status conv_bwd_data_work(const conv_bwd_plan plan, double *useful_flop
 
 /* Compute dx from dy and w on `stream` (a cudaStream_t; NULL = legacy
  * default stream).  dy, w, dx are device pointers in the plan's layout and
- * dtype; they must not overlap.  Asynchronous: returns after enqueueing the
- * fill kernel (only if some pixel is uncovered) and one sub-GEMM kernel.
+ * dtype; they must not overlap.  Asynchronous: returns after enqueueing one
+ * kernel (the CUDA-core path adds a fill kernel where some pixel is
+ * uncovered).  Runs of one plan must not overlap on the GPU: the plan's
+ * status word and, for wide bf16 problems, its work-splitting scratch
+ * (allocated by conv_bwd_data_create) are shared by its runs.
  * Errors: INVALID_ARG (null or overlapping pointers), MISALIGNED (bf16 NHWC
  * tensor-core path needs 16-byte aligned dy, w, dx), CUDA (launch failure or
  * plan created without a device). */

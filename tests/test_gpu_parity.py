@@ -223,6 +223,35 @@ def test_cp_async_producer_variant(B, monkeypatch, idx):
     check_full(c, got, g, dy, w)
 
 
+SK_CASES = [
+    _mk("sk_page3_small", N=2, C=256, K=256, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)),
+    _mk("sk_one_tile_deep_k", N=1, C=256, K=2048, Hi=16, Wi=16, Y=1, X=1),          # 32 units over many pairs
+    _mk("sk_multiclass", N=2, C=512, K=192, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2)),
+    _mk("sk_ragged_n", N=3, C=264, K=64, Hi=6, Wi=7, Y=3, X=3, pad=(1, 1)),
+    _mk("sk_dil2_fill", N=4, C=256, K=256, Hi=12, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)),
+]
+
+
+@pytest.mark.parametrize("forced", ["1", "0"])
+@pytest.mark.parametrize("c", SK_CASES, ids=lambda c: c.name)
+def test_stream_k_and_whole_tiles(B, monkeypatch, c, forced):
+    """The 2-SM kernel with stream-K (units split across SM pairs, partial
+    tiles added by the owning pair) and with whole tiles; each run twice so
+    the second launch's flags carry a new epoch."""
+    g, dy, w = inputs(c)
+    monkeypatch.setenv("CONVBWD_DEBUG_STREAMK", forced)
+    plan = B.Plan.from_case(c)
+    assert plan.path()[0] == "tcgen05"
+    dy_s, w_s, dx_s = plan.shapes()
+    dyd, wd = to_dev(dy, c.dtype), to_dev(w, c.dtype)
+    for _ in range(2):
+        dx = torch.full(dx_s, float("nan"), dtype=torch.bfloat16, device="cuda")
+        plan.run(dyd, wd, dx)
+        st, det = plan.status()
+        assert st == B.OK, (B.status_string(st), hex(det))
+        check_full(c, dx.float().cpu().numpy().astype(np.float64), g, dy, w)
+
+
 def test_deterministic_and_stream_ordered(B):
     c = TC_CASES[4]
     g, dy, w = inputs(c)
