@@ -337,10 +337,27 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
             if (lo[q] < -128 || lo[q] > 127 || hi[q] < -128 || hi[q] > 127) p->im2col = false;
     }
     if (const char *f = env("CONVBWD_DEBUG_NOIM2COL")) p->im2col = p->im2col && f[0] == '0';
-    // 256 x 256 tiles on SM pairs (tcgen05 cta_group::2) where the tile is wide
-    // enough: each SM then loads only half of B.
-    p->two_sm = p->path == CONV_BWD_PATH_TCGEN05 && p->im2col && p->bn == 256;
+    // 256-row tiles on SM pairs (tcgen05 cta_group::2): each SM then loads only
+    // half of B.  Tile width 256, or 128 where 256-wide tiles would leave most
+    // SM pairs without a tile.
+    p->two_sm = p->path == CONV_BWD_PATH_TCGEN05 && p->im2col && g.Cg >= 256;  // (C/G < 256: 1-SM tiles measured faster)
     if (const char *f = env("CONVBWD_DEBUG_NO2SM")) p->two_sm = p->two_sm && f[0] == '0';
+    if (p->two_sm) {
+        int64_t tiles256 = 0, tiles128 = 0;
+        for (const ClassDesc &c : p->classes) {
+            const int64_t mt = (c.M + 255) / 256;
+            tiles256 += (int64_t)g.G * mt * ((g.Cg + 255) / 256);
+            tiles128 += (int64_t)g.G * mt * ((g.Cg + 127) / 128);
+        }
+        int sms = 0, dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaGetLastError();
+        const int64_t pairs = sms > 0 ? sms / 2 : 74;
+        p->bn = tiles256 * 2 >= pairs ? 256 : 128;
+        (void)tiles128;
+    }
+    if (const char *f = env("CONVBWD_DEBUG_BN"))
+        if (p->path == CONV_BWD_PATH_TCGEN05 && (!std::strcmp(f, "128") || !std::strcmp(f, "256"))) p->bn = std::atoi(f);
 
     // Schedule: classes with the longest reduction first (LPT), tiles of one
     // class contiguous; BM = 256 rows on SM pairs, 128 for the 1-SM
@@ -602,7 +619,7 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
                     p->epoch = p->epoch >= 0x7ffffffe ? 1 : p->epoch + 1;
                     tp.epoch = p->epoch;
                 }
-                if (launch_tc2(tp, 2 * pairs, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+                if (launch_tc2(tp, p->bn, 2 * pairs, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
                 continue;
             }
             int grid = (int)std::min<int64_t>(total, p->num_sms);

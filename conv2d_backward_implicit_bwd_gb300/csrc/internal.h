@@ -119,7 +119,7 @@ cudaError_t launch_fill(const FillParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_simt(const SimtParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_grouped(const GroupedParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_tc(const TcParams &p, int bn, int grid, cudaStream_t s);
-cudaError_t launch_tc2(const TcParams &p, int grid, cudaStream_t s);
+cudaError_t launch_tc2(const TcParams &p, int bn, int grid, cudaStream_t s);
 int tc2_max_pairs(int num_sms);
 cudaError_t launch_selftest_wait(int32_t *status, int64_t budget, cudaStream_t s);
 size_t tc_smem_bytes(int bn, bool im2col);

@@ -2,14 +2,14 @@
 //
 // Same sub-GEMMs as tc_sm103.cu (one per filter-tap residue class and group,
 // the v4r1 backward-data split of pages "Backward data" and "[igemm_dynamic]
-// v4r1 bwd dynamic kernel"), but each output tile is 256 (m) x 256 (c) and is
-// computed by a cluster of two CTAs on two SMs:
+// v4r1 bwd dynamic kernel"), but each output tile is 256 (m) x BN (c), BN in
+// {256, 128}, and is computed by a cluster of two CTAs on two SMs:
 //   * CTA rank r of the pair loads the tile's A rows [128r, 128r+128) (TMA
 //     im2col, one map per class, exactly as in the 1-SM kernel) and the B
-//     columns [128r, 128r+128) (two TMA boxes of 64 k x 64 c) into its own
+//     columns [r*BN/2, (r+1)*BN/2) (TMA boxes of 64 k x 64 c) into its own
 //     shared memory.  Both CTAs' loads complete on the leader's (rank 0)
 //     stage barrier (`.cta_group::2` TMA), which expects the bytes of both.
-//   * The leader's single MMA thread issues M=256, N=256, K=16
+//   * The leader's single MMA thread issues M=256, N=BN, K=16
 //     `tcgen05.mma.cta_group::2` instructions that read A and B from both
 //     CTAs' shared memory and accumulate rows [128r, 128r+128) in CTA r's
 //     TMEM; each stage is committed back to both CTAs' empty barriers and each
@@ -31,23 +31,25 @@
 
 namespace cbd {
 
+template <int BN_>
 struct Tc2Cfg {
-    static constexpr int BN = 256;          // tile width of the pair (= MMA N)
-    static constexpr int BNH = 128;         // columns of B held by each CTA
-    static constexpr int STAGES = 6;
+    static constexpr int BN = BN_;          // tile width of the pair (= MMA N): 256 or 128
+    static constexpr int BNH = BN / 2;      // columns of B held by each CTA
+    static constexpr int STAGES = BN == 256 ? 6 : 8;
     static constexpr int A_BYTES = 128 * 64 * 2;
     static constexpr int B_BYTES = BNH * 64 * 2;
-    static constexpr int TMEM_COLS = 2 * BN;  // double-buffered 256-column accumulator
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int TMEM_COLS = 2 * BN;  // double-buffered accumulator
     static constexpr int STAGE_OUT_BYTES = 4 * 32 * 128;  // epilogue staging: 4 warps x 32 rows x 128 B
+    static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + STAGE_OUT_BYTES + BAR_BYTES;
     static constexpr int MMA_WARP = 5;
     static constexpr int THREADS = 192;
 };
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
+template <int BN_>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS, 1)
     tc2_dgrad_kernel(const __grid_constant__ TcParams p) {
-    using Cfg = Tc2Cfg;
+    using Cfg = Tc2Cfg<BN_>;
     constexpr int S = Cfg::STAGES;
     constexpr int BN = Cfg::BN;
     extern __shared__ uint8_t smem_raw[];
@@ -257,18 +259,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg::THREADS, 1)
     }
 }
 
-cudaError_t launch_tc2(const TcParams &p, int grid, cudaStream_t s) {
-    if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
+template <int BN>
+static cudaError_t launch_tc2_bn(const TcParams &p, int grid, cudaStream_t s) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc2_dgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Cfg::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(tc2_dgrad_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Tc2Cfg<BN>::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    tc2_dgrad_kernel<<<grid, Tc2Cfg::THREADS, Tc2Cfg::SMEM, s>>>(p);
+    tc2_dgrad_kernel<BN><<<grid, Tc2Cfg<BN>::THREADS, Tc2Cfg<BN>::SMEM, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_tc2(const TcParams &p, int bn, int grid, cudaStream_t s) {
+    if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
+    return bn == 256 ? launch_tc2_bn<256>(p, grid, s) : launch_tc2_bn<128>(p, grid, s);
 }
 
 int tc2_max_pairs(int num_sms) {
@@ -276,11 +284,11 @@ int tc2_max_pairs(int num_sms) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-    cudaFuncSetAttribute(tc2_dgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Cfg::SMEM);
+    cudaFuncSetAttribute(tc2_dgrad_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Cfg<256>::SMEM);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
-    cfg.blockDim = dim3(Tc2Cfg::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Tc2Cfg::SMEM;
+    cfg.blockDim = dim3(Tc2Cfg<256>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Tc2Cfg<256>::SMEM;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
@@ -289,7 +297,7 @@ int tc2_max_pairs(int num_sms) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, tc2_dgrad_kernel, &cfg) != cudaSuccess || clusters <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, tc2_dgrad_kernel<256>, &cfg) != cudaSuccess || clusters <= 0) {
         cudaGetLastError();
         clusters = num_sms / 2;
     }
