@@ -36,12 +36,21 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 # DRAM traffic of the tensor-core kernel per launch on this workload, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), valid only for
 # the kernel source whose sha256 is recorded with it.
-TRAFFIC = {}
+TRAFFIC = {
+    # ncu --set full, tc2_dgrad_kernel<256>, one launch on the page-3 shape:
+    # dram__bytes_read.sum 33.63 MB + dram__bytes_write.sum 1.76 MB
+    "cfg3_bf16_16x1x512x2048_1x2_s1x2": {"sha": "c00d37e8f6ae509e", "bytes": 35.39e6},
+    # grouped_dgrad_kernel<8, 2> on the 64x56x56x256 G=32 layer: 25.79 MB + 44.48 MB
+    "cfg4_bf16_resnext_64x56x56x256_g32_3x3_s2": {"sha": "c00d37e8f6ae509e", "bytes": 70.27e6},
+}
 
 
 def kernel_sha() -> str:
-    p = os.path.join(ROOT, "conv2d_backward_implicit_bwd_gb300", "csrc", "tc_sm103.cu")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    """Hash of the sources that define the tensor-core kernels' behaviour."""
+    h = hashlib.sha256()
+    for f in ("tc_common.cuh", "tc2_sm103.cu", "tc_sm103.cu", "grouped.cu"):
+        h.update(open(os.path.join(ROOT, "conv2d_backward_implicit_bwd_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def load_peaks():
