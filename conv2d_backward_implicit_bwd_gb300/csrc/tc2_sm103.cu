@@ -43,7 +43,14 @@ struct Tc2Cfg {
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + STAGE_OUT_BYTES + BAR_BYTES;
     static constexpr int MMA_WARP = 5;
-    static constexpr int THREADS = 192;
+    // TMA issue is serialised per issuing thread (~70 SM clocks per tile-mode
+    // load, more for an im2col load), so the loads of a stage are spread over
+    // warps on different SM sub-partitions: warp 4 issues A, warps 6, 7 one
+    // 64-column B box each
+    static constexpr bool SPLIT_PRODUCER = true;
+    static constexpr int B_WARP = 6;                  // first B warp; BNH / 64 of them
+    static constexpr int B_WARPS = SPLIT_PRODUCER ? BNH / 64 : 0;
+    static constexpr int THREADS = 32 * (6 + B_WARPS);
 };
 
 template <int BN_>
@@ -101,8 +108,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
             record_status(p.status, kDevFaultIndex);
     }
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ producer
+    if (warp == 4 || (Cfg::SPLIT_PRODUCER && warp >= Cfg::B_WARP)) {
+        // ------------------------------------------------------------ producer(s)
+        const bool do_a = warp == 4;  // A loads + the stage's byte count
+        // B boxes of this warp: all of them (single producer) or box warp - B_WARP
+        const int cb_lo = Cfg::SPLIT_PRODUCER ? (warp == 4 ? 0 : warp - Cfg::B_WARP) : 0;
+        const int cb_hi = Cfg::SPLIT_PRODUCER ? (warp == 4 ? 0 : cb_lo + 1) : Cfg::BNH / 64;
         if (lane == 0) {
             const uint32_t full_leader0 = mapa_shared(full0, 0);
             uint32_t it = 0;
@@ -129,12 +140,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                         break;
                     }
                     const uint32_t bar = full_leader0 + 8 * s;
-                    if (leader) mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(2 * (Cfg::A_BYTES + Cfg::B_BYTES)));
-                    tma_load_im2col_pair(smem_u32(sA + s * Cfg::A_BYTES), amap, bar, tcd.gi * g.Kg + k0, bw, bh, n0,
-                                         (uint16_t)((c.taps_x - 1 - i) * g.DW), (uint16_t)((c.taps_y - 1 - j) * g.DH));
+                    // (B loads of a split producer may complete before this arrive:
+                    // the transaction count dips below zero while the arrival is
+                    // still pending, so the phase cannot complete early)
+                    if (do_a) {
+                        if (leader)
+                            mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(2 * (Cfg::A_BYTES + Cfg::B_BYTES)));
+                        tma_load_im2col_pair(smem_u32(sA + s * Cfg::A_BYTES), amap, bar, tcd.gi * g.Kg + k0, bw, bh,
+                                             n0, (uint16_t)((c.taps_x - 1 - i) * g.DW),
+                                             (uint16_t)((c.taps_y - 1 - j) * g.DH));
+                    }
                     const uint32_t bdst = smem_u32(sB + s * Cfg::B_BYTES);
-#pragma unroll
-                    for (int cb = 0; cb < Cfg::BNH / 64; ++cb)
+                    for (int cb = cb_lo; cb < cb_hi; ++cb)
                         tma_load_5d_pair(bdst + cb * 8192, &p.tmap_w, bar, tcd.nb * BN + (int)rank * Cfg::BNH + cb * 64,
                                          c.tx + g.XT * i, c.ty + g.YT * j, k0, tcd.gi);
                     issued = true;
@@ -149,6 +166,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
         // ------------------------------------------------------------ MMA (leader only)
         if (leader && lane == 0) {
             constexpr uint32_t idesc = idesc_bf16<BN, 256>();
+            const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), 8192, 1024);
             uint32_t it = 0, tc = 0;
             bool ok = true, issued = false;
             SegmentIter segs(p, pair, npairs);
@@ -164,19 +183,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 const uint32_t d_tmem = tmem_base + b * BN;
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const uint32_t s = it % S, ph = (it / S) & 1;
+                    // the stage barrier orders the TMA writes of both CTAs before the MMA
+                    // reads them; no tcgen05 fence is needed per stage
                     if (!mbar_wait_bounded(full0 + 8 * s, ph, p.wait_budget, abort_flag, p.status, kDevTimeoutMma)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sA + s * Cfg::A_BYTES);
-                    const uint32_t b_addr = smem_u32(sB + s * Cfg::B_BYTES);
+                    // descriptors: start address in 16-byte units in the low bits; k step of
+                    // 16 elements = 32 bytes in A (K-major), 16 rows = 2048 bytes in B (MN-major)
+                    const uint64_t ad0 = a_desc0 + (uint64_t)((s * Cfg::A_BYTES) >> 4);
+                    const uint64_t bd0 = b_desc0 + (uint64_t)((s * Cfg::B_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(b_addr + kk * 2048, 8192, 1024);
-                        tc_mma2(d_tmem, ad, bd, idesc, (kb != sg.kb0 || kk != 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma2(d_tmem, ad0 + (uint64_t)(2 * kk), bd0 + (uint64_t)(128 * kk), idesc,
+                                (kb != sg.kb0 || kk != 0) ? 1u : 0u);
                     issued = true;
                     tc_commit2_mc(empty0 + 8 * s, (uint16_t)0x3);
                 }
@@ -188,7 +208,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < 4) {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int row = warp * 32 + lane;  // TMEM lane = this CTA's tile row
         __nv_bfloat16 *dx = static_cast<__nv_bfloat16 *>(p.dx);
