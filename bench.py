@@ -36,19 +36,19 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 # DRAM traffic of the tensor-core kernel per launch on this workload, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), valid only for
 # the kernel source whose sha256 is recorded with it.
+# Per-launch DRAM traffic of each workload's GEMM kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the sources
+# that decide what that launch does are unchanged (hash below).
+TC2_SOURCES = ("tc_common.cuh", "tc2_sm103.cu", "capi.cpp", "internal.h")
+GROUPED_SOURCES = ("tc_common.cuh", "grouped.cu", "capi.cpp", "internal.h")
 TRAFFIC = {
-    # ncu --set full, tc2_dgrad_kernel<256>, one launch on the page-3 shape:
-    # dram__bytes_read.sum 33.63 MB + dram__bytes_write.sum 1.76 MB
-    "cfg3_bf16_16x1x512x2048_1x2_s1x2": {"sha": "c00d37e8f6ae509e", "bytes": 35.39e6},
-    # grouped_dgrad_kernel<8, 2> on the 64x56x56x256 G=32 layer: 25.79 MB + 44.48 MB
-    "cfg4_bf16_resnext_64x56x56x256_g32_3x3_s2": {"sha": "c00d37e8f6ae509e", "bytes": 70.27e6},
 }
 
 
-def kernel_sha() -> str:
-    """Hash of the sources that define the tensor-core kernels' behaviour."""
+def kernel_sha(files=TC2_SOURCES) -> str:
+    """Hash of the sources that define a kernel launch's behaviour."""
     h = hashlib.sha256()
-    for f in ("tc_common.cuh", "tc2_sm103.cu", "tc_sm103.cu", "grouped.cu"):
+    for f in files:
         h.update(open(os.path.join(ROOT, "conv2d_backward_implicit_bwd_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -326,7 +326,7 @@ def main():
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": peaks["source"] + " (HBM copy)", "kernel": kernel_name, "kernel_ms": kmean}
     tr = TRAFFIC.get(case.name)
-    roof["traffic"] = tr["bytes"] if tr and tr.get("sha") == kernel_sha() else None
+    roof["traffic"] = tr["bytes"] if tr and tr.get("sha") == kernel_sha(tr["files"]) else None
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

@@ -21,7 +21,7 @@ PATH_NAMES = {PATH_TCGEN05: "tcgen05", PATH_SIMT: "simt", PATH_GROUPED: "grouped
 
 EXPORTED = [
     "conv_bwd_data_create", "conv_bwd_data_destroy", "conv_bwd_data_out_dims", "conv_bwd_data_num_subgemms",
-    "conv_bwd_data_subgemm_info", "conv_bwd_data_coverage", "conv_bwd_data_path", "conv_bwd_data_work",
+    "conv_bwd_data_subgemm_info", "conv_bwd_data_coverage", "conv_bwd_data_path", "conv_bwd_data_tile", "conv_bwd_data_work",
     "conv_bwd_data_run", "conv_bwd_data_run_host", "conv_bwd_data_get_status", "conv_bwd_data_set_timing",
     "conv_bwd_data_last_timing", "conv_bwd_data_selftest_wait_timeout", "conv_bwd_status_string",
     "conv_bwd_data_version", "conv_bwd_data_run_noalloc",
@@ -56,6 +56,7 @@ def _load():
         "conv_bwd_data_subgemm_info": [vp, i32, P(i32), P(i32), P(i64), P(i64), P(i64), P(i32), P(i32)],
         "conv_bwd_data_coverage": [vp, vp, vp],
         "conv_bwd_data_path": [vp, P(i32), P(i32)],
+        "conv_bwd_data_tile": [vp, P(i32), P(i32), P(i32)],
         "conv_bwd_data_work": [vp, P(ctypes.c_double), P(ctypes.c_double)],
         "conv_bwd_data_run": [vp, vp, vp, vp, vp],
         "conv_bwd_data_run_host": [vp, vp, vp, vp, vp, vp, vp, vp],
@@ -164,6 +165,12 @@ class Plan:
         p, n = ctypes.c_int32(), ctypes.c_int32()
         _check(_lib.conv_bwd_data_path(self._h, ctypes.byref(p), ctypes.byref(n)), "path")
         return PATH_NAMES.get(p.value, str(p.value)), n.value
+
+    def tile(self):
+        """(rows, columns, SMs) of one output tile of the GEMM kernel."""
+        m, n, k = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(_lib.conv_bwd_data_tile(self._h, ctypes.byref(m), ctypes.byref(n), ctypes.byref(k)), "tile")
+        return m.value, n.value, k.value
 
     def work(self):
         f, b = ctypes.c_double(), ctypes.c_double()

@@ -49,11 +49,12 @@ struct conv_bwd_plan_s {
     cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
     // TMA descriptor cache (keyed by the filter pointer)
     const void *tmap_w_ptr = nullptr;
-    CUtensorMap tmap_w;
+    CUtensorMap tmap_w, tmap_w_half;
     const void *tmap_a_ptr = nullptr;     // dy pointer the per-class im2col maps were encoded for
     std::vector<CUtensorMap> tmap_a;      // per class (gemm_id order)
     bool im2col = false;                  // A rows by TMA im2col loads (else cp.async gather)
     bool two_sm = false;                  // 256x256 tiles on SM pairs (cta_group::2)
+    int32_t cl = 1;                       // SM pairs per cluster (2: the pairs share B by multicast)
     int max_pairs = 0;                    // co-resident SM pairs of the 2-SM kernel
     float4 *d_partials = nullptr;         // stream-K workspace: per pair and CTA, one 128x256 fp32 tile
     int32_t *d_flags = nullptr;           // stream-K flags, tagged with the launch epoch
@@ -143,7 +144,8 @@ PFN_encodeTiled get_encode_tiled() {
 // w (KYXC, bf16) as a 5-D tensor {Cg, X, Y, Kg, G}: a box {64, 1, 1, 64, 1}
 // is a 64(k) x 64(c) slice of one filter tap, c contiguous (128 bytes per k
 // row, 128-byte swizzle).  Coordinates past Cg or past Kg (the next group's
-// rows) read as zero.
+// rows) read as zero.  A second map with box {64, 1, 1, 32, 1} loads half of
+// such a slice (the B pieces that clusters of SM pairs share).
 bool encode_w_map(conv_bwd_plan_s *p, const void *w) {
     PFN_encodeTiled enc = get_encode_tiled();
     if (!enc) return false;
@@ -156,6 +158,10 @@ bool encode_w_map(conv_bwd_plan_s *p, const void *w) {
     CUresult r = enc(&p->tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(w), dims, strides, box,
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      l2_promotion(), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    box[3] = 32;
+    r = enc(&p->tmap_w_half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2_promotion(), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -314,11 +320,13 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
     // Kernel path.
     bool tc_ok = d.dtype == CONV_BWD_BF16 && d.layout == CONV_BWD_NHWC_KYXC && g.Cg % 8 == 0 && g.Kg % 8 == 0 &&
                  d.K % 8 == 0 && d.C % 8 == 0 && g.Cg >= 64 && d.Hi < 16384 && d.Wi < 16384;
-    // narrow groups: memory-bound direct kernel (w staged in shared memory)
+    // narrow groups: memory-bound kernel on warp-level MMAs (dy rows and w
+    // fragments staged in shared memory)
     bool grouped_ok = d.dtype == CONV_BWD_BF16 && d.layout == CONV_BWD_NHWC_KYXC && g.Cg == g.Kg &&
-                      (g.Cg == 8 || g.Cg == 16) && g.G % 8 == 0 &&
-                      (int64_t)d.K * d.Y * d.X * g.Cg * 4 <= 160 * 1024 && d.Y * d.X <= 16 &&
-                      d.N * d.Hi * d.stride_w * (d.K / 8) < (1LL << 30);
+                      (g.Cg == 8 || g.Cg == 16) && g.G % 8 == 0 && d.Y * d.X <= 64 &&
+                      d.Hi < (1 << 20) && d.Wi < (1 << 20) && d.stride_w <= 64 &&
+                      d.N * d.Hi * ((d.Wi + 15) / 16) < (1LL << 31);  // item count (chunks of >= 16 pixels)
+    if (grouped_ok) grouped_ok = grouped_layout(g).smem <= 200 * 1024;
     p->path = tc_ok ? CONV_BWD_PATH_TCGEN05 : (grouped_ok ? CONV_BWD_PATH_GROUPED : CONV_BWD_PATH_SIMT);
     if (const char *f = env("CONVBWD_DEBUG_PATH")) {
         if (!std::strcmp(f, "simt")) p->path = CONV_BWD_PATH_SIMT;
@@ -338,31 +346,54 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
     }
     if (const char *f = env("CONVBWD_DEBUG_NOIM2COL")) p->im2col = p->im2col && f[0] == '0';
     // 256-row tiles on SM pairs (tcgen05 cta_group::2): each SM then loads only
-    // half of B.  Tile width 256, or 128 where 256-wide tiles would leave most
-    // SM pairs without a tile.
+    // half of B.  The tile width comes from a wave-count cost model:
+    //   time ~ ceil(tiles(bn) / pairs) * cost(bn)
+    // with the measured cost of one tile relative to a 256-wide one (same K):
+    // 128 wide 0.85 (more operand bytes per output), 512 wide 1.785 (two N=256
+    // MMAs per k slice, fewer A bytes per output, single-buffered accumulator).
+    // Where 256-wide tiles fill at most one wave, clusters of two pairs share B
+    // by multicast (measured 5% faster there, slower when several waves queue).
     p->two_sm = p->path == CONV_BWD_PATH_TCGEN05 && p->im2col && g.Cg >= 256;  // (C/G < 256: 1-SM tiles measured faster)
     if (const char *f = env("CONVBWD_DEBUG_NO2SM")) p->two_sm = p->two_sm && f[0] == '0';
+    if (const char *f = env("CONVBWD_DEBUG_2SM"))
+        if (f[0] == '1') p->two_sm = p->path == CONV_BWD_PATH_TCGEN05 && p->im2col && g.Cg >= 128;
     if (p->two_sm) {
-        int64_t tiles256 = 0, tiles128 = 0;
-        for (const ClassDesc &c : p->classes) {
-            const int64_t mt = (c.M + 255) / 256;
-            tiles256 += (int64_t)g.G * mt * ((g.Cg + 255) / 256);
-            tiles128 += (int64_t)g.G * mt * ((g.Cg + 127) / 128);
-        }
         int sms = 0, dev = 0;
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         cudaGetLastError();
         const int64_t pairs = sms > 0 ? sms / 2 : 74;
-        p->bn = tiles256 * 2 >= pairs ? 256 : 128;
-        (void)tiles128;
+        auto tiles_of = [&](int bn) {
+            int64_t t = 0;
+            for (const ClassDesc &c : p->classes) t += (int64_t)g.G * ((c.M + 255) / 256) * ((g.Cg + bn - 1) / bn);
+            return t;
+        };
+        const int widths[3] = {128, 256, 512};
+        const double cost[3] = {0.85, 1.0, 1.785};
+        double best = 1e300;
+        for (int i = 0; i < 3; ++i) {
+            if (widths[i] > 128 && g.Cg <= widths[i] / 2) continue;  // at least half the tile is real columns
+            const double t = (double)((tiles_of(widths[i]) + pairs - 1) / pairs) * cost[i];
+            if (t < best) {
+                best = t;
+                p->bn = widths[i];
+            }
+        }
+        p->cl = (p->bn == 256 && tiles_of(256) <= pairs) ? 2 : 1;
     }
-    if (const char *f = env("CONVBWD_DEBUG_BN"))
+    if (const char *f = env("CONVBWD_DEBUG_BN")) {
         if (p->path == CONV_BWD_PATH_TCGEN05 && (!std::strcmp(f, "128") || !std::strcmp(f, "256"))) p->bn = std::atoi(f);
+        if (p->two_sm && !std::strcmp(f, "512")) p->bn = 512;
+        p->cl = 1;
+    }
+    if (const char *f = env("CONVBWD_DEBUG_CL"))
+        if (p->two_sm) p->cl = f[0] == '2' ? 2 : 1;
+    if (const char *f = env("CONVBWD_DEBUG_STREAMK"))
+        if (f[0] == '1') p->cl = 1;  // stream-K runs with one pair per cluster
 
     // Schedule: classes with the longest reduction first (LPT), tiles of one
     // class contiguous; BM = 256 rows on SM pairs, 128 for the 1-SM
     // tensor-core kernel, 64 for SIMT.
-    const int bm = p->path == CONV_BWD_PATH_TCGEN05 ? (p->two_sm ? 256 : 128) : 64;
+    const int bm = p->path == CONV_BWD_PATH_TCGEN05 ? (p->two_sm ? 256 * p->cl : 128) : 64;
     const int n_tiles = (g.Cg + p->bn - 1) / p->bn;
     p->sched.resize(p->classes.size());
     std::iota(p->sched.begin(), p->sched.end(), 0);
@@ -490,6 +521,15 @@ conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t
     return CONV_BWD_OK;
 }
 
+conv_bwd_status conv_bwd_data_tile(const conv_bwd_plan p, int32_t *tile_m, int32_t *tile_n, int32_t *sms) {
+    if (!p) return CONV_BWD_ERR_INVALID_ARG;
+    const bool tc = p->path == CONV_BWD_PATH_TCGEN05, grouped = p->path == CONV_BWD_PATH_GROUPED;
+    if (tile_m) *tile_m = grouped ? 0 : tc ? (p->two_sm ? 256 * p->cl : 128) : 64;
+    if (tile_n) *tile_n = grouped ? 0 : p->bn;
+    if (sms) *sms = tc && p->two_sm ? 2 * p->cl : 1;
+    return CONV_BWD_OK;
+}
+
 conv_bwd_status conv_bwd_data_work(const conv_bwd_plan p, double *flop, double *bytes) {
     if (!p) return CONV_BWD_ERR_INVALID_ARG;
     if (flop) *flop = p->useful_flop;
@@ -575,6 +615,7 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             TcParams tp;
             std::memset(&tp, 0, sizeof(tp));
             tp.tmap_w = p->tmap_w;
+            tp.tmap_w_half = p->tmap_w_half;
             tp.dy = dy; tp.dx = dx; tp.status = p->d_status; tp.wait_budget = p->wait_budget;
             tp.g = g;
             tp.n_tiles = (g.Cg + p->bn - 1) / p->bn;
@@ -600,6 +641,11 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             }
             tp.total_tiles = (int)total;
             tp.units_total = (int)std::min<int64_t>(units, 0x7fffffff);
+            if (p->two_sm && p->cl == 2) {
+                const int clusters = (int)std::min<int64_t>(total, tc2_max_clusters(p->num_sms, 2));
+                if (launch_tc2(tp, p->bn, 2, 4 * clusters, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+                continue;
+            }
             if (p->two_sm) {
                 const int maxp = tc2_max_pairs(p->num_sms);
                 int pairs = (int)std::min<int64_t>(total, maxp);
@@ -608,7 +654,7 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
                 // what the better balance saves on the shapes measured here.
                 bool sk = false;
                 if (const char *f = env("CONVBWD_DEBUG_STREAMK"))
-                    sk = p->d_partials && f[0] == '1' && units < 0x7fffffff && maxp <= p->max_pairs;
+                    sk = p->d_partials && f[0] == '1' && units < 0x7fffffff && maxp <= p->max_pairs && p->bn <= 256;
                 if (sk) {
                     // every worker gets at least one unit: a worker without units would
                     // never raise the flag its tile's owner waits for
@@ -619,7 +665,7 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
                     p->epoch = p->epoch >= 0x7ffffffe ? 1 : p->epoch + 1;
                     tp.epoch = p->epoch;
                 }
-                if (launch_tc2(tp, p->bn, 2 * pairs, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+                if (launch_tc2(tp, p->bn, 1, 2 * pairs, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
                 continue;
             }
             int grid = (int)std::min<int64_t>(total, p->num_sms);

@@ -2,187 +2,317 @@
 // G a multiple of 8), e.g. the grouped 3x3 layers of ResNeXt-style networks
 // (a workload named on page "[igemm_dynamic] v4r1 bwd dynamic kernel").
 //
-// With 8 channels per group the arithmetic intensity is ~14 FLOP per byte:
-// the kernel is bound by HBM traffic (dy read, dx written), not by math, so it
-// runs on CUDA cores and is built around coalescing instead of a padded GEMM.
-//   * A warp owns 8 consecutive groups and 8 (16-channel groups: 4) dx pixels
-//     of one row that belong to the same column residue class (wi = r, r + sw,
-//     ...; the v4r1 split of pages "Backward data" and "[igemm_dynamic] v4r1
-//     bwd dynamic kernel" applied per pixel), so all share the class's taps.
-//   * Lane = 8 * pixel slot + group: for every pixel the 8 lanes of a slot load
-//     and store one full 128-byte line (8 groups x 8 bf16 channels).
-//   * w is staged once per CTA in shared memory as fp32 [y][x][k][c/4][g]; the
-//     8 groups of a warp read one 128-byte wavefront per chunk, reused for all
-//     of the lane's pixels.  Accumulators stay small (8 fp32 per pixel), so
-//     occupancy stays high.
-//   * A row's residue class, taps and first dy row come from small tables of
-//     the planner's class decomposition: no per-pixel divisions.
-//   * Pixels that no tap reaches are written as +0 by the same pass (no
-//     separate fill).
-// Accumulation in fp32 (packed fma.rn.f32x2: two output channels per
-// instruction, each an ordinary fp32 fused multiply-add), one RNE rounding to
-// bf16 per output.
+// With 8 channels per group the arithmetic intensity is ~14 FLOP per byte, so
+// the kernel is bound by HBM traffic (dy read, dx written).  Per group and
+// filter tap the contraction is a dense 8x8 (16x16) block:
+//   dx[p, c] += sum over k < Kg of dy[p', k] * w[gi*Kg + k, y, x, c]
+// which the warp-level tensor-core instruction mma.sync m16n8k8 (m16n8k16)
+// executes exactly, with no padding: 16 dx pixels x 8 channels x 8 k per
+// instruction.  That takes the multiply-adds off the CUDA-core issue slots,
+// which bounded a direct FMA kernel; the design is then about moving bytes:
+//   * A CTA owns one block of 8 groups (128 or 256 contiguous bytes per
+//     pixel) and walks items (n, hi, 64-pixel chunk of the row).  Per item it
+//     stages the dy rows of the row class's taps (cp.async, 16 bytes per
+//     thread, zero-filled outside dy) in shared memory -- the next item's rows
+//     load while the current item computes (two buffers).
+//   * Warp w computes group w of the block.  For every column residue class
+//     (the v4r1 split of pages "Backward data" and "[igemm_dynamic] v4r1 bwd
+//     dynamic kernel", per pixel) and tap (j, i), the dy pixels of 16
+//     consecutive outputs are consecutive staged pixels: one ldmatrix reads
+//     the A fragment.  B fragments (w) are built once per CTA for all taps.
+//   * Pixel lines in shared memory are XOR-swizzled in 16-byte segments so
+//     that 8 consecutive pixels' segment of one group hit 8 bank groups.
+//   * Accumulators (fp32) go back through a swizzled shared-memory tile as
+//     bf16 (RNE) and leave as full 128-byte lines of dx; pixels no tap reaches
+//     are written as +0 by the same pass (no separate fill).
 #include <cuda_bf16.h>
 #include <stdint.h>
 
 #include <algorithm>
 
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace cbd {
 
-__device__ __forceinline__ void bf16x8_to_float(const uint4 &u, float *f) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
+template <int CG>
+struct GCfg {
+    static constexpr int LINE = 8 * CG * 2;     // bytes per pixel of one 8-group block
+    static constexpr int SEGS = LINE / 16;      // 16-byte segments per pixel line
+    static constexpr int NR = CG == 8 ? 1 : 4;  // B-fragment registers per (tap, lane)
+    static constexpr int NT = CG / 8;           // n-tiles of 8 output channels
+    static constexpr int MT = 4;                // m-tiles of 16 pixels per residue and chunk (at most)
+};
+
+// shared-memory address of segment s of staged pixel q (segments XOR-swizzled
+// by q mod 8 so that 8 consecutive pixels' segment s fall in 8 bank groups)
+template <int CG>
+__device__ __forceinline__ uint32_t seg_addr(uint32_t base, int q, int s) {
+    return base + (uint32_t)q * GCfg<CG>::LINE + ((uint32_t)(s ^ (q & 7)) << 4);
 }
 
-__device__ __forceinline__ uint4 float_to_bf16x8(const float *f) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-        w[i] = *reinterpret_cast<uint32_t *>(&h);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
+__device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
-// Warp layout: lane = 8 * slot + gl, slot in [0, 4) picks pixels, gl in [0, 8)
-// one of 8 consecutive groups.  A warp item is one dx row segment: image n,
-// row hi, column residue r (pixels wi = r, r + sw, ...) and 8 groups; it walks
-// the segment 4*PPL pixels at a time, each lane owning PPL of them.
-template <int CG, int PPL>
-__global__ void __launch_bounds__(256) grouped_dgrad_kernel(const __grid_constant__ GroupedParams p) {
-    constexpr int V = CG / 8;   // 16-byte bf16 vectors per group row of dy / dx
-    constexpr int F4 = CG / 4;  // float4 chunks per group row of w
-    constexpr int PIX = 4 * PPL;
-    extern __shared__ float4 wsm[];  // w as fp32 [y][x][k][chunk][g] (float4 per entry)
+struct GItem {
+    int n, hi, w0, wend, tyn, ty, ht, wo_lo;
+};
+
+// item = (n, hi, chunk) -> its row class and staged column window (item count
+// < 2^31, checked by the planner)
+__device__ __forceinline__ GItem decode_item(const GroupedParams &p, int it, int nwch) {
     const Geom &g = p.g;
-    const uint4 *w = static_cast<const uint4 *>(p.w);
-    const uint4 *dy = static_cast<const uint4 *>(p.dy);
-    uint4 *dx = static_cast<uint4 *>(p.dx);
+    GItem m;
+    const int rest = it / nwch;
+    m.w0 = (it - rest * nwch) * p.wch;
+    m.n = rest / g.Hi;
+    m.hi = rest - m.n * g.Hi;
+    m.wend = min(m.w0 + p.wch, g.Wi);
+    const int rc = p.row_class[m.hi % g.sh];
+    m.tyn = rc >> 16;
+    m.ty = rc & 0xFFFF;
+    m.ht = (m.hi + g.ph - m.ty * g.dh) / g.sh;  // exact when tyn > 0
+    m.wo_lo = floor_div(m.w0 + g.pw - (g.X - 1) * g.dw, g.sw);
+    return m;
+}
 
-    // stage w: global bf16 [g*Kg + k][y][x][c] -> shared fp32 [y][x][k][c/4][g]
-    const int rows = g.K * g.Y * g.X;  // (k_global, y, x) rows of CG channels
-    for (int e = threadIdx.x; e < rows * V; e += blockDim.x) {
-        const int v = e % V, rr = e / V;
-        const int x = rr % g.X, y = (rr / g.X) % g.Y, kg = rr / (g.X * g.Y);
-        const int gi = kg / CG, k = kg % CG;
-        float f[8];
-        bf16x8_to_float(w[e], f);
-        const int base = (((y * g.X + x) * CG + k) * F4 + 2 * v) * g.G + gi;
-        wsm[base] = make_float4(f[0], f[1], f[2], f[3]);
-        wsm[base + g.G] = make_float4(f[4], f[5], f[6], f[7]);
+template <int CG>
+__global__ void __launch_bounds__(128) grouped_dgrad_kernel(const __grid_constant__ GroupedParams p) {
+    using C = GCfg<CG>;
+    constexpr int LOG_SEGS = CG == 8 ? 3 : 4;
+    constexpr int NTHREADS = 128;
+    extern __shared__ __align__(128) uint8_t gsm[];
+    const Geom &g = p.g;
+    const uint32_t *wfrag = reinterpret_cast<const uint32_t *>(gsm);  // [tap][NR][lane][8 groups]
+    const uint32_t buf0 = smem_u32(gsm + p.wfrag_bytes);             // two buffers of [tyn][span] pixel lines
+    const uint32_t outb = buf0 + 2 * p.buf_bytes;                    // [wch] pixel lines
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int gb = blockIdx.x % p.gblocks;
+    const int cta = blockIdx.x / p.gblocks, ncta = gridDim.x / p.gblocks;
+    const int64_t cofs = (int64_t)gb * 8 * CG;  // first channel of the block (dy and dx)
+
+    // B fragments of the block's 8 groups for every tap.  The groups' w rows
+    // (8*CG rows of Y*X*CG contiguous bf16) are first copied to shared memory
+    // (16-byte loads), then lane (gid, tig) takes, for group gl,
+    // w[gi*Kg + k][y][x][n] with k = 2 tig (+1) (+8 for the second half of a
+    // 16-deep step) and n = gid (+8 for the second n-tile)
+    {
+        const int ntap = g.Y * g.X;
+        const int rowh = ntap * CG;          // bf16 per k row
+        const int nraw = 8 * CG * rowh / 8;  // 16-byte pieces of the block's rows
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.w) + cofs * rowh);
+        uint4 *raw = reinterpret_cast<uint4 *>(gsm + p.wfrag_bytes);
+        for (int e = threadIdx.x; e < nraw; e += NTHREADS) raw[e] = src[e];
+        __syncthreads();
+        const uint16_t *rw = reinterpret_cast<const uint16_t *>(raw);
+        uint32_t *wf = reinterpret_cast<uint32_t *>(gsm);
+        for (int e = threadIdx.x; e < ntap * C::NR * 32 * 8; e += NTHREADS) {
+            const int gl = e & 7, l = (e >> 3) & 31, r = (e >> 8) % C::NR, tap = e / (256 * C::NR);
+            const int nt = r >> 1, kh = r & 1;
+            const int n = nt * 8 + (l >> 2), k = 2 * (l & 3) + 8 * kh;
+            const int base = (gl * CG + k) * rowh + tap * CG + n;
+            wf[e] = (uint32_t)rw[base] | ((uint32_t)rw[base + rowh] << 16);
+        }
+        __syncthreads();
     }
-    __syncthreads();
 
-    const int lane = threadIdx.x & 31;
-    const int gl = lane & 7, slot = lane >> 3;
-    const int warps = gridDim.x * (blockDim.x >> 5);
-    const int total = g.N * g.Hi * g.sw * p.gblocks;  // < 2^31 (checked by the planner)
-    for (int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < total; item += warps) {
-        const int gb = item % p.gblocks;
-        int rest = item / p.gblocks;
-        const int r = rest % g.sw;
-        rest /= g.sw;
-        const int hi = rest % g.Hi, n = rest / g.Hi;
-        if (r >= g.Wi) continue;
-        const int gi = gb * 8 + gl;
-        // residue classes of this row and column: ty/tx, taps, and the class index
-        // of the first pixel (ht for the row; wt of pixel wi = r for the column)
-        const int rc = p.row_class[hi % g.sh], cc = p.col_class[r];
-        const int taps_y = rc >> 16, ty = rc & 0xFFFF;
-        const int taps_x = cc >> 16, tx = cc & 0xFFFF;
-        const int ht = (hi + g.ph - ty * g.dh) / g.sh;   // exact when taps_y > 0
-        const int wt0 = (r + g.pw - tx * g.dw) / g.sw;   // exact when taps_x > 0; +1 per pixel step
-        const int cnt = (g.Wi - r + g.sw - 1) / g.sw;    // pixels of this residue in the row
-        uint4 *orow = dx + (((int64_t)n * g.Hi + hi) * g.Wi * g.C + (int64_t)gi * CG) / 8;
-        const int kv = g.K / 8;  // dy pixel stride in 16-byte vectors
-        for (int p0 = 0; p0 < cnt; p0 += PIX) {
-            // accumulators as fp32 pairs (channels c, c + 1): one packed f32x2 FMA
-            // updates two outputs
-            uint64_t acc[PPL][CG / 2];
-#pragma unroll
-            for (int q = 0; q < PPL; ++q)
-#pragma unroll
-                for (int c = 0; c < CG / 2; ++c) acc[q][c] = 0ull;
-            for (int jj = 0; jj < taps_y; ++jj) {
-                const int ho = ht - jj * g.DH;
-                if (ho < 0 || ho >= g.Ho) continue;
-                const int y = ty + g.YT * jj;
-                const int64_t rowv = ((int64_t)n * g.Ho + ho) * g.Wo * kv + gi * V;
-                for (int ii = 0; ii < taps_x; ++ii) {
-                    const int x = tx + g.XT * ii;
-                    uint4 raw[PPL][V];
-#pragma unroll
-                    for (int q = 0; q < PPL; ++q) {
-                        const int pq = p0 + slot + 4 * q;
-                        const int wo = wt0 + pq - ii * g.DW;
-                        const bool ok = pq < cnt && wo >= 0 && wo < g.Wo;
-#pragma unroll
-                        for (int v = 0; v < V; ++v)
-                            raw[q][v] = ok ? dy[rowv + (int64_t)wo * kv + v] : make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    const ulonglong2 *wt =
-                        reinterpret_cast<const ulonglong2 *>(wsm) + (y * g.X + x) * CG * F4 * g.G + gi;
-#pragma unroll
-                    for (int k = 0; k < CG; ++k) {
-                        uint64_t wp[CG / 2];
-#pragma unroll
-                        for (int f = 0; f < F4; ++f) {
-                            const ulonglong2 a = wt[(k * F4 + f) * g.G];
-                            wp[2 * f] = a.x;
-                            wp[2 * f + 1] = a.y;
-                        }
-#pragma unroll
-                        for (int q = 0; q < PPL; ++q) {
-                            const uint4 u = raw[q][k / 8];
-                            const uint32_t word = (k % 8) < 2 ? u.x : (k % 8) < 4 ? u.y : (k % 8) < 6 ? u.z : u.w;
-                            const uint32_t bits = (k & 1) ? (word & 0xFFFF0000u) : (word << 16);
-                            uint64_t d2;
-                            asm("mov.b64 %0, {%1, %1};" : "=l"(d2) : "r"(bits));
-#pragma unroll
-                            for (int c = 0; c < CG / 2; ++c)
-                                asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc[q][c]) : "l"(d2), "l"(wp[c]));
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < PPL; ++q) {
-                const int pq = p0 + slot + 4 * q;
-                if (pq >= cnt) continue;
-                float f[CG];
-#pragma unroll
-                for (int c = 0; c < CG / 2; ++c) {
-                    f[2 * c] = __uint_as_float((uint32_t)acc[q][c]);
-                    f[2 * c + 1] = __uint_as_float((uint32_t)(acc[q][c] >> 32));
-                }
-                uint4 *o = orow + (int64_t)(r + g.sw * pq) * g.C / 8;
-#pragma unroll
-                for (int v = 0; v < V; ++v) o[v] = float_to_bf16x8(&f[8 * v]);
+    const int nwch = (g.Wi + p.wch - 1) / p.wch;
+    const int items = g.N * g.Hi * nwch;
+    const int64_t kbytes = (int64_t)g.K * 2;
+    const int mi = lane >> 3;                       // ldmatrix: lane addresses row lane % 8 of matrix mi
+    const int trow = (mi & 1) * 8 + (lane & 7);     // this lane's A row within the 16-row tile
+
+    auto stage = [&](const GItem &m, int b) {
+        const uint32_t bb = buf0 + (uint32_t)b * p.buf_bytes;
+        for (int jj = 0; jj < m.tyn; ++jj) {
+            const int ho = m.ht - jj * g.DH;
+            const bool hok = ho >= 0 && ho < g.Ho;
+            const uint8_t *rowp = static_cast<const uint8_t *>(p.dy) +
+                                  ((int64_t)m.n * g.Ho + (hok ? ho : 0)) * g.Wo * kbytes + cofs * 2;
+            const uint32_t rb = bb + (uint32_t)(jj * p.span * C::LINE);
+            for (int e = threadIdx.x; e < (p.span << LOG_SEGS); e += NTHREADS) {
+                const int q = e >> LOG_SEGS, s = e & (C::SEGS - 1);
+                const int wo = m.wo_lo + q;
+                const bool ok = hok && wo >= 0 && wo < g.Wo;
+                const uint8_t *src = ok ? rowp + wo * kbytes + s * 16 : static_cast<const uint8_t *>(p.dy);
+                cp_async_16(seg_addr<CG>(rb, q, s), src, ok ? 16u : 0u);
             }
         }
+    };
+
+    int b = 0;
+    GItem m = decode_item(p, cta < items ? cta : 0, nwch);
+    if (cta < items) stage(m, 0);
+    cp_async_commit();
+    for (int it = cta; it < items; it += ncta, b ^= 1) {
+        const bool more = it + ncta < items;
+        const GItem mn = decode_item(p, more ? it + ncta : it, nwch);
+        if (more) stage(mn, b ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+
+        // units (column residue r, 16-pixel m-tile) of this item, warp w takes
+        // units w, w + 4, ...; a unit covers all 8 groups of the block
+        const uint32_t bb = buf0 + (uint32_t)b * p.buf_bytes;
+        const int per_r = (((p.wch / g.sw) + 15) >> 4);  // m-tile slots per residue
+        for (int u = warp; u < g.sw * per_r; u += 4) {
+            const int r = u / per_r, mt = u - r * per_r;
+            const int cnt = (m.wend - (m.w0 + r) + g.sw - 1) / g.sw;  // outputs wi = w0 + r + sw t in the chunk
+            if (mt * 16 >= cnt) continue;
+            const int cc = p.col_class[r];  // w0 is a multiple of sw
+            const int txn = cc >> 16, tx = cc & 0xFFFF;
+            float acc[8][4 * C::NT];
+#pragma unroll
+            for (int gl = 0; gl < 8; ++gl)
+#pragma unroll
+                for (int v = 0; v < 4 * C::NT; ++v) acc[gl][v] = 0.f;
+            if (m.tyn > 0 && txn > 0) {
+                const int wt0 = (m.w0 + r + g.pw - tx * g.dw) / g.sw;  // exact
+                for (int jj = 0; jj < m.tyn; ++jj) {
+                    const int ho = m.ht - jj * g.DH;
+                    if (ho < 0 || ho >= g.Ho) continue;  // staged as zeros: nothing to add
+                    const int y = m.ty + g.YT * jj;
+                    const uint32_t rowb = bb + (uint32_t)(jj * p.span * C::LINE);
+                    for (int ii = 0; ii < txn; ++ii) {
+                        const int tap = y * g.X + tx + g.XT * ii;
+                        const int q = min(wt0 - ii * g.DW - m.wo_lo + mt * 16 + trow, p.span - 1);
+                        const uint32_t arow = rowb + (uint32_t)q * C::LINE;
+                        const int qs = q & 7;
+                        const uint4 *wl = reinterpret_cast<const uint4 *>(wfrag + (tap * C::NR * 32 + lane) * 8);
+#pragma unroll
+                        for (int r2 = 0; r2 < C::NR; ++r2) {
+                            // fragments of the 8 groups: two 16-byte loads
+                            const uint4 f0 = wl[r2 * 64], f1 = wl[r2 * 64 + 1];
+                            const uint32_t bfr[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                            if (CG == 8) {
+#pragma unroll
+                                for (int gp = 0; gp < 4; ++gp) {
+                                    // matrices: rows 0-7 | 8-15 of group 2gp, then of group 2gp + 1
+                                    const int seg = 2 * gp + (mi >> 1);
+                                    uint32_t a0, a1, a2, a3;
+                                    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                                                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                                                 : "r"(arow + ((uint32_t)(seg ^ qs) << 4)));
+                                    asm volatile(
+                                        "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, "
+                                        "{%6}, {%0, %1, %2, %3};"
+                                        : "+f"(acc[2 * gp][0]), "+f"(acc[2 * gp][1]), "+f"(acc[2 * gp][2]),
+                                          "+f"(acc[2 * gp][3])
+                                        : "r"(a0), "r"(a1), "r"(bfr[2 * gp]));
+                                    asm volatile(
+                                        "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, "
+                                        "{%6}, {%0, %1, %2, %3};"
+                                        : "+f"(acc[2 * gp + 1][0]), "+f"(acc[2 * gp + 1][1]), "+f"(acc[2 * gp + 1][2]),
+                                          "+f"(acc[2 * gp + 1][3])
+                                        : "r"(a2), "r"(a3), "r"(bfr[2 * gp + 1]));
+                                }
+                            } else {
+                                // r2 = 2 nt + kh: the A fragments of a group serve both n-tiles,
+                                // so they are loaded with the kh = 0 fragments and kept
+                                (void)bfr;
+                            }
+                        }
+                        if (CG == 16) {
+#pragma unroll
+                            for (int gl = 0; gl < 8; ++gl) {
+                                // matrices (rows 0-7 | 8-15) x (k 0-7 | 8-15) of group gl
+                                const int seg = 2 * gl + (mi >> 1);
+                                uint32_t a0, a1, a2, a3;
+                                asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                                             : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                                             : "r"(arow + ((uint32_t)(seg ^ qs) << 4)));
+#pragma unroll
+                                for (int nt = 0; nt < C::NT; ++nt) {
+                                    const uint32_t b0 = wfrag[((tap * C::NR + 2 * nt) * 32 + lane) * 8 + gl];
+                                    const uint32_t b1 = wfrag[((tap * C::NR + 2 * nt + 1) * 32 + lane) * 8 + gl];
+                                    asm volatile(
+                                        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                                        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                                        : "+f"(acc[gl][4 * nt]), "+f"(acc[gl][4 * nt + 1]), "+f"(acc[gl][4 * nt + 2]),
+                                          "+f"(acc[gl][4 * nt + 3])
+                                        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            // accumulators -> bf16 -> output tile at chunk pixel r + sw t: lane
+            // (gid, tig) holds rows gid, gid + 8 and channels nt*8 + 2 tig (+1)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int t = mt * 16 + gid + 8 * h;
+                if (t >= cnt) continue;
+                const int q = r + g.sw * t;
+                const uint32_t orow = outb + (uint32_t)q * C::LINE + 4 * tig;
+                const int qs = q & 7;
+#pragma unroll
+                for (int gl = 0; gl < 8; ++gl)
+#pragma unroll
+                    for (int nt = 0; nt < C::NT; ++nt) {
+                        __nv_bfloat162 v = __floats2bfloat162_rn(acc[gl][4 * nt + 2 * h], acc[gl][4 * nt + 2 * h + 1]);
+                        const uint32_t a = orow + ((uint32_t)((gl * C::NT + nt) ^ qs) << 4);
+                        asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(*reinterpret_cast<uint32_t *>(&v))
+                                     : "memory");
+                    }
+            }
+        }
+        __syncthreads();
+        // output tile -> dx: full 16-byte segments, consecutive threads on consecutive segments
+        const int npx = m.wend - m.w0;
+        uint8_t *dxb = static_cast<uint8_t *>(p.dx) + ((((int64_t)m.n * g.Hi + m.hi) * g.Wi + m.w0) * g.C + cofs) * 2;
+        const int64_t cbytes = (int64_t)g.C * 2;
+        for (int e = threadIdx.x; e < (npx << LOG_SEGS); e += NTHREADS) {
+            const int s = e & (C::SEGS - 1), q = e >> LOG_SEGS;
+            uint4 v;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(seg_addr<CG>(outb, q, s)));
+            *reinterpret_cast<uint4 *>(dxb + q * cbytes + s * 16) = v;
+        }
+        m = mn;
     }
+    cp_async_wait<0>();
 }
 
-cudaError_t launch_grouped(const GroupedParams &p, int num_sms, cudaStream_t s) {
-    const size_t smem = (size_t)p.g.K * p.g.Y * p.g.X * p.g.Cg * 4;  // fp32 copy of w
-    const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(4, (size_t)(220 * 1024) / std::max<size_t>(smem, 1)));
-    const int blocks = (num_sms > 0 ? num_sms : 148) * per_sm;
-    if (p.g.Cg == 8) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_dgrad_kernel<8, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        grouped_dgrad_kernel<8, 2><<<blocks, 256, smem, s>>>(p);
-    } else {
-        cudaError_t e = cudaFuncSetAttribute(grouped_dgrad_kernel<16, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        grouped_dgrad_kernel<16, 1><<<blocks, 256, smem, s>>>(p);
+// Chunk width, staged span and shared memory of a geometry (the planner
+// checks that it fits; the launch uses the same numbers).
+GroupedLayout grouped_layout(const Geom &g) {
+    GroupedLayout L;
+    const int line = 8 * g.Cg * 2;
+    const int nr = g.Cg == 8 ? 1 : 4;
+    const int tymax = (g.Y + g.YT - 1) / g.YT;
+    L.wfrag_bytes = g.Y * g.X * 8 * nr * 32 * 4;
+    const int raw_w = 8 * g.Cg * g.Y * g.X * g.Cg * 2;  // the block's w rows, staged once at the start
+    for (int wch = 64; wch >= 16; wch /= 2) {
+        L.wch = std::max(g.sw, wch - wch % g.sw);
+        L.span = (L.wch - 1 + (g.X - 1) * g.dw) / g.sw + 2;
+        L.buf_bytes = tymax * L.span * line;
+        L.smem = L.wfrag_bytes + std::max(2 * L.buf_bytes + L.wch * line, raw_w);
+        if (L.smem <= 200 * 1024 && L.wch / g.sw <= 64) break;
     }
+    return L;
+}
+
+template <int CG>
+static cudaError_t launch_grouped_cg(const GroupedParams &p, const GroupedLayout &L, int num_sms, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_dgrad_kernel<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
+    if (e != cudaSuccess) return e;
+    const int per_sm = std::max(1, std::min(16, (227 * 1024) / (L.smem + 1024)));
+    const int sms = num_sms > 0 ? num_sms : 148;
+    const int per_gb = std::max(1, (sms * per_sm + p.gblocks - 1) / p.gblocks);
+    grouped_dgrad_kernel<CG><<<per_gb * p.gblocks, 128, L.smem, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_grouped(GroupedParams &p, int num_sms, cudaStream_t s) {
+    const GroupedLayout L = grouped_layout(p.g);
+    p.wch = L.wch;
+    p.span = L.span;
+    p.wfrag_bytes = L.wfrag_bytes;
+    p.buf_bytes = L.buf_bytes;
+    return p.g.Cg == 8 ? launch_grouped_cg<8>(p, L, num_sms, s) : launch_grouped_cg<16>(p, L, num_sms, s);
 }
 
 }  // namespace cbd

@@ -71,6 +71,7 @@ struct FillParams {
 // Tensor-core (tcgen05) kernel parameters.
 struct TcParams {  // 128-byte aligned through CUtensorMap
     CUtensorMap tmap_w;   // w viewed as 5-D {Cg, X, Y, Kg, G}, box {64, 1, 1, 64, 1}, 128B swizzle
+    CUtensorMap tmap_w_half;  // the same view with box {64, 1, 1, 32, 1} (B pieces shared between SM pairs)
     CUtensorMap tmap_a[kMaxTcClasses];  // per class: dy as im2col {K, Wo, Ho, N}, 64 ch x 128 px, 128B swizzle
     const void *dy;
     void *dx;
@@ -102,7 +103,16 @@ struct GroupedParams {
     int32_t gblocks;         // G / 8
     int32_t row_class[64];   // per row residue hi % sh: (taps_y << 16) | ty (taps 0: no class writes it)
     int32_t col_class[64];   // per column residue wi % sw: (taps_x << 16) | tx
+    int32_t wch;             // dx pixels per item (a multiple of sw)
+    int32_t span;            // staged dy pixels per tap row (covers every tap of an item)
+    int32_t wfrag_bytes;     // shared memory of the w fragments
+    int32_t buf_bytes;       // shared memory of one staged-dy buffer
 };
+
+struct GroupedLayout {
+    int32_t wch, span, wfrag_bytes, buf_bytes, smem;
+};
+GroupedLayout grouped_layout(const Geom &g);
 
 // Status codes written by kernels (first writer wins).
 enum : int32_t {
@@ -117,9 +127,10 @@ enum : int32_t {
 
 cudaError_t launch_fill(const FillParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_simt(const SimtParams &p, int dtype, cudaStream_t s);
-cudaError_t launch_grouped(const GroupedParams &p, int num_sms, cudaStream_t s);
+cudaError_t launch_grouped(GroupedParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_tc(const TcParams &p, int bn, int grid, cudaStream_t s);
-cudaError_t launch_tc2(const TcParams &p, int bn, int grid, cudaStream_t s);
+cudaError_t launch_tc2(const TcParams &p, int bn, int cl, int grid, cudaStream_t s);  // cl: SM pairs per cluster
+int tc2_max_clusters(int num_sms, int cl);
 int tc2_max_pairs(int num_sms);
 cudaError_t launch_selftest_wait(int32_t *status, int64_t budget, cudaStream_t s);
 size_t tc_smem_bytes(int bn, bool im2col);

@@ -3,22 +3,25 @@
 // Same sub-GEMMs as tc_sm103.cu (one per filter-tap residue class and group,
 // the v4r1 backward-data split of pages "Backward data" and "[igemm_dynamic]
 // v4r1 bwd dynamic kernel"), but each output tile is 256 (m) x BN (c), BN in
-// {256, 128}, and is computed by a cluster of two CTAs on two SMs:
+// {128, 256, 512}, and is computed by a cluster of two CTAs on two SMs:
 //   * CTA rank r of the pair loads the tile's A rows [128r, 128r+128) (TMA
-//     im2col, one map per class, exactly as in the 1-SM kernel) and the B
-//     columns [r*BN/2, (r+1)*BN/2) (TMA boxes of 64 k x 64 c) into its own
-//     shared memory.  Both CTAs' loads complete on the leader's (rank 0)
-//     stage barrier (`.cta_group::2` TMA), which expects the bytes of both.
-//   * The leader's single MMA thread issues M=256, N=BN, K=16
-//     `tcgen05.mma.cta_group::2` instructions that read A and B from both
-//     CTAs' shared memory and accumulate rows [128r, 128r+128) in CTA r's
-//     TMEM; each stage is committed back to both CTAs' empty barriers and each
-//     finished tile to both CTAs' accumulator-full barriers (multicast).
+//     im2col, one map per class, exactly as in the 1-SM kernel) and its half
+//     of the B columns of every MMA of the tile (TMA boxes of 64 k x 64 c)
+//     into its own shared memory.  Both CTAs' loads complete on the leader's
+//     (rank 0) stage barrier (`.cta_group::2` TMA), which expects the bytes of
+//     both.
+//   * The leader's single MMA thread issues M=256, N=min(BN, 256), K=16
+//     `tcgen05.mma.cta_group::2` instructions (two per k slice for BN=512)
+//     that read A and B from both CTAs' shared memory and accumulate rows
+//     [128r, 128r+128) in CTA r's TMEM; each stage is committed back to both
+//     CTAs' empty barriers and each finished tile to both CTAs'
+//     accumulator-full barriers (multicast).
 //   * Each CTA's four epilogue warps drain their own TMEM rows (RNE to bf16,
 //     16-byte stores to the class's strided dx pixels) and release the
 //     leader's accumulator-empty barrier (remote arrive from the peer).
 // Per SM and per 128x256x64 step this moves 32 KB of operands into shared
-// memory instead of 48 KB (each SM loads only half of B), and six stages fit.
+// memory instead of 48 KB (each SM loads only half of B); a 512-wide tile
+// moves 24 KB per 128x256x64 of work.
 // Every barrier wait is bounded; both CTAs meet in a cluster barrier before
 // deallocating TMEM and exiting.
 #include <cuda.h>
@@ -31,32 +34,48 @@
 
 namespace cbd {
 
-template <int BN_>
+template <int BN_, int CL_>
 struct Tc2Cfg {
-    static constexpr int BN = BN_;          // tile width of the pair (= MMA N): 256 or 128
+    static constexpr int BN = BN_;          // tile width of the pair: 128, 256 or 512
+    // SM pairs per cluster: 1, or 2 pairs that compute two 256-row blocks of
+    // the same columns and share B -- CTA h of pair pr loads k rows
+    // [32pr, 32pr + 32) of B half h and multicasts them to CTA h of both pairs,
+    // so each SM reads half of its B from L2
+    static constexpr int CL = CL_;
+    static constexpr int CTAS = 2 * CL;
     static constexpr int BNH = BN / 2;      // columns of B held by each CTA
-    static constexpr int STAGES = BN == 256 ? 6 : 8;
+    // one MMA instruction is at most 256 wide: a 512-wide tile issues two per
+    // 16-deep k slice (columns [0, 256) and [256, 512) of the tile), which
+    // halves the A bytes per output column; its accumulator takes all 512
+    // TMEM columns, so it is single-buffered
+    static constexpr int MMA_N = BN < 256 ? BN : 256;
+    static constexpr int NMMA = BN / MMA_N;
+    static constexpr int QPM = MMA_N / 128;  // 64-column B boxes per MMA per CTA
+    static constexpr int STAGES = BN == 512 ? 4 : BN == 256 ? 6 : 8;
+    static constexpr int ACC_BUFS = BN == 512 ? 1 : 2;
     static constexpr int A_BYTES = 128 * 64 * 2;
     static constexpr int B_BYTES = BNH * 64 * 2;
-    static constexpr int TMEM_COLS = 2 * BN;  // double-buffered accumulator
+    static constexpr int TMEM_COLS = ACC_BUFS * BN;
     static constexpr int STAGE_OUT_BYTES = 4 * 32 * 128;  // epilogue staging: 4 warps x 32 rows x 128 B
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + STAGE_OUT_BYTES + BAR_BYTES;
     static constexpr int MMA_WARP = 5;
     // TMA issue is serialised per issuing thread (~70 SM clocks per tile-mode
     // load, more for an im2col load), so the loads of a stage are spread over
-    // warps on different SM sub-partitions: warp 4 issues A, warps 6, 7 one
-    // 64-column B box each
-    static constexpr bool SPLIT_PRODUCER = true;
-    static constexpr int B_WARP = 6;                  // first B warp; BNH / 64 of them
-    static constexpr int B_WARPS = SPLIT_PRODUCER ? BNH / 64 : 0;
-    static constexpr int THREADS = 32 * (6 + B_WARPS);
+    // warps on different SM sub-partitions: warp 4 issues A, warps 6.. the
+    // 64-column B boxes (one or two each)
+    static constexpr int B_WARP = 6;
+    static constexpr int BOXES = BNH / 64;
+    static constexpr int B_WARPS = BOXES < 2 ? BOXES : 2;
+    static constexpr int BOXES_PER_WARP = BOXES / B_WARPS;
+    static constexpr int THREADS = 32 * (B_WARP + B_WARPS);
 };
 
-template <int BN_>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS, 1)
+template <int BN_, int CL_>
+__global__ void __cluster_dims__(2 * CL_, 1, 1) __launch_bounds__(Tc2Cfg<BN_, CL_>::THREADS, 1)
     tc2_dgrad_kernel(const __grid_constant__ TcParams p) {
-    using Cfg = Tc2Cfg<BN_>;
+    using Cfg = Tc2Cfg<BN_, CL_>;
+    constexpr int CL = Cfg::CL;
     constexpr int S = Cfg::STAGES;
     constexpr int BN = Cfg::BN;
     extern __shared__ uint8_t smem_raw[];
@@ -68,18 +87,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
 
-    const uint32_t rank = cluster_ctarank();  // 0 = leader of the pair
+    const uint32_t q_rank = cluster_ctarank();
+    const uint32_t pr = q_rank >> 1;          // pair within the cluster
+    const uint32_t rank = q_rank & 1;         // CTA within the pair: 0 = leader
+    const uint32_t pl = q_rank & ~1u;         // cluster rank of this pair's leader
     const bool leader = rank == 0;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
     const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const Geom &g = p.g;
-    const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
+    // scheduling unit: the cluster (its pairs take the 256-row blocks of one
+    // 256*CL-row tile); stream-K runs only with one pair per cluster
+    const int pair = blockIdx.x / Cfg::CTAS, npairs = gridDim.x / Cfg::CTAS;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8 * s, 1);   // leader: one arrive.expect_tx for both CTAs' bytes
-            mbar_init(empty0 + 8 * s, 1);  // one multicast commit per stage
+            mbar_init(empty0 + 8 * s, CL);  // one multicast commit per stage from each pair's leader
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8 * b, 1);   // one multicast commit per tile
@@ -94,7 +118,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
         tc_fence_before();
     }
     if (warp == 4 && lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_w)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(CL == 1 ? &p.tmap_w : &p.tmap_w_half))
+                     : "memory");
         for (int ci = 0; ci < p.num_classes; ++ci)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_a[ci])) : "memory");
     }
@@ -104,18 +129,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
     const uint32_t tmem_base = *tmem_slot;
     if (threadIdx.x == 0 && !leader) {
         // the pair's MMAs write this CTA's rows at the leader's TMEM address
-        if (ld_shared_cluster_u32(mapa_shared(smem_u32(tmem_slot), 0)) != tmem_base)
+        if (ld_shared_cluster_u32(mapa_shared(smem_u32(tmem_slot), pl)) != tmem_base)
             record_status(p.status, kDevFaultIndex);
     }
 
-    if (warp == 4 || (Cfg::SPLIT_PRODUCER && warp >= Cfg::B_WARP)) {
-        // ------------------------------------------------------------ producer(s)
+    if (warp == 4 || warp >= Cfg::B_WARP) {
+        // ------------------------------------------------------------ producers
         const bool do_a = warp == 4;  // A loads + the stage's byte count
-        // B boxes of this warp: all of them (single producer) or box warp - B_WARP
-        const int cb_lo = Cfg::SPLIT_PRODUCER ? (warp == 4 ? 0 : warp - Cfg::B_WARP) : 0;
-        const int cb_hi = Cfg::SPLIT_PRODUCER ? (warp == 4 ? 0 : cb_lo + 1) : Cfg::BNH / 64;
+        // B boxes of this warp
+        const int cb_lo = do_a ? 0 : (warp - Cfg::B_WARP) * Cfg::BOXES_PER_WARP;
+        const int cb_hi = do_a ? 0 : cb_lo + Cfg::BOXES_PER_WARP;
         if (lane == 0) {
-            const uint32_t full_leader0 = mapa_shared(full0, 0);
+            const uint32_t full_leader0 = mapa_shared(full0, pl);
+            const uint16_t bmask = (uint16_t)((1u << rank) | (1u << (2 + rank)));  // CTA `rank` of both pairs
             uint32_t it = 0;
             bool ok = true, issued = false;
             SegmentIter segs(p, pair, npairs);
@@ -124,7 +150,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 const TileCoord tcd = decode_tile(p, sg.t);
                 const ClassDesc &c = p.cls[tcd.ci];
                 const int HTWT = c.HT * c.WT;
-                const int m0 = tcd.mb * 256 + (int)rank * 128;
+                const int m0 = tcd.mb * (256 * CL) + (int)pr * 256 + (int)rank * 128;
                 const int n0 = m0 / HTWT, rem = m0 - n0 * HTWT;
                 const int bh = c.ht_lo + rem / c.WT - (c.taps_y - 1) * g.DH;
                 const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
@@ -151,9 +177,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                                              (uint16_t)((c.taps_y - 1 - j) * g.DH));
                     }
                     const uint32_t bdst = smem_u32(sB + s * Cfg::B_BYTES);
-                    for (int cb = cb_lo; cb < cb_hi; ++cb)
-                        tma_load_5d_pair(bdst + cb * 8192, &p.tmap_w, bar, tcd.nb * BN + (int)rank * Cfg::BNH + cb * 64,
-                                         c.tx + g.XT * i, c.ty + g.YT * j, k0, tcd.gi);
+                    // box q feeds MMA q / QPM: this CTA's half of that MMA's columns
+                    for (int cb = cb_lo; cb < cb_hi; ++cb) {
+                        const int col = tcd.nb * BN + (cb / Cfg::QPM) * Cfg::MMA_N + (int)rank * (Cfg::MMA_N / 2) +
+                                        (cb % Cfg::QPM) * 64;
+                        if (CL == 1)
+                            tma_load_5d_pair(bdst + cb * 8192, &p.tmap_w, bar, col, c.tx + g.XT * i,
+                                             c.ty + g.YT * j, k0, tcd.gi);
+                        else  // k rows [32pr, 32pr + 32) of the box, to both pairs
+                            tma_load_5d_pair_mc(bdst + cb * 8192 + pr * 4096, &p.tmap_w_half, bar, col,
+                                                c.tx + g.XT * i, c.ty + g.YT * j, k0 + 32 * (int)pr, tcd.gi, bmask);
+                    }
                     issued = true;
                 }
             }
@@ -165,7 +199,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
     } else if (warp == Cfg::MMA_WARP) {
         // ------------------------------------------------------------ MMA (leader only)
         if (leader && lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16<BN, 256>();
+            constexpr uint32_t idesc = idesc_bf16<Cfg::MMA_N, 256>();
             const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
             const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), 8192, 1024);
             uint32_t it = 0, tc = 0;
@@ -173,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
             SegmentIter segs(p, pair, npairs);
             Segment sg;
             for (; ok && segs.next(p, sg); ++tc) {
-                const uint32_t b = tc & 1, tph = (tc >> 1) & 1;
+                const uint32_t b = tc % Cfg::ACC_BUFS, tph = (tc / Cfg::ACC_BUFS) & 1;
                 if (!mbar_wait_bounded(tempty0 + 8 * b, tph ^ 1, p.wait_budget, abort_flag, p.status,
                                        kDevTimeoutMma)) {
                     ok = false;
@@ -195,13 +229,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                     const uint64_t bd0 = b_desc0 + (uint64_t)((s * Cfg::B_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc_mma2(d_tmem, ad0 + (uint64_t)(2 * kk), bd0 + (uint64_t)(128 * kk), idesc,
-                                (kb != sg.kb0 || kk != 0) ? 1u : 0u);
+#pragma unroll
+                        for (int h = 0; h < Cfg::NMMA; ++h)
+                            tc_mma2(d_tmem + h * Cfg::MMA_N, ad0 + (uint64_t)(2 * kk),
+                                    bd0 + (uint64_t)(128 * kk + h * ((Cfg::QPM * 8192) >> 4)), idesc,
+                                    (kb != sg.kb0 || kk != 0) ? 1u : 0u);
                     issued = true;
-                    tc_commit2_mc(empty0 + 8 * s, (uint16_t)0x3);
+                    // the slot is free once every pair that reads it is done (B is shared)
+                    tc_commit2_mc(empty0 + 8 * s, (uint16_t)(CL == 1 ? 0x3 : 0xF));
                 }
                 if (!ok) break;
-                tc_commit2_mc(tfull0 + 8 * b, (uint16_t)0x3);
+                tc_commit2_mc(tfull0 + 8 * b, (uint16_t)(0x3u << (2 * pr)));
             }
             if (!ok && issued) {
                 for (int q = 0; q < 100; ++q) __nanosleep(1000);
@@ -212,7 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int row = warp * 32 + lane;  // TMEM lane = this CTA's tile row
         __nv_bfloat16 *dx = static_cast<__nv_bfloat16 *>(p.dx);
-        const uint32_t tempty_leader0 = mapa_shared(tempty0, 0);
+        const uint32_t tempty_leader0 = mapa_shared(tempty0, pl);
         uint32_t tc = 0;
         if (p.fill) fill_uncovered(p, threadIdx.x, 128);  // threads 0..127 are the epilogue warps
         SegmentIter segs(p, pair, npairs);
@@ -221,7 +259,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
         for (; segs.next(p, sg); ++tc) {
             const TileCoord tcd = decode_tile(p, sg.t);
             const ClassDesc &c = p.cls[tcd.ci];
-            const uint32_t b = tc & 1, tph = (tc >> 1) & 1;
+            const uint32_t b = tc % Cfg::ACC_BUFS, tph = (tc / Cfg::ACC_BUFS) & 1;
             bool ok = mbar_wait_bounded(tfull0 + 8 * b, tph, p.wait_budget, abort_flag, p.status, kDevTimeoutEpilogue);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
@@ -237,7 +275,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 if (threadIdx.x == 0) st_release_gpu(p.flags + pair * 2 + rank, p.epoch);
                 continue;
             }
-            const int m = tcd.mb * 256 + (int)rank * 128 + row;
+            const int m = tcd.mb * (256 * CL) + (int)pr * 256 + (int)rank * 128 + row;
             const bool rvalid = m < c.M;
             int64_t off = 0;
             if (rvalid) {
@@ -279,50 +317,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
     }
 }
 
-template <int BN>
+template <int BN, int CL>
 static cudaError_t launch_tc2_bn(const TcParams &p, int grid, cudaStream_t s) {
+    using Cfg = Tc2Cfg<BN, CL>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc2_dgrad_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Tc2Cfg<BN>::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(tc2_dgrad_kernel<BN, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    tc2_dgrad_kernel<BN><<<grid, Tc2Cfg<BN>::THREADS, Tc2Cfg<BN>::SMEM, s>>>(p);
+    tc2_dgrad_kernel<BN, CL><<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_tc2(const TcParams &p, int bn, int grid, cudaStream_t s) {
+cudaError_t launch_tc2(const TcParams &p, int bn, int cl, int grid, cudaStream_t s) {
     if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
-    return bn == 256 ? launch_tc2_bn<256>(p, grid, s) : launch_tc2_bn<128>(p, grid, s);
+    if (cl == 2 && p.streamk) return cudaErrorInvalidValue;  // stream-K runs with one pair per cluster
+    if (cl == 2) {
+        if (bn == 512) return launch_tc2_bn<512, 2>(p, grid, s);
+        return bn == 256 ? launch_tc2_bn<256, 2>(p, grid, s) : launch_tc2_bn<128, 2>(p, grid, s);
+    }
+    if (bn == 512) return launch_tc2_bn<512, 1>(p, grid, s);
+    return bn == 256 ? launch_tc2_bn<256, 1>(p, grid, s) : launch_tc2_bn<128, 1>(p, grid, s);
 }
 
-int tc2_max_pairs(int num_sms) {
-    static int cached[64] = {};
+// Clusters of `cl` SM pairs that can be resident at once (1 CTA per SM).
+int tc2_max_clusters(int num_sms, int cl) {
+    static int cached[64][3] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-    cudaFuncSetAttribute(tc2_dgrad_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Cfg<256>::SMEM);
+    const int ci = cl == 2 ? 2 : 1;
+    if (dev >= 0 && dev < 64 && cached[dev][ci]) return cached[dev][ci];
+    using Cfg = Tc2Cfg<256, 1>;
+    cudaFuncSetAttribute(tc2_dgrad_kernel<256, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
-    cfg.blockDim = dim3(Tc2Cfg<256>::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Tc2Cfg<256>::SMEM;
+    cfg.gridDim = dim3((unsigned)(num_sms & ~(2 * ci - 1)), 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.x = 2 * ci;
     attr.val.clusterDim.y = 1;
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, tc2_dgrad_kernel<256>, &cfg) != cudaSuccess || clusters <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, tc2_dgrad_kernel<256, 1>, &cfg) != cudaSuccess || clusters <= 0) {
         cudaGetLastError();
-        clusters = num_sms / 2;
+        clusters = num_sms / (2 * ci);
     }
-    if (dev >= 0 && dev < 64) cached[dev] = clusters;
+    if (dev >= 0 && dev < 64) cached[dev][ci] = clusters;
     return clusters;
 }
+
+int tc2_max_pairs(int num_sms) { return tc2_max_clusters(num_sms, 1); }
 
 }  // namespace cbd

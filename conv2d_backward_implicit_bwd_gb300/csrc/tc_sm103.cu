@@ -20,15 +20,16 @@
 //   warps 0-3      epilogue: tcgen05.ld of the fp32 accumulator (warp q reads
 //                  TMEM lanes 32q..32q+31 = tile rows), RNE to bf16, 16-byte
 //                  stores to the class's strided dx pixels;
-//   warp 4         producer (im2col mode, the default): one lane issues, per
+//   warp 4         A producer (im2col mode, the default): one lane issues, per
 //                  stage, a single TMA im2col load of the 128 A rows -- each
 //                  class has its own rank-4 map over dy whose bounding box is
 //                  the class's (ht, wt) range shifted to tap (taps-1), so the
 //                  map walks the class rows in (n, ht, wt) order and the tap
 //                  (j, i) is the im2col offset; rows outside dy (padding,
 //                  borders, the flip's out-of-range taps, the M tail) read as
-//                  zero -- plus the BN/64 TMA boxes of B (w is c-contiguous, so
-//                  B is MN-major: 64 k x 64 c per box);
+//                  zero; the BN/64 TMA boxes of B (w is c-contiguous, so B is
+//                  MN-major: 64 k x 64 c per box) come from BN/64 more warps
+//                  after the MMA warp, one box each;
 //   warps 4..4+S-1 producers (cp.async mode, where a 64-channel block may cross
 //                  a group boundary or a bounding box exceeds the im2col corner
 //                  range): producer warp s loads every stage of slot s,
@@ -67,7 +68,12 @@ struct TcCfg {
     static constexpr int STAGE_OUT_BYTES = 4 * 32 * 128;  // epilogue staging: 4 warps x 32 rows x 128 B
     static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + ROWTAB_BYTES + STAGE_OUT_BYTES + BAR_BYTES;
     static constexpr int MMA_WARP = 4 + PRODUCER_WARPS;
-    static constexpr int THREADS = 32 * (MMA_WARP + 1);
+    // im2col mode: TMA issue is serialised per issuing thread, so warp 4 issues
+    // only the A load and warps B_WARP.. one 64-column B box each, on other SM
+    // sub-partitions
+    static constexpr int B_WARP = MMA_WARP + 1;
+    static constexpr int B_WARPS = IM2COL ? BN / 64 : 0;
+    static constexpr int THREADS = 32 * (MMA_WARP + 1 + B_WARPS);
 };
 
 template <int BN, bool IM2COL>
@@ -117,11 +123,14 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (IM2COL && warp == 4) {
-        // ------------------------------------------------------------ producer (TMA)
-        // One lane issues every load: per stage one im2col load of the 128 A
-        // rows (the class's map walks its (n, ht, wt) rows in order; the tap
-        // is the im2col offset) and the BN/64 boxes of B.
+    if (IM2COL && (warp == 4 || warp >= Cfg::B_WARP)) {
+        // ------------------------------------------------------------ producers (TMA)
+        // Lane 0 of warp 4 issues per stage the im2col load of the 128 A rows
+        // (the class's map walks its (n, ht, wt) rows in order; the tap is the
+        // im2col offset) and the stage's byte count; lane 0 of B warp q issues
+        // B box q (64 k x 64 c).
+        const bool do_a = warp == 4;
+        const int cb_lo = do_a ? 0 : warp - Cfg::B_WARP, cb_hi = do_a ? 0 : cb_lo + 1;
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true, issued = false;
@@ -147,12 +156,17 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
                         break;
                     }
                     const uint32_t full_s = full0 + 8 * s;
-                    mbar_arrive_expect_tx(full_s, (uint32_t)(Cfg::A_BYTES + Cfg::B_BYTES));
-                    tma_load_im2col(smem_u32(sA + s * Cfg::A_BYTES), amap, full_s, tcd.gi * g.Kg + k0, bw, bh, n0,
-                                    (uint16_t)((c.taps_x - 1 - i) * g.DW), (uint16_t)((c.taps_y - 1 - j) * g.DH));
+                    // (a B box may land before this arrive: the transaction count
+                    // dips below zero while the single arrival is still pending,
+                    // so the phase cannot complete early)
+                    if (do_a) {
+                        mbar_arrive_expect_tx(full_s, (uint32_t)(Cfg::A_BYTES + Cfg::B_BYTES));
+                        tma_load_im2col(smem_u32(sA + s * Cfg::A_BYTES), amap, full_s, tcd.gi * g.Kg + k0, bw, bh,
+                                        n0, (uint16_t)((c.taps_x - 1 - i) * g.DW),
+                                        (uint16_t)((c.taps_y - 1 - j) * g.DH));
+                    }
                     const uint32_t bdst = smem_u32(sB + s * Cfg::B_BYTES);
-#pragma unroll
-                    for (int cb = 0; cb < BN / 64; ++cb)
+                    for (int cb = cb_lo; cb < cb_hi; ++cb)
                         tma_load_5d(bdst + cb * 8192, &p.tmap_w, full_s, tcd.nb * BN + cb * 64, c.tx + g.XT * i,
                                     c.ty + g.YT * j, k0, tcd.gi);
                     issued = true;
@@ -295,7 +309,7 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < 4) {
         // ------------------------------------------------------------ epilogue
         const int row = warp * 32 + lane;  // TMEM lane = tile row
         __nv_bfloat16 *dx = static_cast<__nv_bfloat16 *>(p.dx);

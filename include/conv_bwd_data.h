@@ -134,6 +134,12 @@ conv_bwd_status conv_bwd_data_coverage(const conv_bwd_plan plan, uint8_t *row_ma
  * kernel launches one run() makes (fill + sub-GEMM kernel). */
 conv_bwd_status conv_bwd_data_path(const conv_bwd_plan plan, int32_t *path, int32_t *launches_per_run);
 
+/* Output tile of the plan's GEMM kernel: rows (M) and columns (C/G) per tile,
+ * and the number of SMs that share one tile (2 for the SM-pair tensor-core
+ * kernel, else 1).  The grouped kernel reports 0 x 0 (it has no tiles).  Any
+ * output pointer may be NULL. */
+conv_bwd_status conv_bwd_data_tile(const conv_bwd_plan plan, int32_t *tile_m, int32_t *tile_n, int32_t *sms_per_tile);
+
 /* Useful work: 2 * N * K * (C/G) * Th * Tw floating-point operations, where
  * Th = #{(ho, y): 0 <= ho*sh - ph + y*dh < Hi} counts only taps that land
  * inside dx (likewise Tw).  Also the algorithmic bytes: dy, w and dx each

@@ -252,6 +252,52 @@ def test_stream_k_and_whole_tiles(B, monkeypatch, c, forced):
         check_full(c, dx.float().cpu().numpy().astype(np.float64), g, dy, w)
 
 
+# 2-SM kernel variants: 512-wide pair tiles (two N=256 MMAs per k slice, one
+# accumulator buffer), pair tiles for C/G = 128..255, and clusters of two SM
+# pairs sharing B by TMA multicast (512-row tiles; an odd count of 256-row
+# blocks leaves the second pair of the last tile without rows).
+W512 = {"CONVBWD_DEBUG_BN": "512"}
+PAIR = {"CONVBWD_DEBUG_2SM": "1"}
+CL2 = {"CONVBWD_DEBUG_CL": "2"}
+CL2_256 = {"CONVBWD_DEBUG_CL": "2", "CONVBWD_DEBUG_BN": "256"}
+CL2_512 = {"CONVBWD_DEBUG_CL": "2", "CONVBWD_DEBUG_BN": "512"}
+PAIR_CASES = [
+    (_mk("w512_ragged_n", N=3, C=768, K=192, Hi=9, Wi=7, Y=3, X=3, pad=(1, 1), stride=(2, 2)), W512),
+    (_mk("w512_page3", N=2, C=1024, K=512, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)), W512),
+    (_mk("w512_ragged_m", N=4, C=512, K=128, Hi=17, Wi=15, Y=3, X=3, pad=(1, 1)), W512),
+    (_mk("w512_groups2", N=2, C=1024, K=256, Hi=8, Wi=9, Y=3, X=3, pad=(1, 1), groups=2), W512),
+    (_mk("w512_tail8", N=2, C=520, K=64, Hi=7, Wi=7, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)), W512),
+    (_mk("pair_cg128", N=2, C=128, K=128, Hi=12, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)), PAIR),
+    (_mk("pair_cg200", N=2, C=200, K=40, Hi=11, Wi=6, Y=2, X=4, pad=(0, 3), stride=(3, 1), dil=(2, 3)), PAIR),
+    (_mk("pair_5x5s3", N=2, C=128, K=128, Hi=19, Wi=17, Y=5, X=5, pad=(2, 2), stride=(3, 3)), PAIR),
+    (_mk("cl2_page3", N=4, C=512, K=256, Hi=1, Wi=128, Y=1, X=2, stride=(1, 2)), CL2),
+    (_mk("cl2_odd_blocks", N=3, C=256, K=96, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2)), CL2),
+    (_mk("cl2_kg_tail", N=2, C=384, K=160, Hi=9, Wi=10, Y=3, X=3, pad=(1, 1)), CL2_256),
+    (_mk("cl2_groups2", N=2, C=512, K=256, Hi=8, Wi=9, Y=3, X=3, pad=(1, 1), stride=(1, 2), groups=2), CL2),
+    (_mk("cl2_dil2_fill", N=4, C=256, K=256, Hi=12, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)), CL2_256),
+    (_mk("cl2_w512", N=3, C=1024, K=128, Hi=11, Wi=9, Y=3, X=3, pad=(1, 1), stride=(2, 2)), CL2_512),
+    (_mk("cl2_w512_one_block", N=1, C=512, K=64, Hi=8, Wi=8, Y=1, X=1), CL2_512),
+]
+
+
+@pytest.mark.parametrize("c,env", PAIR_CASES, ids=[c.name for c, _ in PAIR_CASES])
+def test_pair_tile_variants(B, monkeypatch, c, env):
+    g, dy, w = inputs(c)
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    for _ in range(2):  # the second run reuses the plan
+        got, plan = gpu_dgrad(B, c, dy, w)
+        assert plan.path()[0] == "tcgen05"
+        tm, tn, sms = plan.tile()
+        # SM pairs (256-row tiles), or clusters of two pairs (512-row tiles)
+        assert sms in (2, 4) and tm == 128 * sms, plan.tile()
+        if "CONVBWD_DEBUG_CL" in env:
+            assert sms == 4, plan.tile()
+        if "CONVBWD_DEBUG_BN" in env:
+            assert tn == int(env["CONVBWD_DEBUG_BN"]), plan.tile()
+        check_full(c, got, g, dy, w)
+
+
 def test_deterministic_and_stream_ordered(B):
     c = TC_CASES[4]
     g, dy, w = inputs(c)
