@@ -15,16 +15,18 @@
 //     stages the dy rows of the row class's taps (cp.async, 16 bytes per
 //     thread, zero-filled outside dy) in shared memory -- the next item's rows
 //     load while the current item computes (two buffers).
-//   * Warp w computes group w of the block.  For every column residue class
-//     (the v4r1 split of pages "Backward data" and "[igemm_dynamic] v4r1 bwd
-//     dynamic kernel", per pixel) and tap (j, i), the dy pixels of 16
-//     consecutive outputs are consecutive staged pixels: one ldmatrix reads
-//     the A fragment.  B fragments (w) are built once per CTA for all taps.
+//   * A warp computes one unit: 16 outputs of one column residue class (the
+//     v4r1 split of pages "Backward data" and "[igemm_dynamic] v4r1 bwd dynamic
+//     kernel", per pixel) for all 8 groups.  Per tap (j, i) the dy pixels of
+//     16 consecutive outputs are consecutive staged pixels, so ldmatrix reads
+//     the A fragments directly; B fragments (w) are built once per CTA for all
+//     taps.
 //   * Pixel lines in shared memory are XOR-swizzled in 16-byte segments so
 //     that 8 consecutive pixels' segment of one group hit 8 bank groups.
-//   * Accumulators (fp32) go back through a swizzled shared-memory tile as
-//     bf16 (RNE) and leave as full 128-byte lines of dx; pixels no tap reaches
-//     are written as +0 by the same pass (no separate fill).
+//   * Accumulators (fp32) leave as bf16 (RNE) straight from the fragments: the
+//     4 lanes of a fragment row write one group's 16 contiguous bytes, the 8
+//     groups of a store pass a pixel's full line; pixels no tap reaches are
+//     written as +0 by the same pass (no separate fill).
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -51,28 +53,40 @@ __device__ __forceinline__ uint32_t seg_addr(uint32_t base, int q, int s) {
     return base + (uint32_t)q * GCfg<CG>::LINE + ((uint32_t)(s ^ (q & 7)) << 4);
 }
 
-__device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 struct GItem {
-    int n, hi, w0, wend, tyn, ty, ht, wo_lo;
+    int n, hi, wc;       // image, dx row, chunk of the row
+    int w0, npx;         // first dx column and pixel count of the chunk
+    int tyn, ty, ht;     // the row's class: taps, first tap, class row
+    int wo_lo;           // first staged dy column
 };
 
-// item = (n, hi, chunk) -> its row class and staged column window (item count
-// < 2^31, checked by the planner)
-__device__ __forceinline__ GItem decode_item(const GroupedParams &p, int it, int nwch) {
+// row class and staged window of item (n, hi, wc)
+__device__ __forceinline__ void finish_item(const GroupedParams &p, GItem &m) {
     const Geom &g = p.g;
-    GItem m;
-    const int rest = it / nwch;
-    m.w0 = (it - rest * nwch) * p.wch;
-    m.n = rest / g.Hi;
-    m.hi = rest - m.n * g.Hi;
-    m.wend = min(m.w0 + p.wch, g.Wi);
+    m.w0 = m.wc * p.wch;
+    m.npx = min(p.wch, g.Wi - m.w0);
     const int rc = p.row_class[m.hi % g.sh];
     m.tyn = rc >> 16;
     m.ty = rc & 0xFFFF;
     m.ht = (m.hi + g.ph - m.ty * g.dh) / g.sh;  // exact when tyn > 0
-    m.wo_lo = floor_div(m.w0 + g.pw - (g.X - 1) * g.dw, g.sw);
-    return m;
+    m.wo_lo = m.wc * (p.wch / g.sw) + p.wo_c;
+}
+
+// the item `step` items after m (step = CTAs per group block, pre-split into
+// chunk / row / image digits on the host): mixed-radix add with carries
+__device__ __forceinline__ GItem next_item(const GroupedParams &p, const GItem &m) {
+    const Geom &g = p.g;
+    GItem r;
+    r.wc = m.wc + p.step_wc;
+    int carry = r.wc >= p.nwch;
+    r.wc -= carry ? p.nwch : 0;
+    r.hi = m.hi + p.step_hi + carry;
+    carry = r.hi >= g.Hi;
+    r.hi -= carry ? g.Hi : 0;
+    r.n = m.n + p.step_n + carry;
+    finish_item(p, r);
+    return r;
 }
 
 template <int CG>
@@ -80,11 +94,11 @@ __global__ void __launch_bounds__(128) grouped_dgrad_kernel(const __grid_constan
     using C = GCfg<CG>;
     constexpr int LOG_SEGS = CG == 8 ? 3 : 4;
     constexpr int NTHREADS = 128;
+    constexpr int PSTEP = NTHREADS / GCfg<CG>::SEGS;  // staged pixels per pass of the CTA
     extern __shared__ __align__(128) uint8_t gsm[];
     const Geom &g = p.g;
     const uint32_t *wfrag = reinterpret_cast<const uint32_t *>(gsm);  // [tap][NR][lane][8 groups]
     const uint32_t buf0 = smem_u32(gsm + p.wfrag_bytes);             // two buffers of [tyn][span] pixel lines
-    const uint32_t outb = buf0 + 2 * p.buf_bytes;                    // [wch] pixel lines
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const int gb = blockIdx.x % p.gblocks;
@@ -116,8 +130,6 @@ __global__ void __launch_bounds__(128) grouped_dgrad_kernel(const __grid_constan
         __syncthreads();
     }
 
-    const int nwch = (g.Wi + p.wch - 1) / p.wch;
-    const int items = g.N * g.Hi * nwch;
     const int64_t kbytes = (int64_t)g.K * 2;
     const int mi = lane >> 3;                       // ldmatrix: lane addresses row lane % 8 of matrix mi
     const int trow = (mi & 1) * 8 + (lane & 7);     // this lane's A row within the 16-row tile
@@ -129,63 +141,69 @@ __global__ void __launch_bounds__(128) grouped_dgrad_kernel(const __grid_constan
             const bool hok = ho >= 0 && ho < g.Ho;
             const uint8_t *rowp = static_cast<const uint8_t *>(p.dy) +
                                   ((int64_t)m.n * g.Ho + (hok ? ho : 0)) * g.Wo * kbytes + cofs * 2;
-            const uint32_t rb = bb + (uint32_t)(jj * p.span * C::LINE);
-            for (int e = threadIdx.x; e < (p.span << LOG_SEGS); e += NTHREADS) {
-                const int q = e >> LOG_SEGS, s = e & (C::SEGS - 1);
-                const int wo = m.wo_lo + q;
+            // thread t copies segment t % SEGS of pixels t / SEGS, + PSTEP, ...: the
+            // segment's swizzled slot is the same for all of them (PSTEP % 8 == 0)
+            const int s = threadIdx.x & (C::SEGS - 1);
+            int q = threadIdx.x >> LOG_SEGS;
+            uint32_t dst = seg_addr<CG>(bb + (uint32_t)(jj * p.span * C::LINE), q, s);
+            int wo = m.wo_lo + q;
+            const uint8_t *src = rowp + (int64_t)wo * kbytes + s * 16;
+            for (; q < p.span; q += PSTEP, wo += PSTEP, dst += PSTEP * C::LINE, src += PSTEP * kbytes) {
                 const bool ok = hok && wo >= 0 && wo < g.Wo;
-                const uint8_t *src = ok ? rowp + wo * kbytes + s * 16 : static_cast<const uint8_t *>(p.dy);
-                cp_async_16(seg_addr<CG>(rb, q, s), src, ok ? 16u : 0u);
+                cp_async_16(dst, ok ? src : static_cast<const uint8_t *>(p.dy), ok ? 16u : 0u);
             }
         }
     };
 
+    // first item of this CTA: (n, hi, wc) = cta in mixed radix (N, Hi, nwch)
+    GItem m;
+    m.wc = cta % p.nwch;
+    m.hi = (cta / p.nwch) % g.Hi;
+    m.n = cta / (p.nwch * g.Hi);
+    finish_item(p, m);
     int b = 0;
-    GItem m = decode_item(p, cta < items ? cta : 0, nwch);
-    if (cta < items) stage(m, 0);
+    if (m.n < g.N) stage(m, 0);
     cp_async_commit();
-    for (int it = cta; it < items; it += ncta, b ^= 1) {
-        const bool more = it + ncta < items;
-        const GItem mn = decode_item(p, more ? it + ncta : it, nwch);
-        if (more) stage(mn, b ^ 1);
+    const int nunits = g.sw * p.per_r;
+    while (m.n < g.N) {
+        const GItem mn = next_item(p, m);
+        if (mn.n < g.N) stage(mn, b ^ 1);
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
 
-        // units (column residue r, 16-pixel m-tile) of this item, warp w takes
-        // units w, w + 4, ...; a unit covers all 8 groups of the block
+        // units (column residue r, 16-pixel m-tile mt) of this item: warp w
+        // takes units w, w + 4, ...; a unit covers all 8 groups of the block
         const uint32_t bb = buf0 + (uint32_t)b * p.buf_bytes;
-        const int per_r = (((p.wch / g.sw) + 15) >> 4);  // m-tile slots per residue
-        for (int u = warp; u < g.sw * per_r; u += 4) {
-            const int r = u / per_r, mt = u - r * per_r;
-            const int cnt = (m.wend - (m.w0 + r) + g.sw - 1) / g.sw;  // outputs wi = w0 + r + sw t in the chunk
-            if (mt * 16 >= cnt) continue;
-            const int cc = p.col_class[r];  // w0 is a multiple of sw
-            const int txn = cc >> 16, tx = cc & 0xFFFF;
-            float acc[8][4 * C::NT];
+        const int64_t cbytes = (int64_t)g.C * 2;
+        uint8_t *dxrow = static_cast<uint8_t *>(p.dx) + ((((int64_t)m.n * g.Hi + m.hi) * g.Wi + m.w0) * g.C + cofs) * 2;
+        int r = warp / p.per_r, mt = warp - r * p.per_r;
+        for (int u = warp; u < nunits; u += 4) {
+            if (r + g.sw * 16 * mt < m.npx) {
+                const int cc = p.col_class[r];  // w0 is a multiple of sw
+                const int txn = cc >> 16, tx = cc & 0xFFFF;
+                float acc[8][4 * C::NT];
 #pragma unroll
-            for (int gl = 0; gl < 8; ++gl)
+                for (int gl = 0; gl < 8; ++gl)
 #pragma unroll
-                for (int v = 0; v < 4 * C::NT; ++v) acc[gl][v] = 0.f;
-            if (m.tyn > 0 && txn > 0) {
-                const int wt0 = (m.w0 + r + g.pw - tx * g.dw) / g.sw;  // exact
-                for (int jj = 0; jj < m.tyn; ++jj) {
-                    const int ho = m.ht - jj * g.DH;
-                    if (ho < 0 || ho >= g.Ho) continue;  // staged as zeros: nothing to add
-                    const int y = m.ty + g.YT * jj;
-                    const uint32_t rowb = bb + (uint32_t)(jj * p.span * C::LINE);
-                    for (int ii = 0; ii < txn; ++ii) {
-                        const int tap = y * g.X + tx + g.XT * ii;
-                        const int q = min(wt0 - ii * g.DW - m.wo_lo + mt * 16 + trow, p.span - 1);
-                        const uint32_t arow = rowb + (uint32_t)q * C::LINE;
-                        const int qs = q & 7;
-                        const uint4 *wl = reinterpret_cast<const uint4 *>(wfrag + (tap * C::NR * 32 + lane) * 8);
-#pragma unroll
-                        for (int r2 = 0; r2 < C::NR; ++r2) {
-                            // fragments of the 8 groups: two 16-byte loads
-                            const uint4 f0 = wl[r2 * 64], f1 = wl[r2 * 64 + 1];
-                            const uint32_t bfr[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                    for (int v = 0; v < 4 * C::NT; ++v) acc[gl][v] = 0.f;
+                if (m.tyn > 0 && txn > 0) {
+                    const int qrow = p.col_q[r] + mt * 16 + trow;  // staged pixel of this lane's row, tap i = 0
+                    for (int jj = 0; jj < m.tyn; ++jj) {
+                        const int ho = m.ht - jj * g.DH;
+                        if (ho < 0 || ho >= g.Ho) continue;  // staged as zeros: nothing to add
+                        const int y = m.ty + g.YT * jj;
+                        const uint32_t rowb = bb + (uint32_t)(jj * p.span * C::LINE);
+                        for (int ii = 0; ii < txn; ++ii) {
+                            const int tap = y * g.X + tx + g.XT * ii;
+                            const int q = min(qrow - ii * g.DW, p.span - 1);
+                            const uint32_t arow = rowb + (uint32_t)q * C::LINE;
+                            const int qs = q & 7;
                             if (CG == 8) {
+                                // fragments of the 8 groups: two 16-byte loads
+                                const uint4 *wl = reinterpret_cast<const uint4 *>(wfrag + (tap * 32 + lane) * 8);
+                                const uint4 f0 = wl[0], f1 = wl[1];
+                                const uint32_t bfr[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
                                 for (int gp = 0; gp < 4; ++gp) {
                                     // matrices: rows 0-7 | 8-15 of group 2gp, then of group 2gp + 1
@@ -208,70 +226,57 @@ __global__ void __launch_bounds__(128) grouped_dgrad_kernel(const __grid_constan
                                         : "r"(a2), "r"(a3), "r"(bfr[2 * gp + 1]));
                                 }
                             } else {
-                                // r2 = 2 nt + kh: the A fragments of a group serve both n-tiles,
-                                // so they are loaded with the kh = 0 fragments and kept
-                                (void)bfr;
-                            }
-                        }
-                        if (CG == 16) {
 #pragma unroll
-                            for (int gl = 0; gl < 8; ++gl) {
-                                // matrices (rows 0-7 | 8-15) x (k 0-7 | 8-15) of group gl
-                                const int seg = 2 * gl + (mi >> 1);
-                                uint32_t a0, a1, a2, a3;
-                                asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                                             : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                                             : "r"(arow + ((uint32_t)(seg ^ qs) << 4)));
+                                for (int gl = 0; gl < 8; ++gl) {
+                                    // matrices (rows 0-7 | 8-15) x (k 0-7 | 8-15) of group gl
+                                    const int seg = 2 * gl + (mi >> 1);
+                                    uint32_t a0, a1, a2, a3;
+                                    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                                                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                                                 : "r"(arow + ((uint32_t)(seg ^ qs) << 4)));
 #pragma unroll
-                                for (int nt = 0; nt < C::NT; ++nt) {
-                                    const uint32_t b0 = wfrag[((tap * C::NR + 2 * nt) * 32 + lane) * 8 + gl];
-                                    const uint32_t b1 = wfrag[((tap * C::NR + 2 * nt + 1) * 32 + lane) * 8 + gl];
-                                    asm volatile(
-                                        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-                                        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-                                        : "+f"(acc[gl][4 * nt]), "+f"(acc[gl][4 * nt + 1]), "+f"(acc[gl][4 * nt + 2]),
-                                          "+f"(acc[gl][4 * nt + 3])
-                                        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                                    for (int nt = 0; nt < C::NT; ++nt) {
+                                        const uint32_t b0 = wfrag[((tap * C::NR + 2 * nt) * 32 + lane) * 8 + gl];
+                                        const uint32_t b1 = wfrag[((tap * C::NR + 2 * nt + 1) * 32 + lane) * 8 + gl];
+                                        asm volatile(
+                                            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                                            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                                            : "+f"(acc[gl][4 * nt]), "+f"(acc[gl][4 * nt + 1]),
+                                              "+f"(acc[gl][4 * nt + 2]), "+f"(acc[gl][4 * nt + 3])
+                                            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                                    }
                                 }
                             }
                         }
                     }
                 }
+                // accumulators -> bf16 -> dx: lane (gid, tig) holds rows gid, gid + 8
+                // and channels nt*8 + 2 tig (+1) of every group: 4-byte stores, the
+                // 4 lanes of a row covering one group's 16 contiguous bytes
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int q = r + g.sw * (mt * 16 + gid + 8 * h);
+                    if (q >= m.npx) continue;
+                    uint32_t *o = reinterpret_cast<uint32_t *>(dxrow + q * cbytes) + tig;
+#pragma unroll
+                    for (int gl = 0; gl < 8; ++gl)
+#pragma unroll
+                        for (int nt = 0; nt < C::NT; ++nt) {
+                            __nv_bfloat162 v =
+                                __floats2bfloat162_rn(acc[gl][4 * nt + 2 * h], acc[gl][4 * nt + 2 * h + 1]);
+                            o[(gl * C::NT + nt) * 4] = *reinterpret_cast<uint32_t *>(&v);
+                        }
+                }
             }
-            // accumulators -> bf16 -> output tile at chunk pixel r + sw t: lane
-            // (gid, tig) holds rows gid, gid + 8 and channels nt*8 + 2 tig (+1)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int t = mt * 16 + gid + 8 * h;
-                if (t >= cnt) continue;
-                const int q = r + g.sw * t;
-                const uint32_t orow = outb + (uint32_t)q * C::LINE + 4 * tig;
-                const int qs = q & 7;
-#pragma unroll
-                for (int gl = 0; gl < 8; ++gl)
-#pragma unroll
-                    for (int nt = 0; nt < C::NT; ++nt) {
-                        __nv_bfloat162 v = __floats2bfloat162_rn(acc[gl][4 * nt + 2 * h], acc[gl][4 * nt + 2 * h + 1]);
-                        const uint32_t a = orow + ((uint32_t)((gl * C::NT + nt) ^ qs) << 4);
-                        asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(*reinterpret_cast<uint32_t *>(&v))
-                                     : "memory");
-                    }
+            mt += 4;
+            while (mt >= p.per_r) {
+                mt -= p.per_r;
+                ++r;
             }
         }
-        __syncthreads();
-        // output tile -> dx: full 16-byte segments, consecutive threads on consecutive segments
-        const int npx = m.wend - m.w0;
-        uint8_t *dxb = static_cast<uint8_t *>(p.dx) + ((((int64_t)m.n * g.Hi + m.hi) * g.Wi + m.w0) * g.C + cofs) * 2;
-        const int64_t cbytes = (int64_t)g.C * 2;
-        for (int e = threadIdx.x; e < (npx << LOG_SEGS); e += NTHREADS) {
-            const int s = e & (C::SEGS - 1), q = e >> LOG_SEGS;
-            uint4 v;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                         : "r"(seg_addr<CG>(outb, q, s)));
-            *reinterpret_cast<uint4 *>(dxb + q * cbytes + s * 16) = v;
-        }
+        __syncthreads();  // every warp is done with buffer b before it is restaged
         m = mn;
+        b ^= 1;
     }
     cp_async_wait<0>();
 }
@@ -289,7 +294,7 @@ GroupedLayout grouped_layout(const Geom &g) {
         L.wch = std::max(g.sw, wch - wch % g.sw);
         L.span = (L.wch - 1 + (g.X - 1) * g.dw) / g.sw + 2;
         L.buf_bytes = tymax * L.span * line;
-        L.smem = L.wfrag_bytes + std::max(2 * L.buf_bytes + L.wch * line, raw_w);
+        L.smem = L.wfrag_bytes + std::max(2 * L.buf_bytes, raw_w);
         if (L.smem <= 200 * 1024 && L.wch / g.sw <= 64) break;
     }
     return L;
@@ -301,17 +306,37 @@ static cudaError_t launch_grouped_cg(const GroupedParams &p, const GroupedLayout
     if (e != cudaSuccess) return e;
     const int per_sm = std::max(1, std::min(16, (227 * 1024) / (L.smem + 1024)));
     const int sms = num_sms > 0 ? num_sms : 148;
-    const int per_gb = std::max(1, (sms * per_sm + p.gblocks - 1) / p.gblocks);
-    grouped_dgrad_kernel<CG><<<per_gb * p.gblocks, 128, L.smem, s>>>(p);
+    int per_gb = std::max(1, (sms * per_sm + p.gblocks - 1) / p.gblocks);
+    const int64_t items = (int64_t)p.g.N * p.g.Hi * p.nwch;
+    per_gb = (int)std::min<int64_t>(per_gb, items);
+    GroupedParams q = p;
+    q.step_wc = per_gb % q.nwch;
+    q.step_hi = (per_gb / q.nwch) % q.g.Hi;
+    q.step_n = per_gb / (q.nwch * q.g.Hi);
+    grouped_dgrad_kernel<CG><<<per_gb * p.gblocks, 128, L.smem, s>>>(q);
     return cudaGetLastError();
 }
 
 cudaError_t launch_grouped(GroupedParams &p, int num_sms, cudaStream_t s) {
     const GroupedLayout L = grouped_layout(p.g);
+    const Geom &g = p.g;
     p.wch = L.wch;
     p.span = L.span;
     p.wfrag_bytes = L.wfrag_bytes;
     p.buf_bytes = L.buf_bytes;
+    p.nwch = (g.Wi + L.wch - 1) / L.wch;
+    p.per_r = (L.wch / g.sw + 15) / 16;
+    // first staged dy column of a chunk at w0 (a multiple of sw):
+    // floor((w0 + pw - (X-1) dw) / sw) = w0 / sw + floor((pw - (X-1) dw) / sw)
+    const int a = g.pw - (g.X - 1) * g.dw;
+    p.wo_c = a >= 0 ? a / g.sw : -((-a + g.sw - 1) / g.sw);
+    // residue r of a class with first tap tx: its output t = 0 reads dy column
+    // (w0 + r + pw - tx dw) / sw for tap i = 0, staged at that minus the first column
+    for (int r = 0; r < g.sw && r < 64; ++r) {
+        const int tx = p.col_class[r] & 0xFFFF;
+        const int num = r + g.pw - tx * g.dw;  // a multiple of sw where the class has taps
+        p.col_q[r] = ((p.col_class[r] >> 16) > 0 ? num / g.sw : 0) - p.wo_c;
+    }
     return p.g.Cg == 8 ? launch_grouped_cg<8>(p, L, num_sms, s) : launch_grouped_cg<16>(p, L, num_sms, s);
 }
 

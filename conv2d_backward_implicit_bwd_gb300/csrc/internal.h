@@ -103,10 +103,15 @@ struct GroupedParams {
     int32_t gblocks;         // G / 8
     int32_t row_class[64];   // per row residue hi % sh: (taps_y << 16) | ty (taps 0: no class writes it)
     int32_t col_class[64];   // per column residue wi % sw: (taps_x << 16) | tx
+    int32_t col_q[64];       // per column residue r: staged pixel of output t = 0, tap i = 0
     int32_t wch;             // dx pixels per item (a multiple of sw)
     int32_t span;            // staged dy pixels per tap row (covers every tap of an item)
     int32_t wfrag_bytes;     // shared memory of the w fragments
     int32_t buf_bytes;       // shared memory of one staged-dy buffer
+    int32_t nwch;            // items per dx row
+    int32_t per_r;           // 16-pixel m-tiles per column residue and item
+    int32_t wo_c;            // first staged dy column of an item = w0 / sw + wo_c
+    int32_t step_wc, step_hi, step_n;  // the item stride (CTAs per group block) as (chunk, row, image)
 };
 
 struct GroupedLayout {

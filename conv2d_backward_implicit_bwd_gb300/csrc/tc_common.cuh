@@ -90,6 +90,32 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Split TMEM load: issue 32 columns without waiting, and wait for every
+// outstanding load of this warp.  The wait names the destination registers
+// as read-write operands, so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                   "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
+                   "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+                 :
+                 : "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets (16-byte units), descriptor version 1, 128-byte swizzle.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
@@ -144,16 +170,52 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64]) {
 // written by each thread (its row) into the warp's 4 KB shared-memory slice
 // with XOR-swizzled 16-byte chunks, then read back so that 8 lanes cover one
 // row's 128 contiguous bytes: every store instruction writes four full
-// 128-byte row segments instead of 32 scattered 16-byte pieces.  `off` is the
-// dx element offset of this thread's row at the tile's first channel, `col0`
-// that channel's index within the group; channels >= Cg are not written.
-// With `parts` set, the fp32 partial tiles of `nparts` stream-K workers
-// (slots `pstride` float4 apart, layout [64 column chunks of 4][128 rows],
-// this thread's row `prow`) are added before rounding.
+// 128-byte row segments instead of 32 scattered 16-byte pieces.  TMEM is read
+// 32 columns at a time, the next load in flight while the current columns are
+// converted and stored.  `off` is the dx element offset of this thread's row
+// at the tile's first channel, `col0` that channel's index within the group;
+// channels >= Cg are not written.  With `parts` set, the fp32 partial tiles of
+// `nparts` stream-K workers (slots `pstride` float4 apart, layout [64 column
+// chunks of 4][128 rows], this thread's row `prow`) are added before rounding.
+__device__ __forceinline__ void add_partials32(uint32_t (&v)[32], const float4 *parts, int nparts, size_t pstride,
+                                               int prow, int cc, int half) {
+    for (int w = 0; w < nparts; ++w) {
+        const float4 *pp = parts + (size_t)w * pstride + (size_t)(cc * 16 + half * 8) * 128 + prow;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 a = pp[(size_t)i * 128];
+            v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + a.x);
+            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + a.y);
+            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + a.z);
+            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + a.w);
+        }
+    }
+}
+
+// 32 fp32 columns of this thread's row -> bf16 -> 16-byte chunks 4*half .. 4*half+3
+// of the row's 128 staged bytes (chunk index XOR row % 8)
+__device__ __forceinline__ void stage_half(const uint32_t (&v)[32], uint32_t sbase, int lane, int half) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 h2 =
+                __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]), __uint_as_float(v[8 * q + 2 * e + 1]));
+            pk[e] = *reinterpret_cast<uint32_t *>(&h2);
+        }
+        const uint32_t a = sbase + (uint32_t)lane * 128u + ((uint32_t)((4 * half + q) ^ (lane & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]),
+                     "r"(pk[3])
+                     : "memory");
+    }
+}
+
 template <int BN>
 __device__ __forceinline__ void epilogue_rows(uint32_t taddr, uint8_t *stage, int lane, bool rvalid, int64_t off,
                                               int col0, int Cg, __nv_bfloat16 *dx, const float4 *parts = nullptr,
                                               int nparts = 0, size_t pstride = 0, int prow = 0) {
+    constexpr int NC = BN / 64;
     const uint32_t sbase = smem_u32(stage);
     int64_t roff[8];
     bool rok[8];
@@ -166,35 +228,18 @@ __device__ __forceinline__ void epilogue_rows(uint32_t taddr, uint8_t *stage, in
         rok[it] = __shfl_sync(0xffffffffu, rvalid ? 1 : 0, row) != 0;
     }
     const int ch = lane & 7;
+    uint32_t va[32], vb[32];
+    tmem_ld32_issue(taddr, va);
+    tmem_wait_ld(va);
 #pragma unroll 1
-    for (int cc = 0; cc < BN / 64; ++cc) {
-        uint32_t v[64];
-        tmem_ld64(taddr + cc * 64, v);
-        for (int w = 0; w < nparts; ++w) {
-            const float4 *pp = parts + (size_t)w * pstride + (size_t)(cc * 16) * 128 + prow;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 a = pp[(size_t)i * 128];
-                v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + a.x);
-                v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + a.y);
-                v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + a.z);
-                v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + a.w);
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]),
-                                                          __uint_as_float(v[8 * q + 2 * e + 1]));
-                pk[e] = *reinterpret_cast<uint32_t *>(&h2);
-            }
-            const uint32_t a = sbase + (uint32_t)lane * 128u + ((uint32_t)(q ^ (lane & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]),
-                         "r"(pk[3])
-                         : "memory");
-        }
+    for (int cc = 0; cc < NC; ++cc) {
+        tmem_ld32_issue(taddr + cc * 64 + 32, vb);
+        add_partials32(va, parts, nparts, pstride, prow, cc, 0);
+        stage_half(va, sbase, lane, 0);
+        tmem_wait_ld(vb);
+        if (cc + 1 < NC) tmem_ld32_issue(taddr + (cc + 1) * 64, va);
+        add_partials32(vb, parts, nparts, pstride, prow, cc, 1);
+        stage_half(vb, sbase, lane, 1);
         __syncwarp();
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
@@ -209,11 +254,12 @@ __device__ __forceinline__ void epilogue_rows(uint32_t taddr, uint8_t *stage, in
             if (rok[it] && col < Cg) *reinterpret_cast<uint4 *>(dx + roff[it] + cc * 64 + ch * 8) = val;
         }
         __syncwarp();
+        if (cc + 1 < NC) tmem_wait_ld(va);
     }
 }
 
-// Stream-K contributor: this thread's accumulator row -> fp32 partial slot
-// (layout [64 column chunks of 4][128 rows]: a warp writes 512 contiguous bytes).
+// Park one warp's 32 accumulator rows as an fp32 partial tile (stream-K
+// contributor): column chunk c of 4 floats of row r at slot[c * 128 + r].
 template <int BN>
 __device__ __forceinline__ void store_partial_rows(uint32_t taddr, int prow, float4 *slot) {
 #pragma unroll 1
