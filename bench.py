@@ -42,6 +42,12 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 TC2_SOURCES = ("tc_common.cuh", "tc2_sm103.cu", "capi.cpp", "internal.h")
 GROUPED_SOURCES = ("tc_common.cuh", "grouped.cu", "capi.cpp", "internal.h")
 TRAFFIC = {
+    # ncu --set full, tc2_dgrad_kernel<512, 1>, one launch on the page-3 shape:
+    # dram__bytes_read.sum 33.63 MB + dram__bytes_write.sum 1.02 MB
+    "cfg3_bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "sha": "726ce1d6449ec854", "bytes": 34.655e6},
+    # grouped_dgrad_kernel<8> on the 64x56x56x256 G=32 layer: 25.81 MB + 44.98 MB
+    "cfg4_bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": GROUPED_SOURCES, "sha": "c4c49777803f970d",
+                                                  "bytes": 70.785e6},
 }
 
 
@@ -312,8 +318,9 @@ def main():
 
     peaks = load_peaks()
     kmean = sum(kern_ms) / len(kern_ms)
-    kernel_name = {"tcgen05": "tc2_dgrad_kernel / tc_dgrad_kernel", "grouped": "grouped_dgrad_kernel",
-                   "simt": "simt_dgrad_kernel"}[path]
+    tm, tn, tsms = plan.tile()
+    kernel_name = {"tcgen05": (f"tc2_dgrad_kernel<{tn}, {tsms // 2}>" if tsms >= 2 else f"tc_dgrad_kernel<{tn}>"),
+                   "grouped": f"grouped_dgrad_kernel<{case.C // case.groups}>", "simt": "simt_dgrad_kernel"}[path]
     if path == "tcgen05":
         achieved = useful / (kmean * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
