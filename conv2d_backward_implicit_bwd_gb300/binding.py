@@ -24,7 +24,7 @@ EXPORTED = [
     "conv_bwd_data_subgemm_info", "conv_bwd_data_coverage", "conv_bwd_data_path", "conv_bwd_data_tile", "conv_bwd_data_work",
     "conv_bwd_data_run", "conv_bwd_data_run_host", "conv_bwd_data_get_status", "conv_bwd_data_set_timing",
     "conv_bwd_data_last_timing", "conv_bwd_data_selftest_wait_timeout", "conv_bwd_status_string",
-    "conv_bwd_data_version", "conv_bwd_data_run_noalloc",
+    "conv_bwd_data_version", "conv_bwd_data_run_noalloc", "conv_bwd_data_run_forward",
 ]
 
 
@@ -59,6 +59,7 @@ def _load():
         "conv_bwd_data_tile": [vp, P(i32), P(i32), P(i32)],
         "conv_bwd_data_work": [vp, P(ctypes.c_double), P(ctypes.c_double)],
         "conv_bwd_data_run": [vp, vp, vp, vp, vp],
+        "conv_bwd_data_run_forward": [vp, vp, vp, vp, vp],
         "conv_bwd_data_run_host": [vp, vp, vp, vp, vp, vp, vp, vp],
         "conv_bwd_data_get_status": [vp, vp, P(i32)],
         "conv_bwd_data_set_timing": [vp, i32],
@@ -187,6 +188,18 @@ class Plan:
         """Raw-pointer form; returns the status code instead of raising."""
         return _lib.conv_bwd_data_run(self._h, ctypes.c_void_p(dy_ptr), ctypes.c_void_p(w_ptr),
                                       ctypes.c_void_p(dx_ptr), ctypes.c_void_p(stream_handle))
+
+    def run_forward(self, x, w, y, stream=None):
+        """y <- conv(x, w), the forward convolution of the plan's geometry (x has
+        dx's shape, y has dy's shape; bf16 NHWC plans)."""
+        _check(_lib.conv_bwd_data_run_forward(self._h, ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w.data_ptr()),
+                                              ctypes.c_void_p(y.data_ptr()), _stream_handle(stream)),
+               "conv_bwd_data_run_forward")
+
+    def run_forward_ptr(self, x_ptr: int, w_ptr: int, y_ptr: int, stream_handle: int = 0) -> int:
+        """Raw-pointer form of run_forward; returns the status code."""
+        return _lib.conv_bwd_data_run_forward(self._h, ctypes.c_void_p(x_ptr), ctypes.c_void_p(w_ptr),
+                                              ctypes.c_void_p(y_ptr), ctypes.c_void_p(stream_handle))
 
     def run_host(self, dy_h, w_h, dx_h, dy_d, w_d, dx_d, stream=None):
         """Host buffers in, host buffer out (copies ordered on the stream)."""

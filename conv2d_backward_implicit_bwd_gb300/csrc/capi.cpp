@@ -59,6 +59,10 @@ struct conv_bwd_plan_s {
     float4 *d_partials = nullptr;         // stream-K workspace: per pair and CTA, one 128x256 fp32 tile
     int32_t *d_flags = nullptr;           // stream-K flags, tagged with the launch epoch
     int32_t epoch = 0;
+    // forward convolution with the same geometry (the adjoint of run): maps
+    // keyed by the x and w pointers
+    const void *fwd_x_ptr = nullptr, *fwd_w_ptr = nullptr;
+    CUtensorMap fwd_tmap_x, fwd_tmap_w;
     std::mutex mu;
 };
 
@@ -215,6 +219,56 @@ bool encode_a_maps(conv_bwd_plan_s *p, const void *dy) {
     return true;
 }
 
+// Forward convolution: the im2col walk over x visits the Wo x Ho base pixels
+// (wo*sw - pw, ho*sh - ph) with traversal strides (sw, sh), so the bounding box
+// runs from (-pw, -ph) to the last base pixel.
+void fwd_corners(const Geom &g, int lo[2], int hi[2]) {
+    lo[0] = -g.pw;
+    lo[1] = -g.ph;
+    hi[0] = -g.pw + (g.Wo - 1) * g.sw - (g.Wi - 1);
+    hi[1] = -g.ph + (g.Ho - 1) * g.sh - (g.Hi - 1);
+}
+
+bool fwd_supported(const conv_bwd_plan_s *p) {
+    const conv_bwd_desc &d = p->desc;
+    const Geom &g = p->g;
+    if (d.dtype != CONV_BWD_BF16 || d.layout != CONV_BWD_NHWC_KYXC) return false;
+    if (g.Cg % 8 || g.Kg % 8 || (g.G > 1 && g.Cg % 64)) return false;
+    if (g.sh > 8 || g.sw > 8 || (g.X - 1) * g.dw > 127 || (g.Y - 1) * g.dh > 127) return false;
+    if ((int64_t)d.N * g.Ho * g.Wo >= (1LL << 31) - 128) return false;
+    int lo[2], hi[2];
+    fwd_corners(g, lo, hi);
+    for (int q = 0; q < 2; ++q)
+        if (lo[q] < -128 || lo[q] > 127 || hi[q] < -128 || hi[q] > 127) return false;
+    return true;
+}
+
+int fwd_bn(const Geom &g) { return g.Kg >= 256 ? 256 : 128; }
+
+bool encode_fwd_maps(conv_bwd_plan_s *p, const void *x, const void *w) {
+    PFN_encodeIm2col enc_i = get_encode_im2col();
+    PFN_encodeTiled enc_t = get_encode_tiled();
+    if (!enc_i || !enc_t) return false;
+    const Geom &g = p->g;
+    cuuint64_t xdims[4] = {(cuuint64_t)g.C, (cuuint64_t)g.Wi, (cuuint64_t)g.Hi, (cuuint64_t)g.N};
+    cuuint64_t xstr[3] = {(cuuint64_t)g.C * 2, (cuuint64_t)g.Wi * g.C * 2, (cuuint64_t)g.Hi * g.Wi * g.C * 2};
+    cuuint32_t trav[4] = {1, (cuuint32_t)g.sw, (cuuint32_t)g.sh, 1};
+    int lo[2], hi[2];
+    fwd_corners(g, lo, hi);
+    if (enc_i(&p->fwd_tmap_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), xdims, xstr, lo, hi, 64, 128,
+              trav, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2_promotion(),
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    cuuint64_t wdims[5] = {(cuuint64_t)g.Cg, (cuuint64_t)g.X, (cuuint64_t)g.Y, (cuuint64_t)g.Kg, (cuuint64_t)g.G};
+    cuuint64_t wstr[4] = {(cuuint64_t)g.Cg * 2, (cuuint64_t)g.X * g.Cg * 2, (cuuint64_t)g.Y * g.X * g.Cg * 2,
+                          (cuuint64_t)g.Kg * g.Y * g.X * g.Cg * 2};
+    cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)fwd_bn(g), 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return enc_t(&p->fwd_tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(w), wdims, wstr, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2_promotion(),
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 const char *env(const char *k) {
     const char *v = std::getenv(k);
     return (v && *v) ? v : nullptr;
@@ -343,6 +397,8 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
         im2col_corners(g, c, lo, hi);
         for (int q = 0; q < 2; ++q)
             if (lo[q] < -128 || lo[q] > 127 || hi[q] < -128 || hi[q] > 127) p->im2col = false;
+        // the tap is the im2col offset: keep it within 7 bits
+        if ((c.taps_x - 1) * g.DW > 127 || (c.taps_y - 1) * g.DH > 127) p->im2col = false;
     }
     if (const char *f = env("CONVBWD_DEBUG_NOIM2COL")) p->im2col = p->im2col && f[0] == '0';
     // 256-row tiles on SM pairs (tcgen05 cta_group::2): each SM then loads only
@@ -707,6 +763,43 @@ conv_bwd_status conv_bwd_data_run_host(conv_bwd_plan p, const void *dy_h, const 
     conv_bwd_status st = conv_bwd_data_run(p, dy_d, w_d, dx_d, stream);
     if (st != CONV_BWD_OK) return st;
     if (cudaMemcpyAsync(dx_h, dx_d, ndx, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_run_forward(conv_bwd_plan p, const void *x, const void *w, void *y, void *stream) {
+    if (!p || !x || !w || !y) return CONV_BWD_ERR_INVALID_ARG;
+    if (!fwd_supported(p)) return CONV_BWD_ERR_UNSUPPORTED;
+    if (!p->has_device || !p->d_status) return CONV_BWD_ERR_CUDA;
+    const conv_bwd_desc &d = p->desc;
+    const Geom &g = p->g;
+    const size_t nx = (size_t)d.N * d.C * d.Hi * d.Wi * 2, nw = (size_t)d.K * g.Cg * d.Y * d.X * 2,
+                 ny = (size_t)d.N * d.K * g.Ho * g.Wo * 2;
+    if (ranges_overlap(x, nx, y, ny) || ranges_overlap(w, nw, y, ny)) return CONV_BWD_ERR_INVALID_ARG;
+    if (((uintptr_t)x | (uintptr_t)w | (uintptr_t)y) % 16) return CONV_BWD_ERR_MISALIGNED;
+    std::lock_guard<std::mutex> lock(p->mu);
+    if (p->fwd_x_ptr != x || p->fwd_w_ptr != w) {
+        if (!encode_fwd_maps(p, x, w)) return CONV_BWD_ERR_CUDA;
+        p->fwd_x_ptr = x;
+        p->fwd_w_ptr = w;
+    }
+    FwdParams fp;
+    std::memset(&fp, 0, sizeof(fp));
+    fp.tmap_x = p->fwd_tmap_x;
+    fp.tmap_w = p->fwd_tmap_w;
+    fp.y = y;
+    fp.status = p->d_status;
+    fp.wait_budget = p->wait_budget;
+    fp.g = g;
+    const int bn = fwd_bn(g);
+    const int64_t M = (int64_t)d.N * g.Ho * g.Wo;
+    fp.m_tiles = (int)((M + 127) / 128);
+    fp.n_tiles = (g.Kg + bn - 1) / bn;
+    fp.kb_per_tap = (g.Cg + 63) / 64;
+    const int64_t total = (int64_t)fp.m_tiles * fp.n_tiles * g.G;
+    if (total >= (1LL << 31)) return CONV_BWD_ERR_UNSUPPORTED;
+    fp.total_tiles = (int)total;
+    const int grid = (int)std::min<int64_t>(total, p->num_sms);
+    if (launch_fwd(fp, bn, grid, (cudaStream_t)stream) != cudaSuccess) return CONV_BWD_ERR_CUDA;
     return CONV_BWD_OK;
 }
 

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(128) grouped_dgrad_kernel(const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const int gb = blockIdx.x % p.gblocks;
-    const int cta = blockIdx.x / p.gblocks, ncta = gridDim.x / p.gblocks;
+    const int cta = blockIdx.x / p.gblocks;
     const int64_t cofs = (int64_t)gb * 8 * CG;  // first channel of the block (dy and dx)
 
     // B fragments of the block's 8 groups for every tap.  The groups' w rows

@@ -94,6 +94,20 @@ struct TcParams {  // 128-byte aligned through CUtensorMap
     ClassDesc cls[kMaxTcClasses];
 };
 
+// Forward-convolution kernel parameters (x has dx's shape, y has dy's shape).
+struct FwdParams {
+    CUtensorMap tmap_x;   // x as im2col {C, Wi, Hi, N}, traversal strides (sw, sh), 64 ch x 128 px, 128B swizzle
+    CUtensorMap tmap_w;   // w as {Cg, X, Y, Kg, G}, box {64, 1, 1, BN, 1}: B rows of 64 c (K-major)
+    void *y;
+    int32_t *status;
+    int64_t wait_budget;
+    Geom g;
+    int32_t m_tiles;      // ceil(N*Ho*Wo / 128)
+    int32_t n_tiles;      // ceil(Kg / BN)
+    int32_t total_tiles;  // m_tiles * n_tiles * G
+    int32_t kb_per_tap;   // ceil(Cg / 64)
+};
+
 // Narrow-group kernel parameters (C/G = K/G in {8, 16}, G % 8 == 0).
 struct GroupedParams {
     const void *dy;
@@ -135,6 +149,7 @@ cudaError_t launch_simt(const SimtParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_grouped(GroupedParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_tc(const TcParams &p, int bn, int grid, cudaStream_t s);
 cudaError_t launch_tc2(const TcParams &p, int bn, int cl, int grid, cudaStream_t s);  // cl: SM pairs per cluster
+cudaError_t launch_fwd(const FwdParams &p, int bn, int grid, cudaStream_t s);
 int tc2_max_clusters(int num_sms, int cl);
 int tc2_max_pairs(int num_sms);
 cudaError_t launch_selftest_wait(int32_t *status, int64_t budget, cudaStream_t s);

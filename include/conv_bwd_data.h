@@ -134,6 +134,24 @@ conv_bwd_status conv_bwd_data_coverage(const conv_bwd_plan plan, uint8_t *row_ma
  * kernel launches one run() makes (fill + sub-GEMM kernel). */
 conv_bwd_status conv_bwd_data_path(const conv_bwd_plan plan, int32_t *path, int32_t *launches_per_run);
 
+/* Forward convolution with the plan's geometry, y = conv(x, w): the operator
+ * whose adjoint run() computes (pages "Backward data" -- the forward kernels the
+ * backward-data lowering is paired with -- and "Non-unit stride input backward
+ * different input and dispatches between BOO and Fusilli", whose torch-IR input
+ * is the backward of aten.convolution):
+ *   y[n, ho, wo, k] = sum over c in group(k), y', x' of
+ *                     x[n, ho*sh - ph + y'*dh, wo*sw - pw + x'*dw, c] * w[k, y', x', c mod Cg]
+ * x has dx's shape ([N][Hi][Wi][C]), y has dy's shape ([N][Ho][Wo][K]), w is
+ * run()'s filter; all bf16, caller-owned device pointers, 16-byte aligned; y
+ * is fully overwritten (fp32 accumulation, one RNE rounding per element).
+ * Supported: bf16 NHWC/KYXC plans with C/G and K/G multiples of 8, C/G a
+ * multiple of 64 when G > 1, strides <= 8, (X-1)*dw and (Y-1)*dh <= 127 and
+ * the im2col bounding box of x within [-128, 127] per dimension; other plans
+ * return CONV_BWD_ERR_UNSUPPORTED before anything is launched.  Stream-ordered
+ * like run(), sharing its status word (read it with get_status).  Errors:
+ * INVALID_ARG (NULL or overlapping y), MISALIGNED, CUDA. */
+conv_bwd_status conv_bwd_data_run_forward(conv_bwd_plan plan, const void *x, const void *w, void *y, void *stream);
+
 /* Output tile of the plan's GEMM kernel: rows (M) and columns (C/G) per tile,
  * and the number of SMs that share one tile (2 for the SM-pair tensor-core
  * kernel, else 1).  The grouped kernel reports 0 x 0 (it has no tiles).  Any

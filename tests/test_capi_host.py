@@ -174,6 +174,18 @@ def test_run_argument_errors_without_device(B):
         assert p.run_ptr(4096, 8192, 1 << 20) == B.ERR_CUDA
 
 
+def test_forward_entry_host_checks(B):
+    """conv_bwd_data_run_forward rejects unsupported plans before touching a device."""
+    assert B.Plan(1, 64, 64, 8, 8, 3, 3, (1, 1), dtype="f32").run_forward_ptr(4096, 8192, 1 << 20) == B.ERR_UNSUPPORTED
+    narrow = B.Plan(1, 64, 64, 8, 8, 3, 3, (1, 1), groups=2, layout="nhwc", dtype="bf16")  # C/G = 32
+    assert narrow.run_forward_ptr(4096, 8192, 1 << 20) == B.ERR_UNSUPPORTED
+    ok = B.Plan(1, 64, 64, 8, 8, 3, 3, (1, 1), layout="nhwc", dtype="bf16")
+    assert ok.run_forward_ptr(0, 8192, 1 << 20) == B.ERR_INVALID_ARG
+    import torch
+    if not torch.cuda.is_available():
+        assert ok.run_forward_ptr(4096, 8192, 1 << 20) == B.ERR_CUDA
+
+
 def test_status_strings(B):
     for s in range(7):
         assert B.status_string(s).startswith("CONV_BWD_")
