@@ -63,6 +63,13 @@ struct conv_bwd_plan_s {
     // keyed by the x and w pointers
     const void *fwd_x_ptr = nullptr, *fwd_w_ptr = nullptr;
     CUtensorMap fwd_tmap_x, fwd_tmap_w;
+    // pipelined run_host: batch chunks run on plans of their own (sharing this
+    // plan's status word) so that the copies of one chunk overlap the compute
+    // of another; [0] has chunk_n images, [1] the last chunk's count if smaller
+    conv_bwd_plan_s *chunk_plan[2] = {nullptr, nullptr};
+    int32_t chunk_n = 0, chunks = 0;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    std::vector<cudaEvent_t> hev;  // start, done, then per chunk: inputs copied, output computed
     std::mutex mu;
 };
 
@@ -289,6 +296,48 @@ conv_bwd_status validate(const conv_bwd_desc *d) {
     if (eh < 0 || ew < 0) return CONV_BWD_ERR_INVALID_ARG;
     if (d->stride_h > 64 || d->stride_w > 64) return CONV_BWD_ERR_UNSUPPORTED;
     return CONV_BWD_OK;
+}
+
+}  // namespace
+
+namespace cbd {
+conv_bwd_status plan_create_borrowed_status(const conv_bwd_desc *desc, int32_t *status, conv_bwd_plan *out);
+}
+
+namespace {
+
+// Batch chunks for the pipelined host path: 4 chunks of ceil(N/4) images when
+// the copies are large enough to be worth overlapping, else 1 (plain path).
+// Sets up the chunk plans, copy streams and events on first use.
+int host_chunks(conv_bwd_plan_s *p, size_t ndy, size_t ndx) {
+    const conv_bwd_desc &d = p->desc;
+    if (d.N < 2 || ndy + ndx < (16u << 20)) return 1;
+    if (p->chunks) return p->chunks;
+    p->chunks = 1;  // stays 1 (plain path) if any of the setup below fails
+    const int64_t nc = (d.N + 3) / 4;
+    const int chunks = (int)((d.N + nc - 1) / nc);
+    const int64_t tail = d.N - (int64_t)(chunks - 1) * nc;
+    conv_bwd_desc cd = d;
+    cd.N = nc;
+    if (plan_create_borrowed_status(&cd, p->d_status, &p->chunk_plan[0]) != CONV_BWD_OK) return 1;
+    if (tail != nc) {
+        cd.N = tail;
+        if (plan_create_borrowed_status(&cd, p->d_status, &p->chunk_plan[1]) != CONV_BWD_OK) return 1;
+    }
+    if (cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    p->hev.assign(2 + 2 * chunks, nullptr);
+    for (auto &e : p->hev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            return 1;
+        }
+    p->chunk_n = (int32_t)nc;
+    p->chunks = chunks;
+    return chunks;
 }
 
 }  // namespace
@@ -525,8 +574,13 @@ conv_bwd_status conv_bwd_data_destroy(conv_bwd_plan p) {
         cudaFree(p->d_flags);
         for (auto &e : p->ev)
             if (e) cudaEventDestroy(e);
+        for (auto &e : p->hev)
+            if (e) cudaEventDestroy(e);
+        if (p->h2d) cudaStreamDestroy(p->h2d);
+        if (p->d2h) cudaStreamDestroy(p->d2h);
         if (cur != p->device && cur >= 0) cudaSetDevice(cur);
     }
+    for (auto *c : p->chunk_plan) conv_bwd_data_destroy(c);  // borrowed status: frees only their own state
     delete p;
     return CONV_BWD_OK;
 }
@@ -758,12 +812,54 @@ conv_bwd_status conv_bwd_data_run_host(conv_bwd_plan p, const void *dy_h, const 
     size_t ndy = (size_t)d.N * d.K * p->g.Ho * p->g.Wo * es, nw = (size_t)d.K * p->g.Cg * d.Y * d.X * es,
            ndx = (size_t)d.N * d.C * d.Hi * d.Wi * es;
     cudaStream_t s = (cudaStream_t)stream;
-    if (cudaMemcpyAsync(dy_d, dy_h, ndy, cudaMemcpyHostToDevice, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
-    if (cudaMemcpyAsync(w_d, w_h, nw, cudaMemcpyHostToDevice, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
-    conv_bwd_status st = conv_bwd_data_run(p, dy_d, w_d, dx_d, stream);
-    if (st != CONV_BWD_OK) return st;
-    if (cudaMemcpyAsync(dx_h, dx_d, ndx, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
-    return CONV_BWD_OK;
+    int chunks;
+    {
+        std::lock_guard<std::mutex> lock(p->mu);
+        chunks = host_chunks(p, ndy, ndx);
+    }
+    if (chunks <= 1) {
+        if (cudaMemcpyAsync(dy_d, dy_h, ndy, cudaMemcpyHostToDevice, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        if (cudaMemcpyAsync(w_d, w_h, nw, cudaMemcpyHostToDevice, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        conv_bwd_status st = conv_bwd_data_run(p, dy_d, w_d, dx_d, stream);
+        if (st != CONV_BWD_OK) return st;
+        if (cudaMemcpyAsync(dx_h, dx_d, ndx, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        return CONV_BWD_OK;
+    }
+    // Pipelined over batch chunks (N is the outermost dimension of dy and dx in
+    // both layouts): the copy stream brings w and then dy chunk by chunk, the
+    // caller's stream runs chunk i once its dy is in, the second copy stream
+    // returns dx chunk i once it is computed; the caller's stream finally waits
+    // for the last copy, so everything stays ordered on `stream`.
+    std::lock_guard<std::mutex> lock(p->mu);
+    cudaEvent_t *ev = p->hev.data();
+    const size_t dy_img = ndy / d.N, dx_img = ndx / d.N;
+    auto n_of = [&](int i) { return i + 1 < chunks ? (int64_t)p->chunk_n : d.N - (int64_t)(chunks - 1) * p->chunk_n; };
+    bool ok = cudaEventRecord(ev[0], s) == cudaSuccess && cudaStreamWaitEvent(p->h2d, ev[0], 0) == cudaSuccess &&
+              cudaStreamWaitEvent(p->d2h, ev[0], 0) == cudaSuccess &&
+              cudaMemcpyAsync(w_d, w_h, nw, cudaMemcpyHostToDevice, p->h2d) == cudaSuccess;
+    for (int i = 0; ok && i < chunks; ++i) {
+        const size_t off = (size_t)i * p->chunk_n * dy_img;
+        ok = cudaMemcpyAsync(static_cast<char *>(dy_d) + off, static_cast<const char *>(dy_h) + off,
+                             (size_t)n_of(i) * dy_img, cudaMemcpyHostToDevice, p->h2d) == cudaSuccess &&
+             cudaEventRecord(ev[2 + 2 * i], p->h2d) == cudaSuccess;
+    }
+    for (int i = 0; ok && i < chunks; ++i) {
+        conv_bwd_plan_s *cp = (i + 1 < chunks || !p->chunk_plan[1]) ? p->chunk_plan[0] : p->chunk_plan[1];
+        ok = cudaStreamWaitEvent(s, ev[2 + 2 * i], 0) == cudaSuccess;
+        if (!ok) break;
+        conv_bwd_status st = conv_bwd_data_run(cp, static_cast<char *>(dy_d) + (size_t)i * p->chunk_n * dy_img, w_d,
+                                               static_cast<char *>(dx_d) + (size_t)i * p->chunk_n * dx_img, stream);
+        if (st != CONV_BWD_OK) return st;
+        ok = cudaEventRecord(ev[3 + 2 * i], s) == cudaSuccess;
+    }
+    for (int i = 0; ok && i < chunks; ++i) {
+        const size_t off = (size_t)i * p->chunk_n * dx_img;
+        ok = cudaStreamWaitEvent(p->d2h, ev[3 + 2 * i], 0) == cudaSuccess &&
+             cudaMemcpyAsync(static_cast<char *>(dx_h) + off, static_cast<const char *>(dx_d) + off,
+                             (size_t)n_of(i) * dx_img, cudaMemcpyDeviceToHost, p->d2h) == cudaSuccess;
+    }
+    ok = ok && cudaEventRecord(ev[1], p->d2h) == cudaSuccess && cudaStreamWaitEvent(s, ev[1], 0) == cudaSuccess;
+    return ok ? CONV_BWD_OK : CONV_BWD_ERR_CUDA;
 }
 
 conv_bwd_status conv_bwd_data_run_forward(conv_bwd_plan p, const void *x, const void *w, void *y, void *stream) {

@@ -179,8 +179,14 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan plan, const void *dy, const void
 /* End-to-end variant with host buffers: copies dy_host/w_host into the
  * caller's device buffers dy_dev/w_dev, runs, and copies dx_dev back into
  * dx_host, all ordered on `stream` (use pinned host memory for async
- * copies).  Returns after enqueueing; synchronise the stream before reading
- * dx_host.  Same errors as conv_bwd_data_run. */
+ * copies).  When the copies are large (dy + dx >= 16 MiB, N >= 2) the work is
+ * pipelined over up to 4 batch chunks: two copy streams owned by the plan
+ * bring dy chunk by chunk and return dx chunk by chunk while `stream` computes
+ * the chunk in between; they start after the work already queued on `stream`,
+ * and `stream` waits for the last copy, so the ordering seen by the caller is
+ * unchanged.  Calls on one plan must not overlap (as for run).  Returns after
+ * enqueueing; synchronise the stream before reading dx_host.  Same errors as
+ * conv_bwd_data_run. */
 conv_bwd_status conv_bwd_data_run_host(conv_bwd_plan plan, const void *dy_host, const void *w_host, void *dx_host,
                                        void *dy_dev, void *w_dev, void *dx_dev, void *stream);
 

@@ -323,6 +323,38 @@ def test_run_host_end_to_end(B):
     check_full(c, dx_h.float().numpy().astype(np.float64), g, dy, w)
 
 
+HOST_PIPE_CASES = [
+    _mk("host_pipe_tail_2sm", N=7, C=512, K=512, Hi=40, Wi=40, Y=3, X=3, pad=(1, 1), sigma=0.05),
+    _mk("host_pipe_fill", N=7, C=256, K=256, Hi=64, Wi=64, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2),
+        sigma=0.05),
+]
+
+
+@pytest.mark.parametrize("c", HOST_PIPE_CASES, ids=lambda c: c.name)
+def test_run_host_pipelined_chunks(B, c):
+    """run_host over batch chunks (chunks of 2 images plus a 1-image tail, each
+    on its own plan, copies on the plan's copy streams): every image is
+    computed and copied back, including the tail and the uncovered pixels."""
+    g, dy, w = inputs(c)
+    plan = B.Plan.from_case(c)
+    dy_s, w_s, dx_s = plan.shapes()
+    dy_h = torch.from_numpy(dy.view(np.int16)).view(torch.bfloat16).pin_memory()
+    w_h = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).pin_memory()
+    dx_h = torch.full(dx_s, float("nan"), dtype=torch.bfloat16).pin_memory()
+    dy_d = torch.empty(dy_s, dtype=torch.bfloat16, device="cuda")
+    w_d = torch.empty(w_s, dtype=torch.bfloat16, device="cuda")
+    dx_d = torch.full(dx_s, float("nan"), dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):  # the second call reuses the chunk plans, streams and events
+        plan.run_host(dy_h, w_h, dx_h, dy_d, w_d, dx_d)
+        st, det = plan.status()
+        assert st == B.OK, (B.status_string(st), hex(det))
+        got = dx_h.float().numpy().astype(np.float64)
+        assert np.all(np.isfinite(got)), "unwritten (NaN) outputs"
+        check_full(c, got, g, dy, w, n_range=(c.N - 1, c.N))  # the tail chunk's image
+        check_points(c, got, g, dy, w, count=800, seed=zlib.crc32(c.name.encode()) % 1000)
+        dx_h.fill_(float("nan"))
+
+
 def test_overlap_and_alignment_errors(B):
     c = TC_CASES[1]
     plan = B.Plan.from_case(c)
