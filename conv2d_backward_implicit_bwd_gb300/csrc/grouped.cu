@@ -90,14 +90,14 @@ __device__ __forceinline__ GItem next_item(const GroupedParams &p, const GItem &
 }
 
 template <int CG>
-__global__ void __launch_bounds__(128) grouped_dgrad_kernel(const __grid_constant__ GroupedParams p) {
+__global__ void __launch_bounds__(128, CG == 8 ? 5 : 3) grouped_dgrad_kernel(const __grid_constant__ GroupedParams p) {
     using C = GCfg<CG>;
     constexpr int LOG_SEGS = CG == 8 ? 3 : 4;
     constexpr int NTHREADS = 128;
     constexpr int PSTEP = NTHREADS / GCfg<CG>::SEGS;  // staged pixels per pass of the CTA
     extern __shared__ __align__(128) uint8_t gsm[];
     const Geom &g = p.g;
-    const uint32_t *wfrag = reinterpret_cast<const uint32_t *>(gsm);  // [tap][NR][lane][8 groups]
+    const uint32_t *wfrag = reinterpret_cast<const uint32_t *>(gsm);  // B fragments (layout below)
     const uint32_t buf0 = smem_u32(gsm + p.wfrag_bytes);             // two buffers of [tyn][span] pixel lines
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
@@ -121,7 +121,11 @@ __global__ void __launch_bounds__(128) grouped_dgrad_kernel(const __grid_constan
         const uint16_t *rw = reinterpret_cast<const uint16_t *>(raw);
         uint32_t *wf = reinterpret_cast<uint32_t *>(gsm);
         for (int e = threadIdx.x; e < ntap * C::NR * 32 * 8; e += NTHREADS) {
-            const int gl = e & 7, l = (e >> 3) & 31, r = (e >> 8) % C::NR, tap = e / (256 * C::NR);
+            // CG = 8: [tap][group half][lane][4 groups] (16 contiguous bytes per lane
+            // and half: conflict-free 16-byte loads); CG = 16: [tap][NR][lane][8 groups]
+            const int gl = CG == 8 ? ((e >> 7) & 1) * 4 + (e & 3) : e & 7;
+            const int l = CG == 8 ? (e >> 2) & 31 : (e >> 3) & 31;
+            const int r = (e >> 8) % C::NR, tap = e / (256 * C::NR);
             const int nt = r >> 1, kh = r & 1;
             const int n = nt * 8 + (l >> 2), k = 2 * (l & 3) + 8 * kh;
             const int base = (gl * CG + k) * rowh + tap * CG + n;
@@ -201,8 +205,8 @@ __global__ void __launch_bounds__(128) grouped_dgrad_kernel(const __grid_constan
                             const int qs = q & 7;
                             if (CG == 8) {
                                 // fragments of the 8 groups: two 16-byte loads
-                                const uint4 *wl = reinterpret_cast<const uint4 *>(wfrag + (tap * 32 + lane) * 8);
-                                const uint4 f0 = wl[0], f1 = wl[1];
+                                const uint4 *wl = reinterpret_cast<const uint4 *>(wfrag + tap * 256 + lane * 4);
+                                const uint4 f0 = wl[0], f1 = wl[32];
                                 const uint32_t bfr[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
                                 for (int gp = 0; gp < 4; ++gp) {
@@ -304,7 +308,14 @@ template <int CG>
 static cudaError_t launch_grouped_cg(const GroupedParams &p, const GroupedLayout &L, int num_sms, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(grouped_dgrad_kernel<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
     if (e != cudaSuccess) return e;
-    const int per_sm = std::max(1, std::min(16, (227 * 1024) / (L.smem + 1024)));
+    // CTAs that fit on an SM at once (registers and shared memory): the item
+    // loop is persistent, so the grid must be exactly one wave
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grouped_dgrad_kernel<CG>, 128, L.smem) != cudaSuccess ||
+        per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 1;
+    }
     const int sms = num_sms > 0 ? num_sms : 148;
     int per_gb = std::max(1, (sms * per_sm + p.gblocks - 1) / p.gblocks);
     const int64_t items = (int64_t)p.g.N * p.g.Hi * p.nwch;
