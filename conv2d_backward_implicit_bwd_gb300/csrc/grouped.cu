@@ -39,6 +39,11 @@ namespace cbd {
 
 template <int CG>
 struct GCfg {
+    // 2 warps per CTA for 8-channel groups: with the units of an item in
+    // (residue, m-tile) order, each warp then takes one m-tile of every residue
+    // class, and classes with many and few taps share out evenly
+    static constexpr int THREADS = CG == 8 ? 64 : 128;
+    static constexpr int WARPS = THREADS / 32;
     static constexpr int LINE = 8 * CG * 2;     // bytes per pixel of one 8-group block
     static constexpr int SEGS = LINE / 16;      // 16-byte segments per pixel line
     static constexpr int NR = CG == 8 ? 1 : 4;  // B-fragment registers per (tap, lane)
@@ -90,10 +95,10 @@ __device__ __forceinline__ GItem next_item(const GroupedParams &p, const GItem &
 }
 
 template <int CG>
-__global__ void __launch_bounds__(128, CG == 8 ? 5 : 3) grouped_dgrad_kernel(const __grid_constant__ GroupedParams p) {
+__global__ void __launch_bounds__(GCfg<CG>::THREADS, CG == 8 ? 10 : 3) grouped_dgrad_kernel(const __grid_constant__ GroupedParams p) {
     using C = GCfg<CG>;
     constexpr int LOG_SEGS = CG == 8 ? 3 : 4;
-    constexpr int NTHREADS = 128;
+    constexpr int NTHREADS = C::THREADS;
     constexpr int PSTEP = NTHREADS / GCfg<CG>::SEGS;  // staged pixels per pass of the CTA
     extern __shared__ __align__(128) uint8_t gsm[];
     const Geom &g = p.g;
@@ -177,12 +182,12 @@ __global__ void __launch_bounds__(128, CG == 8 ? 5 : 3) grouped_dgrad_kernel(con
         __syncthreads();
 
         // units (column residue r, 16-pixel m-tile mt) of this item: warp w
-        // takes units w, w + 4, ...; a unit covers all 8 groups of the block
+        // takes units w, w + WARPS, ...; a unit covers all 8 groups of the block
         const uint32_t bb = buf0 + (uint32_t)b * p.buf_bytes;
         const int64_t cbytes = (int64_t)g.C * 2;
         uint8_t *dxrow = static_cast<uint8_t *>(p.dx) + ((((int64_t)m.n * g.Hi + m.hi) * g.Wi + m.w0) * g.C + cofs) * 2;
         int r = warp / p.per_r, mt = warp - r * p.per_r;
-        for (int u = warp; u < nunits; u += 4) {
+        for (int u = warp; u < nunits; u += C::WARPS) {
             if (r + g.sw * 16 * mt < m.npx) {
                 const int cc = p.col_class[r];  // w0 is a multiple of sw
                 const int txn = cc >> 16, tx = cc & 0xFFFF;
@@ -272,7 +277,7 @@ __global__ void __launch_bounds__(128, CG == 8 ? 5 : 3) grouped_dgrad_kernel(con
                         }
                 }
             }
-            mt += 4;
+            mt += C::WARPS;
             while (mt >= p.per_r) {
                 mt -= p.per_r;
                 ++r;
@@ -311,7 +316,8 @@ static cudaError_t launch_grouped_cg(const GroupedParams &p, const GroupedLayout
     // CTAs that fit on an SM at once (registers and shared memory): the item
     // loop is persistent, so the grid must be exactly one wave
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grouped_dgrad_kernel<CG>, 128, L.smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grouped_dgrad_kernel<CG>, GCfg<CG>::THREADS, L.smem) !=
+            cudaSuccess ||
         per_sm < 1) {
         cudaGetLastError();
         per_sm = 1;
@@ -324,7 +330,7 @@ static cudaError_t launch_grouped_cg(const GroupedParams &p, const GroupedLayout
     q.step_wc = per_gb % q.nwch;
     q.step_hi = (per_gb / q.nwch) % q.g.Hi;
     q.step_n = per_gb / (q.nwch * q.g.Hi);
-    grouped_dgrad_kernel<CG><<<per_gb * p.gblocks, 128, L.smem, s>>>(q);
+    grouped_dgrad_kernel<CG><<<per_gb * p.gblocks, GCfg<CG>::THREADS, L.smem, s>>>(q);
     return cudaGetLastError();
 }
 
