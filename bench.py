@@ -37,16 +37,17 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), valid only for
 # the kernel source whose sha256 is recorded with it.
 # Per-launch DRAM traffic of each workload's GEMM kernel, from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the sources
-# that decide what that launch does are unchanged (hash below).
-TC2_SOURCES = ("tc_common.cuh", "tc2_sm103.cu", "capi.cpp", "internal.h")
-GROUPED_SOURCES = ("tc_common.cuh", "grouped.cu", "capi.cpp", "internal.h")
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel's
+# sources are unchanged (hash below) and the plan launches the same tile shape.
+TC2_SOURCES = ("tc_common.cuh", "tc2_sm103.cu", "internal.h")
+GROUPED_SOURCES = ("tc_common.cuh", "grouped.cu", "internal.h")
 TRAFFIC = {
     # ncu --set full, tc2_dgrad_kernel<512, 1>, one launch on the page-3 shape:
     # dram__bytes_read.sum 33.63 MB + dram__bytes_write.sum 1.02 MB
-    "cfg3_bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "sha": "726ce1d6449ec854", "bytes": 34.655e6},
+    "cfg3_bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "tile": (256, 512, 2), "sha": "ab0351bdfb6cfadd",
+                                         "bytes": 34.655e6},
     # grouped_dgrad_kernel<8> on the 64x56x56x256 G=32 layer: 25.76 MB + 42.90 MB
-    "cfg4_bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": GROUPED_SOURCES, "sha": "fb5793dd9605a29b",
+    "cfg4_bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": GROUPED_SOURCES, "tile": (0, 0, 1), "sha": "f1a6f68bd6ba28fd",
                                                   "bytes": 68.657e6},
 }
 
@@ -333,7 +334,8 @@ def main():
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": peaks["source"] + " (HBM copy)", "kernel": kernel_name, "kernel_ms": kmean}
     tr = TRAFFIC.get(case.name)
-    roof["traffic"] = tr["bytes"] if tr and tr.get("sha") == kernel_sha(tr["files"]) else None
+    roof["traffic"] = (tr["bytes"] if tr and tr["sha"] == kernel_sha(tr["files"]) and tuple(plan.tile()) == tr["tile"]
+                       else None)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
