@@ -125,6 +125,24 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The slowest rank's time: every rank gets max(x) (identity when world == 1).
+    The tensor lives on ``device`` (a CUDA device under NCCL, CPU under gloo)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(useful_flop_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput of ``world`` replicas, each doing the same work,
+    timed by the slowest rank (weak scaling)."""
+    return useful_flop_per_rank * world / (ms * 1e-3) / 1e12
+
+
 def make_inputs(case, plan):
     from conv2d_backward_implicit_bwd_gb300 import workloads as wl
     dy_s, w_s, dx_s = plan.shapes()
@@ -289,12 +307,8 @@ def main():
             plan.run(dy_d, w_d, dx_d, stream)
             kern_ms.append(plan.last_timing()[1])
         plan.set_timing(False)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([mean_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms = float(t.item())
-    value = useful * world / (mean_ms * 1e-3) / 1e12
+    mean_ms = max_over_ranks(mean_ms, world, "cuda")
+    value = job_tflops(useful, world, mean_ms)
 
     # end-to-end through the host-buffer entry point (pinned host memory)
     dy_p, w_p = dy_h.pin_memory(), w_h.pin_memory()
@@ -310,11 +324,7 @@ def main():
         if i >= 2:
             e2e_ms.append(a.elapsed_time(b))
     e2e_mean = sum(e2e_ms) / len(e2e_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_mean], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_mean = float(t.item())
+    e2e_mean = max_over_ranks(e2e_mean, world, "cuda")
     esz = 2 if case.dtype == wl.BF16 else 4
 
     peaks = load_peaks()
@@ -350,7 +360,7 @@ def main():
                    "kernel_path": path, "useful_flop_per_step": useful, "algo_bytes_per_step": algo_bytes},
         "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
         "roofline": roof,
-        "e2e": {"value": useful * world / (e2e_mean * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_tflops(useful, world, e2e_mean), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(dy_h.numel() + w_h.numel()) * esz,
                 "d2h_bytes_per_step": int(np.prod(dx_s)) * esz, "ms_per_step": e2e_mean},
         "gpu_launches": launches * args.steps,
