@@ -306,6 +306,8 @@ conv_bwd_status plan_create_borrowed_status(const conv_bwd_desc *desc, int32_t *
 
 namespace {
 
+int kHostChunks = 4;  // batch chunks of the pipelined host path (CONVBWD_DEBUG_HOST_CHUNKS overrides)
+
 // Batch chunks for the pipelined host path: 4 chunks of ceil(N/4) images when
 // the copies are large enough to be worth overlapping, else 1 (plain path).
 // Sets up the chunk plans, copy streams and events on first use.
@@ -314,7 +316,9 @@ int host_chunks(conv_bwd_plan_s *p, size_t ndy, size_t ndx) {
     if (d.N < 2 || ndy + ndx < (16u << 20)) return 1;
     if (p->chunks) return p->chunks;
     p->chunks = 1;  // stays 1 (plain path) if any of the setup below fails
-    const int64_t nc = (d.N + 3) / 4;
+    if (const char *f = env("CONVBWD_DEBUG_HOST_CHUNKS")) kHostChunks = std::max(1, std::min(64, std::atoi(f)));
+    if (kHostChunks < 2) return 1;
+    const int64_t nc = (d.N + kHostChunks - 1) / kHostChunks;
     const int chunks = (int)((d.N + nc - 1) / nc);
     const int64_t tail = d.N - (int64_t)(chunks - 1) * nc;
     conv_bwd_desc cd = d;
