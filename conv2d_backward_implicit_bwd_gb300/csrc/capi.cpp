@@ -70,6 +70,11 @@ struct conv_bwd_plan_s {
     int32_t chunk_n = 0, chunks = 0;
     cudaStream_t h2d = nullptr, d2h = nullptr;
     std::vector<cudaEvent_t> hev;  // start, done, then per chunk: inputs copied, output computed
+    // bf16 NCHW/GKCYX problems on the tensor-core (or narrow-group) path: layout
+    // transposes into plan-owned NHWC/KYXC scratch around a plan of the same
+    // geometry in NHWC/KYXC (sharing this plan's status word)
+    conv_bwd_plan_s *nhwc_plan = nullptr;
+    void *t_dy = nullptr, *t_w = nullptr, *t_dx = nullptr;
     std::mutex mu;
 };
 
@@ -313,7 +318,7 @@ int kHostChunks = 4;  // batch chunks of the pipelined host path (CONVBWD_DEBUG_
 // Sets up the chunk plans, copy streams and events on first use.
 int host_chunks(conv_bwd_plan_s *p, size_t ndy, size_t ndx) {
     const conv_bwd_desc &d = p->desc;
-    if (d.N < 2 || ndy + ndx < (16u << 20)) return 1;
+    if (d.N < 2 || ndy + ndx < (16u << 20) || p->nhwc_plan) return 1;
     if (p->chunks) return p->chunks;
     p->chunks = 1;  // stays 1 (plain path) if any of the setup below fails
     if (const char *f = env("CONVBWD_DEBUG_HOST_CHUNKS")) kHostChunks = std::max(1, std::min(64, std::atoi(f)));
@@ -553,6 +558,29 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                     p->d_flags = nullptr;
                 }
             }
+            // bf16 NCHW/GKCYX: run the NHWC/KYXC plan of the same geometry between
+            // layout transposes when that plan is on a tensor-core path
+            if (d.dtype == CONV_BWD_BF16 && d.layout == CONV_BWD_NCHW_GKCYX && !env("CONVBWD_DEBUG_NO_TRANSPOSE")) {
+                conv_bwd_desc nd = d;
+                nd.layout = CONV_BWD_NHWC_KYXC;
+                conv_bwd_plan child = nullptr;
+                if (plan_create_borrowed_status(&nd, p->d_status, &child) == CONV_BWD_OK && child->path != CONV_BWD_PATH_SIMT) {
+                    const size_t ndy = (size_t)d.N * d.K * g.Ho * g.Wo * 2, nw = (size_t)d.K * g.Cg * d.Y * d.X * 2,
+                                 ndx = (size_t)d.N * d.C * d.Hi * d.Wi * 2;
+                    if (cudaMalloc(&p->t_dy, ndy) == cudaSuccess && cudaMalloc(&p->t_w, nw) == cudaSuccess &&
+                        cudaMalloc(&p->t_dx, ndx) == cudaSuccess) {
+                        p->nhwc_plan = child;
+                        child = nullptr;
+                    } else {
+                        cudaGetLastError();
+                        cudaFree(p->t_dy);
+                        cudaFree(p->t_w);
+                        cudaFree(p->t_dx);
+                        p->t_dy = p->t_w = p->t_dx = nullptr;
+                    }
+                }
+                conv_bwd_data_destroy(child);
+            }
         } else {
             p->owns_status = false;  // run() becomes possible once a status word is attached
         }
@@ -580,11 +608,15 @@ conv_bwd_status conv_bwd_data_destroy(conv_bwd_plan p) {
             if (e) cudaEventDestroy(e);
         for (auto &e : p->hev)
             if (e) cudaEventDestroy(e);
+        cudaFree(p->t_dy);
+        cudaFree(p->t_w);
+        cudaFree(p->t_dx);
         if (p->h2d) cudaStreamDestroy(p->h2d);
         if (p->d2h) cudaStreamDestroy(p->d2h);
         if (cur != p->device && cur >= 0) cudaSetDevice(cur);
     }
     for (auto *c : p->chunk_plan) conv_bwd_data_destroy(c);  // borrowed status: frees only their own state
+    conv_bwd_data_destroy(p->nhwc_plan);
     delete p;
     return CONV_BWD_OK;
 }
@@ -625,6 +657,11 @@ conv_bwd_status conv_bwd_data_coverage(const conv_bwd_plan p, uint8_t *row_mask,
 
 conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t *launches) {
     if (!p) return CONV_BWD_ERR_INVALID_ARG;
+    if (p->nhwc_plan) {  // dy and w transposed in, dx transposed out, around the NHWC plan's kernels
+        conv_bwd_status st = conv_bwd_data_path(p->nhwc_plan, path, launches);
+        if (launches) *launches += 3;
+        return st;
+    }
     if (path) *path = p->path;
     int gemm_launches = p->classes.empty() ? 0 : 1;
     if (p->path == CONV_BWD_PATH_TCGEN05) gemm_launches = (int)((p->classes.size() + kMaxTcClasses - 1) / kMaxTcClasses);
@@ -637,6 +674,7 @@ conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t
 
 conv_bwd_status conv_bwd_data_tile(const conv_bwd_plan p, int32_t *tile_m, int32_t *tile_n, int32_t *sms) {
     if (!p) return CONV_BWD_ERR_INVALID_ARG;
+    if (p->nhwc_plan) return conv_bwd_data_tile(p->nhwc_plan, tile_m, tile_n, sms);
     const bool tc = p->path == CONV_BWD_PATH_TCGEN05, grouped = p->path == CONV_BWD_PATH_GROUPED;
     if (tile_m) *tile_m = grouped ? 0 : tc ? (p->two_sm ? 256 * p->cl : 128) : 64;
     if (tile_n) *tile_n = grouped ? 0 : p->bn;
@@ -667,6 +705,19 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
         return CONV_BWD_ERR_MISALIGNED;
     cudaStream_t s = (cudaStream_t)stream;
     std::lock_guard<std::mutex> lock(p->mu);
+
+    if (p->nhwc_plan) {
+        // dy [N][K][Ho*Wo] -> [N][Ho*Wo][K], w [K][Cg][Y*X] -> [K][Y*X][Cg], the
+        // NHWC/KYXC plan's kernels, dx [N][Hi*Wi][C] -> [N][C][Hi*Wi]
+        if (launch_transpose_b16(dy, p->t_dy, d.N, d.K, (int64_t)g.Ho * g.Wo, p->num_sms, s) != cudaSuccess ||
+            launch_transpose_b16(w, p->t_w, d.K, g.Cg, (int64_t)d.Y * d.X, p->num_sms, s) != cudaSuccess)
+            return CONV_BWD_ERR_CUDA;
+        conv_bwd_status st = conv_bwd_data_run(p->nhwc_plan, p->t_dy, p->t_w, p->t_dx, stream);
+        if (st != CONV_BWD_OK) return st;
+        if (launch_transpose_b16(p->t_dx, dx, d.N, (int64_t)d.Hi * d.Wi, d.C, p->num_sms, s) != cudaSuccess)
+            return CONV_BWD_ERR_CUDA;
+        return CONV_BWD_OK;
+    }
 
     if (p->timing) {
         for (auto &e : p->ev)
@@ -921,10 +972,12 @@ conv_bwd_status conv_bwd_data_get_status(conv_bwd_plan p, void *stream, int32_t 
 conv_bwd_status conv_bwd_data_set_timing(conv_bwd_plan p, int32_t enable) {
     if (!p) return CONV_BWD_ERR_INVALID_ARG;
     p->timing = enable != 0;
+    if (p->nhwc_plan) conv_bwd_data_set_timing(p->nhwc_plan, enable);
     return CONV_BWD_OK;
 }
 
 conv_bwd_status conv_bwd_data_last_timing(conv_bwd_plan p, float *fill_ms, float *gemm_ms) {
+    if (p && p->nhwc_plan) return conv_bwd_data_last_timing(p->nhwc_plan, fill_ms, gemm_ms);  // its kernels
     if (!p || !p->timing || !p->ev[3]) return CONV_BWD_ERR_INVALID_ARG;
     float f = 0.f, m = 0.f;
     if (p->fill_ran) {

@@ -150,6 +150,9 @@ cudaError_t launch_grouped(GroupedParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_tc(const TcParams &p, int bn, int grid, cudaStream_t s);
 cudaError_t launch_tc2(const TcParams &p, int bn, int cl, int grid, cudaStream_t s);  // cl: SM pairs per cluster
 cudaError_t launch_fwd(const FwdParams &p, int bn, int grid, cudaStream_t s);
+// out[b][c][r] = in[b][r][c] for bf16 elements (layout changes of NCHW/GKCYX problems)
+cudaError_t launch_transpose_b16(const void *in, void *out, int64_t batch, int64_t R, int64_t Cc, int num_sms,
+                                 cudaStream_t s);
 int tc2_max_clusters(int num_sms, int cl);
 int tc2_max_pairs(int num_sms);
 cudaError_t launch_selftest_wait(int32_t *status, int64_t budget, cudaStream_t s);

@@ -245,4 +245,53 @@ cudaError_t launch_selftest_wait(int32_t *status, int64_t budget, cudaStream_t s
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Layout transposes for bf16 NCHW/GKCYX problems on the tensor-core path:
+// out[b][c][r] = in[b][r][c] (r < R, c < Cc), 64x64 tiles through shared
+// memory so that both the reads and the writes run along contiguous rows.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) transpose_b16_kernel(const uint16_t *__restrict__ in, uint16_t *__restrict__ out,
+                                                            int64_t batch, int64_t R, int64_t Cc) {
+    __shared__ uint16_t t[64][66];
+    const int64_t tr_n = (R + 63) / 64, tc_n = (Cc + 63) / 64;
+    const int64_t tiles = batch * tr_n * tc_n;
+    const int x = threadIdx.x & 31, y = threadIdx.x >> 5;  // 32 x 8 threads
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t tc = tile % tc_n, rest = tile / tc_n;
+        const int64_t tr = rest % tr_n, b = rest / tr_n;
+        const uint16_t *src = in + b * R * Cc;
+        uint16_t *dst = out + b * R * Cc;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int64_t r = tr * 64 + y + 8 * k;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t c = tc * 64 + x + 32 * h;
+                t[y + 8 * k][x + 32 * h] = (r < R && c < Cc) ? src[r * Cc + c] : (uint16_t)0;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int64_t c = tc * 64 + y + 8 * k;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t r = tr * 64 + x + 32 * h;
+                if (r < R && c < Cc) dst[c * R + r] = t[x + 32 * h][y + 8 * k];
+            }
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_transpose_b16(const void *in, void *out, int64_t batch, int64_t R, int64_t Cc, int num_sms,
+                                 cudaStream_t s) {
+    const int64_t tiles = batch * ((R + 63) / 64) * ((Cc + 63) / 64);
+    if (tiles <= 0) return cudaSuccess;
+    const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 148) * 8;
+    transpose_b16_kernel<<<(unsigned)(tiles < cap ? tiles : cap), 256, 0, s>>>(
+        static_cast<const uint16_t *>(in), static_cast<uint16_t *>(out), batch, R, Cc);
+    return cudaGetLastError();
+}
+
 }  // namespace cbd

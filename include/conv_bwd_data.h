@@ -90,10 +90,15 @@ typedef struct conv_bwd_plan_s *conv_bwd_plan;
 
 /* Which kernel family runs the sub-GEMMs of a plan. */
 typedef enum {
-    CONV_BWD_PATH_TCGEN05 = 0, /* bf16 NHWC: persistent tcgen05/TMEM implicit GEMM */
+    CONV_BWD_PATH_TCGEN05 = 0, /* bf16: persistent tcgen05/TMEM implicit GEMM */
     CONV_BWD_PATH_SIMT = 1,    /* fp32 (or bf16 fallback): CUDA-core tiled implicit GEMM */
-    CONV_BWD_PATH_GROUPED = 2  /* bf16 NHWC, C/G = K/G in {8, 16}, G % 8 == 0: memory-bound direct kernel */
+    CONV_BWD_PATH_GROUPED = 2  /* bf16, C/G = K/G in {8, 16}, G % 8 == 0: memory-bound warp-MMA kernel */
 } conv_bwd_path;
+/* The tensor-core and narrow-group kernels read NHWC/KYXC.  A bf16 NCHW/GKCYX
+ * plan whose NHWC/KYXC twin takes one of them gets plan-owned scratch (dy, w
+ * and dx in NHWC/KYXC, allocated by create) and each run transposes dy and w
+ * into it, runs the twin's kernels and transposes dx back (path() reports the
+ * twin's path with 3 more launches). */
 
 /* Validate the descriptor and plan on the host: forward output size, tilde
  * factors, non-empty sub-GEMM list (consecutive gemmIds), coverage of dx,
@@ -101,7 +106,9 @@ typedef enum {
  * allocates the plan's device status word on the current device (run() must
  * then be called with that device current).  Without a device the plan is
  * still created (so the planner can be queried) and run() returns
- * CONV_BWD_ERR_CUDA.  *out is set to NULL on failure.
+ * CONV_BWD_ERR_CUDA.  bf16 NCHW/GKCYX plans on a tensor-core path also
+ * allocate the NHWC/KYXC scratch (if that fails they keep the CUDA-core
+ * path).  *out is set to NULL on failure.
  * Errors: INVALID_ARG (non-positive sizes, pad < 0, stride/dilation < 1,
  * C or K not divisible by groups, empty forward output, unknown enum),
  * UNSUPPORTED (stride > 64, more than 2^31-1 elements in a tensor, bf16 in a

@@ -197,6 +197,32 @@ def test_cuda_core_path_full(B, c):
     check_full(c, got, g, dy, w)
 
 
+# bf16 NCHW/GKCYX problems whose NHWC/KYXC twin runs on a tensor-core path:
+# dy and w are transposed into plan-owned scratch, dx transposed back.
+NCHW_TC_CASES = [
+    _mk("nchw_bf16_tc", N=2, C=256, K=128, Hi=9, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2), layout=wl.NCHW),
+    _mk("nchw_bf16_pair", N=2, C=512, K=256, Hi=7, Wi=8, Y=3, X=3, pad=(1, 1), layout=wl.NCHW),
+    _mk("nchw_bf16_grouped", N=2, C=256, K=256, Hi=9, Wi=10, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=32,
+        layout=wl.NCHW),
+    _mk("nchw_bf16_fill", N=2, C=128, K=128, Hi=12, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2),
+        layout=wl.NCHW),
+    _mk("nchw_bf16_ragged", N=3, C=200, K=40, Hi=11, Wi=6, Y=2, X=4, pad=(0, 3), stride=(3, 1), dil=(2, 3),
+        layout=wl.NCHW),
+    _mk("nchw_bf16_odd_hw", N=1, C=64, K=72, Hi=13, Wi=67, Y=1, X=3, pad=(0, 1), stride=(1, 2), layout=wl.NCHW),
+]
+
+
+@pytest.mark.parametrize("c", NCHW_TC_CASES, ids=lambda c: c.name)
+def test_nchw_bf16_through_transposes(B, c):
+    g, dy, w = inputs(c)
+    for _ in range(2):  # the second run reuses the scratch
+        got, plan = gpu_dgrad(B, c, dy, w)
+        name, launches = plan.path()
+        assert name in ("tcgen05", "grouped"), plan.path()
+        assert launches >= 4, plan.path()  # two transposes in, the kernels, one transpose out
+        check_full(c, got, g, dy, w)
+
+
 def test_forced_simt_matches_tensor_core_path(B, monkeypatch):
     """The tensor-core kernel and the CUDA-core kernel agree on a bf16 case
     (both compared with the oracle too)."""
