@@ -1,12 +1,13 @@
 """Benchmark: dgrad useful-MAC TFLOP/s on one GB300, printed as one JSON line.
 
-Default workload: the page-3 dgrad shape (bf16 NHWC, N=16, Hi=1, Wi=512,
+Default workload: the dgrad shape of page "Non-unit stride input backward different
+input and dispatches between BOO and Fusilli" (bf16 NHWC, N=16, Hi=1, Wi=512,
 C=K=2048, 1x2 filter, stride (1, 2), pad 0 -> dy 16x1x256x2048), seeded
 synthetic inputs N(0,1)*0.02 rounded to bf16.  A "step" is one
 conv_bwd_data_run (every kernel of the path) with dy and w resident in HBM;
 L2 is flushed (a 512 MiB write) before every step, outside the step's events.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg3]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
 
 Under torchrun (N > 1) every rank runs an independent replica of the same
@@ -42,12 +43,12 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 TC2_SOURCES = ("tc_common.cuh", "tc2_sm103.cu", "internal.h")
 GROUPED_SOURCES = ("tc_common.cuh", "grouped.cu", "internal.h")
 TRAFFIC = {
-    # ncu --set full, tc2_dgrad_kernel<512, 1>, one launch on the page-3 shape:
+    # ncu --set full, tc2_dgrad_kernel<512, 1>, one launch on the 16x1x512x2048 shape:
     # dram__bytes_read.sum 33.63 MB + dram__bytes_write.sum 1.02 MB
-    "cfg3_bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "tile": (256, 512, 2), "sha": "ab0351bdfb6cfadd",
+    "bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "tile": (256, 512, 2), "sha": "ab0351bdfb6cfadd",
                                          "bytes": 34.655e6},
     # grouped_dgrad_kernel<8> on the 64x56x56x256 G=32 layer: 25.76 MB + 42.90 MB
-    "cfg4_bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": GROUPED_SOURCES, "tile": (0, 0, 1), "sha": "f1a6f68bd6ba28fd",
+    "bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": GROUPED_SOURCES, "tile": (0, 0, 1), "sha": "f1a6f68bd6ba28fd",
                                                   "bytes": 68.657e6},
 }
 
@@ -223,7 +224,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="cfg3")
+    ap.add_argument("--workload", default="bf16_16x1x512x2048_1x2_s1x2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
@@ -350,7 +351,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": value / PAGE_TFLOPS if case.name.startswith("cfg3") else None,
+        "vs_baseline": value / PAGE_TFLOPS if case.name.startswith("bf16_16x1x512x2048") else None,
         "dtype": case.dtype, "data": f"synthetic (seeded {case.dist}, sigma {case.sigma}, {case.dtype} RNE)",
         "config": {"workload": case.name, "N": case.N, "C": case.C, "K": case.K, "Hi": case.Hi, "Wi": case.Wi,
                    "Y": case.Y, "X": case.X, "pad": list(case.pad), "stride": list(case.stride),

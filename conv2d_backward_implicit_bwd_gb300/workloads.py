@@ -61,41 +61,42 @@ def _sweep():
     rows = [(14, 1, 1, 1), (14, 3, 1, 1), (15, 1, 1, 1), (16, 1, 1, 1), (14, 3, 1, 2)]
     out = []
     for i, (h, f, p, s) in enumerate(rows):
-        out.append(Case(name=f"cfg2{'abcde'[i]}_fp32_{h}x{h}_{f}x{f}_p{p}_s{s}", Hi=h, Wi=h, Y=f, X=f,
-                        pad=(p, p), stride=(s, s), seed=2000 + i, tags=("cfg2",), **base))
+        out.append(Case(name=f"fp32_32x32x{h}x{h}_{f}x{f}_p{p}_s{s}", Hi=h, Wi=h, Y=f, X=f,
+                        pad=(p, p), stride=(s, s), seed=2000 + i, tags=("fp32_small",), **base))
     return out
 
 
 CASES = [
-    Case(name="cfg1_fp32_2x16x15x15_3x3_p1_s2", N=2, C=16, K=16, Hi=15, Wi=15, Y=3, X=3, pad=(1, 1),
-         stride=(2, 2), dtype=F32, layout=NCHW, dist="uniform", seed=1000, tags=("cfg1",)),
+    Case(name="fp32_2x16x15x15_3x3_p1_s2", N=2, C=16, K=16, Hi=15, Wi=15, Y=3, X=3, pad=(1, 1),
+         stride=(2, 2), dtype=F32, layout=NCHW, dist="uniform", seed=1000, tags=("fp32_small",)),
     *_sweep(),
-    Case(name="cfg3_bf16_16x1x512x2048_1x2_s1x2", N=16, C=2048, K=2048, Hi=1, Wi=512, Y=1, X=2,
+    Case(name="bf16_16x1x512x2048_1x2_s1x2", N=16, C=2048, K=2048, Hi=1, Wi=512, Y=1, X=2,
          pad=(0, 0), stride=(1, 2), dtype=BF16, layout=NHWC, dist="normal", sigma=0.02, seed=3000,
-         tags=("cfg3", "large")),
-    Case(name="cfg4_bf16_resnext_64x56x56x256_g32_3x3_s2", N=64, C=256, K=256, Hi=56, Wi=56, Y=3, X=3,
+         tags=("large",)),
+    Case(name="bf16_resnext_64x56x56x256_g32_3x3_s2", N=64, C=256, K=256, Hi=56, Wi=56, Y=3, X=3,
          pad=(1, 1), stride=(2, 2), groups=32, dtype=BF16, layout=NHWC, dist="normal", sigma=0.05,
-         seed=4000, tags=("cfg4",)),
-    Case(name="cfg5a_bf16_32x28x28x512_3x3_s2_p1_d2", N=32, C=512, K=512, Hi=28, Wi=28, Y=3, X=3,
+         seed=4000, tags=("grouped",)),
+    Case(name="bf16_32x28x28x512_3x3_s2_p1_d2", N=32, C=512, K=512, Hi=28, Wi=28, Y=3, X=3,
          pad=(1, 1), stride=(2, 2), dil=(2, 2), dtype=BF16, layout=NHWC, dist="normal", sigma=0.05,
-         seed=5000, tags=("cfg5", "large")),
-    Case(name="cfg5b_bf16_32x14x14_1024_2048_1x1_s2", N=32, C=1024, K=2048, Hi=14, Wi=14, Y=1, X=1,
+         seed=5000, tags=("large",)),
+    Case(name="bf16_32x14x14_1024_2048_1x1_s2", N=32, C=1024, K=2048, Hi=14, Wi=14, Y=1, X=1,
          pad=(0, 0), stride=(2, 2), dtype=BF16, layout=NHWC, dist="normal", sigma=0.05, seed=5001,
-         tags=("cfg5",)),
-    Case(name="cfg5c_bf16_32x57x57x128_5x5_s3_p2", N=32, C=128, K=128, Hi=57, Wi=57, Y=5, X=5,
+         tags=("ridge",)),
+    Case(name="bf16_32x57x57x128_5x5_s3_p2", N=32, C=128, K=128, Hi=57, Wi=57, Y=5, X=5,
          pad=(2, 2), stride=(3, 3), dtype=BF16, layout=NHWC, dist="normal", sigma=0.05, seed=5002,
-         tags=("cfg5",)),
+         tags=("ridge",)),
 ]
 
 BY_NAME = {c.name: c for c in CASES}
 
 
 def case(name: str) -> Case:
+    """A workload by its name or by a prefix of it that only one name has."""
     if name in BY_NAME:
         return BY_NAME[name]
-    for c in CASES:  # allow the short prefix ("cfg3", "cfg5a", ...)
-        if c.name.split("_")[0] == name:
-            return c
+    hits = [c for c in CASES if c.name.startswith(name)]
+    if len(hits) == 1:
+        return hits[0]
     raise KeyError(name)
 
 

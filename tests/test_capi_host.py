@@ -121,32 +121,32 @@ def _class_rows(c, dim):
     return out
 
 
-def test_survey_table_cfg1(B):
-    p = B.Plan.from_case(wl.case("cfg1"))
+def test_class_table_fp32_2x16x15x15(B):
+    p = B.Plan.from_case(wl.case("fp32_2x16x15x15"))
     got = [(s["ty"], s["tx"], s["taps_y"] * s["taps_x"], s["M"]) for s in map(p.subgemm, range(p.num_subgemms()))]
     assert got == [(0, 0, 4, 98), (0, 1, 2, 112), (1, 0, 2, 112), (1, 1, 1, 128)]
 
 
-def test_cfg5_class_structure(B):
-    a = B.Plan.from_case(wl.case("cfg5a"))   # stride 2, dilation 2: one class, 9 taps, 1/4 of dx written
+def test_class_structure_of_strided_bf16_layers(B):
+    a = B.Plan.from_case(wl.case("bf16_32x28x28x512"))   # stride 2, dilation 2: one class, 9 taps, 1/4 of dx written
     assert a.num_subgemms() == 1 and a.subgemm(0)["taps_y"] * a.subgemm(0)["taps_x"] == 9
     rows, cols = a.coverage()
     assert rows.sum() == 14 and cols.sum() == 14
-    b = B.Plan.from_case(wl.case("cfg5b"))   # 1x1 stride 2: one class of four non-empty
+    b = B.Plan.from_case(wl.case("bf16_32x14x14_1024"))   # 1x1 stride 2: one class of four non-empty
     assert b.num_subgemms() == 1 and b.subgemm(0)["M"] == 32 * 7 * 7
-    c = B.Plan.from_case(wl.case("cfg5c"))   # 5x5 stride 3: nine classes
+    c = B.Plan.from_case(wl.case("bf16_32x57x57x128"))   # 5x5 stride 3: nine classes
     taps = sorted(s["taps_y"] * s["taps_x"] for s in map(c.subgemm, range(c.num_subgemms())))
     assert taps == sorted([4, 4, 2, 4, 4, 2, 2, 2, 1])
 
 
 def test_paths(B):
-    assert B.Plan.from_case(wl.case("cfg3")).path()[0] == "tcgen05"
-    assert B.Plan.from_case(wl.case("cfg5a")).path()[0] == "tcgen05"
-    assert B.Plan.from_case(wl.case("cfg1")).path()[0] == "simt"
-    assert B.Plan.from_case(wl.case("cfg4")).path() == ("grouped", 1)  # writes every pixel itself
+    assert B.Plan.from_case(wl.case("bf16_16x1x512x2048")).path()[0] == "tcgen05"
+    assert B.Plan.from_case(wl.case("bf16_32x28x28x512")).path()[0] == "tcgen05"
+    assert B.Plan.from_case(wl.case("fp32_2x16x15x15")).path()[0] == "simt"
+    assert B.Plan.from_case(wl.case("bf16_resnext_64x56x56x256")).path() == ("grouped", 1)  # writes every pixel itself
     # launches per run: the tensor-core kernel zeroes uncovered pixels itself
-    assert B.Plan.from_case(wl.case("cfg3")).path()[1] == 1
-    assert B.Plan.from_case(wl.case("cfg5a")).path()[1] == 1
+    assert B.Plan.from_case(wl.case("bf16_16x1x512x2048")).path()[1] == 1
+    assert B.Plan.from_case(wl.case("bf16_32x28x28x512")).path()[1] == 1
     # the CUDA-core path launches the fill kernel where some pixel is uncovered
     assert B.Plan(1, 4, 4, 9, 9, 1, 1, stride=(2, 2)).path() == ("simt", 2)
 

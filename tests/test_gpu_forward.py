@@ -40,7 +40,7 @@ FWD_CASES = [
     _mk("fwd_3x3s2_ragged_k", N=3, C=128, K=136, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2)),
     _mk("fwd_dil2", N=2, C=64, K=128, Hi=12, Wi=12, Y=3, X=3, pad=(2, 2), dil=(2, 2)),
     _mk("fwd_groups2", N=2, C=128, K=64, Hi=10, Wi=9, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=2),
-    _mk("fwd_page3_small", N=2, C=256, K=256, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)),
+    _mk("fwd_1x2_s1x2_small", N=2, C=256, K=256, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)),
     _mk("fwd_c_tail", N=2, C=72, K=40, Hi=7, Wi=9, Y=2, X=3, pad=(0, 1), stride=(2, 1)),
     _mk("fwd_5x5s3", N=2, C=64, K=64, Hi=19, Wi=17, Y=5, X=5, pad=(2, 2), stride=(3, 3)),
     _mk("fwd_many_tiles", N=4, C=64, K=256, Hi=20, Wi=20, Y=3, X=3, pad=(1, 1)),

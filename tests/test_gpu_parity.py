@@ -88,7 +88,7 @@ def check_points(c, got, g, dy, w, count=1500, seed=0):
     assert np.all(np.abs(gv - vals) <= bound)
 
 
-SMALL = [c for c in wl.CASES if c.tags[0] in ("cfg1", "cfg2")]
+SMALL = [c for c in wl.CASES if c.tags[0] == "fp32_small"]
 
 
 @pytest.mark.parametrize("c", SMALL, ids=lambda c: c.name)
@@ -99,7 +99,7 @@ def test_small_configs_full(B, c):
     check_full(c, got, g, dy, w)
 
 
-LARGE = {"cfg3": (0, 1), "cfg4": None, "cfg5a": (0, 2), "cfg5b": (0, 4), "cfg5c": (0, 3)}
+LARGE = {"bf16_16x1x512x2048": (0, 1), "bf16_resnext_64x56x56x256": None, "bf16_32x28x28x512": (0, 2), "bf16_32x14x14_1024": (0, 4), "bf16_32x57x57x128": (0, 3)}
 
 
 @pytest.mark.parametrize("name", list(LARGE))
@@ -110,7 +110,7 @@ def test_large_configs(B, name):
     assert np.all(np.isfinite(got)), "unwritten (NaN) outputs"
     check_full(c, got, g, dy, w, n_range=LARGE[name])
     check_points(c, got, g, dy, w, seed=zlib.crc32(name.encode()) % 1000)
-    assert plan.path()[0] == ("grouped" if name == "cfg4" else "tcgen05")
+    assert plan.path()[0] == ("grouped" if name == "bf16_resnext_64x56x56x256" else "tcgen05")
 
 
 def _mk(name, **kw):
@@ -130,7 +130,7 @@ TC_CASES = [
     _mk("tc_filter_gt_input", N=2, C=64, K=64, Hi=3, Wi=3, Y=5, X=5, pad=(2, 2)),
     _mk("tc_stride4_uncovered", N=2, C=128, K=64, Hi=15, Wi=14, Y=3, X=3, pad=(1, 1), stride=(4, 4)),
     _mk("tc_m1", N=1, C=512, K=512, Hi=1, Wi=1, Y=1, X=1),
-    _mk("tc_page3_small", N=2, C=256, K=256, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)),
+    _mk("tc_1x2_s1x2_small", N=2, C=256, K=256, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)),
     _mk("tc_dil2_s2", N=2, C=128, K=128, Hi=12, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)),
     _mk("tc_mixed", N=2, C=200, K=40, Hi=11, Wi=6, Y=2, X=4, pad=(0, 3), stride=(3, 1), dil=(2, 3)),
     _mk("tc_bn256_ragged", N=3, C=264, K=64, Hi=6, Wi=7, Y=3, X=3, pad=(1, 1), stride=(1, 1)),
@@ -250,7 +250,7 @@ def test_cp_async_producer_variant(B, monkeypatch, idx):
 
 
 SK_CASES = [
-    _mk("sk_page3_small", N=2, C=256, K=256, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)),
+    _mk("sk_1x2_s1x2_small", N=2, C=256, K=256, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)),
     _mk("sk_one_tile_deep_k", N=1, C=256, K=2048, Hi=16, Wi=16, Y=1, X=1),          # 32 units over many pairs
     _mk("sk_multiclass", N=2, C=512, K=192, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2)),
     _mk("sk_ragged_n", N=3, C=264, K=64, Hi=6, Wi=7, Y=3, X=3, pad=(1, 1)),
@@ -289,14 +289,14 @@ CL2_256 = {"CONVBWD_DEBUG_CL": "2", "CONVBWD_DEBUG_BN": "256"}
 CL2_512 = {"CONVBWD_DEBUG_CL": "2", "CONVBWD_DEBUG_BN": "512"}
 PAIR_CASES = [
     (_mk("w512_ragged_n", N=3, C=768, K=192, Hi=9, Wi=7, Y=3, X=3, pad=(1, 1), stride=(2, 2)), W512),
-    (_mk("w512_page3", N=2, C=1024, K=512, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)), W512),
+    (_mk("w512_1x2_s1x2", N=2, C=1024, K=512, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)), W512),
     (_mk("w512_ragged_m", N=4, C=512, K=128, Hi=17, Wi=15, Y=3, X=3, pad=(1, 1)), W512),
     (_mk("w512_groups2", N=2, C=1024, K=256, Hi=8, Wi=9, Y=3, X=3, pad=(1, 1), groups=2), W512),
     (_mk("w512_tail8", N=2, C=520, K=64, Hi=7, Wi=7, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)), W512),
     (_mk("pair_cg128", N=2, C=128, K=128, Hi=12, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)), PAIR),
     (_mk("pair_cg200", N=2, C=200, K=40, Hi=11, Wi=6, Y=2, X=4, pad=(0, 3), stride=(3, 1), dil=(2, 3)), PAIR),
     (_mk("pair_5x5s3", N=2, C=128, K=128, Hi=19, Wi=17, Y=5, X=5, pad=(2, 2), stride=(3, 3)), PAIR),
-    (_mk("cl2_page3", N=4, C=512, K=256, Hi=1, Wi=128, Y=1, X=2, stride=(1, 2)), CL2),
+    (_mk("cl2_1x2_s1x2", N=4, C=512, K=256, Hi=1, Wi=128, Y=1, X=2, stride=(1, 2)), CL2),
     (_mk("cl2_odd_blocks", N=3, C=256, K=96, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2)), CL2),
     (_mk("cl2_kg_tail", N=2, C=384, K=160, Hi=9, Wi=10, Y=3, X=3, pad=(1, 1)), CL2_256),
     (_mk("cl2_groups2", N=2, C=512, K=256, Hi=8, Wi=9, Y=3, X=3, pad=(1, 1), stride=(1, 2), groups=2), CL2),
@@ -410,7 +410,7 @@ def test_bounded_wait_gives_up_and_context_survives(B):
 
 def test_per_kernel_timing(B):
     # tensor-core path: one launch (uncovered pixels are zeroed inside it)
-    c = wl.case("cfg5a")
+    c = wl.case("bf16_32x28x28x512")
     plan = B.Plan.from_case(c)
     dy_s, w_s, dx_s = plan.shapes()
     dy = torch.zeros(dy_s, dtype=torch.bfloat16, device="cuda")

@@ -203,7 +203,7 @@ def test_point_evaluation_matches_scatter(c):
 
 
 def test_batch_range_sampling_is_a_slice():
-    c = wl.case("cfg1")
+    c = wl.case("fp32_2x16x15x15")
     g, dy, w = _inputs(c)
     full, fab = oracle.dgrad(g, oracle.LAYOUT_NCHW, dy, w)
     part, pab = oracle.dgrad(g, oracle.LAYOUT_NCHW, dy, w, n_range=(1, 2))
