@@ -214,12 +214,155 @@ __global__ void __launch_bounds__(256) simt_dgrad_kernel(const __grid_constant__
     }
 }
 
+// fp32 variant of the same tiles with a 4-stage cp.async pipeline: each thread
+// gathers its 4 A and 4 B elements of a 16-deep slice with 4-byte copies
+// (zero-filled outside dy, past the class's reduction or past C/G) while the
+// FMAs run on the slices already in shared memory, so the reduction pays one
+// memory latency instead of one per slice.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__global__ void __launch_bounds__(256) simt_dgrad_f32_kernel(const __grid_constant__ SimtParams p) {
+    constexpr int BM = 64, BN = 64, BK = 16, S = 4;
+    __shared__ float As[S][BK][BM + 4];
+    __shared__ float Bs[S][BK][BN + 4];
+    const Geom &g = p.g;
+    const Strides &st = p.st;
+    const float *dy = static_cast<const float *>(p.dy);
+    const float *w = static_cast<const float *>(p.w);
+    float *dx = static_cast<float *>(p.dx);
+
+    const int tile = blockIdx.x;
+    int ci = 0;
+    for (int i = 1; i < p.num_classes; ++i)
+        if (tile >= p.cls[i].tile_begin) ci = i;
+    const ClassDesc &c = p.cls[ci];
+    const int local = tile - c.tile_begin;
+    const int nb = local % p.n_tiles;
+    const int rest = local / p.n_tiles;
+    const int mb = rest % c.m_tiles;
+    const int gi = rest / c.m_tiles;
+
+    const int tid = threadIdx.x;
+    const int HTWT = c.HT * c.WT;
+    const int Kred = c.taps_y * c.taps_x * g.Kg;
+    const int nslices = (Kred + BK - 1) / BK;
+
+    // the A row and the B column this thread gathers
+    const int arow = tid % BM;
+    const int am = mb * BM + arow;
+    int an = -1, aht = 0, awt = 0;
+    if (am < c.M) {
+        an = am / HTWT;
+        const int rem = am - an * HTWT;
+        aht = c.ht_lo + rem / c.WT;
+        awt = c.wt_lo + rem % c.WT;
+    }
+    const int bcol = tid % BN;
+    const int bc = nb * BN + bcol;
+    const float *dy_n = dy + (an >= 0 ? (int64_t)an * st.dy_n : 0) + (int64_t)gi * g.Kg * st.dy_k;
+    const float *w_g = w + (int64_t)gi * g.Kg * st.w_k + (int64_t)(bc < g.Cg ? bc : 0) * st.w_c;
+
+    // the reduction index r = tap*Kg + k of this thread's 4 elements in the next
+    // slice to issue, kept as (k, i, j) counters advanced by BK per slice (no
+    // divisions in the loop)
+    int qk[4], qi[4], qj[4], qr[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int r = tid / BM + 4 * q;
+        const int tap = r / g.Kg;
+        qk[q] = r - tap * g.Kg;
+        qj[q] = tap / c.taps_x;
+        qi[q] = tap - qj[q] * c.taps_x;
+        qr[q] = r;
+    }
+    auto issue = [&](int slice) {
+        const int sb = slice % S;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int kk = tid / BM + 4 * q;
+            const float *sa = dy, *sbp = w;
+            bool va = false, vb = false;
+            if (qr[q] < Kred) {
+                const int ho = aht - qj[q] * g.DH, wo = awt - qi[q] * g.DW;
+                va = an >= 0 && ho >= 0 && ho < g.Ho && wo >= 0 && wo < g.Wo;
+                if (va) sa = dy_n + (int64_t)qk[q] * st.dy_k + (int64_t)ho * st.dy_h + (int64_t)wo * st.dy_w;
+                vb = bc < g.Cg;
+                if (vb)
+                    sbp = w_g + (int64_t)qk[q] * st.w_k + (int64_t)(c.ty + g.YT * qj[q]) * st.w_y +
+                          (int64_t)(c.tx + g.XT * qi[q]) * st.w_x;
+            }
+            cp_async_4(smem_u32(&As[sb][kk][arow]), sa, va ? 4u : 0u);
+            cp_async_4(smem_u32(&Bs[sb][kk][bcol]), sbp, vb ? 4u : 0u);
+            // advance to the next slice: r += BK
+            qr[q] += BK;
+            qk[q] += BK;
+            while (qk[q] >= g.Kg) {
+                qk[q] -= g.Kg;
+                if (++qi[q] == c.taps_x) {
+                    qi[q] = 0;
+                    ++qj[q];
+                }
+            }
+        }
+    };
+
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+    for (int sl = 0; sl < S - 1; ++sl) {
+        if (sl < nslices) issue(sl);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    const int tr = tid / 16, tc = tid % 16;
+    for (int sl = 0; sl < nslices; ++sl) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(S - 2) : "memory");  // slice sl has landed
+        __syncthreads();
+        if (sl + S - 1 < nslices) issue(sl + S - 1);  // refills the buffer read in iteration sl - 1
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        const int sb = sl % S;
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[sb][kk][tr * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[sb][kk][tc * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = mb * BM + tr * 4 + i;
+        if (m >= c.M) continue;
+        const int n = m / HTWT;
+        const int rem = m - n * HTWT;
+        const int hi = (c.ht_lo + rem / c.WT) * g.sh + c.ty * g.dh - g.ph;
+        const int wi = (c.wt_lo + rem % c.WT) * g.sw + c.tx * g.dw - g.pw;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int cc = nb * BN + tc * 4 + j;
+            if (cc >= g.Cg) continue;
+            dx[n * st.dx_n + (int64_t)(gi * g.Cg + cc) * st.dx_c + hi * st.dx_h + wi * st.dx_w] = acc[i][j];
+        }
+    }
+}
+
 cudaError_t launch_simt(const SimtParams &p, int dtype, cudaStream_t s) {
     if (p.total_tiles <= 0) return cudaSuccess;
     if (dtype == 1)
         simt_dgrad_kernel<__nv_bfloat16><<<p.total_tiles, 256, 0, s>>>(p);
     else
-        simt_dgrad_kernel<float><<<p.total_tiles, 256, 0, s>>>(p);
+        simt_dgrad_f32_kernel<<<p.total_tiles, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
