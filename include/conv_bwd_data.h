@@ -100,6 +100,20 @@ typedef enum {
  * into it, runs the twin's kernels and transposes dx back (path() reports the
  * twin's path with 3 more launches). */
 
+/* Planner overrides, read at create (for tests and measurements; unset in
+ * normal use):
+ *   CONVBWD_DEBUG_PATH=simt          CUDA-core path for every plan
+ *   CONVBWD_DEBUG_NOIM2COL=1         cp.async A producer instead of TMA im2col
+ *   CONVBWD_DEBUG_2SM=1 / _NO2SM=1   SM-pair kernel for C/G >= 128 / never
+ *   CONVBWD_DEBUG_BN=128|256|512     tile width; CONVBWD_DEBUG_CL=1|2 pairs per cluster
+ *   CONVBWD_DEBUG_STREAMK=1          stream-K schedule on the SM-pair kernel
+ *   CONVBWD_DEBUG_RASTER_M=1         tiles walk m-blocks first
+ *   CONVBWD_DEBUG_GRID=n             cap the 1-SM kernel's grid
+ *   CONVBWD_DEBUG_L2PROMO=0|1       TMA L2 promotion none / 128 B (default 256 B)
+ *   CONVBWD_DEBUG_WAIT_SECONDS=s     budget of every bounded device wait (default 2)
+ *   CONVBWD_DEBUG_HOST_CHUNKS=n      batch chunks of the pipelined run_host (default 4)
+ *   CONVBWD_DEBUG_NO_TRANSPOSE=1     bf16 NCHW plans stay on the CUDA-core path */
+
 /* Validate the descriptor and plan on the host: forward output size, tilde
  * factors, non-empty sub-GEMM list (consecutive gemmIds), coverage of dx,
  * kernel path and tile schedule.  If a CUDA device is visible, also
