@@ -187,6 +187,9 @@ SIMT_CASES = (wl.random_tiny_cases(40, seed=31, accept=_ok) +
                       dtype=wl.F32, dist="uniform"),
                   _mk("simt_f32_wide", N=1, C=130, K=70, Hi=6, Wi=5, Y=2, X=3, pad=(1, 1), stride=(1, 2),
                       dtype=wl.F32, layout=wl.NCHW, dist="uniform"),
+                  # 3/4 of dx uncovered: the fill kernel writes 2.45 MB of zeros before the GEMM
+                  _mk("simt_f32_fill_56", N=4, C=64, K=64, Hi=56, Wi=57, Y=3, X=3, pad=(1, 1), stride=(2, 2),
+                      dil=(2, 2), dtype=wl.F32, layout=wl.NHWC, dist="uniform"),
               ])
 
 
