@@ -40,6 +40,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 # Per-launch DRAM traffic of each workload's GEMM kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel's
 # sources are unchanged (hash below) and the plan launches the same tile shape.
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / bf16 tensor rates of the part
 TC2_SOURCES = ("tc_common.cuh", "tc2_sm103.cu", "internal.h")
 GROUPED_SOURCES = ("tc_common.cuh", "grouped.cu", "internal.h")
 TRAFFIC = {
@@ -332,13 +333,22 @@ def main():
     kmean = sum(kern_ms) / len(kern_ms)
     tm, tn, tsms = plan.tile()
     kernel_name = {"tcgen05": (f"tc2_dgrad_kernel<{tn}, {tsms // 2}>" if tsms >= 2 else f"tc_dgrad_kernel<{tn}>"),
-                   "grouped": f"grouped_dgrad_kernel<{case.C // case.groups}>", "simt": "simt_dgrad_kernel"}[path]
+                   "grouped": f"grouped_dgrad_kernel<{case.C // case.groups}>", "simt": "simt_dgrad_kernel",
+                   "tf32": "tf32_dgrad_kernel"}[path]
     if path == "tcgen05":
         achieved = useful / (kmean * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": peaks["source"] + " (bf16 dense, burst)", "kernel": kernel_name,
                 "kernel_ms": kmean}
+    elif path == "tf32":
+        # three TF32 products per useful fp32 multiply-add: the ceiling is the
+        # dense TF32 rate (bf16 rate x the nominal 1.1 / 2.25 ratio) over 3
+        achieved = useful / (kmean * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"] * TF32_PER_BF16 / 3.0
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": peaks["source"] + " (bf16 dense, burst) x 1.1/2.25 (TF32) / 3 (products per MAC)",
+                "kernel": kernel_name, "kernel_ms": kmean}
     else:
         achieved = algo_bytes / (kmean * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]

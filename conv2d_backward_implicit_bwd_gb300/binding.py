@@ -16,8 +16,8 @@ LIB_PATH = os.path.join(PKG, "lib", "libconv_bwd_data.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_DEVICE_FAULT = range(7)
 F32, BF16 = 0, 1
 NCHW_GKCYX, NHWC_KYXC = 0, 1
-PATH_TCGEN05, PATH_SIMT, PATH_GROUPED = 0, 1, 2
-PATH_NAMES = {PATH_TCGEN05: "tcgen05", PATH_SIMT: "simt", PATH_GROUPED: "grouped"}
+PATH_TCGEN05, PATH_SIMT, PATH_GROUPED, PATH_TF32 = 0, 1, 2, 3
+PATH_NAMES = {PATH_TCGEN05: "tcgen05", PATH_SIMT: "simt", PATH_GROUPED: "grouped", PATH_TF32: "tf32"}
 
 EXPORTED = [
     "conv_bwd_data_create", "conv_bwd_data_destroy", "conv_bwd_data_out_dims", "conv_bwd_data_num_subgemms",

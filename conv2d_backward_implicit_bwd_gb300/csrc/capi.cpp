@@ -22,6 +22,7 @@
 
 #include "../../include/conv_bwd_data.h"
 #include "internal.h"
+#include "tf32.h"
 
 using namespace cbd;
 
@@ -75,6 +76,13 @@ struct conv_bwd_plan_s {
     // geometry in NHWC/KYXC (sharing this plan's status word)
     conv_bwd_plan_s *nhwc_plan = nullptr;
     void *t_dy = nullptr, *t_w = nullptr, *t_dx = nullptr;
+    // fp32 tensor-core path: the filter split into hi and lo parts, laid out
+    // [G][C/G][Y][X][K/G] (re-split by every run, w being an input).  Owned by
+    // the plan that allocated them; an NCHW parent lends its own to its NHWC
+    // twin, a pipelined run_host to its chunk plans.
+    float *w_hi = nullptr, *w_lo = nullptr;
+    bool owns_wsplit = false;
+    int32_t w_gkcyx = 0;  // 1: run() receives the filter as GKCYX (the NCHW parent's w)
     std::mutex mu;
 };
 
@@ -216,18 +224,45 @@ bool encode_a_maps(conv_bwd_plan_s *p, const void *dy) {
     PFN_encodeIm2col enc = get_encode_im2col();
     if (!enc) return false;
     const Geom &g = p->g;
+    // 128-byte pixel rows: 64 bf16 channels, or 32 fp32 ones (fp32 tensor-core path)
+    const bool f32 = p->desc.dtype == CONV_BWD_F32;
+    const cuuint64_t es = f32 ? 4 : 2;
     p->tmap_a.resize(p->classes.size());
     cuuint64_t dims[4] = {(cuuint64_t)g.K, (cuuint64_t)g.Wo, (cuuint64_t)g.Ho, (cuuint64_t)g.N};
-    cuuint64_t strides[3] = {(cuuint64_t)g.K * 2, (cuuint64_t)g.Wo * g.K * 2, (cuuint64_t)g.Ho * g.Wo * g.K * 2};
+    cuuint64_t strides[3] = {(cuuint64_t)g.K * es, (cuuint64_t)g.Wo * g.K * es, (cuuint64_t)g.Ho * g.Wo * g.K * es};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     for (size_t i = 0; i < p->classes.size(); ++i) {
         int lo[2], hi[2];
         im2col_corners(g, p->classes[i], lo, hi);
-        CUresult r = enc(&p->tmap_a[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(dy), dims, strides, lo,
-                         hi, 64, 128, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         l2_promotion(), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        CUresult r = enc(&p->tmap_a[i], f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                         const_cast<void *>(dy), dims, strides, lo, hi, f32 ? 32 : 64, 128, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2_promotion(),
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return false;
     }
+    return true;
+}
+
+// fp32 tensor-core path: the split filter (w_hi, w_lo, [G][Cg][Y][X][Kg]) as
+// 5-D {Kg, X, Y, Cg, G}; a box {32, 1, 1, 128, 1} is 128 c rows of 32 k
+// (128 bytes, 128-byte swizzle: B K-major).  k past Kg and c past Cg read as
+// zero.
+bool encode_tf32_w_maps(conv_bwd_plan_s *p) {
+    PFN_encodeTiled enc = get_encode_tiled();
+    if (!enc) return false;
+    const Geom &g = p->g;
+    cuuint64_t dims[5] = {(cuuint64_t)g.Kg, (cuuint64_t)g.X, (cuuint64_t)g.Y, (cuuint64_t)g.Cg, (cuuint64_t)g.G};
+    cuuint64_t strides[4] = {(cuuint64_t)g.Kg * 4, (cuuint64_t)g.X * g.Kg * 4, (cuuint64_t)g.Y * g.X * g.Kg * 4,
+                             (cuuint64_t)g.Cg * g.Y * g.X * g.Kg * 4};
+    cuuint32_t box[5] = {(cuuint32_t)kTf32BK, 1, 1, (cuuint32_t)kTf32BN, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    float *parts[2] = {p->w_hi, p->w_lo};
+    CUtensorMap *maps[2] = {&p->tmap_w, &p->tmap_w_half};
+    for (int i = 0; i < 2; ++i)
+        if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, parts[i], dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2_promotion(),
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
     return true;
 }
 
@@ -333,6 +368,12 @@ int host_chunks(conv_bwd_plan_s *p, size_t ndy, size_t ndx) {
         cd.N = tail;
         if (plan_create_borrowed_status(&cd, p->d_status, &p->chunk_plan[1]) != CONV_BWD_OK) return 1;
     }
+    for (auto *c : p->chunk_plan)
+        if (c) {  // fp32 tensor-core chunks split the filter into this plan's buffers (same stream, in turn)
+            c->w_hi = p->w_hi;
+            c->w_lo = p->w_lo;
+            c->w_gkcyx = p->w_gkcyx;
+        }
     if (cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking) != cudaSuccess) {
         cudaGetLastError();
@@ -439,11 +480,27 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                       d.Hi < (1 << 20) && d.Wi < (1 << 20) && d.stride_w <= 64 &&
                       d.N * d.Hi * ((d.Wi + 15) / 16) < (1LL << 31);  // item count (chunks of >= 16 pixels)
     if (grouped_ok) grouped_ok = grouped_layout(g).smem <= 200 * 1024;
-    p->path = tc_ok ? CONV_BWD_PATH_TCGEN05 : (grouped_ok ? CONV_BWD_PATH_GROUPED : CONV_BWD_PATH_SIMT);
-    if (const char *f = env("CONVBWD_DEBUG_PATH")) {
-        if (!std::strcmp(f, "simt")) p->path = CONV_BWD_PATH_SIMT;
+    // fp32 on the tensor cores (three-term TF32 split) for problems large
+    // enough to pay for the filter split launch; NHWC/KYXC, 32-channel TMA
+    // im2col blocks that stay inside a group, 16-byte pixel strides
+    bool tf32_ok = d.dtype == CONV_BWD_F32 && d.layout == CONV_BWD_NHWC_KYXC && d.K % 4 == 0 && d.C % 4 == 0 &&
+                   g.Cg % 4 == 0 && g.Kg % 4 == 0 && (g.G == 1 || g.Kg % kTf32BK == 0) && d.Hi < 16384 &&
+                   d.Wi < 16384;
+    for (const ClassDesc &c : p->classes) {
+        int lo[2], hi[2];
+        im2col_corners(g, c, lo, hi);
+        for (int q = 0; q < 2; ++q)
+            if (lo[q] < -128 || lo[q] > 127 || hi[q] < -128 || hi[q] > 127) tf32_ok = false;
+        if ((c.taps_x - 1) * g.DW > 127 || (c.taps_y - 1) * g.DH > 127) tf32_ok = false;
     }
-    p->bn = (p->path == CONV_BWD_PATH_TCGEN05) ? (g.Cg >= 256 ? 256 : 128) : 64;
+    const char *force = env("CONVBWD_DEBUG_PATH");
+    const bool tf32_big = p->useful_flop >= kTf32MinFlop || (force && !std::strcmp(force, "tf32"));
+    p->path = tc_ok ? CONV_BWD_PATH_TCGEN05
+                    : (grouped_ok ? CONV_BWD_PATH_GROUPED
+                                  : (tf32_ok && tf32_big ? CONV_BWD_PATH_TF32 : CONV_BWD_PATH_SIMT));
+    if (force && !std::strcmp(force, "simt")) p->path = CONV_BWD_PATH_SIMT;
+    p->bn = (p->path == CONV_BWD_PATH_TCGEN05) ? (g.Cg >= 256 ? 256 : 128)
+                                               : (p->path == CONV_BWD_PATH_TF32 ? kTf32BN : 64);
     if (const char *f = env("CONVBWD_DEBUG_BN"))
         if (p->path == CONV_BWD_PATH_TCGEN05 && (!std::strcmp(f, "128") || !std::strcmp(f, "256"))) p->bn = std::atoi(f);
     // im2col loads read 64 channels past k0 of dy's flat K axis, exact only
@@ -507,7 +564,8 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
     // Schedule: classes with the longest reduction first (LPT), tiles of one
     // class contiguous; BM = 256 rows on SM pairs, 128 for the 1-SM
     // tensor-core kernel, 64 for SIMT.
-    const int bm = p->path == CONV_BWD_PATH_TCGEN05 ? (p->two_sm ? 256 * p->cl : 128) : 64;
+    const int bm = p->path == CONV_BWD_PATH_TCGEN05 ? (p->two_sm ? 256 * p->cl : 128)
+                                                    : (p->path == CONV_BWD_PATH_TF32 ? 128 : 64);
     const int n_tiles = (g.Cg + p->bn - 1) / p->bn;
     p->sched.resize(p->classes.size());
     std::iota(p->sched.begin(), p->sched.end(), 0);
@@ -558,17 +616,43 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                     p->d_flags = nullptr;
                 }
             }
-            // bf16 NCHW/GKCYX: run the NHWC/KYXC plan of the same geometry between
-            // layout transposes when that plan is on a tensor-core path
-            if (d.dtype == CONV_BWD_BF16 && d.layout == CONV_BWD_NCHW_GKCYX && !env("CONVBWD_DEBUG_NO_TRANSPOSE")) {
+            const size_t nsplit = (size_t)d.K * g.Cg * d.Y * d.X * sizeof(float);
+            if (p->path == CONV_BWD_PATH_TF32) {
+                if (cudaMalloc(&p->w_hi, nsplit) == cudaSuccess && cudaMalloc(&p->w_lo, nsplit) == cudaSuccess) {
+                    p->owns_wsplit = true;
+                } else {
+                    cudaGetLastError();
+                    cudaFree(p->w_hi);
+                    cudaFree(p->w_lo);
+                    p->w_hi = p->w_lo = nullptr;
+                    p->path = CONV_BWD_PATH_SIMT;  // keeps its 64x64 schedule below
+                }
+            }
+            // NCHW/GKCYX: run the NHWC/KYXC plan of the same geometry between
+            // layout transposes when that plan is on a tensor-core path (bf16:
+            // dy, w and dx transposed; fp32: dy and dx, the filter split reads
+            // GKCYX directly)
+            if (d.layout == CONV_BWD_NCHW_GKCYX && !env("CONVBWD_DEBUG_NO_TRANSPOSE")) {
                 conv_bwd_desc nd = d;
                 nd.layout = CONV_BWD_NHWC_KYXC;
                 conv_bwd_plan child = nullptr;
-                if (plan_create_borrowed_status(&nd, p->d_status, &child) == CONV_BWD_OK && child->path != CONV_BWD_PATH_SIMT) {
-                    const size_t ndy = (size_t)d.N * d.K * g.Ho * g.Wo * 2, nw = (size_t)d.K * g.Cg * d.Y * d.X * 2,
-                                 ndx = (size_t)d.N * d.C * d.Hi * d.Wi * 2;
-                    if (cudaMalloc(&p->t_dy, ndy) == cudaSuccess && cudaMalloc(&p->t_w, nw) == cudaSuccess &&
-                        cudaMalloc(&p->t_dx, ndx) == cudaSuccess) {
+                if (plan_create_borrowed_status(&nd, p->d_status, &child) == CONV_BWD_OK &&
+                    child->path != CONV_BWD_PATH_SIMT) {
+                    const bool f32 = d.dtype == CONV_BWD_F32;
+                    const size_t ndy = (size_t)d.N * d.K * g.Ho * g.Wo * es, nw = (size_t)d.K * g.Cg * d.Y * d.X * es,
+                                 ndx = (size_t)d.N * d.C * d.Hi * d.Wi * es;
+                    bool ok = cudaMalloc(&p->t_dy, ndy) == cudaSuccess && cudaMalloc(&p->t_dx, ndx) == cudaSuccess;
+                    if (ok && f32)
+                        ok = cudaMalloc(&p->w_hi, nsplit) == cudaSuccess && cudaMalloc(&p->w_lo, nsplit) == cudaSuccess;
+                    else if (ok)
+                        ok = cudaMalloc(&p->t_w, nw) == cudaSuccess;
+                    if (ok) {
+                        if (f32) {
+                            p->owns_wsplit = true;
+                            child->w_hi = p->w_hi;
+                            child->w_lo = p->w_lo;
+                            child->w_gkcyx = 1;
+                        }
                         p->nhwc_plan = child;
                         child = nullptr;
                     } else {
@@ -576,7 +660,10 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                         cudaFree(p->t_dy);
                         cudaFree(p->t_w);
                         cudaFree(p->t_dx);
+                        cudaFree(p->w_hi);
+                        cudaFree(p->w_lo);
                         p->t_dy = p->t_w = p->t_dx = nullptr;
+                        p->w_hi = p->w_lo = nullptr;
                     }
                 }
                 conv_bwd_data_destroy(child);
@@ -611,6 +698,10 @@ conv_bwd_status conv_bwd_data_destroy(conv_bwd_plan p) {
         cudaFree(p->t_dy);
         cudaFree(p->t_w);
         cudaFree(p->t_dx);
+        if (p->owns_wsplit) {
+            cudaFree(p->w_hi);
+            cudaFree(p->w_lo);
+        }
         if (p->h2d) cudaStreamDestroy(p->h2d);
         if (p->d2h) cudaStreamDestroy(p->d2h);
         if (cur != p->device && cur >= 0) cudaSetDevice(cur);
@@ -657,9 +748,9 @@ conv_bwd_status conv_bwd_data_coverage(const conv_bwd_plan p, uint8_t *row_mask,
 
 conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t *launches) {
     if (!p) return CONV_BWD_ERR_INVALID_ARG;
-    if (p->nhwc_plan) {  // dy and w transposed in, dx transposed out, around the NHWC plan's kernels
+    if (p->nhwc_plan) {  // dy (and bf16 w) transposed in, dx transposed out, around the NHWC plan's kernels
         conv_bwd_status st = conv_bwd_data_path(p->nhwc_plan, path, launches);
-        if (launches) *launches += 3;
+        if (launches) *launches += p->t_w ? 3 : 2;
         return st;
     }
     if (path) *path = p->path;
@@ -668,6 +759,8 @@ conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t
     // the grouped kernel writes every pixel; the tensor-core kernels zero uncovered pixels themselves
     const bool fill = p->any_uncovered && (p->path == CONV_BWD_PATH_SIMT || p->classes.empty());
     if (p->path == CONV_BWD_PATH_GROUPED) gemm_launches = 1;
+    if (p->path == CONV_BWD_PATH_TF32)  // the filter split, then the tensor-core kernel (which fills)
+        gemm_launches = 1 + (int)((p->classes.size() + kMaxTcClasses - 1) / kMaxTcClasses);
     if (launches) *launches = (fill ? 1 : 0) + gemm_launches;
     return CONV_BWD_OK;
 }
@@ -676,7 +769,7 @@ conv_bwd_status conv_bwd_data_tile(const conv_bwd_plan p, int32_t *tile_m, int32
     if (!p) return CONV_BWD_ERR_INVALID_ARG;
     if (p->nhwc_plan) return conv_bwd_data_tile(p->nhwc_plan, tile_m, tile_n, sms);
     const bool tc = p->path == CONV_BWD_PATH_TCGEN05, grouped = p->path == CONV_BWD_PATH_GROUPED;
-    if (tile_m) *tile_m = grouped ? 0 : tc ? (p->two_sm ? 256 * p->cl : 128) : 64;
+    if (tile_m) *tile_m = grouped ? 0 : tc ? (p->two_sm ? 256 * p->cl : 128) : p->path == CONV_BWD_PATH_TF32 ? 128 : 64;
     if (tile_n) *tile_n = grouped ? 0 : p->bn;
     if (sms) *sms = tc && p->two_sm ? 2 * p->cl : 1;
     return CONV_BWD_OK;
@@ -703,18 +796,23 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
     if ((p->path == CONV_BWD_PATH_TCGEN05 || p->path == CONV_BWD_PATH_GROUPED) &&
         ((uintptr_t)dy | (uintptr_t)w | (uintptr_t)dx) % 16)
         return CONV_BWD_ERR_MISALIGNED;
+    if (p->path == CONV_BWD_PATH_TF32 && ((uintptr_t)dy | (uintptr_t)dx) % 16) return CONV_BWD_ERR_MISALIGNED;
+    if (p->path == CONV_BWD_PATH_TF32 && !p->w_hi) return CONV_BWD_ERR_UNSUPPORTED;  // a plan without its scratch
     cudaStream_t s = (cudaStream_t)stream;
     std::lock_guard<std::mutex> lock(p->mu);
 
     if (p->nhwc_plan) {
-        // dy [N][K][Ho*Wo] -> [N][Ho*Wo][K], w [K][Cg][Y*X] -> [K][Y*X][Cg], the
-        // NHWC/KYXC plan's kernels, dx [N][Hi*Wi][C] -> [N][C][Hi*Wi]
-        if (launch_transpose_b16(dy, p->t_dy, d.N, d.K, (int64_t)g.Ho * g.Wo, p->num_sms, s) != cudaSuccess ||
-            launch_transpose_b16(w, p->t_w, d.K, g.Cg, (int64_t)d.Y * d.X, p->num_sms, s) != cudaSuccess)
+        // dy [N][K][Ho*Wo] -> [N][Ho*Wo][K], (bf16) w [K][Cg][Y*X] -> [K][Y*X][Cg],
+        // the NHWC/KYXC plan's kernels, dx [N][Hi*Wi][C] -> [N][C][Hi*Wi]; the
+        // fp32 twin's filter split reads GKCYX itself
+        auto transpose = d.dtype == CONV_BWD_F32 ? launch_transpose_b32 : launch_transpose_b16;
+        if (transpose(dy, p->t_dy, d.N, d.K, (int64_t)g.Ho * g.Wo, p->num_sms, s) != cudaSuccess)
             return CONV_BWD_ERR_CUDA;
-        conv_bwd_status st = conv_bwd_data_run(p->nhwc_plan, p->t_dy, p->t_w, p->t_dx, stream);
+        if (p->t_w && transpose(w, p->t_w, d.K, g.Cg, (int64_t)d.Y * d.X, p->num_sms, s) != cudaSuccess)
+            return CONV_BWD_ERR_CUDA;
+        conv_bwd_status st = conv_bwd_data_run(p->nhwc_plan, p->t_dy, p->t_w ? p->t_w : w, p->t_dx, stream);
         if (st != CONV_BWD_OK) return st;
-        if (launch_transpose_b16(p->t_dx, dx, d.N, (int64_t)d.Hi * d.Wi, d.C, p->num_sms, s) != cudaSuccess)
+        if (transpose(p->t_dx, dx, d.N, (int64_t)d.Hi * d.Wi, d.C, p->num_sms, s) != cudaSuccess)
             return CONV_BWD_ERR_CUDA;
         return CONV_BWD_OK;
     }
@@ -750,7 +848,8 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
     }
     // the tensor-core kernels zero uncovered pixels themselves (epilogue warps,
     // during the first tile's main loop); other paths use the fill kernel
-    if (p->any_uncovered && (p->path != CONV_BWD_PATH_TCGEN05 || p->classes.empty())) {
+    if (p->any_uncovered &&
+        ((p->path != CONV_BWD_PATH_TCGEN05 && p->path != CONV_BWD_PATH_TF32) || p->classes.empty())) {
         FillParams fp{};
         fp.dx = dx; fp.esize = (int)es; fp.layout = d.layout;
         fp.N = g.N; fp.C = g.C; fp.Hi = g.Hi; fp.Wi = g.Wi; fp.sh = g.sh; fp.sw = g.sw;
@@ -764,6 +863,50 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
         p->fill_ran = true;
     }
     if (p->classes.empty()) return CONV_BWD_OK;
+
+    if (p->path == CONV_BWD_PATH_TF32) {
+        if (p->tmap_w_ptr != p->w_hi) {
+            if (!encode_tf32_w_maps(p)) return CONV_BWD_ERR_CUDA;
+            p->tmap_w_ptr = p->w_hi;
+        }
+        if (p->tmap_a_ptr != dy) {
+            if (!encode_a_maps(p, dy)) return CONV_BWD_ERR_CUDA;
+            p->tmap_a_ptr = dy;
+        }
+        if (launch_tf32_split_w(static_cast<const float *>(w), p->w_hi, p->w_lo, g, p->w_gkcyx, p->num_sms, s) !=
+            cudaSuccess)
+            return CONV_BWD_ERR_CUDA;
+        if (p->timing) cudaEventRecord(p->ev[2], s);  // the sub-GEMM kernel's time excludes the filter split
+        for (size_t c0 = 0; c0 < p->sched.size(); c0 += kMaxTcClasses) {
+            TcParams tp;
+            std::memset(&tp, 0, sizeof(tp));
+            tp.tmap_w = p->tmap_w;            // w_hi
+            tp.tmap_w_half = p->tmap_w_half;  // w_lo
+            tp.dy = dy; tp.dx = dx; tp.status = p->d_status; tp.wait_budget = p->wait_budget;
+            tp.g = g;
+            tp.n_tiles = (g.Cg + kTf32BN - 1) / kTf32BN;
+            tp.kb_per_tap = (g.Kg + kTf32BK - 1) / kTf32BK;
+            tp.im2col = 1;
+            tp.fill = (c0 == 0 && p->any_uncovered) ? 1 : 0;
+            tp.cov_h = p->cov_h;
+            tp.cov_w = p->cov_w == all_w ? ~0ull : p->cov_w;
+            const size_t nc = std::min<size_t>(kMaxTcClasses, p->sched.size() - c0);
+            tp.num_classes = (int)nc;
+            int64_t total = 0;
+            for (size_t i = 0; i < nc; ++i) {
+                const int idx = p->sched[c0 + i];
+                tp.cls[i] = p->classes[(size_t)idx];
+                tp.cls[i].tile_begin = (int)total;
+                total += (int64_t)g.G * tp.cls[i].m_tiles * tp.n_tiles;
+                tp.tmap_a[i] = p->tmap_a[(size_t)idx];
+            }
+            tp.total_tiles = (int)total;
+            const int grid = (int)std::min<int64_t>(total, p->num_sms);
+            if (launch_tf32(tp, grid, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        }
+        if (p->timing) cudaEventRecord(p->ev[3], s);
+        return CONV_BWD_OK;
+    }
 
     if (p->path == CONV_BWD_PATH_TCGEN05) {
         if (p->tmap_w_ptr != w) {

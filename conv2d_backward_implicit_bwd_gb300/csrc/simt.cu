@@ -6,6 +6,7 @@
 
 #include "device_util.cuh"
 #include "internal.h"
+#include "tf32.h"
 
 namespace cbd {
 
@@ -389,28 +390,30 @@ cudaError_t launch_selftest_wait(int32_t *status, int64_t budget, cudaStream_t s
 }
 
 // ---------------------------------------------------------------------------
-// Layout transposes for bf16 NCHW/GKCYX problems on the tensor-core path:
-// out[b][c][r] = in[b][r][c] (r < R, c < Cc), 64x64 tiles through shared
-// memory so that both the reads and the writes run along contiguous rows.
+// Layout transposes for NCHW/GKCYX problems on the tensor-core paths (2-byte
+// elements for bf16, 4-byte for fp32): out[b][c][r] = in[b][r][c] (r < R,
+// c < Cc), 64x64 tiles through shared memory so that both the reads and the
+// writes run along contiguous rows.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) transpose_b16_kernel(const uint16_t *__restrict__ in, uint16_t *__restrict__ out,
-                                                            int64_t batch, int64_t R, int64_t Cc) {
-    __shared__ uint16_t t[64][66];
+template <typename T>
+__global__ void __launch_bounds__(256) transpose_kernel(const T *__restrict__ in, T *__restrict__ out, int64_t batch,
+                                                        int64_t R, int64_t Cc) {
+    __shared__ T t[64][64 + 4 / sizeof(T)];  // one extra 4-byte word per row: conflict-free columns
     const int64_t tr_n = (R + 63) / 64, tc_n = (Cc + 63) / 64;
     const int64_t tiles = batch * tr_n * tc_n;
     const int x = threadIdx.x & 31, y = threadIdx.x >> 5;  // 32 x 8 threads
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int64_t tc = tile % tc_n, rest = tile / tc_n;
         const int64_t tr = rest % tr_n, b = rest / tr_n;
-        const uint16_t *src = in + b * R * Cc;
-        uint16_t *dst = out + b * R * Cc;
+        const T *src = in + b * R * Cc;
+        T *dst = out + b * R * Cc;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int64_t r = tr * 64 + y + 8 * k;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int64_t c = tc * 64 + x + 32 * h;
-                t[y + 8 * k][x + 32 * h] = (r < R && c < Cc) ? src[r * Cc + c] : (uint16_t)0;
+                t[y + 8 * k][x + 32 * h] = (r < R && c < Cc) ? src[r * Cc + c] : (T)0;
             }
         }
         __syncthreads();
@@ -427,14 +430,74 @@ __global__ void __launch_bounds__(256) transpose_b16_kernel(const uint16_t *__re
     }
 }
 
-cudaError_t launch_transpose_b16(const void *in, void *out, int64_t batch, int64_t R, int64_t Cc, int num_sms,
-                                 cudaStream_t s) {
+// Narrow inner dimension (Cc < 32, e.g. the Y*X taps of a filter): a block
+// takes a slab of up to 64 rows of one batch item, which is contiguous in the
+// input (at most 64*31 elements), stages it in shared memory with all of a
+// thread's loads in flight at once, and writes its Cc output rows of up to 64
+// contiguous elements each.
+constexpr int kNarrowRows = 64;
+template <typename T>
+__global__ void __launch_bounds__(256) transpose_narrow_kernel(const T *__restrict__ in, T *__restrict__ out,
+                                                               int64_t batch, int64_t R, int64_t Cc) {
+    constexpr int PER = kNarrowRows * 32 / 256;  // elements per thread, upper bound
+    __shared__ T slab[kNarrowRows * 32];
+    const int64_t slabs_r = (R + kNarrowRows - 1) / kNarrowRows;
+    const int cc = (int)Cc;
+    for (int64_t sl = blockIdx.x; sl < batch * slabs_r; sl += gridDim.x) {
+        const int64_t b = sl / slabs_r;
+        const int64_t r0 = (sl - b * slabs_r) * kNarrowRows;
+        const int nr = (int)(R - r0 < kNarrowRows ? R - r0 : kNarrowRows);
+        const int n = nr * cc;
+        const T *src = in + (b * R + r0) * Cc;
+        T v[PER];
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const int e = threadIdx.x + 256 * q;
+            if (256 * q < n) v[q] = e < n ? src[e] : (T)0;  // (block-uniform skip of empty passes)
+        }
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const int e = threadIdx.x + 256 * q;
+            if (256 * q < n && e < n) slab[e] = v[q];
+        }
+        __syncthreads();
+        T *dst = out + b * Cc * R + r0;
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            if (256 * q >= kNarrowRows * cc) break;
+            const int e = threadIdx.x + 256 * q;  // output row c = e / 64, element r = e % 64
+            const int c = e / kNarrowRows, r = e % kNarrowRows;
+            if (c < cc && r < nr) dst[(int64_t)c * R + r] = slab[r * cc + c];
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T>
+static cudaError_t launch_transpose(const void *in, void *out, int64_t batch, int64_t R, int64_t Cc, int num_sms,
+                                   cudaStream_t s) {
     const int64_t tiles = batch * ((R + 63) / 64) * ((Cc + 63) / 64);
     if (tiles <= 0) return cudaSuccess;
     const int64_t cap = (int64_t)(num_sms > 0 ? num_sms : 148) * 8;
-    transpose_b16_kernel<<<(unsigned)(tiles < cap ? tiles : cap), 256, 0, s>>>(
-        static_cast<const uint16_t *>(in), static_cast<uint16_t *>(out), batch, R, Cc);
+    if (Cc < 32) {
+        const int64_t blocks = batch * ((R + kNarrowRows - 1) / kNarrowRows);
+        transpose_narrow_kernel<T><<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(
+            static_cast<const T *>(in), static_cast<T *>(out), batch, R, Cc);
+        return cudaGetLastError();
+    }
+    transpose_kernel<T><<<(unsigned)(tiles < cap ? tiles : cap), 256, 0, s>>>(static_cast<const T *>(in),
+                                                                              static_cast<T *>(out), batch, R, Cc);
     return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_b16(const void *in, void *out, int64_t batch, int64_t R, int64_t Cc, int num_sms,
+                                 cudaStream_t s) {
+    return launch_transpose<uint16_t>(in, out, batch, R, Cc, num_sms, s);
+}
+
+cudaError_t launch_transpose_b32(const void *in, void *out, int64_t batch, int64_t R, int64_t Cc, int num_sms,
+                                 cudaStream_t s) {
+    return launch_transpose<uint32_t>(in, out, batch, R, Cc, num_sms, s);
 }
 
 }  // namespace cbd

@@ -85,6 +85,17 @@ CASES = [
     Case(name="bf16_32x57x57x128_5x5_s3_p2", N=32, C=128, K=128, Hi=57, Wi=57, Y=5, X=5,
          pad=(2, 2), stride=(3, 3), dtype=BF16, layout=NHWC, dist="normal", sigma=0.05, seed=5002,
          tags=("ridge",)),
+    # fp32 problems large enough for the fp32 tensor-core path: the dilated
+    # stress shape in fp32 (NHWC, and NCHW as the fp32 sweep is laid out), and
+    # the 3x3 stride-1 sweep shape with 256 channels
+    Case(name="fp32_nhwc_32x28x28x512_3x3_s2_p1_d2", N=32, C=512, K=512, Hi=28, Wi=28, Y=3, X=3,
+         pad=(1, 1), stride=(2, 2), dil=(2, 2), dtype=F32, layout=NHWC, dist="uniform", seed=6000,
+         tags=("fp32_large",)),
+    Case(name="fp32_nchw_32x28x28x512_3x3_s2_p1_d2", N=32, C=512, K=512, Hi=28, Wi=28, Y=3, X=3,
+         pad=(1, 1), stride=(2, 2), dil=(2, 2), dtype=F32, layout=NCHW, dist="uniform", seed=6001,
+         tags=("fp32_large",)),
+    Case(name="fp32_nchw_32x256x14x14_3x3_p1_s1", N=32, C=256, K=256, Hi=14, Wi=14, Y=3, X=3,
+         pad=(1, 1), dtype=F32, layout=NCHW, dist="uniform", seed=6002, tags=("fp32_large",)),
 ]
 
 BY_NAME = {c.name: c for c in CASES}

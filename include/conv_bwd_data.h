@@ -30,8 +30,9 @@
  * allocator; PyTorch in the bundled binding).  The library owns the plan
  * (host memory), one 16-byte device status word per plan and, for bf16
  * problems that run on SM pairs, a stream-K scratch of 256 KB per pair (fp32
- * partial tiles and flags, ~19 MB on 152 SMs), all allocated by
- * conv_bwd_data_create when a CUDA device is present.  conv_bwd_data_run
+ * partial tiles and flags, ~19 MB on 152 SMs); fp32 plans on the tensor-core
+ * path also own two fp32 copies of the filter (its hi and lo parts), all
+ * allocated by conv_bwd_data_create when a CUDA device is present.  conv_bwd_data_run
  * allocates nothing, never synchronises and is ordered on the given stream.
  *
  * Layouts (all tensors dense, row-major in the order written):
@@ -42,7 +43,12 @@
  * [gi*K/G, (gi+1)*K/G).  Ho = (Hi + 2*ph - dh*(Y-1) - 1)/sh + 1, likewise Wo.
  * Padding is symmetric per dimension.
  *
- * Numerics.  fp32 tensors: fp32 FFMA on CUDA cores (no TF32).  bf16 tensors:
+ * Numerics.  fp32 tensors: fp32 FFMA on CUDA cores; large problems (path
+ * CONV_BWD_PATH_TF32) run on the tensor cores with each operand split as
+ * x = hi + lo (hi = x rounded to a 10-bit mantissa, lo = x - hi exactly) and
+ * three TF32 products hi*hi + hi*lo + lo*hi accumulated in fp32 per term,
+ * which keeps each product within about 2^-20 of the exact one (plain TF32
+ * would be 2^-10 and miss the fp32 tolerance).  bf16 tensors:
  * bf16 x bf16 products accumulated in fp32 (tensor cores for the NHWC path),
  * one round-to-nearest-even conversion to bf16 at the end (the `arith.extf`,
  * `arith.mulf`/`arith.addf` in f32 and `arith.truncf` ops of the BOO IR on
@@ -92,17 +98,21 @@ typedef struct conv_bwd_plan_s *conv_bwd_plan;
 typedef enum {
     CONV_BWD_PATH_TCGEN05 = 0, /* bf16: persistent tcgen05/TMEM implicit GEMM */
     CONV_BWD_PATH_SIMT = 1,    /* fp32 (or bf16 fallback): CUDA-core tiled implicit GEMM */
-    CONV_BWD_PATH_GROUPED = 2  /* bf16, C/G = K/G in {8, 16}, G % 8 == 0: memory-bound warp-MMA kernel */
+    CONV_BWD_PATH_GROUPED = 2, /* bf16, C/G = K/G in {8, 16}, G % 8 == 0: memory-bound warp-MMA kernel */
+    CONV_BWD_PATH_TF32 = 3     /* fp32 NHWC/KYXC with >= 1e9 useful FLOP, K, C, C/G, K/G multiples of 4
+                                  (K/G of 32 when G > 1): tcgen05 kind::tf32 with a three-term split */
 } conv_bwd_path;
-/* The tensor-core and narrow-group kernels read NHWC/KYXC.  A bf16 NCHW/GKCYX
- * plan whose NHWC/KYXC twin takes one of them gets plan-owned scratch (dy, w
- * and dx in NHWC/KYXC, allocated by create) and each run transposes dy and w
- * into it, runs the twin's kernels and transposes dx back (path() reports the
- * twin's path with 3 more launches). */
+/* The tensor-core and narrow-group kernels read NHWC/KYXC.  An NCHW/GKCYX
+ * plan whose NHWC/KYXC twin takes one of them gets plan-owned scratch (dy and
+ * dx in NHWC, plus w in KYXC for bf16, allocated by create) and each run
+ * transposes dy (and the bf16 w) into it, runs the twin's kernels and
+ * transposes dx back (path() reports the twin's path with 3 more launches for
+ * bf16, 2 for fp32, whose filter split reads GKCYX directly). */
 
 /* Planner overrides, read at create (for tests and measurements; unset in
  * normal use):
  *   CONVBWD_DEBUG_PATH=simt          CUDA-core path for every plan
+ *   CONVBWD_DEBUG_PATH=tf32          fp32 tensor-core path whatever the problem size
  *   CONVBWD_DEBUG_NOIM2COL=1         cp.async A producer instead of TMA im2col
  *   CONVBWD_DEBUG_2SM=1 / _NO2SM=1   SM-pair kernel for C/G >= 128 / never
  *   CONVBWD_DEBUG_BN=128|256|512     tile width; CONVBWD_DEBUG_CL=1|2 pairs per cluster
@@ -112,7 +122,7 @@ typedef enum {
  *   CONVBWD_DEBUG_L2PROMO=0|1       TMA L2 promotion none / 128 B (default 256 B)
  *   CONVBWD_DEBUG_WAIT_SECONDS=s     budget of every bounded device wait (default 2)
  *   CONVBWD_DEBUG_HOST_CHUNKS=n      batch chunks of the pipelined run_host (default 4)
- *   CONVBWD_DEBUG_NO_TRANSPOSE=1     bf16 NCHW plans stay on the CUDA-core path */
+ *   CONVBWD_DEBUG_NO_TRANSPOSE=1     NCHW plans stay on the CUDA-core path */
 
 /* Validate the descriptor and plan on the host: forward output size, tilde
  * factors, non-empty sub-GEMM list (consecutive gemmIds), coverage of dx,
@@ -193,8 +203,9 @@ conv_bwd_status conv_bwd_data_work(const conv_bwd_plan plan, double *useful_flop
  * status word and, for wide bf16 problems, its work-splitting scratch
  * (allocated by conv_bwd_data_create) are shared by its runs.
  * Errors: INVALID_ARG (null or overlapping pointers), MISALIGNED (bf16 NHWC
- * tensor-core path needs 16-byte aligned dy, w, dx), CUDA (launch failure or
- * plan created without a device). */
+ * tensor-core path needs 16-byte aligned dy, w, dx; the fp32 tensor-core path
+ * 16-byte aligned dy and dx), CUDA (launch failure or plan created without a
+ * device). */
 conv_bwd_status conv_bwd_data_run(conv_bwd_plan plan, const void *dy, const void *w, void *dx, void *stream);
 
 /* End-to-end variant with host buffers: copies dy_host/w_host into the

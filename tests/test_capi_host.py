@@ -151,6 +151,23 @@ def test_paths(B):
     assert B.Plan(1, 4, 4, 9, 9, 1, 1, stride=(2, 2)).path() == ("simt", 2)
 
 
+def test_fp32_tensor_core_path_selection(B, monkeypatch):
+    """fp32 NHWC problems above 1e9 useful FLOP take the three-term TF32
+    tensor-core path (filter split + one kernel, which zeroes uncovered pixels
+    itself); smaller ones, shapes outside its alignment and group rules, and
+    NCHW plans without a device stay on the CUDA cores."""
+    big = B.Plan.from_case(wl.case("fp32_nhwc_32x28x28x512"))
+    assert big.path() == ("tf32", 2) and big.tile() == (128, 128, 1)
+    assert B.Plan(2, 64, 64, 14, 14, 3, 3, pad=(1, 1), layout="nhwc").path()[0] == "simt"       # 0.03 GFLOP
+    assert B.Plan(8, 254, 256, 28, 28, 3, 3, pad=(1, 1), layout="nhwc").path()[0] == "simt"     # C % 4 != 0
+    assert B.Plan(8, 256, 256, 28, 28, 3, 3, pad=(1, 1), groups=16, layout="nhwc").path()[0] == "simt"  # K/G = 16
+    assert B.Plan(16, 256, 256, 28, 28, 3, 3, pad=(1, 1), groups=8, layout="nhwc").path()[0] == "tf32"  # K/G = 32
+    monkeypatch.setenv("CONVBWD_DEBUG_PATH", "tf32")
+    assert B.Plan(2, 64, 64, 14, 14, 3, 3, pad=(1, 1), layout="nhwc").path() == ("tf32", 2)
+    monkeypatch.setenv("CONVBWD_DEBUG_PATH", "simt")
+    assert B.Plan.from_case(wl.case("fp32_nhwc_32x28x28x512")).path()[0] == "simt"
+
+
 @pytest.mark.parametrize("kw,status", [
     (dict(N=0), 1), (dict(C=3, groups=2), 1), (dict(Y=40), 1), (dict(stride=(0, 1)), 1),
     (dict(pad=(-1, 0)), 1), (dict(dil=(1, 0)), 1), (dict(stride=(65, 1)), 2), (dict(layout=7), 1),
