@@ -83,6 +83,7 @@ struct conv_bwd_plan_s {
     float *w_hi = nullptr, *w_lo = nullptr;
     bool owns_wsplit = false;
     int32_t w_gkcyx = 0;  // 1: run() receives the filter as GKCYX (the NCHW parent's w)
+    int32_t tf32_split = -1;  // tail split of the fp32 tensor-core schedule: -1 by cost, 0 never, 1 always
     std::mutex mu;
 };
 
@@ -558,8 +559,10 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
     }
     if (const char *f = env("CONVBWD_DEBUG_CL"))
         if (p->two_sm) p->cl = f[0] == '2' ? 2 : 1;
-    if (const char *f = env("CONVBWD_DEBUG_STREAMK"))
+    if (const char *f = env("CONVBWD_DEBUG_STREAMK")) {
         if (f[0] == '1') p->cl = 1;  // stream-K runs with one pair per cluster
+        p->tf32_split = f[0] == '1' ? 1 : 0;
+    }
 
     // Schedule: classes with the longest reduction first (LPT), tiles of one
     // class contiguous; BM = 256 rows on SM pairs, 128 for the 1-SM
@@ -901,7 +904,27 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
                 tp.tmap_a[i] = p->tmap_a[(size_t)idx];
             }
             tp.total_tiles = (int)total;
-            const int grid = (int)std::min<int64_t>(total, p->num_sms);
+            // Tiles that do not fill a last round of the SMs are cut into equal
+            // k-block ranges over every SM (added into dx after a zeroing launch)
+            // when that round would leave at least a fifth of the SMs idle and
+            // each range keeps a few k blocks.
+            const int nsm = std::max(1, p->num_sms);
+            int grid = (int)std::min<int64_t>(total, nsm);
+            const int64_t t_dp = (total / nsm) * nsm, tail = total - t_dp;
+            int64_t tail_units = 0;
+            for (size_t i = 0; i < nc; ++i) {
+                const ClassDesc &c = tp.cls[i];
+                const int64_t te = i + 1 < nc ? tp.cls[i + 1].tile_begin : total;
+                const int64_t lo = std::max<int64_t>(c.tile_begin, t_dp);
+                if (te > lo) tail_units += (te - lo) * c.taps_y * c.taps_x * tp.kb_per_tap;
+            }
+            bool split = tail > 0 && tail * 5 <= (int64_t)nsm * 4 && tail_units >= 4LL * nsm;
+            if (p->tf32_split >= 0) split = tail > 0 && p->tf32_split == 1;
+            if (split) {
+                tp.streamk = 1;
+                tp.units_total = (int)std::min<int64_t>(tail_units, 0x7fffffff);
+                grid = nsm;
+            }
             if (launch_tf32(tp, grid, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
         }
         if (p->timing) cudaEventRecord(p->ev[3], s);

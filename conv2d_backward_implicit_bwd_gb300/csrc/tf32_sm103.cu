@@ -132,7 +132,7 @@ __device__ __forceinline__ void fill_uncovered_f32(const TcParams &p, int tid, i
 // swizzled by row), then 8 lanes per row store 4 rows per instruction.
 __device__ __forceinline__ void store_chunk_f32(const uint32_t (&v)[32], uint32_t sbase, int lane,
                                                 const int64_t (&roff)[8], const bool (&rok)[8], int col, int Cg,
-                                                float *dx) {
+                                                float *dx, bool atomic) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         const uint32_t a = sbase + (uint32_t)lane * 128u + ((uint32_t)(q ^ (lane & 7)) << 4);
@@ -151,7 +151,13 @@ __device__ __forceinline__ void store_chunk_f32(const uint32_t (&v)[32], uint32_
                      : "=f"(val.x), "=f"(val.y), "=f"(val.z), "=f"(val.w)
                      : "r"(a)
                      : "memory");
-        if (rok[it] && col + ch * 4 < Cg) *reinterpret_cast<float4 *>(dx + roff[it] + ch * 4) = val;
+        if (rok[it] && col + ch * 4 < Cg) {
+            float4 *dst = reinterpret_cast<float4 *>(dx + roff[it] + ch * 4);
+            if (atomic)
+                atomicAdd(dst, val);
+            else
+                *dst = val;
+        }
     }
     __syncwarp();
 }
@@ -162,7 +168,7 @@ __device__ __forceinline__ void store_chunk_f32(const uint32_t (&v)[32], uint32_
 // are not written.  The next 32 columns load while the current ones store.
 template <int BN>
 __device__ __forceinline__ void epilogue_rows_f32(uint32_t taddr, uint8_t *stage, int lane, bool rvalid, int64_t off,
-                                                  int col0, int Cg, float *dx) {
+                                                  int col0, int Cg, float *dx, bool atomic) {
     constexpr int NC = BN / 32;
     static_assert(NC % 2 == 0, "chunks are drained in pairs");
     const uint32_t sbase = smem_u32(stage);
@@ -182,11 +188,91 @@ __device__ __forceinline__ void epilogue_rows_f32(uint32_t taddr, uint8_t *stage
 #pragma unroll 1
     for (int cc = 0; cc < NC; cc += 2) {
         tmem_ld32_issue(taddr + (cc + 1) * 32, vb);
-        store_chunk_f32(va, sbase, lane, roff, rok, col0 + cc * 32, Cg, dx + cc * 32);
+        store_chunk_f32(va, sbase, lane, roff, rok, col0 + cc * 32, Cg, dx + cc * 32, atomic);
         tmem_wait_ld(vb);
         if (cc + 2 < NC) tmem_ld32_issue(taddr + (cc + 2) * 32, va);
-        store_chunk_f32(vb, sbase, lane, roff, rok, col0 + (cc + 1) * 32, Cg, dx + (cc + 1) * 32);
+        store_chunk_f32(vb, sbase, lane, roff, rok, col0 + (cc + 1) * 32, Cg, dx + (cc + 1) * 32, atomic);
         if (cc + 2 < NC) tmem_wait_ld(va);
+    }
+}
+
+// Work of CTA w of nw.  Whole tiles w, w + nw, ... below t_dp (every full
+// round of tiles); with p.streamk the remaining tiles (fewer than nw) are cut
+// into equal ranges of their k blocks, one range per CTA, so that the last
+// round occupies every SM.  A range that does not cover its whole tile ends in
+// an atomic epilogue (fp32 adds into dx, which the launch before zeroed);
+// every tail segment is added atomically, whole or not.
+struct Tf32Seg {
+    int t, kb0, kb1;
+    bool atomic;
+};
+struct Tf32Iter {
+    int nw, T, t_dp, next_t;
+    int64_t u, u_end;
+    __device__ __forceinline__ Tf32Iter(const TcParams &p, int w, int nw_) : nw(nw_), T(p.total_tiles), next_t(w) {
+        t_dp = p.streamk ? (T / nw) * nw : T;
+        u = (int64_t)w * p.units_total / nw;
+        u_end = (int64_t)(w + 1) * p.units_total / nw;
+    }
+    __device__ __forceinline__ static int nkb(const TcParams &p, int ci) {
+        return p.cls[ci].taps_y * p.cls[ci].taps_x * p.kb_per_tap;
+    }
+    __device__ __forceinline__ bool next(const TcParams &p, Tf32Seg &sg) {
+        if (next_t < t_dp) {
+            sg.t = next_t;
+            sg.kb0 = 0;
+            sg.kb1 = nkb(p, class_of_tile(p, next_t));
+            sg.atomic = false;
+            next_t += nw;
+            return true;
+        }
+        if (!p.streamk || u >= u_end) return false;
+        // tail tiles class by class (each class's tiles are contiguous) to the
+        // one that holds unit u
+        int64_t base = 0;
+        for (int ci = 0; ci < p.num_classes; ++ci) {
+            const int tb = p.cls[ci].tile_begin;
+            const int te = ci + 1 < p.num_classes ? p.cls[ci + 1].tile_begin : T;
+            const int lo = tb > t_dp ? tb : t_dp;
+            if (lo >= te) continue;
+            const int n = nkb(p, ci);
+            const int64_t cu = (int64_t)(te - lo) * n;
+            if (u < base + cu) {
+                const int tl = (int)((u - base) / n);
+                const int64_t ts = base + (int64_t)tl * n;  // unit of this tile's k block 0
+                sg.t = lo + tl;
+                sg.kb0 = (int)(u - ts);
+                sg.kb1 = (int)(u_end - ts < n ? u_end - ts : n);
+                sg.atomic = true;
+                u = ts + sg.kb1;
+                return true;
+            }
+            base += cu;
+        }
+        return false;
+    }
+};
+
+// Zero the dx region of every tail tile (t >= t_dp) before the kernel adds
+// its k-block ranges into it: one block per tile, 128 rows x 128 channels.
+__global__ void __launch_bounds__(256) tf32_zero_tiles_kernel(const __grid_constant__ TcParams p, int t_dp) {
+    const Geom &g = p.g;
+    float *dx = static_cast<float *>(p.dx);
+    for (int t = t_dp + blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        const TileCoord tcd = decode_tile(p, t);
+        const ClassDesc &c = p.cls[tcd.ci];
+        const int HTWT = c.HT * c.WT;
+        for (int e = threadIdx.x; e < 128 * (kTf32BN / 4); e += blockDim.x) {
+            const int r = e / (kTf32BN / 4), q = e % (kTf32BN / 4);
+            const int m = tcd.mb * 128 + r;
+            const int col = tcd.nb * kTf32BN + 4 * q;
+            if (m >= c.M || col >= g.Cg) continue;
+            const int n = m / HTWT, rem = m - n * HTWT;
+            const int hi = (c.ht_lo + rem / c.WT) * g.sh + c.ty * g.dh - g.ph;
+            const int wi = (c.wt_lo + rem % c.WT) * g.sw + c.tx * g.dw - g.pw;
+            const int64_t off = (((int64_t)n * g.Hi + hi) * g.Wi + wi) * g.C + (int64_t)tcd.gi * g.Cg + col;
+            *reinterpret_cast<float4 *>(dx + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
 }
 
@@ -242,10 +328,11 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true, issued = false;
-            for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-                const TileCoord tcd = decode_tile(p, t);
+            Tf32Iter segs(p, blockIdx.x, gridDim.x);
+            Tf32Seg sg;
+            while (ok && segs.next(p, sg)) {
+                const TileCoord tcd = decode_tile(p, sg.t);
                 const ClassDesc &c = p.cls[tcd.ci];
-                const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
                 // first row of the tile -> base pixel of tap (taps_y-1, taps_x-1)
                 const int HTWT = c.HT * c.WT;
                 const int m0 = tcd.mb * 128;
@@ -253,7 +340,7 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
                 const int bh = c.ht_lo + rem / c.WT - (c.taps_y - 1) * g.DH;
                 const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
                 const CUtensorMap *amap = &p.tmap_a[tcd.ci];
-                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const int tap = kb / p.kb_per_tap;
                     const int k0 = (kb - tap * p.kb_per_tap) * kTf32BK;
                     const int j = tap / c.taps_x, i = tap - j * c.taps_x;
@@ -290,11 +377,10 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
         const int st = threadIdx.x - 32 * Cfg::SPLIT_WARP;  // 0..127
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-            const TileCoord tcd = decode_tile(p, t);
-            const ClassDesc &c = p.cls[tcd.ci];
-            const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
-            for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        Tf32Iter segs(p, blockIdx.x, gridDim.x);
+        Tf32Seg sg;
+        while (ok && segs.next(p, sg)) {
+            for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                 const uint32_t s = it % S, ph = (it / S) & 1;
                 if (!mbar_wait_bounded(full0 + 8 * s, ph, p.wait_budget, abort_flag, p.status, kDevTimeoutConvert)) {
                     ok = false;
@@ -331,10 +417,9 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
                                B_LO = (2 * Cfg::A_BYTES + Cfg::B_BYTES) >> 4;
             uint32_t it = 0, tc = 0;
             bool ok = true, issued = false;
-            for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++tc) {
-                const TileCoord tcd = decode_tile(p, t);
-                const ClassDesc &c = p.cls[tcd.ci];
-                const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
+            Tf32Iter segs(p, blockIdx.x, gridDim.x);
+            Tf32Seg sg;
+            for (; ok && segs.next(p, sg); ++tc) {
                 const uint32_t b = tc & 1, tph = (tc >> 1) & 1;
                 if (!mbar_wait_bounded(tempty0 + 8 * b, tph ^ 1, p.wait_budget, abort_flag, p.status,
                                        kDevTimeoutMma)) {
@@ -343,7 +428,7 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + b * BN;
-                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const uint32_t s = it % S, ph = (it / S) & 1;
                     // the split barrier follows the TMA barrier (the splitting
                     // threads waited on it), so both operands have landed
@@ -358,7 +443,7 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
                         // 8-deep k step = 32 bytes along the 128-byte rows of both operands
                         const uint64_t a_hi = d0 + 2 * kk, a_lo = d0 + A_LO + 2 * kk;
                         const uint64_t b_hi = d0 + B_HI + 2 * kk, b_lo = d0 + B_LO + 2 * kk;
-                        tc_mma_tf32(d_tmem, a_hi, b_hi, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_tf32(d_tmem, a_hi, b_hi, idesc, (kb != sg.kb0 || kk != 0) ? 1u : 0u);
                         tc_mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
                         tc_mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
                     }
@@ -379,8 +464,10 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
         float *dx = static_cast<float *>(p.dx);
         uint32_t tc = 0;
         if (p.fill) fill_uncovered_f32(p, threadIdx.x, 128);
-        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++tc) {
-            const TileCoord tcd = decode_tile(p, t);
+        Tf32Iter segs(p, blockIdx.x, gridDim.x);
+        Tf32Seg sg;
+        for (; segs.next(p, sg); ++tc) {
+            const TileCoord tcd = decode_tile(p, sg.t);
             const ClassDesc &c = p.cls[tcd.ci];
             const uint32_t b = tc & 1, tph = (tc >> 1) & 1;
             bool ok = mbar_wait_bounded(tfull0 + 8 * b, tph, p.wait_budget, abort_flag, p.status, kDevTimeoutEpilogue);
@@ -398,7 +485,7 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
                 off = (((int64_t)n * g.Hi + hi) * g.Wi + wi) * g.C + (int64_t)tcd.gi * g.Cg + (int64_t)tcd.nb * BN;
             }
             const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + b * BN;
-            epilogue_rows_f32<BN>(tbase, stage + warp * 4096, lane, rvalid, off, tcd.nb * BN, g.Cg, dx);
+            epilogue_rows_f32<BN>(tbase, stage + warp * 4096, lane, rvalid, off, tcd.nb * BN, g.Cg, dx, sg.atomic);
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * b);
         }
@@ -413,6 +500,15 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
 
 cudaError_t launch_tf32(const TcParams &p, int grid, cudaStream_t s) {
     if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
+    if (p.streamk) {
+        const int t_dp = (p.total_tiles / grid) * grid;
+        const int tail = p.total_tiles - t_dp;
+        if (tail > 0) {
+            tf32_zero_tiles_kernel<<<tail, 256, 0, s>>>(p, t_dp);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+    }
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);

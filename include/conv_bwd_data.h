@@ -116,7 +116,8 @@ typedef enum {
  *   CONVBWD_DEBUG_NOIM2COL=1         cp.async A producer instead of TMA im2col
  *   CONVBWD_DEBUG_2SM=1 / _NO2SM=1   SM-pair kernel for C/G >= 128 / never
  *   CONVBWD_DEBUG_BN=128|256|512     tile width; CONVBWD_DEBUG_CL=1|2 pairs per cluster
- *   CONVBWD_DEBUG_STREAMK=1          stream-K schedule on the SM-pair kernel
+ *   CONVBWD_DEBUG_STREAMK=1|0        stream-K schedule on the SM-pair kernel; on the fp32
+ *                                    tensor-core path, the tail split always / never
  *   CONVBWD_DEBUG_RASTER_M=1         tiles walk m-blocks first
  *   CONVBWD_DEBUG_GRID=n             cap the 1-SM kernel's grid
  *   CONVBWD_DEBUG_L2PROMO=0|1       TMA L2 promotion none / 128 B (default 256 B)

@@ -116,6 +116,20 @@ def test_forced_tf32_matches_oracle(B, monkeypatch, c):
     check_full(c, got, g, dy, w)
 
 
+@pytest.mark.parametrize("split", ["1", "0"])
+@pytest.mark.parametrize("idx", [0, 1, 3, 5])
+def test_tail_split_schedule(B, monkeypatch, idx, split):
+    """Tiles of the last round cut into k-block ranges over every SM (fp32
+    atomic adds into a zeroed dx region) against whole tiles only."""
+    c = FORCED[idx]
+    monkeypatch.setenv("CONVBWD_DEBUG_PATH", "tf32")
+    monkeypatch.setenv("CONVBWD_DEBUG_STREAMK", split)
+    g, dy, w = inputs(c)
+    got, plan = run_gpu(B, c, dy, w)
+    assert plan.path()[0] == "tf32"
+    check_full(c, got, g, dy, w)
+
+
 def test_tf32_matches_cuda_core_path(B, monkeypatch):
     """The same problem on the tensor cores and on the CUDA cores: both within
     the fp32 bound of the oracle and within twice that bound of each other."""
