@@ -523,37 +523,58 @@ cudaError_t launch_tf32(const TcParams &p, int grid, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------
-// Filter split: one output element per thread, in output order (k fastest),
-// so the writes are coalesced; the filter is small and its reads hit L2.
+// Filter split: per group and tap, the [Kg][Cg] plane of w (KYXC: c
+// contiguous; GKCYX: c at a stride of the tap count) becomes the [Cg][Kg]
+// plane of w_hi / w_lo (k contiguous, planes of one c row a tap apart), in
+// 32 x 32 tiles through shared memory so that reads run along c and writes
+// along k.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) tf32_split_w_kernel(const float *__restrict__ w, float *__restrict__ w_hi,
-                                                           float *__restrict__ w_lo, int64_t total, int Kg, int Cg,
-                                                           int taps, int64_t s_k, int64_t s_c, int64_t s_t) {
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
-        const int k = (int)(e % Kg);
-        int64_t rest = e / Kg;
-        const int t = (int)(rest % taps);
-        rest /= taps;
-        const int c = (int)(rest % Cg);
-        const int64_t gi = rest / Cg;
-        const float v = w[(gi * Kg + k) * s_k + (int64_t)c * s_c + (int64_t)t * s_t];
-        const float h = tf32_round(v);
-        w_hi[e] = h;
-        w_lo[e] = v - h;
+                                                           float *__restrict__ w_lo, int G, int Kg, int Cg, int taps,
+                                                           int gkcyx) {
+    __shared__ float tile[32][33];
+    const int kt = (Kg + 31) / 32, ct = (Cg + 31) / 32;
+    const int64_t tiles = (int64_t)G * taps * kt * ct;
+    const int x = threadIdx.x & 31, y = threadIdx.x >> 5;  // 32 x 8 threads
+    // source element strides of (k, c, tap) and destination strides of (c, tap)
+    const int64_t s_k = (int64_t)Cg * taps, s_c = gkcyx ? taps : 1, s_t = gkcyx ? 1 : Cg;
+    const int64_t d_c = (int64_t)taps * Kg, d_t = Kg;
+    for (int64_t tl = blockIdx.x; tl < tiles; tl += gridDim.x) {
+        int64_t r = tl;
+        const int cb = (int)(r % ct); r /= ct;
+        const int kb = (int)(r % kt); r /= kt;
+        const int t = (int)(r % taps);
+        const int64_t gi = r / taps;
+        const float *src = w + gi * Kg * s_k + (int64_t)t * s_t;
+        const int64_t dst0 = gi * Cg * d_c + (int64_t)t * d_t;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int k = kb * 32 + y + 8 * q, c = cb * 32 + x;
+            tile[y + 8 * q][x] = (k < Kg && c < Cg) ? src[k * s_k + c * s_c] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int c = cb * 32 + y + 8 * q, k = kb * 32 + x;
+            if (k < Kg && c < Cg) {
+                const float v = tile[x][y + 8 * q];
+                const float h = tf32_round(v);
+                const int64_t o = dst0 + c * d_c + k;
+                w_hi[o] = h;
+                w_lo[o] = v - h;
+            }
+        }
+        __syncthreads();
     }
 }
 
 cudaError_t launch_tf32_split_w(const float *w, float *w_hi, float *w_lo, const Geom &g, int gkcyx, int num_sms,
                                 cudaStream_t s) {
     const int taps = g.Y * g.X;
-    const int64_t total = (int64_t)g.G * g.Cg * taps * g.Kg;
-    if (total <= 0) return cudaSuccess;
-    // element strides of w[k][c][tap] (k over all groups)
-    const int64_t s_k = (int64_t)g.Cg * taps;
-    const int64_t s_c = gkcyx ? taps : 1;
-    const int64_t s_t = gkcyx ? 1 : g.Cg;
-    const int64_t blocks = std::min<int64_t>((total + 255) / 256, (int64_t)(num_sms > 0 ? num_sms : 148) * 8);
-    tf32_split_w_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, w_hi, w_lo, total, g.Kg, g.Cg, taps, s_k, s_c, s_t);
+    const int64_t tiles = (int64_t)g.G * taps * ((g.Kg + 31) / 32) * ((g.Cg + 31) / 32);
+    if (tiles <= 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>(tiles, (int64_t)(num_sms > 0 ? num_sms : 148) * 8);
+    tf32_split_w_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, w_hi, w_lo, g.G, g.Kg, g.Cg, taps, gkcyx);
     return cudaGetLastError();
 }
 
