@@ -18,8 +18,10 @@
 // the same whether the MMA truncates or rounds its fp32 inputs.
 //
 // Tile 128 (m) x 128 (c), k step 32 channels (one 128-byte swizzled row per
-// operand row), 3 pipeline slots of A, A_lo, B_hi, B_lo (64 KB each).  Roles
-// (one CTA per SM, persistent over the tiles):
+// operand row), 4 pipeline slots of A, B_hi, B_lo (48 KB each) in shared
+// memory; the split A of each slot lives in tensor memory (A operand of the
+// MMA), so shared memory carries only the TMA writes, one read of A and the
+// MMA's reads of B.  Roles (one CTA per SM, persistent over the tiles):
 //   warps 0-3   epilogue: tcgen05.ld of the fp32 accumulator (warp q reads
 //               TMEM lanes 32q..32q+31 = tile rows), staged through shared
 //               memory and written as 16-byte stores, 8 lanes per 128 bytes of
@@ -30,14 +32,15 @@
 //               im2col offset, rows outside dy read as zero) and the stage's
 //               byte count;
 //   warp 5      TMEM allocation and the single-thread tcgen05.mma issue
-//               (kind::tf32, M=128, N=128, K=8), committing each stage back to
-//               its slot and each finished tile to the epilogue (accumulator
-//               double-buffered in TMEM);
+//               (kind::tf32, M=128, N=128, K=8, A from TMEM, B from shared
+//               memory), committing each stage back to its slot and each
+//               finished tile to the epilogue (accumulator double-buffered in
+//               TMEM);
 //   warp 6      B producer: the hi and lo boxes of the pre-split filter
 //               (k contiguous, so B is K-major like A);
-//   warps 7-10  split A: rewrite each landed A element as hi in place and
-//               write lo to the A_lo slot (elementwise, so the swizzled layout
-//               carries over), fence to the async proxy and arrive.
+//   warps 7-10  split A: each thread reads one landed A row (its TMEM lane),
+//               writes hi and lo to the slot's 64 TMEM columns (tcgen05.st),
+//               waits for the stores and arrives.
 // Every barrier wait is bounded; on a timeout the kernel records the status
 // word, drains what it started and returns.
 #include <cuda.h>
@@ -56,11 +59,14 @@ constexpr int32_t kDevTimeoutConvert = 0x105;
 
 struct Tf32Cfg {
     static constexpr int BN = kTf32BN;
-    static constexpr int STAGES = 3;
+    static constexpr int STAGES = 4;
     static constexpr int A_BYTES = 128 * 128;  // 128 rows x 32 fp32
     static constexpr int B_BYTES = BN * 128;   // BN rows x 32 fp32
-    static constexpr int SLOT_BYTES = 2 * A_BYTES + 2 * B_BYTES;  // A (hi in place), A lo, B hi, B lo
-    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int SLOT_BYTES = A_BYTES + 2 * B_BYTES;  // A (fp32, as loaded), B hi, B lo
+    // TMEM: the double-buffered accumulator in columns [0, 2*BN), then per slot
+    // the split A (32 columns of hi, 32 of lo; lane = tile row)
+    static constexpr int A_COL = 2 * BN;
+    static constexpr int TMEM_COLS = 512;
     static constexpr int STAGE_OUT_BYTES = 4 * 32 * 128;  // epilogue staging: 4 warps x 32 rows x 128 B
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = 1024 + STAGES * SLOT_BYTES + STAGE_OUT_BYTES + BAR_BYTES;
@@ -69,6 +75,7 @@ struct Tf32Cfg {
     static constexpr int THREADS = 32 * (SPLIT_WARP + SPLIT_WARPS);
 };
 static_assert(Tf32Cfg::SMEM <= 227 * 1024, "shared memory of the fp32 tensor-core kernel");
+static_assert(Tf32Cfg::A_COL + Tf32Cfg::STAGES * 64 <= Tf32Cfg::TMEM_COLS, "tensor memory of the fp32 kernel");
 
 // Instruction descriptor, kind::tf32: fp32 accumulator, tf32 A and B, both
 // K-major, M = 128, N = BN.
@@ -81,13 +88,27 @@ __device__ __forceinline__ constexpr uint32_t idesc_tf32() {
            | ((uint32_t)(128 >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
+// A from tensor memory (lane = row, one 32-bit column per k), B from shared memory.
+__device__ __forceinline__ void tc_mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 columns of this warp's 32 TMEM lanes from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
 }
 
@@ -360,8 +381,8 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
                                         (uint16_t)((c.taps_x - 1 - i) * g.DW), (uint16_t)((c.taps_y - 1 - j) * g.DH));
                     } else {
                         const int y = c.ty + g.YT * j, x = c.tx + g.XT * i;
-                        tma_load_5d(a_dst + 2 * Cfg::A_BYTES, &p.tmap_w, full_s, k0, x, y, tcd.nb * BN, tcd.gi);
-                        tma_load_5d(a_dst + 2 * Cfg::A_BYTES + Cfg::B_BYTES, &p.tmap_w_half, full_s, k0, x, y,
+                        tma_load_5d(a_dst + Cfg::A_BYTES, &p.tmap_w, full_s, k0, x, y, tcd.nb * BN, tcd.gi);
+                        tma_load_5d(a_dst + Cfg::A_BYTES + Cfg::B_BYTES, &p.tmap_w_half, full_s, k0, x, y,
                                     tcd.nb * BN, tcd.gi);
                     }
                     issued = true;
@@ -374,7 +395,12 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
         __syncwarp();
     } else if (warp >= Cfg::SPLIT_WARP) {
         // ------------------------------------------------------------ A split (4 warps)
-        const int st = threadIdx.x - 32 * Cfg::SPLIT_WARP;  // 0..127
+        // a warp may address only its quarter of the TMEM lanes: warp q % 4
+        // takes tile rows 32*(q % 4) .. +31, one row (32 fp32 = 128 swizzled
+        // bytes) per thread, and writes hi and lo as 32 TMEM columns each
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16) + Cfg::A_COL;
         uint32_t it = 0;
         bool ok = true;
         Tf32Iter segs(p, blockIdx.x, gridDim.x);
@@ -386,25 +412,28 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
                     ok = false;
                     break;
                 }
-                const uint32_t a = slot_a(s);
+                const uint32_t a = slot_a(s) + (uint32_t)row * 128u;
+                uint32_t hi[32], lo[32];
 #pragma unroll
-                for (int q = 0; q < Cfg::A_BYTES / 16 / Cfg::SPLIT_THREADS; ++q) {
-                    const uint32_t off = (uint32_t)(st + Cfg::SPLIT_THREADS * q) * 16u;
+                for (int j = 0; j < 8; ++j) {
+                    // k = 4j .. 4j+3 sit in 16-byte chunk j, stored at chunk j ^ (row % 8)
                     float4 v;
                     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                                 : "r"(a + off)
+                                 : "r"(a + ((uint32_t)(j ^ (row & 7)) << 4))
                                  : "memory");
-                    const float4 h = make_float4(tf32_round(v.x), tf32_round(v.y), tf32_round(v.z), tf32_round(v.w));
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a + off), "f"(h.x), "f"(h.y),
-                                 "f"(h.z), "f"(h.w)
-                                 : "memory");
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a + Cfg::A_BYTES + off),
-                                 "f"(v.x - h.x), "f"(v.y - h.y), "f"(v.z - h.z), "f"(v.w - h.w)
-                                 : "memory");
+                    const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float h = tf32_round(e[q]);
+                        hi[4 * j + q] = __float_as_uint(h);
+                        lo[4 * j + q] = __float_as_uint(e[q] - h);
+                    }
                 }
-                // the MMA reads these through the async proxy
-                fence_proxy_async_smem();
+                tmem_st32(lane_base + s * 64, hi);
+                tmem_st32(lane_base + s * 64 + 32, lo);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
                 mbar_arrive(split0 + 8 * s);
             }
         }
@@ -413,8 +442,7 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_tf32<BN>();
             const uint64_t desc0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
-            constexpr uint64_t A_LO = Cfg::A_BYTES >> 4, B_HI = (2 * Cfg::A_BYTES) >> 4,
-                               B_LO = (2 * Cfg::A_BYTES + Cfg::B_BYTES) >> 4;
+            constexpr uint64_t B_HI = Cfg::A_BYTES >> 4, B_LO = (Cfg::A_BYTES + Cfg::B_BYTES) >> 4;
             uint32_t it = 0, tc = 0;
             bool ok = true, issued = false;
             Tf32Iter segs(p, blockIdx.x, gridDim.x);
@@ -431,21 +459,22 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const uint32_t s = it % S, ph = (it / S) & 1;
                     // the split barrier follows the TMA barrier (the splitting
-                    // threads waited on it), so both operands have landed
+                    // threads waited on it), so B has landed and A sits in TMEM
                     if (!mbar_wait_bounded(split0 + 8 * s, ph, p.wait_budget, abort_flag, p.status, kDevTimeoutMma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint64_t d0 = desc0 + (uint64_t)((s * Cfg::SLOT_BYTES) >> 4);
+                    const uint32_t a_t = tmem_base + Cfg::A_COL + s * 64;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        // 8-deep k step = 32 bytes along the 128-byte rows of both operands
-                        const uint64_t a_hi = d0 + 2 * kk, a_lo = d0 + A_LO + 2 * kk;
+                        // 8-deep k step: 8 TMEM columns of A, 32 bytes along B's 128-byte rows
+                        const uint32_t a_hi = a_t + 8 * kk, a_lo = a_t + 32 + 8 * kk;
                         const uint64_t b_hi = d0 + B_HI + 2 * kk, b_lo = d0 + B_LO + 2 * kk;
-                        tc_mma_tf32(d_tmem, a_hi, b_hi, idesc, (kb != sg.kb0 || kk != 0) ? 1u : 0u);
-                        tc_mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
-                        tc_mma_tf32(d_tmem, a_lo, b_hi, idesc, 1u);
+                        tc_mma_tf32_ts(d_tmem, a_hi, b_hi, idesc, (kb != sg.kb0 || kk != 0) ? 1u : 0u);
+                        tc_mma_tf32_ts(d_tmem, a_hi, b_lo, idesc, 1u);
+                        tc_mma_tf32_ts(d_tmem, a_lo, b_hi, idesc, 1u);
                     }
                     issued = true;
                     tc_commit(empty0 + 8 * s);
