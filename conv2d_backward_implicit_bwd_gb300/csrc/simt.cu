@@ -441,11 +441,13 @@ __global__ void __launch_bounds__(256) transpose_narrow_kernel(const T *__restri
                                                                int64_t batch, int64_t R, int64_t Cc) {
     constexpr int PER = kNarrowRows * 32 / 256;  // elements per thread, upper bound
     __shared__ T slab[kNarrowRows * 32];
-    const int64_t slabs_r = (R + kNarrowRows - 1) / kNarrowRows;
+    // a tensor holds fewer than 2^31 elements, so slab indices fit 32 bits
+    const int slabs_r = (int)((R + kNarrowRows - 1) / kNarrowRows);
+    const int slabs = (int)batch * slabs_r;
     const int cc = (int)Cc;
-    for (int64_t sl = blockIdx.x; sl < batch * slabs_r; sl += gridDim.x) {
+    for (int sl = blockIdx.x; sl < slabs; sl += gridDim.x) {
         const int64_t b = sl / slabs_r;
-        const int64_t r0 = (sl - b * slabs_r) * kNarrowRows;
+        const int64_t r0 = (int64_t)(sl - (int)b * slabs_r) * kNarrowRows;
         const int nr = (int)(R - r0 < kNarrowRows ? R - r0 : kNarrowRows);
         const int n = nr * cc;
         const T *src = in + (b * R + r0) * Cc;
