@@ -163,7 +163,9 @@ conv_bwd_status conv_bwd_data_subgemm_info(const conv_bwd_plan plan, int32_t id,
 conv_bwd_status conv_bwd_data_coverage(const conv_bwd_plan plan, uint8_t *row_mask, uint8_t *col_mask);
 
 /* Kernel path chosen by the planner (conv_bwd_path) and the number of
- * kernel launches one run() makes (fill + sub-GEMM kernel). */
+ * kernel launches one run() makes (fill + sub-GEMM kernel; the fp32
+ * tensor-core path counts its filter split and kernel, not the optional tile
+ * zeroing; NCHW plans add their transposes). */
 conv_bwd_status conv_bwd_data_path(const conv_bwd_plan plan, int32_t *path, int32_t *launches_per_run);
 
 /* Forward convolution with the plan's geometry, y = conv(x, w): the operator
@@ -200,9 +202,13 @@ conv_bwd_status conv_bwd_data_work(const conv_bwd_plan plan, double *useful_flop
  * default stream).  dy, w, dx are device pointers in the plan's layout and
  * dtype; they must not overlap.  Asynchronous: returns after enqueueing one
  * kernel (the CUDA-core path adds a fill kernel where some pixel is
- * uncovered).  Runs of one plan must not overlap on the GPU: the plan's
- * status word and, for wide bf16 problems, its work-splitting scratch
- * (allocated by conv_bwd_data_create) are shared by its runs.
+ * uncovered; the fp32 tensor-core path first splits the filter and, when it
+ * cuts its last round of tiles into k-block ranges, zeroes those tiles' dx
+ * region; NCHW plans on a tensor-core path add their layout transposes).
+ * Runs of one plan must not overlap on the GPU: the plan's status word and,
+ * for wide bf16 problems, its work-splitting scratch, for fp32 tensor-core
+ * plans the split filter (allocated by conv_bwd_data_create) are shared by
+ * its runs.
  * Errors: INVALID_ARG (null or overlapping pointers), MISALIGNED (bf16 NHWC
  * tensor-core path needs 16-byte aligned dy, w, dx; the fp32 tensor-core path
  * 16-byte aligned dy and dx), CUDA (launch failure or plan created without a
