@@ -347,6 +347,26 @@ conv_bwd_status plan_create_borrowed_status(const conv_bwd_desc *desc, int32_t *
 
 namespace {
 
+// fp32 tensor-core schedule of one launch (classes cls[0..nc) holding `total`
+// tiles): tiles that do not fill a last round of the SMs are cut into equal
+// k-block ranges over every SM (added into dx after a zeroing launch) when that
+// round would leave at least a fifth of the SMs idle and each range keeps a few
+// k blocks.  Returns whether to cut, and the k blocks of those tiles.
+bool tf32_tail_split(const conv_bwd_plan_s *p, const ClassDesc *cls, size_t nc, int64_t total, int kb_per_tap,
+                     int64_t *tail_units) {
+    const int nsm = std::max(1, p->num_sms);
+    const int64_t t_dp = (total / nsm) * nsm, tail = total - t_dp;
+    int64_t units = 0;
+    for (size_t i = 0; i < nc; ++i) {
+        const int64_t te = i + 1 < nc ? cls[i + 1].tile_begin : total;
+        const int64_t lo = std::max<int64_t>(cls[i].tile_begin, t_dp);
+        if (te > lo) units += (te - lo) * cls[i].taps_y * cls[i].taps_x * kb_per_tap;
+    }
+    *tail_units = units;
+    if (p->tf32_split >= 0) return tail > 0 && p->tf32_split == 1;
+    return tail > 0 && tail * 5 <= (int64_t)nsm * 4 && units >= 4LL * nsm;
+}
+
 int kHostChunks = 4;  // batch chunks of the pipelined host path (CONVBWD_DEBUG_HOST_CHUNKS overrides)
 
 // Batch chunks for the pipelined host path: 4 chunks of ceil(N/4) images when
@@ -762,8 +782,24 @@ conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t
     // the grouped kernel writes every pixel; the tensor-core kernels zero uncovered pixels themselves
     const bool fill = p->any_uncovered && (p->path == CONV_BWD_PATH_SIMT || p->classes.empty());
     if (p->path == CONV_BWD_PATH_GROUPED) gemm_launches = 1;
-    if (p->path == CONV_BWD_PATH_TF32)  // the filter split, then the tensor-core kernel (which fills)
-        gemm_launches = 1 + (int)((p->classes.size() + kMaxTcClasses - 1) / kMaxTcClasses);
+    if (p->path == CONV_BWD_PATH_TF32) {
+        // the filter split, then per launch of up to kMaxTcClasses classes the
+        // tensor-core kernel (which fills), preceded by the tile zeroing when its
+        // last round of tiles is cut into k-block ranges (the same decision as run)
+        gemm_launches = 1;
+        const int n_tiles = (p->g.Cg + kTf32BN - 1) / kTf32BN, kbt = (p->g.Kg + kTf32BK - 1) / kTf32BK;
+        for (size_t c0 = 0; c0 < p->sched.size(); c0 += kMaxTcClasses) {
+            const size_t nc = std::min<size_t>(kMaxTcClasses, p->sched.size() - c0);
+            ClassDesc cls[kMaxTcClasses];
+            int64_t total = 0, units = 0;
+            for (size_t i = 0; i < nc; ++i) {
+                cls[i] = p->classes[(size_t)p->sched[c0 + i]];
+                cls[i].tile_begin = (int)total;
+                total += (int64_t)p->g.G * cls[i].m_tiles * n_tiles;
+            }
+            gemm_launches += 1 + (p->num_sms > 0 && tf32_tail_split(p, cls, nc, total, kbt, &units) ? 1 : 0);
+        }
+    }
     if (launches) *launches = (fill ? 1 : 0) + gemm_launches;
     return CONV_BWD_OK;
 }
@@ -904,22 +940,10 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
                 tp.tmap_a[i] = p->tmap_a[(size_t)idx];
             }
             tp.total_tiles = (int)total;
-            // Tiles that do not fill a last round of the SMs are cut into equal
-            // k-block ranges over every SM (added into dx after a zeroing launch)
-            // when that round would leave at least a fifth of the SMs idle and
-            // each range keeps a few k blocks.
             const int nsm = std::max(1, p->num_sms);
             int grid = (int)std::min<int64_t>(total, nsm);
-            const int64_t t_dp = (total / nsm) * nsm, tail = total - t_dp;
             int64_t tail_units = 0;
-            for (size_t i = 0; i < nc; ++i) {
-                const ClassDesc &c = tp.cls[i];
-                const int64_t te = i + 1 < nc ? tp.cls[i + 1].tile_begin : total;
-                const int64_t lo = std::max<int64_t>(c.tile_begin, t_dp);
-                if (te > lo) tail_units += (te - lo) * c.taps_y * c.taps_x * tp.kb_per_tap;
-            }
-            bool split = tail > 0 && tail * 5 <= (int64_t)nsm * 4 && tail_units >= 4LL * nsm;
-            if (p->tf32_split >= 0) split = tail > 0 && p->tf32_split == 1;
+            const bool split = tf32_tail_split(p, tp.cls, nc, total, tp.kb_per_tap, &tail_units);
             if (split) {
                 tp.streamk = 1;
                 tp.units_total = (int)std::min<int64_t>(tail_units, 0x7fffffff);

@@ -111,8 +111,9 @@ def test_forced_tf32_matches_oracle(B, monkeypatch, c):
     got, plan = run_gpu(B, c, dy, w)
     path, launches = plan.path()
     assert path == "tf32", plan.path()
-    # filter split + kernel, and two transposes around them for NCHW
-    assert launches == (4 if c.layout == wl.NCHW else 2), plan.path()
+    # filter split + kernel (+ the tile zeroing when the last round is cut into
+    # k-block ranges), and two transposes around them for NCHW
+    assert launches - (2 if c.layout == wl.NCHW else 0) in (2, 3), plan.path()
     check_full(c, got, g, dy, w)
 
 
@@ -126,7 +127,9 @@ def test_tail_split_schedule(B, monkeypatch, idx, split):
     monkeypatch.setenv("CONVBWD_DEBUG_STREAMK", split)
     g, dy, w = inputs(c)
     got, plan = run_gpu(B, c, dy, w)
-    assert plan.path()[0] == "tf32"
+    # these problems hold fewer tiles than SMs: every tile is in the last round,
+    # so the split adds the zeroing launch to the filter split and the kernel
+    assert plan.path() == ("tf32", 3 if split == "1" else 2), plan.path()
     check_full(c, got, g, dy, w)
 
 
