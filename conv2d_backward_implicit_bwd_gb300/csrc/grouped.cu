@@ -94,6 +94,25 @@ __device__ __forceinline__ GItem next_item(const GroupedParams &p, const GItem &
     return r;
 }
 
+// Within each quad of lanes (4*k .. 4*k+3, t = lane % 4): o[j] = w[t] of lane
+// 4*k + j, a 4 x 4 transpose of 32-bit words in two butterfly stages (lanes
+// t ^ 1 swap two words, then lanes t ^ 2 swap two), all register indices static.
+__device__ __forceinline__ void quad_transpose(const uint32_t (&w)[4], uint32_t (&o)[4], int lane) {
+    const bool odd = lane & 1, hi2 = lane & 2;
+    // stage 1: pair base p = t & ~1 ends with x = {w_p[t&1], w_p+1[t&1], w_p[2+(t&1)], w_p+1[2+(t&1)]}
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, odd ? w[0] : w[1], 1);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, odd ? w[2] : w[3], 1);
+    const uint32_t x0 = odd ? r0 : w[0], x1 = odd ? w[1] : r0;
+    const uint32_t x2 = odd ? r1 : w[2], x3 = odd ? w[3] : r1;
+    // stage 2: lanes t and t ^ 2 swap their other half
+    const uint32_t q0 = __shfl_xor_sync(0xffffffffu, hi2 ? x0 : x2, 2);
+    const uint32_t q1 = __shfl_xor_sync(0xffffffffu, hi2 ? x1 : x3, 2);
+    o[0] = hi2 ? q0 : x0;
+    o[1] = hi2 ? q1 : x1;
+    o[2] = hi2 ? x2 : q0;
+    o[3] = hi2 ? x3 : q1;
+}
+
 template <int CG>
 __global__ void __launch_bounds__(GCfg<CG>::THREADS, CG == 8 ? 10 : 3) grouped_dgrad_kernel(const __grid_constant__ GroupedParams p) {
     using C = GCfg<CG>;
@@ -265,6 +284,27 @@ __global__ void __launch_bounds__(GCfg<CG>::THREADS, CG == 8 ? 10 : 3) grouped_d
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int q = r + g.sw * (mt * 16 + gid + 8 * h);
+                    if (CG == 8) {
+                        // the 4 lanes of a row swap words so that lane tig holds all
+                        // 8 channels of groups tig and 4 + tig: two 16-byte stores
+                        // per lane, a row's 128-byte line in two instructions
+                        uint32_t wlo[4], whi[4], olo[4], ohi[4];
+#pragma unroll
+                        for (int gl = 0; gl < 4; ++gl) {
+                            __nv_bfloat162 a = __floats2bfloat162_rn(acc[gl][2 * h], acc[gl][2 * h + 1]);
+                            __nv_bfloat162 b = __floats2bfloat162_rn(acc[gl + 4][2 * h], acc[gl + 4][2 * h + 1]);
+                            wlo[gl] = *reinterpret_cast<uint32_t *>(&a);
+                            whi[gl] = *reinterpret_cast<uint32_t *>(&b);
+                        }
+                        quad_transpose(wlo, olo, lane);
+                        quad_transpose(whi, ohi, lane);
+                        if (q < m.npx) {
+                            uint4 *o = reinterpret_cast<uint4 *>(dxrow + q * cbytes);
+                            o[tig] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+                            o[4 + tig] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+                        }
+                        continue;
+                    }
                     if (q >= m.npx) continue;
                     uint32_t *o = reinterpret_cast<uint32_t *>(dxrow + q * cbytes) + tig;
 #pragma unroll
