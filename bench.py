@@ -49,7 +49,7 @@ TRAFFIC = {
     "bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "tile": (256, 512, 2), "sha": "5f8d1699c7352864",
                                     "bytes": 34.193e6},
     # grouped_dgrad_kernel<8> on the 64x56x56x256 G=32 layer: 25.76 MB + 42.64 MB
-    "bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": GROUPED_SOURCES, "tile": (0, 0, 1), "sha": "7552dcdea402cf0f",
+    "bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": GROUPED_SOURCES, "tile": (0, 0, 1), "sha": "d32b3a7c89beda60",
                                              "bytes": 68.403e6},
 }
 

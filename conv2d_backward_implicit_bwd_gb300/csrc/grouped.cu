@@ -23,10 +23,11 @@
 //     taps.
 //   * Pixel lines in shared memory are XOR-swizzled in 16-byte segments so
 //     that 8 consecutive pixels' segment of one group hit 8 bank groups.
-//   * Accumulators (fp32) leave as bf16 (RNE) straight from the fragments: the
-//     4 lanes of a fragment row write one group's 16 contiguous bytes, the 8
-//     groups of a store pass a pixel's full line; pixels no tap reaches are
-//     written as +0 by the same pass (no separate fill).
+//   * Accumulators (fp32) leave as bf16 (RNE) straight from the fragments: for
+//     8-channel groups the 4 lanes of a fragment row swap words so that each
+//     lane holds whole groups and writes 16-byte segments (a pixel's 128-byte
+//     line in two store instructions); pixels no tap reaches are written as +0
+//     by the same pass (no separate fill).
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -279,8 +280,8 @@ __global__ void __launch_bounds__(GCfg<CG>::THREADS, CG == 8 ? 10 : 3) grouped_d
                     }
                 }
                 // accumulators -> bf16 -> dx: lane (gid, tig) holds rows gid, gid + 8
-                // and channels nt*8 + 2 tig (+1) of every group: 4-byte stores, the
-                // 4 lanes of a row covering one group's 16 contiguous bytes
+                // and channels nt*8 + 2 tig (+1) of every group (16-channel groups:
+                // 4-byte stores, the 4 lanes of a row covering 16 contiguous bytes)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int q = r + g.sw * (mt * 16 + gid + 8 * h);
