@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(Tf32Cfg::THREADS, 1) tf32_dgrad_kernel(const _
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 4);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
 
-    // slot s: [A | A_lo | B_hi | B_lo]
+    // slot s: [A (fp32, as loaded) | B_hi | B_lo]; its split A sits in TMEM columns A_COL + 64 s
     auto slot_a = [&](uint32_t s) { return smem_u32(smem + s * Cfg::SLOT_BYTES); };
     const uint32_t full0 = smem_u32(bars), split0 = smem_u32(bars + S), empty0 = smem_u32(bars + 2 * S);
     const uint32_t tfull0 = smem_u32(bars + 3 * S), tempty0 = smem_u32(bars + 3 * S + 2);
