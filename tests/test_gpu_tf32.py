@@ -101,6 +101,10 @@ FORCED = [
     _mk("tf32_many_m_tiles", N=4, C=32, K=96, Hi=33, Wi=31, Y=3, X=3, pad=(1, 1)),
     _mk("tf32_nchw", N=2, C=64, K=96, Hi=9, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2), layout=wl.NCHW),
     _mk("tf32_nchw_groups4", N=2, C=128, K=128, Hi=7, Wi=7, Y=3, X=3, pad=(1, 1), groups=4, layout=wl.NCHW),
+    # 5x5 filter, stride 5: 25 residue classes, so two launches of at most 16 classes each
+    _mk("tf32_25_classes", N=2, C=64, K=36, Hi=23, Wi=21, Y=5, X=5, pad=(2, 2), stride=(5, 5)),
+    # 4 channels per group: one 128-wide n-tile with 124 zero columns
+    _mk("tf32_narrow_cg4", N=2, C=4, K=64, Hi=13, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2)),
 ]
 
 
@@ -111,9 +115,11 @@ def test_forced_tf32_matches_oracle(B, monkeypatch, c):
     got, plan = run_gpu(B, c, dy, w)
     path, launches = plan.path()
     assert path == "tf32", plan.path()
-    # filter split + kernel (+ the tile zeroing when the last round is cut into
-    # k-block ranges), and two transposes around them for NCHW
-    assert launches - (2 if c.layout == wl.NCHW else 0) in (2, 3), plan.path()
+    # filter split + one kernel per 16 classes (+ the tile zeroing of each launch
+    # whose last round is cut into k-block ranges), and two transposes around
+    # them for NCHW
+    kernels = (plan.num_subgemms() + 15) // 16
+    assert launches - (2 if c.layout == wl.NCHW else 0) in range(1 + kernels, 2 + 2 * kernels), plan.path()
     check_full(c, got, g, dy, w)
 
 
