@@ -62,15 +62,31 @@ def kernel_sha(files=TC2_SOURCES) -> str:
     return h.hexdigest()[:16]
 
 
-def load_peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _find_key(d, key):
+    """First value stored under `key` in a JSON document, searched breadth-first
+    (the peaks file may hold them at the top level or under a per-device entry)."""
+    todo = [d]
+    while todo:
+        cur = todo.pop(0)
+        if isinstance(cur, dict):
+            if key in cur and isinstance(cur[key], (int, float)):
+                return float(cur[key])
+            todo.extend(cur.values())
+        elif isinstance(cur, list):
+            todo.extend(cur)
+    return None
+
+
+def load_peaks(root=None):
+    path = os.path.join(root or ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         try:
             d = json.load(open(path))
             out = {"source": "measured"}
             for k in ("bf16_tflops", "bf16_tflops_sustained", "hbm_gbs"):
-                if k in d:
-                    out[k] = float(d[k])
+                v = _find_key(d, k)
+                if v is not None and v > 0:
+                    out[k] = v
             if "bf16_tflops" in out and "hbm_gbs" in out:
                 return out
         except Exception:

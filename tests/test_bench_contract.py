@@ -29,3 +29,21 @@ def test_reference_arm_prints_one_contract_line():
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_peaks_file_is_read_flat_or_nested(tmp_path):
+    """The roofline denominators come from the measured-peaks file when it has
+    the bf16 and HBM figures (at the top level or under a device entry), else
+    from the stated fallback."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.load_peaks(str(tmp_path))["source"] == "fallback"
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 7000.0, "bf16_tflops": 2000.0}))
+    p = bench.load_peaks(str(tmp_path))
+    assert p["source"] == "measured" and p["hbm_gbs"] == 7000.0 and p["bf16_tflops"] == 2000.0
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
+        {"gpus": [{"index": 0, "hbm_gbs": 6900, "bf16_tflops": 1950, "bf16_tflops_sustained": 1700}]}))
+    p = bench.load_peaks(str(tmp_path))
+    assert p["source"] == "measured" and p["bf16_tflops_sustained"] == 1700.0
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 7000.0}))
+    assert bench.load_peaks(str(tmp_path))["source"] == "fallback"
