@@ -589,20 +589,24 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
     // tensor-core kernel, 64 for SIMT.
     const int bm = p->path == CONV_BWD_PATH_TCGEN05 ? (p->two_sm ? 256 * p->cl : 128)
                                                     : (p->path == CONV_BWD_PATH_TF32 ? 128 : 64);
-    const int n_tiles = (g.Cg + p->bn - 1) / p->bn;
     p->sched.resize(p->classes.size());
     std::iota(p->sched.begin(), p->sched.end(), 0);
     std::stable_sort(p->sched.begin(), p->sched.end(), [&](int a, int b) {
         return p->classes[a].taps_y * p->classes[a].taps_x > p->classes[b].taps_y * p->classes[b].taps_x;
     });
-    int64_t tiles = 0;
-    for (int idx : p->sched) {
-        ClassDesc &c = p->classes[idx];
-        c.m_tiles = (c.M + bm - 1) / bm;
-        c.tile_begin = (int)tiles;
-        tiles += (int64_t)g.G * c.m_tiles * n_tiles;
-    }
-    if (tiles > lim) {
+    // per-class m tiles and tile offsets for row tiles of `rows` and the plan's tile width
+    auto schedule = [p, &g](int rows) {
+        const int n_tiles = (g.Cg + p->bn - 1) / p->bn;
+        int64_t total = 0;
+        for (int idx : p->sched) {
+            ClassDesc &c = p->classes[(size_t)idx];
+            c.m_tiles = (c.M + rows - 1) / rows;
+            c.tile_begin = (int)total;
+            total += (int64_t)g.G * c.m_tiles * n_tiles;
+        }
+        return total;
+    };
+    if (schedule(bm) > lim) {
         delete p;
         return CONV_BWD_ERR_UNSUPPORTED;
     }
@@ -644,11 +648,17 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                 if (cudaMalloc(&p->w_hi, nsplit) == cudaSuccess && cudaMalloc(&p->w_lo, nsplit) == cudaSuccess) {
                     p->owns_wsplit = true;
                 } else {
+                    // no room for the split filter: CUDA-core path, rescheduled for its 64x64 tiles
                     cudaGetLastError();
                     cudaFree(p->w_hi);
                     cudaFree(p->w_lo);
                     p->w_hi = p->w_lo = nullptr;
-                    p->path = CONV_BWD_PATH_SIMT;  // keeps its 64x64 schedule below
+                    p->path = CONV_BWD_PATH_SIMT;
+                    p->bn = 64;
+                    if (schedule(64) > lim) {
+                        conv_bwd_data_destroy(p);
+                        return CONV_BWD_ERR_CUDA;
+                    }
                 }
             }
             // NCHW/GKCYX: run the NHWC/KYXC plan of the same geometry between
