@@ -19,6 +19,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/conv_bwd_data.h"
 #include "internal.h"
@@ -55,7 +56,6 @@ struct conv_bwd_plan_s {
     std::vector<CUtensorMap> tmap_a;      // per class (gemm_id order)
     bool im2col = false;                  // A rows by TMA im2col loads (else cp.async gather)
     bool two_sm = false;                  // 256x256 tiles on SM pairs (cta_group::2)
-    int32_t cl = 1;                       // SM pairs per cluster (2: the pairs share B by multicast)
     int max_pairs = 0;                    // co-resident SM pairs of the 2-SM kernel
     float4 *d_partials = nullptr;         // stream-K workspace: per pair and CTA, one 128x256 fp32 tile
     int32_t *d_flags = nullptr;           // stream-K flags, tagged with the launch epoch
@@ -138,6 +138,28 @@ size_t elem_size(int32_t dt) { return dt == CONV_BWD_BF16 ? 2 : 4; }
 
 const char *env(const char *k);
 
+// NVTX range (domain "conv_bwd_data") around each entry point that enqueues
+// work, so that a profiler timeline shows which kernels and copies belong to
+// which call.  Header-only NVTX: without an attached tool the calls return
+// at once.
+nvtxDomainHandle_t nvtx_domain() {
+    static nvtxDomainHandle_t d = nvtxDomainCreateA("conv_bwd_data");
+    return d;
+}
+struct NvtxRange {
+    explicit NvtxRange(const char *name) {
+        nvtxEventAttributes_t a = {};
+        a.version = NVTX_VERSION;
+        a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+        a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+        a.message.ascii = name;
+        nvtxDomainRangePushEx(nvtx_domain(), &a);
+    }
+    ~NvtxRange() { nvtxDomainRangePop(nvtx_domain()); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 // L2 sector promotion of the TMA maps (256 B by default).
 CUtensorMapL2promotion l2_promotion() {
     if (const char *f = env("CONVBWD_DEBUG_L2PROMO")) {
@@ -169,8 +191,7 @@ PFN_encodeTiled get_encode_tiled() {
 // w (KYXC, bf16) as a 5-D tensor {Cg, X, Y, Kg, G}: a box {64, 1, 1, 64, 1}
 // is a 64(k) x 64(c) slice of one filter tap, c contiguous (128 bytes per k
 // row, 128-byte swizzle).  Coordinates past Cg or past Kg (the next group's
-// rows) read as zero.  A second map with box {64, 1, 1, 32, 1} loads half of
-// such a slice (the B pieces that clusters of SM pairs share).
+// rows) read as zero.
 bool encode_w_map(conv_bwd_plan_s *p, const void *w) {
     PFN_encodeTiled enc = get_encode_tiled();
     if (!enc) return false;
@@ -183,10 +204,6 @@ bool encode_w_map(conv_bwd_plan_s *p, const void *w) {
     CUresult r = enc(&p->tmap_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(w), dims, strides, box,
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      l2_promotion(), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return false;
-    box[3] = 32;
-    r = enc(&p->tmap_w_half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(w), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2_promotion(), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -543,8 +560,6 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
     // with the measured cost of one tile relative to a 256-wide one (same K):
     // 128 wide 0.85 (more operand bytes per output), 512 wide 1.785 (two N=256
     // MMAs per k slice, fewer A bytes per output, single-buffered accumulator).
-    // Where 256-wide tiles fill at most one wave, clusters of two pairs share B
-    // by multicast (measured 5% faster there, slower when several waves queue).
     p->two_sm = p->path == CONV_BWD_PATH_TCGEN05 && p->im2col && g.Cg >= 256;  // (C/G < 256: 1-SM tiles measured faster)
     if (const char *f = env("CONVBWD_DEBUG_NO2SM")) p->two_sm = p->two_sm && f[0] == '0';
     if (const char *f = env("CONVBWD_DEBUG_2SM"))
@@ -570,24 +585,17 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                 p->bn = widths[i];
             }
         }
-        p->cl = (p->bn == 256 && tiles_of(256) <= pairs) ? 2 : 1;
     }
     if (const char *f = env("CONVBWD_DEBUG_BN")) {
         if (p->path == CONV_BWD_PATH_TCGEN05 && (!std::strcmp(f, "128") || !std::strcmp(f, "256"))) p->bn = std::atoi(f);
         if (p->two_sm && !std::strcmp(f, "512")) p->bn = 512;
-        p->cl = 1;
     }
-    if (const char *f = env("CONVBWD_DEBUG_CL"))
-        if (p->two_sm) p->cl = f[0] == '2' ? 2 : 1;
-    if (const char *f = env("CONVBWD_DEBUG_STREAMK")) {
-        if (f[0] == '1') p->cl = 1;  // stream-K runs with one pair per cluster
-        p->tf32_split = f[0] == '1' ? 1 : 0;
-    }
+    if (const char *f = env("CONVBWD_DEBUG_STREAMK")) p->tf32_split = f[0] == '1' ? 1 : 0;
 
     // Schedule: classes with the longest reduction first (LPT), tiles of one
     // class contiguous; BM = 256 rows on SM pairs, 128 for the 1-SM
     // tensor-core kernel, 64 for SIMT.
-    const int bm = p->path == CONV_BWD_PATH_TCGEN05 ? (p->two_sm ? 256 * p->cl : 128)
+    const int bm = p->path == CONV_BWD_PATH_TCGEN05 ? (p->two_sm ? 256 : 128)
                                                     : (p->path == CONV_BWD_PATH_TF32 ? 128 : 64);
     p->sched.resize(p->classes.size());
     std::iota(p->sched.begin(), p->sched.end(), 0);
@@ -629,8 +637,10 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                 return CONV_BWD_ERR_CUDA;
             }
             p->has_device = true;
-            if (p->two_sm) {
-                // stream-K workspace (used when whole tiles would leave SM pairs idle)
+            const char *sk = env("CONVBWD_DEBUG_STREAMK");
+            if (p->two_sm && sk && sk[0] == '1') {
+                // stream-K workspace: only for plans created with the opt-in stream-K
+                // schedule (the default whole-tile schedule never touches it)
                 p->max_pairs = tc2_max_pairs(p->num_sms);
                 const size_t slots = (size_t)p->max_pairs * 2;
                 if (cudaMalloc(&p->d_partials, slots * 128 * 64 * sizeof(float4)) != cudaSuccess ||
@@ -645,7 +655,9 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
             }
             const size_t nsplit = (size_t)d.K * g.Cg * d.Y * d.X * sizeof(float);
             if (p->path == CONV_BWD_PATH_TF32) {
-                if (cudaMalloc(&p->w_hi, nsplit) == cudaSuccess && cudaMalloc(&p->w_lo, nsplit) == cudaSuccess) {
+                // (CONVBWD_DEBUG_NO_WSPLIT: take the fallback below as if the allocation had failed)
+                if (!env("CONVBWD_DEBUG_NO_WSPLIT") && cudaMalloc(&p->w_hi, nsplit) == cudaSuccess &&
+                    cudaMalloc(&p->w_lo, nsplit) == cudaSuccess) {
                     p->owns_wsplit = true;
                 } else {
                     // no room for the split filter: CUDA-core path, rescheduled for its 64x64 tiles
@@ -818,9 +830,9 @@ conv_bwd_status conv_bwd_data_tile(const conv_bwd_plan p, int32_t *tile_m, int32
     if (!p) return CONV_BWD_ERR_INVALID_ARG;
     if (p->nhwc_plan) return conv_bwd_data_tile(p->nhwc_plan, tile_m, tile_n, sms);
     const bool tc = p->path == CONV_BWD_PATH_TCGEN05, grouped = p->path == CONV_BWD_PATH_GROUPED;
-    if (tile_m) *tile_m = grouped ? 0 : tc ? (p->two_sm ? 256 * p->cl : 128) : p->path == CONV_BWD_PATH_TF32 ? 128 : 64;
+    if (tile_m) *tile_m = grouped ? 0 : tc ? (p->two_sm ? 256 : 128) : p->path == CONV_BWD_PATH_TF32 ? 128 : 64;
     if (tile_n) *tile_n = grouped ? 0 : p->bn;
-    if (sms) *sms = tc && p->two_sm ? 2 * p->cl : 1;
+    if (sms) *sms = tc && p->two_sm ? 2 : 1;
     return CONV_BWD_OK;
 }
 
@@ -832,6 +844,7 @@ conv_bwd_status conv_bwd_data_work(const conv_bwd_plan p, double *flop, double *
 }
 
 conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w, void *dx, void *stream) {
+    NvtxRange range("conv_bwd_data_run");
     if (!p || !dy || !w || !dx) return CONV_BWD_ERR_INVALID_ARG;
     if (!p->has_device) return CONV_BWD_ERR_CUDA;
     const conv_bwd_desc &d = p->desc;
@@ -980,7 +993,6 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             TcParams tp;
             std::memset(&tp, 0, sizeof(tp));
             tp.tmap_w = p->tmap_w;
-            tp.tmap_w_half = p->tmap_w_half;
             tp.dy = dy; tp.dx = dx; tp.status = p->d_status; tp.wait_budget = p->wait_budget;
             tp.g = g;
             tp.n_tiles = (g.Cg + p->bn - 1) / p->bn;
@@ -1006,11 +1018,6 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             }
             tp.total_tiles = (int)total;
             tp.units_total = (int)std::min<int64_t>(units, 0x7fffffff);
-            if (p->two_sm && p->cl == 2) {
-                const int clusters = (int)std::min<int64_t>(total, tc2_max_clusters(p->num_sms, 2));
-                if (launch_tc2(tp, p->bn, 2, 4 * clusters, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
-                continue;
-            }
             if (p->two_sm) {
                 const int maxp = tc2_max_pairs(p->num_sms);
                 int pairs = (int)std::min<int64_t>(total, maxp);
@@ -1030,7 +1037,7 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
                     p->epoch = p->epoch >= 0x7ffffffe ? 1 : p->epoch + 1;
                     tp.epoch = p->epoch;
                 }
-                if (launch_tc2(tp, p->bn, 1, 2 * pairs, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+                if (launch_tc2(tp, p->bn, 2 * pairs, s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
                 continue;
             }
             int grid = (int)std::min<int64_t>(total, p->num_sms);
@@ -1060,6 +1067,7 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
 
 conv_bwd_status conv_bwd_data_run_host(conv_bwd_plan p, const void *dy_h, const void *w_h, void *dx_h, void *dy_d,
                                        void *w_d, void *dx_d, void *stream) {
+    NvtxRange range("conv_bwd_data_run_host");
     if (!p || !dy_h || !w_h || !dx_h || !dy_d || !w_d || !dx_d) return CONV_BWD_ERR_INVALID_ARG;
     if (!p->has_device) return CONV_BWD_ERR_CUDA;
     const conv_bwd_desc &d = p->desc;
@@ -1118,6 +1126,7 @@ conv_bwd_status conv_bwd_data_run_host(conv_bwd_plan p, const void *dy_h, const 
 }
 
 conv_bwd_status conv_bwd_data_run_forward(conv_bwd_plan p, const void *x, const void *w, void *y, void *stream) {
+    NvtxRange range("conv_bwd_data_run_forward");
     if (!p || !x || !w || !y) return CONV_BWD_ERR_INVALID_ARG;
     if (!fwd_supported(p)) return CONV_BWD_ERR_UNSUPPORTED;
     if (!p->has_device || !p->d_status) return CONV_BWD_ERR_CUDA;

@@ -71,7 +71,7 @@ struct FillParams {
 // Tensor-core (tcgen05) kernel parameters.
 struct TcParams {  // 128-byte aligned through CUtensorMap
     CUtensorMap tmap_w;   // w viewed as 5-D {Cg, X, Y, Kg, G}, box {64, 1, 1, 64, 1}, 128B swizzle
-    CUtensorMap tmap_w_half;  // the same view with box {64, 1, 1, 32, 1} (B pieces shared between SM pairs)
+    CUtensorMap tmap_w_half;  // fp32 tensor-core path only: the low part of the split filter (same view as tmap_w)
     CUtensorMap tmap_a[kMaxTcClasses];  // per class: dy as im2col {K, Wo, Ho, N}, 64 ch x 128 px, 128B swizzle
     const void *dy;
     void *dx;
@@ -148,12 +148,11 @@ cudaError_t launch_fill(const FillParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_simt(const SimtParams &p, int dtype, cudaStream_t s);
 cudaError_t launch_grouped(GroupedParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_tc(const TcParams &p, int bn, int grid, cudaStream_t s);
-cudaError_t launch_tc2(const TcParams &p, int bn, int cl, int grid, cudaStream_t s);  // cl: SM pairs per cluster
+cudaError_t launch_tc2(const TcParams &p, int bn, int grid, cudaStream_t s);  // grid: 2 CTAs per SM pair
 cudaError_t launch_fwd(const FwdParams &p, int bn, int grid, cudaStream_t s);
 // out[b][c][r] = in[b][r][c] for bf16 elements (layout changes of NCHW/GKCYX problems)
 cudaError_t launch_transpose_b16(const void *in, void *out, int64_t batch, int64_t R, int64_t Cc, int num_sms,
                                  cudaStream_t s);
-int tc2_max_clusters(int num_sms, int cl);
 int tc2_max_pairs(int num_sms);
 cudaError_t launch_selftest_wait(int32_t *status, int64_t budget, cudaStream_t s);
 size_t tc_smem_bytes(int bn, bool im2col);

@@ -15,7 +15,8 @@
 //     that read A and B from both CTAs' shared memory and accumulate rows
 //     [128r, 128r+128) in CTA r's TMEM; each stage is committed back to both
 //     CTAs' empty barriers and each finished tile to both CTAs'
-//     accumulator-full barriers (multicast).
+//     accumulator-full barriers (one commit that arrives on the barrier of
+//     both CTAs of the pair).
 //   * Each CTA's four epilogue warps drain their own TMEM rows (RNE to bf16,
 //     16-byte stores to the class's strided dx pixels) and release the
 //     leader's accumulator-empty barrier (remote arrive from the peer).
@@ -34,15 +35,9 @@
 
 namespace cbd {
 
-template <int BN_, int CL_>
+template <int BN_>
 struct Tc2Cfg {
     static constexpr int BN = BN_;          // tile width of the pair: 128, 256 or 512
-    // SM pairs per cluster: 1, or 2 pairs that compute two 256-row blocks of
-    // the same columns and share B -- CTA h of pair pr loads k rows
-    // [32pr, 32pr + 32) of B half h and multicasts them to CTA h of both pairs,
-    // so each SM reads half of its B from L2
-    static constexpr int CL = CL_;
-    static constexpr int CTAS = 2 * CL;
     static constexpr int BNH = BN / 2;      // columns of B held by each CTA
     // one MMA instruction is at most 256 wide: a 512-wide tile issues two per
     // 16-deep k slice (columns [0, 256) and [256, 512) of the tile), which
@@ -71,11 +66,10 @@ struct Tc2Cfg {
     static constexpr int THREADS = 32 * (B_WARP + B_WARPS);
 };
 
-template <int BN_, int CL_>
-__global__ void __cluster_dims__(2 * CL_, 1, 1) __launch_bounds__(Tc2Cfg<BN_, CL_>::THREADS, 1)
+template <int BN_>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS, 1)
     tc2_dgrad_kernel(const __grid_constant__ TcParams p) {
-    using Cfg = Tc2Cfg<BN_, CL_>;
-    constexpr int CL = Cfg::CL;
+    using Cfg = Tc2Cfg<BN_>;
     constexpr int S = Cfg::STAGES;
     constexpr int BN = Cfg::BN;
     extern __shared__ uint8_t smem_raw[];
@@ -87,26 +81,23 @@ __global__ void __cluster_dims__(2 * CL_, 1, 1) __launch_bounds__(Tc2Cfg<BN_, CL
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
 
-    const uint32_t q_rank = cluster_ctarank();
-    const uint32_t pr = q_rank >> 1;          // pair within the cluster
-    const uint32_t rank = q_rank & 1;         // CTA within the pair: 0 = leader
-    const uint32_t pl = q_rank & ~1u;         // cluster rank of this pair's leader
+    const uint32_t rank = cluster_ctarank();  // CTA within the pair: 0 = leader
+    const uint32_t pl = 0;                    // cluster rank of the pair's leader
     const bool leader = rank == 0;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
     const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const Geom &g = p.g;
-    // scheduling unit: the cluster (its pairs take the 256-row blocks of one
-    // 256*CL-row tile); stream-K runs only with one pair per cluster
-    const int pair = blockIdx.x / Cfg::CTAS, npairs = gridDim.x / Cfg::CTAS;
+    // scheduling unit: the pair (cluster of two CTAs)
+    const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8 * s, 1);   // leader: one arrive.expect_tx for both CTAs' bytes
-            mbar_init(empty0 + 8 * s, CL);  // one multicast commit per stage from each pair's leader
+            mbar_init(empty0 + 8 * s, 1);   // one commit per stage from the leader's MMA thread
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull0 + 8 * b, 1);   // one multicast commit per tile
+            mbar_init(tfull0 + 8 * b, 1);   // one commit per tile
             mbar_init(tempty0 + 8 * b, 8);  // leader: 4 epilogue warps of each CTA
         }
         *abort_flag = 0;
@@ -118,8 +109,7 @@ __global__ void __cluster_dims__(2 * CL_, 1, 1) __launch_bounds__(Tc2Cfg<BN_, CL
         tc_fence_before();
     }
     if (warp == 4 && lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(CL == 1 ? &p.tmap_w : &p.tmap_w_half))
-                     : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_w)) : "memory");
         for (int ci = 0; ci < p.num_classes; ++ci)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_a[ci])) : "memory");
     }
@@ -141,7 +131,6 @@ __global__ void __cluster_dims__(2 * CL_, 1, 1) __launch_bounds__(Tc2Cfg<BN_, CL
         const int cb_hi = do_a ? 0 : cb_lo + Cfg::BOXES_PER_WARP;
         if (lane == 0) {
             const uint32_t full_leader0 = mapa_shared(full0, pl);
-            const uint16_t bmask = (uint16_t)((1u << rank) | (1u << (2 + rank)));  // CTA `rank` of both pairs
             uint32_t it = 0;
             bool ok = true, issued = false;
             SegmentIter segs(p, pair, npairs);
@@ -150,7 +139,7 @@ __global__ void __cluster_dims__(2 * CL_, 1, 1) __launch_bounds__(Tc2Cfg<BN_, CL
                 const TileCoord tcd = decode_tile(p, sg.t);
                 const ClassDesc &c = p.cls[tcd.ci];
                 const int HTWT = c.HT * c.WT;
-                const int m0 = tcd.mb * (256 * CL) + (int)pr * 256 + (int)rank * 128;
+                const int m0 = tcd.mb * 256 + (int)rank * 128;
                 const int n0 = m0 / HTWT, rem = m0 - n0 * HTWT;
                 const int bh = c.ht_lo + rem / c.WT - (c.taps_y - 1) * g.DH;
                 const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
@@ -181,12 +170,8 @@ __global__ void __cluster_dims__(2 * CL_, 1, 1) __launch_bounds__(Tc2Cfg<BN_, CL
                     for (int cb = cb_lo; cb < cb_hi; ++cb) {
                         const int col = tcd.nb * BN + (cb / Cfg::QPM) * Cfg::MMA_N + (int)rank * (Cfg::MMA_N / 2) +
                                         (cb % Cfg::QPM) * 64;
-                        if (CL == 1)
-                            tma_load_5d_pair(bdst + cb * 8192, &p.tmap_w, bar, col, c.tx + g.XT * i,
-                                             c.ty + g.YT * j, k0, tcd.gi);
-                        else  // k rows [32pr, 32pr + 32) of the box, to both pairs
-                            tma_load_5d_pair_mc(bdst + cb * 8192 + pr * 4096, &p.tmap_w_half, bar, col,
-                                                c.tx + g.XT * i, c.ty + g.YT * j, k0 + 32 * (int)pr, tcd.gi, bmask);
+                        tma_load_5d_pair(bdst + cb * 8192, &p.tmap_w, bar, col, c.tx + g.XT * i, c.ty + g.YT * j, k0,
+                                         tcd.gi);
                     }
                     issued = true;
                 }
@@ -235,11 +220,11 @@ __global__ void __cluster_dims__(2 * CL_, 1, 1) __launch_bounds__(Tc2Cfg<BN_, CL
                                     bd0 + (uint64_t)(128 * kk + h * ((Cfg::QPM * 8192) >> 4)), idesc,
                                     (kb != sg.kb0 || kk != 0) ? 1u : 0u);
                     issued = true;
-                    // the slot is free once every pair that reads it is done (B is shared)
-                    tc_commit2_mc(empty0 + 8 * s, (uint16_t)(CL == 1 ? 0x3 : 0xF));
+                    // the slot of both CTAs is free once these MMAs have read it
+                    tc_commit2_mc(empty0 + 8 * s, (uint16_t)0x3);
                 }
                 if (!ok) break;
-                tc_commit2_mc(tfull0 + 8 * b, (uint16_t)(0x3u << (2 * pr)));
+                tc_commit2_mc(tfull0 + 8 * b, (uint16_t)0x3);
             }
             if (!ok && issued) {
                 for (int q = 0; q < 100; ++q) __nanosleep(1000);
@@ -275,7 +260,7 @@ __global__ void __cluster_dims__(2 * CL_, 1, 1) __launch_bounds__(Tc2Cfg<BN_, CL
                 if (threadIdx.x == 0) st_release_gpu(p.flags + pair * 2 + rank, p.epoch);
                 continue;
             }
-            const int m = tcd.mb * (256 * CL) + (int)pr * 256 + (int)rank * 128 + row;
+            const int m = tcd.mb * 256 + (int)rank * 128 + row;
             const bool rvalid = m < c.M;
             int64_t off = 0;
             if (rvalid) {
@@ -317,62 +302,54 @@ __global__ void __cluster_dims__(2 * CL_, 1, 1) __launch_bounds__(Tc2Cfg<BN_, CL
     }
 }
 
-template <int BN, int CL>
+template <int BN>
 static cudaError_t launch_tc2_bn(const TcParams &p, int grid, cudaStream_t s) {
-    using Cfg = Tc2Cfg<BN, CL>;
+    using Cfg = Tc2Cfg<BN>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc2_dgrad_kernel<BN, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg::SMEM);
+        cudaError_t e =
+            cudaFuncSetAttribute(tc2_dgrad_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    tc2_dgrad_kernel<BN, CL><<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(p);
+    tc2_dgrad_kernel<BN><<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_tc2(const TcParams &p, int bn, int cl, int grid, cudaStream_t s) {
+cudaError_t launch_tc2(const TcParams &p, int bn, int grid, cudaStream_t s) {
     if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
-    if (cl == 2 && p.streamk) return cudaErrorInvalidValue;  // stream-K runs with one pair per cluster
-    if (cl == 2) {
-        if (bn == 512) return launch_tc2_bn<512, 2>(p, grid, s);
-        return bn == 256 ? launch_tc2_bn<256, 2>(p, grid, s) : launch_tc2_bn<128, 2>(p, grid, s);
-    }
-    if (bn == 512) return launch_tc2_bn<512, 1>(p, grid, s);
-    return bn == 256 ? launch_tc2_bn<256, 1>(p, grid, s) : launch_tc2_bn<128, 1>(p, grid, s);
+    if (bn == 512) return launch_tc2_bn<512>(p, grid, s);
+    return bn == 256 ? launch_tc2_bn<256>(p, grid, s) : launch_tc2_bn<128>(p, grid, s);
 }
 
-// Clusters of `cl` SM pairs that can be resident at once (1 CTA per SM).
-int tc2_max_clusters(int num_sms, int cl) {
-    static int cached[64][3] = {};
+// SM pairs (clusters of two CTAs, one CTA per SM) that can be resident at once.
+int tc2_max_pairs(int num_sms) {
+    static int cached[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    const int ci = cl == 2 ? 2 : 1;
-    if (dev >= 0 && dev < 64 && cached[dev][ci]) return cached[dev][ci];
-    using Cfg = Tc2Cfg<256, 1>;
-    cudaFuncSetAttribute(tc2_dgrad_kernel<256, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+    using Cfg = Tc2Cfg<256>;
+    cudaFuncSetAttribute(tc2_dgrad_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(num_sms & ~(2 * ci - 1)), 1, 1);
+    cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2 * ci;
+    attr.val.clusterDim.x = 2;
     attr.val.clusterDim.y = 1;
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, tc2_dgrad_kernel<256, 1>, &cfg) != cudaSuccess || clusters <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, tc2_dgrad_kernel<256>, &cfg) != cudaSuccess || clusters <= 0) {
         cudaGetLastError();
-        clusters = num_sms / (2 * ci);
+        clusters = num_sms / 2;
     }
-    if (dev >= 0 && dev < 64) cached[dev][ci] = clusters;
+    if (dev >= 0 && dev < 64) cached[dev] = clusters;
     return clusters;
 }
-
-int tc2_max_pairs(int num_sms) { return tc2_max_clusters(num_sms, 1); }
 
 }  // namespace cbd

@@ -346,31 +346,6 @@ __device__ __forceinline__ void tma_load_im2col_pair(uint32_t dst, const CUtenso
         : "memory");
 }
 
-// Pair-mode multicast tile load (clusters of several SM pairs): the box lands
-// at the same shared-memory offset in every CTA of `mask`, and the bytes that
-// land in a CTA complete on the barrier at offset `bar` in the even CTA of
-// that CTA's pair (`bar` is a pair leader's barrier: its peer bit is 0).
-__device__ __forceinline__ void tma_load_5d_pair_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0,
-                                                    int c1, int c2, int c3, int c4, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".cta_group::2 [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "h"(mask)
-        : "memory");
-}
-
-// Multicast tile load: the box lands at the same shared-memory offset in every
-// CTA of `mask`, and each destination's barrier at offset `bar` receives the
-// bytes that landed in that CTA.
-__device__ __forceinline__ void tma_load_5d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
-                                               int c2, int c3, int c4, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "h"(mask)
-        : "memory");
-}
-
 // Zero the dx pixels that no residue class writes (bf16 NHWC, 16-byte
 // stores), spread over the CTAs of the launch: CTA b takes dx rows b,
 // b + gridDim.x, ...; a row no class writes is one contiguous run, a written

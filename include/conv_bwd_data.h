@@ -28,11 +28,11 @@
  *
  * Memory ownership.  The caller owns dy, w, dx and the stream (any
  * allocator; PyTorch in the bundled binding).  The library owns the plan
- * (host memory), one 16-byte device status word per plan and, for bf16
- * problems that run on SM pairs, a stream-K scratch of 256 KB per pair (fp32
- * partial tiles and flags, ~19 MB on 152 SMs); fp32 plans on the tensor-core
- * path also own two fp32 copies of the filter (its hi and lo parts), all
- * allocated by conv_bwd_data_create when a CUDA device is present.  conv_bwd_data_run
+ * (host memory) and one 16-byte device status word per plan; fp32 plans on
+ * the tensor-core path also own two fp32 copies of the filter (its hi and lo
+ * parts), all allocated by conv_bwd_data_create when a CUDA device is present
+ * (plans created with the opt-in stream-K override below also own its
+ * scratch, 256 KB per SM pair).  conv_bwd_data_run
  * allocates nothing, never synchronises and is ordered on the given stream.
  *
  * Layouts (all tensors dense, row-major in the order written):
@@ -115,9 +115,12 @@ typedef enum {
  *   CONVBWD_DEBUG_PATH=tf32          fp32 tensor-core path whatever the problem size
  *   CONVBWD_DEBUG_NOIM2COL=1         cp.async A producer instead of TMA im2col
  *   CONVBWD_DEBUG_2SM=1 / _NO2SM=1   SM-pair kernel for C/G >= 128 / never
- *   CONVBWD_DEBUG_BN=128|256|512     tile width; CONVBWD_DEBUG_CL=1|2 pairs per cluster
- *   CONVBWD_DEBUG_STREAMK=1|0        stream-K schedule on the SM-pair kernel; on the fp32
- *                                    tensor-core path, the tail split always / never
+ *   CONVBWD_DEBUG_BN=128|256|512     tile width
+ *   CONVBWD_DEBUG_STREAMK=1|0        stream-K schedule on the SM-pair kernel (its scratch is
+ *                                    allocated only then); on the fp32 tensor-core path, the
+ *                                    tail split always / never
+ *   CONVBWD_DEBUG_NO_WSPLIT=1        fp32 tensor-core plans behave as if the split filter could
+ *                                    not be allocated (CUDA-core fallback)
  *   CONVBWD_DEBUG_RASTER_M=1         tiles walk m-blocks first
  *   CONVBWD_DEBUG_GRID=n             cap the 1-SM kernel's grid
  *   CONVBWD_DEBUG_L2PROMO=0|1       TMA L2 promotion none / 128 B (default 256 B)
@@ -205,10 +208,11 @@ conv_bwd_status conv_bwd_data_work(const conv_bwd_plan plan, double *useful_flop
  * uncovered; the fp32 tensor-core path first splits the filter and, when it
  * cuts its last round of tiles into k-block ranges, zeroes those tiles' dx
  * region; NCHW plans on a tensor-core path add their layout transposes).
- * Runs of one plan must not overlap on the GPU: the plan's status word and,
- * for wide bf16 problems, its work-splitting scratch, for fp32 tensor-core
- * plans the split filter (allocated by conv_bwd_data_create) are shared by
- * its runs.
+ * Runs of one plan must not overlap on the GPU: the plan's status word (and
+ * for fp32 tensor-core plans the split filter, for plans created with the
+ * stream-K override its scratch) are shared by its runs.  Each call is an
+ * NVTX range "conv_bwd_data_run" in the domain "conv_bwd_data" (as are
+ * run_host and run_forward under their own names).
  * Errors: INVALID_ARG (null or overlapping pointers), MISALIGNED (bf16 NHWC
  * tensor-core path needs 16-byte aligned dy, w, dx; the fp32 tensor-core path
  * 16-byte aligned dy and dx), CUDA (launch failure or plan created without a
