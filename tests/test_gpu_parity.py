@@ -5,9 +5,9 @@ Tolerances per element (ref = oracle value, S = sum over taps of |dy*w|):
   bf16 output: |err| <= 2^-8 * |ref| + 1e-4 * S
 Inputs come from the seeded generators shared with the oracle (byte-identical
 bf16/fp32 values).  dx is pre-filled with NaN so that a pixel the library
-forgets to write shows up as a failure.  Large problems are compared on a
-batch slice computed in full by the oracle plus random sample points from
-every image; everything else is compared element by element.
+forgets to write shows up as a failure.  Every output element is compared with
+the oracle, the five benchmark workloads included (at the plan and launch
+configuration the benchmark times).
 """
 import zlib
 
@@ -77,17 +77,6 @@ def check_full(c, got, g, dy, w, n_range=None):
     return float(np.max(err / np.maximum(bound, 1e-300)))
 
 
-def check_points(c, got, g, dy, w, count=1500, seed=0):
-    rng = np.random.Generator(np.random.PCG64(seed))
-    pts = [(int(rng.integers(c.N)), int(rng.integers(c.C)), int(rng.integers(c.Hi)), int(rng.integers(c.Wi)))
-           for _ in range(count)]
-    vals, abss = oracle.dgrad_points(g, _lay(c), dy, w, pts)
-    idx = [(n, ch, h, x) if c.layout == wl.NCHW else (n, h, x, ch) for (n, ch, h, x) in pts]
-    gv = np.array([got[i] for i in idx])
-    bound = oracle.tolerance(vals, abss, c.dtype)
-    assert np.all(np.abs(gv - vals) <= bound)
-
-
 SMALL = [c for c in wl.CASES if c.tags[0] == "fp32_small"]
 
 
@@ -99,18 +88,18 @@ def test_small_configs_full(B, c):
     check_full(c, got, g, dy, w)
 
 
-LARGE = {"bf16_16x1x512x2048": (0, 1), "bf16_resnext_64x56x56x256": None, "bf16_32x28x28x512": (0, 2), "bf16_32x14x14_1024": (0, 4), "bf16_32x57x57x128": (0, 3)}
+LARGE = ["bf16_16x1x512x2048", "bf16_resnext_64x56x56x256", "bf16_32x28x28x512", "bf16_32x14x14_1024",
+         "bf16_32x57x57x128"]
 
 
-@pytest.mark.parametrize("name", list(LARGE))
+@pytest.mark.parametrize("name", LARGE)
 def test_large_configs(B, name):
+    """The whole dx of each bf16 benchmark workload against the oracle's."""
     c = wl.case(name)
     g, dy, w = inputs(c)
     got, plan = gpu_dgrad(B, c, dy, w)
-    assert np.all(np.isfinite(got)), "unwritten (NaN) outputs"
-    check_full(c, got, g, dy, w, n_range=LARGE[name])
-    check_points(c, got, g, dy, w, seed=zlib.crc32(name.encode()) % 1000)
     assert plan.path()[0] == ("grouped" if name == "bf16_resnext_64x56x56x256" else "tcgen05")
+    check_full(c, got, g, dy, w)
 
 
 def _mk(name, **kw):
@@ -282,14 +271,12 @@ def test_stream_k_and_whole_tiles(B, monkeypatch, c, forced):
 
 
 # 2-SM kernel variants: 512-wide pair tiles (two N=256 MMAs per k slice, one
-# accumulator buffer), pair tiles for C/G = 128..255, and clusters of two SM
-# pairs sharing B by TMA multicast (512-row tiles; an odd count of 256-row
-# blocks leaves the second pair of the last tile without rows).
+# accumulator buffer), 256-wide pair tiles, pair tiles for C/G = 128..255, and
+# pair tiles whose last 256-row block holds fewer than 129 rows (the second
+# CTA of the pair then has no valid rows).
 W512 = {"CONVBWD_DEBUG_BN": "512"}
+W256 = {"CONVBWD_DEBUG_BN": "256"}
 PAIR = {"CONVBWD_DEBUG_2SM": "1"}
-CL2 = {"CONVBWD_DEBUG_CL": "2"}
-CL2_256 = {"CONVBWD_DEBUG_CL": "2", "CONVBWD_DEBUG_BN": "256"}
-CL2_512 = {"CONVBWD_DEBUG_CL": "2", "CONVBWD_DEBUG_BN": "512"}
 PAIR_CASES = [
     (_mk("w512_ragged_n", N=3, C=768, K=192, Hi=9, Wi=7, Y=3, X=3, pad=(1, 1), stride=(2, 2)), W512),
     (_mk("w512_1x2_s1x2", N=2, C=1024, K=512, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)), W512),
@@ -299,13 +286,13 @@ PAIR_CASES = [
     (_mk("pair_cg128", N=2, C=128, K=128, Hi=12, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)), PAIR),
     (_mk("pair_cg200", N=2, C=200, K=40, Hi=11, Wi=6, Y=2, X=4, pad=(0, 3), stride=(3, 1), dil=(2, 3)), PAIR),
     (_mk("pair_5x5s3", N=2, C=128, K=128, Hi=19, Wi=17, Y=5, X=5, pad=(2, 2), stride=(3, 3)), PAIR),
-    (_mk("cl2_1x2_s1x2", N=4, C=512, K=256, Hi=1, Wi=128, Y=1, X=2, stride=(1, 2)), CL2),
-    (_mk("cl2_odd_blocks", N=3, C=256, K=96, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2)), CL2),
-    (_mk("cl2_kg_tail", N=2, C=384, K=160, Hi=9, Wi=10, Y=3, X=3, pad=(1, 1)), CL2_256),
-    (_mk("cl2_groups2", N=2, C=512, K=256, Hi=8, Wi=9, Y=3, X=3, pad=(1, 1), stride=(1, 2), groups=2), CL2),
-    (_mk("cl2_dil2_fill", N=4, C=256, K=256, Hi=12, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)), CL2_256),
-    (_mk("cl2_w512", N=3, C=1024, K=128, Hi=11, Wi=9, Y=3, X=3, pad=(1, 1), stride=(2, 2)), CL2_512),
-    (_mk("cl2_w512_one_block", N=1, C=512, K=64, Hi=8, Wi=8, Y=1, X=1), CL2_512),
+    (_mk("pair_1x2_s1x2", N=4, C=512, K=256, Hi=1, Wi=128, Y=1, X=2, stride=(1, 2)), W256),
+    (_mk("pair_odd_blocks", N=3, C=256, K=96, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2)), W256),
+    (_mk("pair_kg_tail", N=2, C=384, K=160, Hi=9, Wi=10, Y=3, X=3, pad=(1, 1)), W256),
+    (_mk("pair_groups2", N=2, C=512, K=256, Hi=8, Wi=9, Y=3, X=3, pad=(1, 1), stride=(1, 2), groups=2), W256),
+    (_mk("pair_dil2_fill", N=4, C=256, K=256, Hi=12, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)), W256),
+    (_mk("w512_short_last_block", N=3, C=1024, K=128, Hi=11, Wi=9, Y=3, X=3, pad=(1, 1), stride=(2, 2)), W512),
+    (_mk("w512_one_block", N=1, C=512, K=64, Hi=8, Wi=8, Y=1, X=1), W512),
 ]
 
 
@@ -318,10 +305,7 @@ def test_pair_tile_variants(B, monkeypatch, c, env):
         got, plan = gpu_dgrad(B, c, dy, w)
         assert plan.path()[0] == "tcgen05"
         tm, tn, sms = plan.tile()
-        # SM pairs (256-row tiles), or clusters of two pairs (512-row tiles)
-        assert sms in (2, 4) and tm == 128 * sms, plan.tile()
-        if "CONVBWD_DEBUG_CL" in env:
-            assert sms == 4, plan.tile()
+        assert sms == 2 and tm == 256, plan.tile()  # SM pairs, 256-row tiles
         if "CONVBWD_DEBUG_BN" in env:
             assert tn == int(env["CONVBWD_DEBUG_BN"]), plan.tile()
         check_full(c, got, g, dy, w)
@@ -379,8 +363,7 @@ def test_run_host_pipelined_chunks(B, c):
         assert st == B.OK, (B.status_string(st), hex(det))
         got = dx_h.float().numpy().astype(np.float64)
         assert np.all(np.isfinite(got)), "unwritten (NaN) outputs"
-        check_full(c, got, g, dy, w, n_range=(c.N - 1, c.N))  # the tail chunk's image
-        check_points(c, got, g, dy, w, count=800, seed=zlib.crc32(c.name.encode()) % 1000)
+        check_full(c, got, g, dy, w)  # every chunk, the tail chunk's image included
         dx_h.fill_(float("nan"))
 
 

@@ -9,8 +9,8 @@ n tiles with ragged tails, K/G not a multiple of the 32-channel k step, groups,
 uncovered pixels (the kernel's own fill), an empty-class 1x1 stride-2 problem
 and NCHW/GKCYX problems (dy and dx transposed around the NHWC kernel, the
 filter split reading GKCYX directly).  The fp32 workloads above the size
-threshold take the path by themselves and are checked on a full image plus
-sampled points, also through the pipelined host entry point."""
+threshold take the path by themselves and are checked element by element,
+also through the pipelined host entry point."""
 import zlib
 
 import numpy as np
@@ -79,17 +79,6 @@ def check_full(c, got, g, dy, w, n_range=None):
     rel = float(np.max(err / np.maximum(ab, 1e-300)))
     assert rel < 4e-6, rel
     return rel
-
-
-def check_points(c, got, g, dy, w, count=1200, seed=0):
-    rng = np.random.Generator(np.random.PCG64(seed))
-    pts = [(int(rng.integers(c.N)), int(rng.integers(c.C)), int(rng.integers(c.Hi)), int(rng.integers(c.Wi)))
-           for _ in range(count)]
-    vals, abss = oracle.dgrad_points(g, _lay(c), dy, w, pts)
-    idx = [(n, ch, h, x) if c.layout == wl.NCHW else (n, h, x, ch) for (n, ch, h, x) in pts]
-    gv = np.array([got[i] for i in idx])
-    bound = oracle.tolerance(vals, abss, c.dtype)
-    assert np.all(np.abs(gv - vals) <= bound)
 
 
 FORCED = [
@@ -161,8 +150,7 @@ def test_large_fp32_workloads(B, c):
     g, dy, w = inputs(c)
     got, plan = run_gpu(B, c, dy, w)
     assert plan.path()[0] == "tf32", plan.path()
-    check_full(c, got, g, dy, w, n_range=(c.N - 1, c.N))
-    check_points(c, got, g, dy, w, seed=zlib.crc32(c.name.encode()) % 1000)
+    check_full(c, got, g, dy, w)  # every element
 
 
 def test_run_host_pipelined_tf32(B):
@@ -184,8 +172,7 @@ def test_run_host_pipelined_tf32(B):
     assert st == B.OK, (B.status_string(st), hex(det))
     got = dx_h.numpy().astype(np.float64)
     assert np.all(np.isfinite(got)), "unwritten (NaN) outputs"
-    check_full(c, got, g, dy, w, n_range=(c.N - 1, c.N))
-    check_points(c, got, g, dy, w, count=600, seed=7)
+    check_full(c, got, g, dy, w)
 
 
 def test_tf32_alignment_rule(B, monkeypatch):
@@ -199,3 +186,18 @@ def test_tf32_alignment_rule(B, monkeypatch):
     dx = torch.zeros(int(np.prod(dx_s)) + 4, dtype=torch.float32, device="cuda")
     assert plan.run_ptr(dy.data_ptr(), w.data_ptr(), dx.data_ptr() + 4) == B.ERR_MISALIGNED
     torch.cuda.synchronize()
+
+
+def test_split_filter_unavailable_falls_back_to_cuda_cores(B, monkeypatch):
+    """When the plan cannot hold the split filter it runs on the CUDA cores,
+    rescheduled for that kernel's 64-row tiles (several per class here, so a
+    tile count left at the tensor-core kernel's 128 rows would leave rows of
+    dx unwritten)."""
+    monkeypatch.setenv("CONVBWD_DEBUG_PATH", "tf32")
+    monkeypatch.setenv("CONVBWD_DEBUG_NO_WSPLIT", "1")
+    c = _mk("tf32_no_split_filter", N=4, C=96, K=80, Hi=17, Wi=19, Y=3, X=3, pad=(1, 1), stride=(2, 2))
+    g, dy, w = inputs(c)
+    got, plan = run_gpu(B, c, dy, w)
+    assert plan.path()[0] == "simt", plan.path()
+    assert plan.tile()[:2] == (64, 64), plan.tile()
+    check_full(c, got, g, dy, w)

@@ -1,13 +1,15 @@
 """The no-allocation entry point (conv_bwd_data_run_noalloc) against the
-regular one (conv_bwd_data_run).
+oracle and against the regular entry point (conv_bwd_data_run).
 
 Callers such as plugin hosts with their own device-memory pool, or loops that
 must not call cudaMalloc, use the no-allocation call: its kernel keeps its
 status word in a static device array instead of a buffer from
-conv_bwd_data_create.  Two calls in a row must each reproduce the regular
-entry point's dx (the array keeps the previous call's contents, so the second
-call checks that the status word is cleared again).  This file is collected
-last on purpose and must pass alone in a fresh process too.
+conv_bwd_data_create.  Two calls in a row must each match the oracle's dx
+within the bf16 bound, and the regular entry point's dx within that bound too
+(the array keeps the previous call's contents, so the second call checks that
+the status word is cleared again).  The cases cover the 1-SM tensor-core
+kernel (C/G < 256) and the SM-pair kernel (C/G >= 256).  This file is
+collected last on purpose and must pass alone in a fresh process too.
 """
 import numpy as np
 import pytest
@@ -34,6 +36,9 @@ CASES = [
             dtype=wl.BF16, layout=wl.NHWC, dist="normal", sigma=0.5, seed=901),
     wl.Case(name="noalloc_fill", N=2, C=128, K=64, Hi=15, Wi=14, Y=3, X=3, pad=(1, 1), stride=(4, 4),
             dtype=wl.BF16, layout=wl.NHWC, dist="normal", sigma=0.5, seed=902),
+    # C/G >= 256: 256-row tiles on SM pairs
+    wl.Case(name="noalloc_pair", N=2, C=256, K=256, Hi=9, Wi=10, Y=3, X=3, pad=(1, 1), stride=(2, 2),
+            dtype=wl.BF16, layout=wl.NHWC, dist="normal", sigma=0.5, seed=903),
 ]
 
 
@@ -42,25 +47,30 @@ def _dev(a):
 
 
 @pytest.mark.parametrize("c", CASES, ids=lambda c: c.name)
-def test_noalloc_matches_regular_entry_point_twice(B, c):
+def test_noalloc_matches_oracle_and_regular_entry_point_twice(B, c):
     g = oracle.geom(c.N, c.C, c.K, c.Hi, c.Wi, c.Y, c.X, c.pad, c.stride, c.dil, c.groups)
     dy_s, w_s, dx_s = oracle.shapes(g, oracle.LAYOUT_NHWC)
     dy, w = wl.draw(c, dy_s, w_s)
     dyd, wd = _dev(dy), _dev(w)
+    ref_o, absdot = oracle.dgrad(g, oracle.LAYOUT_NHWC, dy, w)
+    bound = oracle.tolerance(ref_o, absdot, "bf16")
     plan = B.Plan.from_case(c)
-    ref = torch.full(dx_s, float("nan"), dtype=torch.bfloat16, device="cuda")
-    plan.run(dyd, wd, ref)
+    assert plan.path()[0] == "tcgen05"
+    want_sms = 2 if c.C // c.groups >= 256 else 1
+    assert plan.tile()[2] == want_sms, plan.tile()
+    reg = torch.full(dx_s, float("nan"), dtype=torch.bfloat16, device="cuda")
+    plan.run(dyd, wd, reg)
     assert plan.status() == (B.OK, 0)
-    ref = ref.float().cpu().numpy().astype(np.float64)
-    _, absdot = oracle.dgrad(g, oracle.LAYOUT_NHWC, dy, w)
-    bound = oracle.tolerance(ref, absdot, "bf16")
+    reg = reg.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(reg - ref_o) <= bound)
     for call in range(2):
         out = torch.full(dx_s, float("nan"), dtype=torch.bfloat16, device="cuda")
         st, det = B.run_noalloc(plan.desc, dyd, wd, out, sync=True)
         assert st == B.OK and det == 0, (call, B.status_string(st), det)
         got = out.float().cpu().numpy().astype(np.float64)
         assert np.all(np.isfinite(got)), call
-        assert np.all(np.abs(got - ref) <= bound), call
+        assert np.all(np.abs(got - ref_o) <= bound), call
+        assert np.all(np.abs(got - reg) <= bound), call
 
 
 def test_noalloc_rejects_other_paths(B):
