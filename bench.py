@@ -6,6 +6,9 @@ C=K=2048, 1x2 filter, stride (1, 2), pad 0 -> dy 16x1x256x2048), seeded
 synthetic inputs N(0,1)*0.02 rounded to bf16.  A "step" is one
 conv_bwd_data_run (every kernel of the path) with dy and w resident in HBM;
 L2 is flushed (a 512 MiB write) before every step, outside the step's events.
+The line also carries `per_workload`: every other workload (the fp32 sweep,
+the grouped layer, the stress set, the fp32 tensor-core shapes) timed the same
+way, each with its own roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
@@ -34,13 +37,10 @@ METRIC = "dgrad useful-MAC TFLOP/s and % of GB300 bf16 dense peak, 1 GPU"
 # whose model the page does not name (6.872e10 useful FLOP -> 124.7 TFLOP/s).
 PAGE_TFLOPS = 124.7
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
-# DRAM traffic of the tensor-core kernel per launch on this workload, from one
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), valid only for
-# the kernel source whose sha256 is recorded with it.
 # Per-launch DRAM traffic of each workload's GEMM kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel's
 # sources are unchanged (hash below) and the plan launches the same tile shape.
-TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / bf16 tensor rates of the part
+TF32_PER_BF16 = 1.1 / 2.25  # NOMINAL dense TF32 / bf16 tensor rates of the part (no measured TF32 peak)
 TC2_SOURCES = ("tc_common.cuh", "tc2_sm103.cu", "internal.h")
 GROUPED_SOURCES = ("tc_common.cuh", "grouped.cu", "internal.h")
 TRAFFIC = {
@@ -235,6 +235,127 @@ def useful_flop_bruteforce(case, g):
     return 2.0 * case.N * case.K * (case.C // case.groups) * th * tw
 
 
+FP32_FFMA_PER_SM_CLK = 128  # fp32 lanes per SM (one FFMA = 2 FLOP per lane per clock)
+
+
+def kernel_label(path, plan, case):
+    tm, tn, tsms = plan.tile()
+    return {"tcgen05": (f"tc2_dgrad_kernel<{tn}>" if tsms >= 2 else f"tc_dgrad_kernel<{tn}>"),
+            "grouped": f"grouped_dgrad_kernel<{case.C // case.groups}>", "simt": "simt_dgrad_kernel",
+            "tf32": "tf32_dgrad_kernel"}[path]
+
+
+def roofline_of(path, case, useful, algo_bytes, kmean_ms, peaks, sm_max_mhz=None, num_sms=None):
+    """Roofline of a workload's dominant kernel.  Tensor-core bf16 kernels are
+    placed against the measured dense bf16 peak, the narrow-group kernel
+    against the measured HBM copy rate; workloads near the ridge (the 1x1 and
+    5x5 stress layers) report both and are graded on the larger fraction."""
+    tflops = useful / (kmean_ms * 1e-3) / 1e12
+    gbs = algo_bytes / (kmean_ms * 1e-3) / 1e9
+    t = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+         "peak_source": peaks["source"] + " (bf16 dense, burst)"}
+    h = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+         "peak_source": peaks["source"] + " (HBM copy)"}
+    t["frac"] = t["achieved"] / t["peak"]
+    h["frac"] = h["achieved"] / h["peak"]
+    if path == "tf32":
+        # three TF32 products per useful fp32 multiply-add; no TF32 peak is
+        # measured on this pool, so the ceiling is the measured bf16 rate times
+        # the part's NOMINAL dense TF32/bf16 ratio (1.1/2.25 PFLOP/s), over 3
+        t["peak"] = peaks["bf16_tflops"] * TF32_PER_BF16 / 3.0
+        t["frac"] = t["achieved"] / t["peak"]
+        t["peak_source"] = (peaks["source"] + " bf16 dense (burst) x nominal TF32/bf16 ratio 1.1/2.25 / 3 products "
+                            "per MAC; nominal ceiling, not a measured TF32 peak")
+        return dict(t, hbm_frac=h["frac"])
+    if path == "simt":
+        # CUDA-core FFMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock
+        mhz = sm_max_mhz or 2070.0
+        sms = num_sms or 152
+        peak = sms * FP32_FFMA_PER_SM_CLK * 2 * mhz * 1e6 / 1e12
+        a = {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+             "peak_source": f"{sms} SMs x {FP32_FFMA_PER_SM_CLK} fp32 lanes x 2 FLOP x {mhz:.0f} MHz (FFMA)"}
+        return dict(a, hbm_frac=h["frac"])
+    tags = case.tags[0] if case.tags else ""
+    if path == "grouped" or tags == "grouped":
+        return dict(h, tensor_frac=t["frac"])
+    if tags == "ridge":
+        best = t if t["frac"] >= h["frac"] else h
+        return dict(best, tensor_frac=t["frac"], hbm_frac=h["frac"], graded_on="max(tensor, hbm)")
+    return dict(t, hbm_frac=h["frac"])
+
+
+def device_inputs(case, plan):
+    import numpy as np
+    import torch
+    from conv2d_backward_implicit_bwd_gb300 import workloads as wl
+    dy, w, dx_s = make_inputs(case, plan)
+    tdt = torch.bfloat16 if case.dtype == wl.BF16 else torch.float32
+    if case.dtype == wl.BF16:
+        dy_h = torch.from_numpy(dy.view(np.int16)).view(torch.bfloat16)
+        w_h = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16)
+    else:
+        dy_h, w_h = torch.from_numpy(dy), torch.from_numpy(w)
+    return dy, w, dy_h, w_h, dy_h.cuda(), w_h.cuda(), torch.empty(dx_s, dtype=tdt, device="cuda"), dx_s, tdt
+
+
+def timed_steps(plan, dy_d, w_d, dx_d, flush, stream, steps):
+    """Per-step device times (ms): L2 flushed before every step, outside the
+    step's events; the flush kernel also keeps the stream busy while the next
+    step is enqueued, so no host latency lands inside a step's events."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        plan.run(dy_d, w_d, dx_d, stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def kernel_steps(plan, launches, step_ms, dy_d, w_d, dx_d, flush, stream, steps):
+    """Device time of the dominant (sub-GEMM) kernel per step: the step itself
+    when it is one launch, else the library's own events around that kernel."""
+    if launches == 1:
+        return step_ms
+    plan.set_timing(True)
+    out = []
+    for _ in range(steps):
+        flush.zero_()
+        plan.run(dy_d, w_d, dx_d, stream)
+        out.append(plan.last_timing()[1])
+    plan.set_timing(False)
+    return out
+
+
+def measure_workload(B, case, steps, warmup, flush, stream, peaks, num_sms):
+    """One per-workload entry: the same timing method as the headline line."""
+    plan = B.Plan.from_case(case)
+    path, launches = plan.path()
+    useful, algo_bytes = plan.work()
+    _, _, _, _, dy_d, w_d, dx_d, _, _ = device_inputs(case, plan)
+    for _ in range(warmup):
+        flush.zero_()
+        plan.run(dy_d, w_d, dx_d, stream)
+    st, det = plan.status(stream)
+    if st != B.OK:
+        raise RuntimeError(f"{case.name}: device status {B.status_string(st)} {det:#x}")
+    step_ms = timed_steps(plan, dy_d, w_d, dx_d, flush, stream, steps)
+    kern_ms = kernel_steps(plan, launches, step_ms, dy_d, w_d, dx_d, flush, stream, steps)
+    st, det = plan.status(stream)
+    if st != B.OK:
+        raise RuntimeError(f"{case.name}: device status {B.status_string(st)} {det:#x}")
+    ms = sum(step_ms) / len(step_ms)
+    kms = sum(kern_ms) / len(kern_ms)
+    roof = roofline_of(path, case, useful, algo_bytes, kms, peaks, num_sms=num_sms)
+    roof["kernel"] = kernel_label(path, plan, case)
+    roof["kernel_ms"] = kms
+    return {"ms_per_step": ms, "tflops": useful / (ms * 1e-3) / 1e12, "gbs": algo_bytes / (ms * 1e-3) / 1e9,
+            "dtype": case.dtype, "path": path, "launches_per_step": launches, "tile": list(plan.tile()),
+            "useful_flop": useful, "algo_bytes": algo_bytes, "steps": steps, "warmup": warmup,
+            "roofline": roof}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -243,9 +364,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="bf16_16x1x512x2048_1x2_s1x2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--pw-steps", type=int, default=30, help="timed steps of each per-workload entry (>= 20)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    args.pw_steps = max(args.pw_steps, 20)
 
     from conv2d_backward_implicit_bwd_gb300 import workloads as wl
     case = wl.case(args.workload)
@@ -266,17 +390,10 @@ def main():
     plan = B.Plan.from_case(case)
     path, launches = plan.path()
     useful, algo_bytes = plan.work()
-    dy, w, dx_s = make_inputs(case, plan)
-    tdt = torch.bfloat16 if case.dtype == wl.BF16 else torch.float32
-    if case.dtype == wl.BF16:
-        dy_h = torch.from_numpy(dy.view(np.int16)).view(torch.bfloat16)
-        w_h = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16)
-    else:
-        dy_h, w_h = torch.from_numpy(dy), torch.from_numpy(w)
-    dy_d, w_d = dy_h.cuda(), w_h.cuda()
-    dx_d = torch.empty(dx_s, dtype=tdt, device="cuda")
+    dy, w, dy_h, w_h, dy_d, w_d, dx_d, dx_s, tdt = device_inputs(case, plan)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
+    num_sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
 
     def barrier():
         if world > 1:
@@ -294,37 +411,17 @@ def main():
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.2)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     t_wall = time.perf_counter()
-    for i in range(args.steps):
-        # the flush kernel keeps the stream busy while the next step is enqueued,
-        # so no host latency lands inside a step's events
-        flush.zero_()
-        evs[i][0].record(stream)
-        plan.run(dy_d, w_d, dx_d, stream)
-        evs[i][1].record(stream)
+    step_ms = timed_steps(plan, dy_d, w_d, dx_d, flush, stream, args.steps)
     barrier()
     t_wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
     st, det = plan.status(stream)
     if st != B.OK:
         raise RuntimeError(f"device status {B.status_string(st)} {det:#x}")
-    step_ms = [a.elapsed_time(b) for a, b in evs]
     mean_ms = sum(step_ms) / len(step_ms)
-    if launches == 1:
-        # the step is exactly one launch of the dominant kernel on this stream
-        kern_ms = step_ms
-    else:
-        # several launches per step: time the sub-GEMM kernel with the library's
-        # own events around it, over the same number of steps
-        plan.set_timing(True)
-        kern_ms = []
-        for i in range(args.steps):
-            flush.zero_()
-            plan.run(dy_d, w_d, dx_d, stream)
-            kern_ms.append(plan.last_timing()[1])
-        plan.set_timing(False)
+    kern_ms = kernel_steps(plan, launches, step_ms, dy_d, w_d, dx_d, flush, stream, args.steps)
     mean_ms = max_over_ranks(mean_ms, world, "cuda")
     value = job_tflops(useful, world, mean_ms)
 
@@ -347,29 +444,10 @@ def main():
 
     peaks = load_peaks()
     kmean = sum(kern_ms) / len(kern_ms)
-    tm, tn, tsms = plan.tile()
-    kernel_name = {"tcgen05": (f"tc2_dgrad_kernel<{tn}, {tsms // 2}>" if tsms >= 2 else f"tc_dgrad_kernel<{tn}>"),
-                   "grouped": f"grouped_dgrad_kernel<{case.C // case.groups}>", "simt": "simt_dgrad_kernel",
-                   "tf32": "tf32_dgrad_kernel"}[path]
-    if path == "tcgen05":
-        achieved = useful / (kmean * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": peaks["source"] + " (bf16 dense, burst)", "kernel": kernel_name,
-                "kernel_ms": kmean}
-    elif path == "tf32":
-        # three TF32 products per useful fp32 multiply-add: the ceiling is the
-        # dense TF32 rate (bf16 rate x the nominal 1.1 / 2.25 ratio) over 3
-        achieved = useful / (kmean * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"] * TF32_PER_BF16 / 3.0
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": peaks["source"] + " (bf16 dense, burst) x 1.1/2.25 (TF32) / 3 (products per MAC)",
-                "kernel": kernel_name, "kernel_ms": kmean}
-    else:
-        achieved = algo_bytes / (kmean * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": peaks["source"] + " (HBM copy)", "kernel": kernel_name, "kernel_ms": kmean}
+    roof = roofline_of(path, case, useful, algo_bytes, kmean, peaks, sm_max_mhz=clocks.get("sm_max_mhz"),
+                       num_sms=num_sms)
+    roof["kernel"] = kernel_label(path, plan, case)
+    roof["kernel_ms"] = kmean
     tr = TRAFFIC.get(case.name)
     roof["traffic"] = (tr["bytes"] if tr and tr["sha"] == kernel_sha(tr["files"]) and tuple(plan.tile()) == tr["tile"]
                        else None)
@@ -394,6 +472,15 @@ def main():
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }
+    if not args.no_per_workload:
+        # every other workload, timed the same way (L2 flushed outside each
+        # step's events, >= 20 steps), on this rank's GPU
+        pw = {}
+        for c in wl.CASES:
+            if c.name == case.name:
+                continue
+            pw[c.name] = measure_workload(B, c, args.pw_steps, args.warmup, flush, stream, peaks, num_sms)
+        line["per_workload"] = pw
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # bounded oracle sample on the host cores (a reported baseline only)
         dts, fr, thr = [], 0.0, 1

@@ -47,3 +47,29 @@ def test_peaks_file_is_read_flat_or_nested(tmp_path):
     assert p["source"] == "measured" and p["bf16_tflops_sustained"] == 1700.0
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 7000.0}))
     assert bench.load_peaks(str(tmp_path))["source"] == "fallback"
+
+
+def test_roofline_kinds():
+    """Tensor-bound workloads are placed against the bf16 peak, the grouped
+    layer against HBM, ridge workloads on the larger of both fractions, the
+    fp32 tensor-core path against the nominal 3xTF32 ceiling and the CUDA-core
+    path against the FFMA rate."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from conv2d_backward_implicit_bwd_gb300 import workloads as wl
+    peaks = {"source": "measured", "bf16_tflops": 2000.0, "hbm_gbs": 8000.0}
+    big = wl.case("bf16_16x1x512x2048")
+    r = bench.roofline_of("tcgen05", big, 2e12, 1e9, 1.0, peaks)  # 2 PFLOP/s, 1 TB/s
+    assert r["bound"] == "tensor" and abs(r["frac"] - 1.0) < 1e-12 and abs(r["hbm_frac"] - 0.125) < 1e-12
+    grp = wl.case("bf16_resnext")
+    r = bench.roofline_of("grouped", grp, 2e9, 4e9, 1.0, peaks)
+    assert r["bound"] == "hbm" and abs(r["frac"] - 0.5) < 1e-12
+    ridge = wl.case("bf16_32x14x14_1024")
+    r = bench.roofline_of("tcgen05", ridge, 2e11, 6e9, 1.0, peaks)  # tensor 0.1, hbm 0.75
+    assert r["bound"] == "hbm" and r["frac"] == r["hbm_frac"] and r["graded_on"] == "max(tensor, hbm)"
+    f32 = wl.case("fp32_nhwc_32x28x28x512")
+    r = bench.roofline_of("tf32", f32, 1e11, 1e9, 1.0, peaks)
+    assert abs(r["peak"] - 2000.0 * 1.1 / 2.25 / 3) < 1e-9 and "nominal" in r["peak_source"]
+    small = wl.case("fp32_2x16x15x15")
+    r = bench.roofline_of("simt", small, 1e9, 1e6, 1.0, peaks, sm_max_mhz=2000.0, num_sms=100)
+    assert r["bound"] == "alu" and abs(r["peak"] - 100 * 128 * 2 * 2000e6 / 1e12) < 1e-9
