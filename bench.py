@@ -241,8 +241,8 @@ FP32_FFMA_PER_SM_CLK = 128  # fp32 lanes per SM (one FFMA = 2 FLOP per lane per 
 def kernel_label(path, plan, case):
     tm, tn, tsms = plan.tile()
     return {"tcgen05": (f"tc2_dgrad_kernel<{tn}>" if tsms >= 2 else f"tc_dgrad_kernel<{tn}>"),
-            "grouped": f"grouped_dgrad_kernel<{case.C // case.groups}>", "simt": "simt_dgrad_kernel",
-            "tf32": "tf32_dgrad_kernel"}[path]
+            "grouped": ("tc_grouped_dgrad_kernel" if tn else f"grouped_dgrad_kernel<{case.C // case.groups}>"),
+            "simt": "simt_dgrad_kernel", "tf32": "tf32_dgrad_kernel"}[path]
 
 
 def roofline_of(path, case, useful, algo_bytes, kmean_ms, peaks, sm_max_mhz=None, num_sms=None):
@@ -328,9 +328,19 @@ def kernel_steps(plan, launches, step_ms, dy_d, w_d, dx_d, flush, stream, steps)
     return out
 
 
-def measure_workload(B, case, steps, warmup, flush, stream, peaks, num_sms):
-    """One per-workload entry: the same timing method as the headline line."""
-    plan = B.Plan.from_case(case)
+def measure_workload(B, case, steps, warmup, flush, stream, peaks, num_sms, env=None):
+    """One per-workload entry: the same timing method as the headline line.
+    `env`: planner overrides in force while the plan is created."""
+    saved = {k: os.environ.get(k) for k in (env or {})}
+    os.environ.update(env or {})
+    try:
+        plan = B.Plan.from_case(case)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
     path, launches = plan.path()
     useful, algo_bytes = plan.work()
     _, _, _, _, dy_d, w_d, dx_d, _, _ = device_inputs(case, plan)
@@ -352,6 +362,7 @@ def measure_workload(B, case, steps, warmup, flush, stream, peaks, num_sms):
     roof["kernel_ms"] = kms
     return {"ms_per_step": ms, "tflops": useful / (ms * 1e-3) / 1e12, "gbs": algo_bytes / (ms * 1e-3) / 1e9,
             "dtype": case.dtype, "path": path, "launches_per_step": launches, "tile": list(plan.tile()),
+            "a_operand": plan.a_operand(), "k_splits": plan.k_splits(),
             "useful_flop": useful, "algo_bytes": algo_bytes, "steps": steps, "warmup": warmup,
             "roofline": roof}
 
@@ -462,7 +473,8 @@ def main():
                    "dil": list(case.dil), "groups": case.groups, "layout": case.layout,
                    "l2": "flushed before every step (512 MiB write, outside the step events)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "kernel_path": path, "useful_flop_per_step": useful, "algo_bytes_per_step": algo_bytes},
+                   "kernel_path": path, "tile": list(plan.tile()), "k_splits": plan.k_splits(),
+                   "useful_flop_per_step": useful, "algo_bytes_per_step": algo_bytes},
         "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
         "roofline": roof,
         "e2e": {"value": job_tflops(useful, world, e2e_mean), "unit": "TFLOP/s",
@@ -481,6 +493,27 @@ def main():
                 continue
             pw[c.name] = measure_workload(B, c, args.pw_steps, args.warmup, flush, stream, peaks, num_sms)
         line["per_workload"] = pw
+        # the shape-specialised SM-pair kernel (dy as a plain matrix, 2-D tiled
+        # loads) against the dynamic im2col kernel on the workloads it applies
+        # to -- the static-vs-dynamic comparison of "[igemm_dynamic] v4r1 bwd
+        # dynamic kernel" (dynamic within 10% of static there)
+        sd = {}
+        for c in wl.CASES:
+            pl = B.Plan.from_case(c)
+            dyn = pw[c.name]["ms_per_step"] if c.name in pw else mean_ms
+            os.environ["CONVBWD_DEBUG_A"] = "plain"
+            try:
+                eligible = B.Plan.from_case(c).a_operand() == "plain" and pl.a_operand() == "im2col"
+            finally:
+                os.environ.pop("CONVBWD_DEBUG_A", None)
+            if not eligible:
+                continue
+            spec = measure_workload(B, c, args.pw_steps, args.warmup, flush, stream, peaks, num_sms,
+                                    env={"CONVBWD_DEBUG_A": "plain"})
+            sd[c.name] = {"dynamic_ms": dyn, "specialised_ms": spec["ms_per_step"],
+                          "dynamic_over_specialised": dyn / spec["ms_per_step"],
+                          "specialised_tflops": spec["tflops"]}
+        line["static_vs_dynamic"] = sd
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # bounded oracle sample on the host cores (a reported baseline only)
         dts, fr, thr = [], 0.0, 1

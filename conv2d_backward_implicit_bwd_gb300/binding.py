@@ -24,7 +24,8 @@ EXPORTED = [
     "conv_bwd_data_subgemm_info", "conv_bwd_data_coverage", "conv_bwd_data_path", "conv_bwd_data_tile", "conv_bwd_data_work",
     "conv_bwd_data_run", "conv_bwd_data_run_host", "conv_bwd_data_get_status", "conv_bwd_data_set_timing",
     "conv_bwd_data_last_timing", "conv_bwd_data_selftest_wait_timeout", "conv_bwd_status_string",
-    "conv_bwd_data_version", "conv_bwd_data_run_noalloc", "conv_bwd_data_run_forward",
+    "conv_bwd_data_version", "conv_bwd_data_run_noalloc", "conv_bwd_data_run_forward", "conv_bwd_data_a_operand",
+    "conv_bwd_data_k_splits",
 ]
 
 
@@ -58,6 +59,8 @@ def _load():
         "conv_bwd_data_path": [vp, P(i32), P(i32)],
         "conv_bwd_data_tile": [vp, P(i32), P(i32), P(i32)],
         "conv_bwd_data_work": [vp, P(ctypes.c_double), P(ctypes.c_double)],
+        "conv_bwd_data_a_operand": [vp, P(i32)],
+        "conv_bwd_data_k_splits": [vp, P(i32)],
         "conv_bwd_data_run": [vp, vp, vp, vp, vp],
         "conv_bwd_data_run_forward": [vp, vp, vp, vp, vp],
         "conv_bwd_data_run_host": [vp, vp, vp, vp, vp, vp, vp, vp],
@@ -172,6 +175,19 @@ class Plan:
         m, n, k = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
         _check(_lib.conv_bwd_data_tile(self._h, ctypes.byref(m), ctypes.byref(n), ctypes.byref(k)), "tile")
         return m.value, n.value, k.value
+
+    def a_operand(self) -> str:
+        """How the GEMM kernel loads dy: "im2col", "plain" (2-D tiles of dy as a
+        matrix; the specialised kernel) or "gather"."""
+        m = ctypes.c_int32()
+        _check(_lib.conv_bwd_data_a_operand(self._h, ctypes.byref(m)), "a_operand")
+        return {0: "im2col", 1: "plain", 2: "gather"}[m.value]
+
+    def k_splits(self) -> int:
+        """SM pairs that share each tile of the split-K schedule (1: whole tiles)."""
+        m = ctypes.c_int32()
+        _check(_lib.conv_bwd_data_k_splits(self._h, ctypes.byref(m)), "k_splits")
+        return m.value
 
     def work(self):
         f, b = ctypes.c_double(), ctypes.c_double()

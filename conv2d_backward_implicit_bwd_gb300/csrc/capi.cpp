@@ -56,9 +56,14 @@ struct conv_bwd_plan_s {
     std::vector<CUtensorMap> tmap_a;      // per class (gemm_id order)
     bool im2col = false;                  // A rows by TMA im2col loads (else cp.async gather)
     bool two_sm = false;                  // 256x256 tiles on SM pairs (cta_group::2)
+    bool a_plain = false;                 // SM-pair kernel specialised for dy read as a plain matrix
+    bool grouped_tc = false;              // narrow groups on tcgen05 (block-diagonal B), else warp-level MMA
     int max_pairs = 0;                    // co-resident SM pairs of the 2-SM kernel
     float4 *d_partials = nullptr;         // stream-K workspace: per pair and CTA, one 128x256 fp32 tile
     int32_t *d_flags = nullptr;           // stream-K flags, tagged with the launch epoch
+    int32_t splitk = 1;                   // SM pairs per tile (split-K reduce-scatter), 1 = whole tiles
+    float4 *d_ws = nullptr;               // split-K workspace: fp32 partials of the other splits' column slices
+    int32_t *d_ws_flags = nullptr;        // split-K flags, one per (tile, split, CTA rank), tagged with the epoch
     int32_t epoch = 0;
     // forward convolution with the same geometry (the adjoint of run): maps
     // keyed by the x and w pointers
@@ -82,6 +87,9 @@ struct conv_bwd_plan_s {
     // twin, a pipelined run_host to its chunk plans.
     float *w_hi = nullptr, *w_lo = nullptr;
     bool owns_wsplit = false;
+#ifdef CBD_PHASE_TIMES
+    unsigned long long *d_phase = nullptr;  // instrumented build: per-CTA timeline of the tensor-core kernel
+#endif
     int32_t w_gkcyx = 0;  // 1: run() receives the filter as GKCYX (the NCHW parent's w)
     int32_t tf32_split = -1;  // tail split of the fp32 tensor-core schedule: -1 by cost, 0 never, 1 always
     std::mutex mu;
@@ -237,11 +245,28 @@ void im2col_corners(const Geom &g, const ClassDesc &c, int lo[2], int hi[2]) {
 }
 
 // One im2col map per class: 64 channels x 128 pixels per load, 128-byte
-// swizzle, pixels outside dy read as zero.
+// swizzle, pixels outside dy read as zero.  Plans specialised for a plain A
+// matrix get a 2-D tiled map of dy as {K, N*Ho*Wo} instead (box 64 x 128,
+// rows past the last pixel read as zero), one copy per class.
 bool encode_a_maps(conv_bwd_plan_s *p, const void *dy) {
+    const Geom &g = p->g;
+    if (p->a_plain) {
+        PFN_encodeTiled enc = get_encode_tiled();
+        if (!enc) return false;
+        p->tmap_a.resize(p->classes.size());
+        cuuint64_t dims[2] = {(cuuint64_t)g.K, (cuuint64_t)g.N * g.Ho * g.Wo};
+        cuuint64_t strides[1] = {(cuuint64_t)g.K * 2};
+        cuuint32_t box[2] = {64, 128};
+        cuuint32_t estr[2] = {1, 1};
+        for (size_t i = 0; i < p->classes.size(); ++i)
+            if (enc(&p->tmap_a[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(dy), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2_promotion(),
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return false;
+        return true;
+    }
     PFN_encodeIm2col enc = get_encode_im2col();
     if (!enc) return false;
-    const Geom &g = p->g;
     // 128-byte pixel rows: 64 bf16 channels, or 32 fp32 ones (fp32 tensor-core path)
     const bool f32 = p->desc.dtype == CONV_BWD_F32;
     const cuuint64_t es = f32 ? 4 : 2;
@@ -384,6 +409,17 @@ bool tf32_tail_split(const conv_bwd_plan_s *p, const ClassDesc *cls, size_t nc, 
     return tail > 0 && tail * 5 <= (int64_t)nsm * 4 && units >= 4LL * nsm;
 }
 
+// K splits of the SM-pair kernel's split-K schedule for this plan (1 = whole
+// tiles): CONVBWD_DEBUG_SPLITK=S forces S where the S * tiles units fit one
+// wave; otherwise none.
+int split_choice(const conv_bwd_plan_s *p) {
+    if (const char *f = env("CONVBWD_DEBUG_SPLITK")) {
+        const int S = std::atoi(f);
+        return S >= 2 && S <= 8 ? S : 1;
+    }
+    return 1;
+}
+
 int kHostChunks = 4;  // batch chunks of the pipelined host path (CONVBWD_DEBUG_HOST_CHUNKS overrides)
 
 // Batch chunks for the pipelined host path: 4 chunks of ceil(N/4) images when
@@ -518,6 +554,26 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                       d.Hi < (1 << 20) && d.Wi < (1 << 20) && d.stride_w <= 64 &&
                       d.N * d.Hi * ((d.Wi + 15) / 16) < (1LL << 31);  // item count (chunks of >= 16 pixels)
     if (grouped_ok) grouped_ok = grouped_layout(g).smem <= 200 * 1024;
+    // narrow groups on tcgen05: the groups of each 64-channel block folded into
+    // one GEMM with a block-diagonal B (resident in shared memory, one 8 KB tile
+    // per filter tap), A by TMA im2col as on the wide path
+    bool grouped_tc = d.dtype == CONV_BWD_BF16 && d.layout == CONV_BWD_NHWC_KYXC && g.Cg == g.Kg &&
+                      (g.Cg == 8 || g.Cg == 16 || g.Cg == 32) && d.C % 64 == 0 && d.Y * d.X <= 12 &&
+                      d.Hi < 16384 && d.Wi < 16384;
+    for (const ClassDesc &c : p->classes) {
+        int lo[2], hi[2];
+        im2col_corners(g, c, lo, hi);
+        for (int q = 0; q < 2; ++q)
+            if (lo[q] < -128 || lo[q] > 127 || hi[q] < -128 || hi[q] > 127) grouped_tc = false;
+        if ((c.taps_x - 1) * g.DW > 127 || (c.taps_y - 1) * g.DH > 127) grouped_tc = false;
+    }
+    // The warp-level MMA kernel stages each dy row once per item and reuses it
+    // for every tap; the tcgen05 kernel re-reads dy per tap from L2 and measured
+    // slower on the ResNeXt layer (78 vs 51 us), so it runs only where the
+    // warp-level kernel does not apply (C/G = 32) or when CONVBWD_DEBUG_GROUPED=tc.
+    const char *gk = env("CONVBWD_DEBUG_GROUPED");
+    if (grouped_ok && !(gk && !std::strcmp(gk, "tc"))) grouped_tc = false;
+    grouped_ok = grouped_ok || grouped_tc;
     // fp32 on the tensor cores (three-term TF32 split) for problems large
     // enough to pay for the filter split launch; NHWC/KYXC, 32-channel TMA
     // im2col blocks that stay inside a group, 16-byte pixel strides
@@ -537,6 +593,7 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                     : (grouped_ok ? CONV_BWD_PATH_GROUPED
                                   : (tf32_ok && tf32_big ? CONV_BWD_PATH_TF32 : CONV_BWD_PATH_SIMT));
     if (force && !std::strcmp(force, "simt")) p->path = CONV_BWD_PATH_SIMT;
+    p->grouped_tc = p->path == CONV_BWD_PATH_GROUPED && grouped_tc;
     p->bn = (p->path == CONV_BWD_PATH_TCGEN05) ? (g.Cg >= 256 ? 256 : 128)
                                                : (p->path == CONV_BWD_PATH_TF32 ? kTf32BN : 64);
     if (const char *f = env("CONVBWD_DEBUG_BN"))
@@ -591,6 +648,20 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
         if (p->two_sm && !std::strcmp(f, "512")) p->bn = 512;
     }
     if (const char *f = env("CONVBWD_DEBUG_STREAMK")) p->tf32_split = f[0] == '1' ? 1 : 0;
+    // Plain-matrix specialisation (SM-pair kernel): every class has one tap and
+    // its rows are all of dy's pixels in order, so A is dy viewed as the matrix
+    // {N*Ho*Wo, K} and loads as 2-D tiles (no im2col offsets).  Off by
+    // default (one dynamic kernel for every shape, as in the dynamic-kernel
+    // pull request); CONVBWD_DEBUG_A=plain selects it where it applies, and
+    // the benchmark reports both on the shapes that qualify.
+    if (p->two_sm) {
+        bool plain = true;
+        for (const ClassDesc &c : p->classes)
+            plain = plain && c.taps_y == 1 && c.taps_x == 1 && c.ht_lo == 0 && c.HT == g.Ho && c.wt_lo == 0 &&
+                    c.WT == g.Wo;
+        const char *f = env("CONVBWD_DEBUG_A");
+        p->a_plain = plain && f && !std::strcmp(f, "plain");
+    }
 
     // Schedule: classes with the longest reduction first (LPT), tiles of one
     // class contiguous; BM = 256 rows on SM pairs, 128 for the 1-SM
@@ -637,6 +708,12 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                 return CONV_BWD_ERR_CUDA;
             }
             p->has_device = true;
+#ifdef CBD_PHASE_TIMES
+            if (cudaMalloc(&p->d_phase, kPhaseLogCtas * kPhaseSlots * sizeof(unsigned long long)) != cudaSuccess) {
+                cudaGetLastError();
+                p->d_phase = nullptr;
+            }
+#endif
             const char *sk = env("CONVBWD_DEBUG_STREAMK");
             if (p->two_sm && sk && sk[0] == '1') {
                 // stream-K workspace: only for plans created with the opt-in stream-K
@@ -651,6 +728,39 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                     cudaFree(p->d_flags);
                     p->d_partials = nullptr;
                     p->d_flags = nullptr;
+                }
+            }
+            if (p->two_sm && !(sk && sk[0] == '1') && p->classes.size() <= (size_t)kMaxTcClasses) {
+                // Split-K with a reduce-scatter of the fp32 partials: S SM pairs per
+                // 256 x 512 tile, each over 1/S of the k-blocks, all tiles in one wave.
+                // The widest tile needs the fewest operand bytes per multiply-add (the
+                // SM pairs are bound by operand delivery), and the split gives a deep,
+                // short layer enough such tiles to fill the GPU.
+                int S = split_choice(p);
+                const int kbt = (g.Kg + 63) / 64;
+                for (const ClassDesc &c : p->classes)  // every split keeps at least two k-blocks
+                    if (c.taps_y * c.taps_x * kbt < 2 * S) S = 1;
+                if (S > 1) {
+                    const int bn_s = g.Cg > 256 ? 512 : 256;
+                    int64_t tiles = 0;
+                    for (const ClassDesc &c : p->classes)
+                        tiles += (int64_t)g.G * ((c.M + 255) / 256) * ((g.Cg + bn_s - 1) / bn_s);
+                    const size_t blk = (size_t)(bn_s / 4) * 128;
+                    const size_t ws = (size_t)tiles * 2 * (S - 1) * blk * sizeof(float4);
+                    const size_t nfl = (size_t)tiles * S * 2;
+                    if (tiles * S <= tc2_max_pairs(p->num_sms) && cudaMalloc(&p->d_ws, ws) == cudaSuccess &&
+                        cudaMalloc(&p->d_ws_flags, nfl * sizeof(int32_t)) == cudaSuccess &&
+                        cudaMemset(p->d_ws_flags, 0, nfl * sizeof(int32_t)) == cudaSuccess) {
+                        p->splitk = S;
+                        p->bn = bn_s;
+                        schedule(256);
+                    } else {
+                        cudaGetLastError();
+                        cudaFree(p->d_ws);
+                        cudaFree(p->d_ws_flags);
+                        p->d_ws = nullptr;
+                        p->d_ws_flags = nullptr;
+                    }
                 }
             }
             const size_t nsplit = (size_t)d.K * g.Cg * d.Y * d.X * sizeof(float);
@@ -734,8 +844,13 @@ conv_bwd_status conv_bwd_data_destroy(conv_bwd_plan p) {
         cudaGetDevice(&cur);
         if (cur != p->device) cudaSetDevice(p->device);
         if (p->owns_status) cudaFree(p->d_status);
+#ifdef CBD_PHASE_TIMES
+        cudaFree(p->d_phase);
+#endif
         cudaFree(p->d_partials);
         cudaFree(p->d_flags);
+        cudaFree(p->d_ws);
+        cudaFree(p->d_ws_flags);
         for (auto &e : p->ev)
             if (e) cudaEventDestroy(e);
         for (auto &e : p->hev)
@@ -801,9 +916,13 @@ conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t
     if (path) *path = p->path;
     int gemm_launches = p->classes.empty() ? 0 : 1;
     if (p->path == CONV_BWD_PATH_TCGEN05) gemm_launches = (int)((p->classes.size() + kMaxTcClasses - 1) / kMaxTcClasses);
-    // the grouped kernel writes every pixel; the tensor-core kernels zero uncovered pixels themselves
-    const bool fill = p->any_uncovered && (p->path == CONV_BWD_PATH_SIMT || p->classes.empty());
-    if (p->path == CONV_BWD_PATH_GROUPED) gemm_launches = 1;
+    // the warp-MMA narrow-group kernel writes every pixel; the tensor-core
+    // kernels zero uncovered pixels themselves; without any class the fill
+    // kernel alone runs
+    const bool mma_grouped = p->path == CONV_BWD_PATH_GROUPED && !p->grouped_tc;
+    const bool fill = p->any_uncovered && (p->path == CONV_BWD_PATH_SIMT || (p->classes.empty() && !mma_grouped));
+    if (p->path == CONV_BWD_PATH_GROUPED)
+        gemm_launches = p->grouped_tc ? (int)((p->classes.size() + kMaxTcClasses - 1) / kMaxTcClasses) : 1;
     if (p->path == CONV_BWD_PATH_TF32) {
         // the filter split, then per launch of up to kMaxTcClasses classes the
         // tensor-core kernel (which fills), preceded by the tile zeroing when its
@@ -830,9 +949,27 @@ conv_bwd_status conv_bwd_data_tile(const conv_bwd_plan p, int32_t *tile_m, int32
     if (!p) return CONV_BWD_ERR_INVALID_ARG;
     if (p->nhwc_plan) return conv_bwd_data_tile(p->nhwc_plan, tile_m, tile_n, sms);
     const bool tc = p->path == CONV_BWD_PATH_TCGEN05, grouped = p->path == CONV_BWD_PATH_GROUPED;
-    if (tile_m) *tile_m = grouped ? 0 : tc ? (p->two_sm ? 256 : 128) : p->path == CONV_BWD_PATH_TF32 ? 128 : 64;
-    if (tile_n) *tile_n = grouped ? 0 : p->bn;
+    if (tile_m) *tile_m = grouped ? (p->grouped_tc ? 128 : 0) : tc ? (p->two_sm ? 256 : 128)
+                                                                   : p->path == CONV_BWD_PATH_TF32 ? 128 : 64;
+    if (tile_n) *tile_n = grouped ? (p->grouped_tc ? 64 : 0) : p->bn;
     if (sms) *sms = tc && p->two_sm ? 2 : 1;
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_k_splits(const conv_bwd_plan p, int32_t *k_splits) {
+    if (!p || !k_splits) return CONV_BWD_ERR_INVALID_ARG;
+    if (p->nhwc_plan) return conv_bwd_data_k_splits(p->nhwc_plan, k_splits);
+    *k_splits = p->path == CONV_BWD_PATH_TCGEN05 ? p->splitk : 1;
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_a_operand(const conv_bwd_plan p, int32_t *a_mode) {
+    if (!p || !a_mode) return CONV_BWD_ERR_INVALID_ARG;
+    if (p->nhwc_plan) return conv_bwd_data_a_operand(p->nhwc_plan, a_mode);
+    const bool tc = p->path == CONV_BWD_PATH_TCGEN05 || p->path == CONV_BWD_PATH_TF32 || p->grouped_tc;
+    *a_mode = !tc ? CONV_BWD_A_GATHER
+                  : (p->a_plain ? CONV_BWD_A_PLAIN
+                                : (p->im2col || p->path != CONV_BWD_PATH_TCGEN05 ? CONV_BWD_A_IM2COL : CONV_BWD_A_GATHER));
     return CONV_BWD_OK;
 }
 
@@ -885,7 +1022,59 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
     }
     p->fill_ran = false;
     const uint64_t all_w = g.sw >= 64 ? ~0ull : ((1ull << g.sw) - 1);
-    if (p->path == CONV_BWD_PATH_GROUPED) {
+    if (p->path == CONV_BWD_PATH_GROUPED && p->grouped_tc && !p->classes.empty()) {
+        // 64-channel group blocks: the kernel sees G' = C / 64 groups of 64
+        // channels and builds each block's block-diagonal B from w itself
+        if (p->tmap_a_ptr != dy) {
+            if (!encode_a_maps(p, dy)) return CONV_BWD_ERR_CUDA;
+            p->tmap_a_ptr = dy;
+        }
+        Geom fg = g;
+        fg.G = g.C / 64;
+        fg.Cg = fg.Kg = 64;
+        if (p->timing) cudaEventRecord(p->ev[2], s);
+        for (size_t c0 = 0; c0 < p->sched.size(); c0 += kMaxTcClasses) {
+            TcParams tp;
+            std::memset(&tp, 0, sizeof(tp));
+            tp.dy = dy; tp.dx = dx; tp.w = w; tp.bd_cg = g.Cg;
+            tp.status = p->d_status; tp.wait_budget = p->wait_budget;
+            tp.g = fg;
+#ifdef CBD_PHASE_TIMES
+            if (p->d_phase && c0 == 0 &&
+                cudaMemsetAsync(p->d_phase, 0, kPhaseLogCtas * kPhaseSlots * sizeof(unsigned long long), s) ==
+                    cudaSuccess)
+                tp.phase_log = p->d_phase;
+#endif
+            tp.n_tiles = 1;
+            tp.kb_per_tap = 1;
+            tp.im2col = 1;
+            tp.fill = (c0 == 0 && p->any_uncovered) ? 1 : 0;
+            tp.cov_h = p->cov_h;
+            tp.cov_w = p->cov_w == all_w ? ~0ull : p->cov_w;
+            const size_t nc = std::min<size_t>(kMaxTcClasses, p->sched.size() - c0);
+            tp.num_classes = (int)nc;
+            int64_t units = 0;  // tiles of one group block
+            for (size_t i = 0; i < nc; ++i) {
+                const int idx = p->sched[c0 + i];
+                tp.cls[i] = p->classes[(size_t)idx];
+                tp.cls[i].m_tiles = (tp.cls[i].M + 127) / 128;
+                tp.cls[i].tile_begin = (int)units;
+                units += tp.cls[i].m_tiles;
+                tp.tmap_a[i] = p->tmap_a[(size_t)idx];
+            }
+            if (units * fg.G > 0x7fffffffLL) return CONV_BWD_ERR_UNSUPPORTED;
+            tp.interleave = 1;
+            for (size_t i = 1; i < nc; ++i) tp.interleave &= tp.cls[i].m_tiles == tp.cls[0].m_tiles;
+            tp.total_tiles = (int)(units * fg.G);
+            // each CTA keeps one group block; as many CTAs per block as fill the SMs
+            const int nsm = std::max(1, p->num_sms);
+            const int64_t per_gb = std::max<int64_t>(1, std::min<int64_t>(units, nsm / fg.G));
+            if (launch_tc_grouped(tp, (int)(per_gb * fg.G), s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        }
+        if (p->timing) cudaEventRecord(p->ev[3], s);
+        return CONV_BWD_OK;
+    }
+    if (p->path == CONV_BWD_PATH_GROUPED && !p->grouped_tc) {
         GroupedParams gp;
         std::memset(&gp, 0, sizeof(gp));
         gp.dy = dy; gp.w = w; gp.dx = dx; gp.g = g;
@@ -998,6 +1187,13 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             tp.n_tiles = (g.Cg + p->bn - 1) / p->bn;
             tp.kb_per_tap = (g.Kg + 63) / 64;
             tp.im2col = p->im2col ? 1 : 0;
+            tp.a_plain = p->a_plain ? 1 : 0;
+#ifdef CBD_PHASE_TIMES
+            if (p->d_phase && c0 == 0 &&
+                cudaMemsetAsync(p->d_phase, 0, kPhaseLogCtas * kPhaseSlots * sizeof(unsigned long long), s) ==
+                    cudaSuccess)
+                tp.phase_log = p->d_phase;
+#endif
             tp.fill = (c0 == 0 && p->any_uncovered) ? 1 : 0;  // first launch zeroes the uncovered pixels
             if (const char *f = env("CONVBWD_DEBUG_RASTER_M")) tp.raster_m = f[0] == '1' ? 1 : 0;
             tp.cov_h = p->cov_h;
@@ -1018,6 +1214,16 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             }
             tp.total_tiles = (int)total;
             tp.units_total = (int)std::min<int64_t>(units, 0x7fffffff);
+            if (p->two_sm && p->splitk > 1) {
+                // one unit per SM pair: split q of tile t on pair t * S + q
+                tp.splitk = p->splitk;
+                tp.partials = p->d_ws;
+                tp.flags = p->d_ws_flags;
+                p->epoch = p->epoch >= 0x7ffffffe ? 1 : p->epoch + 1;
+                tp.epoch = p->epoch;
+                if (launch_tc2(tp, p->bn, (int)(2 * total * p->splitk), s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+                continue;
+            }
             if (p->two_sm) {
                 const int maxp = tc2_max_pairs(p->num_sms);
                 int pairs = (int)std::min<int64_t>(total, maxp);
@@ -1219,6 +1425,20 @@ conv_bwd_status conv_bwd_data_selftest_wait_timeout(void *stream, int64_t budget
 }
 
 }  // extern "C"
+
+#ifdef CBD_PHASE_TIMES
+// Instrumented build only: copy the last tensor-core launch's per-CTA timeline
+// (kPhaseSlots globaltimer stamps per CTA, 0 where a slot was not reached) into
+// `out` (n_ctas rows); synchronises the device.
+extern "C" conv_bwd_status conv_bwd_data_debug_phase_log(conv_bwd_plan p, unsigned long long *out, int32_t n_ctas) {
+    if (!p || !out || n_ctas <= 0 || n_ctas > kPhaseLogCtas || !p->d_phase) return CONV_BWD_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return CONV_BWD_ERR_CUDA;
+    if (cudaMemcpy(out, p->d_phase, (size_t)n_ctas * kPhaseSlots * sizeof(unsigned long long),
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+        return CONV_BWD_ERR_CUDA;
+    return CONV_BWD_OK;
+}
+#endif
 
 namespace cbd {
 

@@ -62,4 +62,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Timeline stamp of the instrumented build (-DCBD_PHASE_TIMES): globaltimer
+// (ns) into slot `slot` of this CTA's row of `log`.  Compiles to nothing
+// otherwise.
+#ifdef CBD_PHASE_TIMES
+#define CBD_PHASE(params, slot)                                                                 \
+    do {                                                                                        \
+        if ((params).phase_log) {                                                               \
+            unsigned long long t_;                                                              \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                              \
+            (params).phase_log[(size_t)blockIdx.x * kPhaseSlots + (slot)] = t_;                 \
+        }                                                                                       \
+    } while (0)
+#else
+#define CBD_PHASE(params, slot) \
+    do {                        \
+    } while (0)
+#endif
+
 }  // namespace cbd

@@ -83,16 +83,52 @@ struct TcParams {  // 128-byte aligned through CUtensorMap
     int32_t kb_per_tap;   // ceil(Kg / 64)
     int32_t total_tiles;
     int32_t im2col;       // 1: A rows by TMA im2col loads (tmap_a), 0: cp.async gather
+    int32_t a_plain;      // 1 (SM-pair kernel): every class reads dy as a plain matrix {K, N*Ho*Wo} (tmap_a 2-D)
     int32_t fill;         // 1: the epilogue warps also zero the dx pixels no class writes
     int32_t raster_m;     // 1: consecutive tiles walk m-blocks first (else n-blocks first)
     int32_t streamk;      // 1: workers take equal ranges of (tile, k-block) units (2-SM kernel)
+    int32_t splitk;       // S > 1 (2-SM kernel): S SM pairs per tile, each a 1/S range of its k-blocks; the
+                          // pairs exchange fp32 partials (workspace `partials`) and each stores 1/S of the columns
     int32_t units_total;  // sum over tiles of their k-blocks
     int32_t epoch;        // tag of this launch's partial-tile flags (never 0)
     float4 *partials;     // stream-K: per worker and CTA rank, one 128 x 256 fp32 partial tile
     int32_t *flags;       // stream-K: per worker and CTA rank, == epoch once its partial is written
     uint64_t cov_h, cov_w;  // residues of rows / columns some class writes (as in FillParams)
+    const void *w;        // narrow-group kernel: the filter (KYXC), read to build its block-diagonal B
+    int32_t bd_cg;        // narrow-group kernel: channels per real group (g holds the folded 64-channel blocks)
+    int32_t interleave;   // narrow-group kernel: classes of equal m-blocks interleaved tile by tile
+#ifdef CBD_PHASE_TIMES
+    unsigned long long *phase_log;  // instrumented build: per CTA, kPhaseSlots globaltimer stamps (ns)
+#endif
     ClassDesc cls[kMaxTcClasses];
 };
+
+#ifdef CBD_PHASE_TIMES
+// Instrumented build only (compiled with -DCBD_PHASE_TIMES): timeline slots of
+// the tensor-core kernels, one globaltimer stamp each per CTA.
+constexpr int kPhaseSlots = 24;
+constexpr int kPhaseLogCtas = 1024;  // CTAs a timeline buffer holds (grids are at most one CTA per SM)
+enum : int {
+    kPhEntry = 0,       // kernel entry (thread 0)
+    kPhSetup = 1,       // barriers initialised, TMEM allocated, CTAs synchronised
+    kPhFillDone = 2,    // epilogue warps finished zeroing uncovered pixels
+    kPhFirstIssue = 3,  // A producer issued its first load
+    kPhFirstFull = 4,   // MMA thread saw the first stage land
+    kPhMma0Done = 5,    // MMA thread committed the first tile
+    kPhEpi0Start = 6,   // epilogue saw the first accumulator
+    kPhEpi0Done = 7,    // epilogue stored the first tile (warp 0)
+    kPhMma1Start = 8,   // MMA thread started the second tile
+    kPhEpi1Start = 9,
+    kPhEpi1Done = 10,
+    kPhMmaLast = 11,    // MMA thread committed its last tile
+    kPhEpiLast = 12,    // epilogue stored its last tile
+    kPhExit = 13,       // after the final CTA barrier (thread 0)
+    kPhLastIssue = 14,  // A producer issued its last load
+    kPhProdStart = 15,  // A producer about to decode its first tile
+    kPhProdWaited = 16, // A producer passed its first empty-slot wait
+    kPhBFirst = 17,     // first B producer issued its first load
+};
+#endif
 
 // Forward-convolution kernel parameters (x has dx's shape, y has dy's shape).
 struct FwdParams {
@@ -150,6 +186,9 @@ cudaError_t launch_grouped(GroupedParams &p, int num_sms, cudaStream_t s);
 cudaError_t launch_tc(const TcParams &p, int bn, int grid, cudaStream_t s);
 cudaError_t launch_tc2(const TcParams &p, int bn, int grid, cudaStream_t s);  // grid: 2 CTAs per SM pair
 cudaError_t launch_fwd(const FwdParams &p, int bn, int grid, cudaStream_t s);
+// narrow groups on tcgen05: 64-channel group blocks, block-diagonal B resident per CTA
+cudaError_t launch_tc_grouped(const TcParams &p, int grid, cudaStream_t s);
+size_t tc_grouped_smem_bytes(int taps);
 // out[b][c][r] = in[b][r][c] for bf16 elements (layout changes of NCHW/GKCYX problems)
 cudaError_t launch_transpose_b16(const void *in, void *out, int64_t batch, int64_t R, int64_t Cc, int num_sms,
                                  cudaStream_t s);

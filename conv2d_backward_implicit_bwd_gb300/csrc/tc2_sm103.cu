@@ -35,6 +35,10 @@
 
 namespace cbd {
 
+// First column of split s's slice of a BN-wide tile cut into S slices
+// (multiples of 64 columns; slice S - 1 ends at BN).
+__device__ __forceinline__ int split_col(int s, int S, int BN) { return (s * BN / S) / 64 * 64; }
+
 template <int BN_>
 struct Tc2Cfg {
     static constexpr int BN = BN_;          // tile width of the pair: 128, 256 or 512
@@ -66,11 +70,18 @@ struct Tc2Cfg {
     static constexpr int THREADS = 32 * (B_WARP + B_WARPS);
 };
 
-template <int BN_>
+// PLAIN: the specialisation for plans whose every class reads dy as a plain
+// matrix (one tap per class, the class rows covering all of dy's pixels in
+// order, e.g. 1x1 filters and the 1x2 stride-(1,2) layer): A rows come from a
+// 2-D tiled map {K, N*Ho*Wo} at row m, with no im2col offsets.  The dynamic
+// kernel (PLAIN = false) serves every shape with the same tiles.
+template <int BN_, bool PLAIN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS, 1)
-    tc2_dgrad_kernel(const __grid_constant__ TcParams p) {
+    tc2_dgrad_kernel(const __grid_constant__ TcParams pm) {
     using Cfg = Tc2Cfg<BN_>;
     constexpr int S = Cfg::STAGES;
+    __shared__ __align__(16) uint8_t s_tail[kTcTailBytes];
+    const TcParams &p = stage_param_tail(pm, s_tail);  // read only after the cluster barrier below
     constexpr int BN = Cfg::BN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -90,6 +101,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
     const Geom &g = p.g;
     // scheduling unit: the pair (cluster of two CTAs)
     const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
+    if (threadIdx.x == 0) CBD_PHASE(pm, kPhEntry);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -109,14 +121,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
         tc_fence_before();
     }
     if (warp == 4 && lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_w)) : "memory");
-        for (int ci = 0; ci < p.num_classes; ++ci)
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_a[ci])) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pm.tmap_w)) : "memory");
+        for (int ci = 0; ci < pm.num_classes; ++ci)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pm.tmap_a[ci])) : "memory");
     }
     // barriers of both CTAs initialised and TMEM allocated before any remote operation
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) CBD_PHASE(pm, kPhSetup);
     if (threadIdx.x == 0 && !leader) {
         // the pair's MMAs write this CTA's rows at the leader's TMEM address
         if (ld_shared_cluster_u32(mapa_shared(smem_u32(tmem_slot), pl)) != tmem_base)
@@ -133,6 +146,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
             const uint32_t full_leader0 = mapa_shared(full0, pl);
             uint32_t it = 0;
             bool ok = true, issued = false;
+            if (do_a) CBD_PHASE(pm, kPhProdStart);
             SegmentIter segs(p, pair, npairs);
             Segment sg;
             while (ok && segs.next(p, sg)) {
@@ -143,7 +157,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 const int n0 = m0 / HTWT, rem = m0 - n0 * HTWT;
                 const int bh = c.ht_lo + rem / c.WT - (c.taps_y - 1) * g.DH;
                 const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
-                const CUtensorMap *amap = &p.tmap_a[tcd.ci];
+                const CUtensorMap *amap = &pm.tmap_a[tcd.ci];
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const int tap = kb / p.kb_per_tap;
                     const int k0 = (kb - tap * p.kb_per_tap) * 64;
@@ -155,27 +169,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                         break;
                     }
                     const uint32_t bar = full_leader0 + 8 * s;
+                    if (do_a && it == 0) CBD_PHASE(pm, kPhProdWaited);
                     // (B loads of a split producer may complete before this arrive:
                     // the transaction count dips below zero while the arrival is
                     // still pending, so the phase cannot complete early)
                     if (do_a) {
                         if (leader)
                             mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(2 * (Cfg::A_BYTES + Cfg::B_BYTES)));
-                        tma_load_im2col_pair(smem_u32(sA + s * Cfg::A_BYTES), amap, bar, tcd.gi * g.Kg + k0, bw, bh,
-                                             n0, (uint16_t)((c.taps_x - 1 - i) * g.DW),
-                                             (uint16_t)((c.taps_y - 1 - j) * g.DH));
+                        if constexpr (PLAIN)
+                            tma_load_2d_pair(smem_u32(sA + s * Cfg::A_BYTES), amap, bar, tcd.gi * g.Kg + k0, m0);
+                        else
+                            tma_load_im2col_pair(smem_u32(sA + s * Cfg::A_BYTES), amap, bar, tcd.gi * g.Kg + k0, bw,
+                                                 bh, n0, (uint16_t)((c.taps_x - 1 - i) * g.DW),
+                                                 (uint16_t)((c.taps_y - 1 - j) * g.DH));
+                        if (it == 0) CBD_PHASE(pm, kPhFirstIssue);
                     }
                     const uint32_t bdst = smem_u32(sB + s * Cfg::B_BYTES);
                     // box q feeds MMA q / QPM: this CTA's half of that MMA's columns
                     for (int cb = cb_lo; cb < cb_hi; ++cb) {
                         const int col = tcd.nb * BN + (cb / Cfg::QPM) * Cfg::MMA_N + (int)rank * (Cfg::MMA_N / 2) +
                                         (cb % Cfg::QPM) * 64;
-                        tma_load_5d_pair(bdst + cb * 8192, &p.tmap_w, bar, col, c.tx + g.XT * i, c.ty + g.YT * j, k0,
+                        tma_load_5d_pair(bdst + cb * 8192, &pm.tmap_w, bar, col, c.tx + g.XT * i, c.ty + g.YT * j, k0,
                                          tcd.gi);
                     }
+                    if (warp == Cfg::B_WARP && it == 0) CBD_PHASE(pm, kPhBFirst);
                     issued = true;
                 }
             }
+            if (do_a && issued) CBD_PHASE(pm, kPhLastIssue);
             if (!ok && issued) {
                 for (int q = 0; q < 100; ++q) __nanosleep(1000);
             }
@@ -199,6 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                     break;
                 }
                 tc_fence_after();
+                if (tc == 1) CBD_PHASE(pm, kPhMma1Start);
                 const uint32_t d_tmem = tmem_base + b * BN;
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const uint32_t s = it % S, ph = (it / S) & 1;
@@ -208,6 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                         ok = false;
                         break;
                     }
+                    if (it == 0) CBD_PHASE(pm, kPhFirstFull);
                     // descriptors: start address in 16-byte units in the low bits; k step of
                     // 16 elements = 32 bytes in A (K-major), 16 rows = 2048 bytes in B (MN-major)
                     const uint64_t ad0 = a_desc0 + (uint64_t)((s * Cfg::A_BYTES) >> 4);
@@ -225,6 +248,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 }
                 if (!ok) break;
                 tc_commit2_mc(tfull0 + 8 * b, (uint16_t)0x3);
+                if (tc == 0) CBD_PHASE(pm, kPhMma0Done);
+                CBD_PHASE(pm, kPhMmaLast);
             }
             if (!ok && issued) {
                 for (int q = 0; q < 100; ++q) __nanosleep(1000);
@@ -238,6 +263,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
         const uint32_t tempty_leader0 = mapa_shared(tempty0, pl);
         uint32_t tc = 0;
         if (p.fill) fill_uncovered(p, threadIdx.x, 128);  // threads 0..127 are the epilogue warps
+        if (threadIdx.x == 0) CBD_PHASE(pm, kPhFillDone);
         SegmentIter segs(p, pair, npairs);
         Segment sg;
         const size_t slot_f4 = (size_t)(BN / 4) * 128;  // one CTA's 128 x BN fp32 partial, in float4
@@ -248,18 +274,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
             bool ok = mbar_wait_bounded(tfull0 + 8 * b, tph, p.wait_budget, abort_flag, p.status, kDevTimeoutEpilogue);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
+            if (threadIdx.x == 0 && tc < 2) CBD_PHASE(pm, tc == 0 ? kPhEpi0Start : kPhEpi1Start);
             const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + b * BN;
-            if (!sg.owner) {
-                // stream-K contributor: park the fp32 partial, then raise this CTA's flag
-                store_partial_rows<BN>(tbase, row, p.partials + (size_t)(pair * 2 + rank) * slot_f4);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);
-                __threadfence();
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (threadIdx.x == 0) st_release_gpu(p.flags + pair * 2 + rank, p.epoch);
-                continue;
-            }
             const int m = tcd.mb * 256 + (int)rank * 128 + row;
             const bool rvalid = m < c.M;
             int64_t off = 0;
@@ -270,6 +286,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 const int hi = (c.ht_lo + rem / c.WT) * g.sh + c.ty * g.dh - g.ph;
                 const int wi = (c.wt_lo + rem % c.WT) * g.sw + c.tx * g.dw - g.pw;
                 off = (((int64_t)n * g.Hi + hi) * g.Wi + wi) * g.C + (int64_t)tcd.gi * g.Cg + (int64_t)tcd.nb * BN;
+            }
+            if (p.splitk > 1) {
+                // split-K reduce-scatter: column slice s of the tile is stored by
+                // the tile's split s.  Every split parks its fp32 partial of the
+                // other slices in the workspace (per tile: [CTA rank][contributor]
+                // blocks of BN/4 x 128 float4, the contributor index skipping the
+                // slice's own split), raises its flag, then adds the other splits'
+                // partials of its own slice while draining it to dx.
+                const int S = p.splitk, q = sg.split;
+                const size_t blk = (size_t)(BN / 4) * 128;
+                float4 *tile_ws = p.partials + (size_t)sg.t * 2 * (S - 1) * blk;
+                for (int s2 = 0; s2 < S; ++s2) {
+                    if (s2 == q) continue;
+                    const int lo = split_col(s2, S, BN), hi = split_col(s2 + 1, S, BN);
+                    const int r = q < s2 ? q : q - 1;
+                    store_partial_chunks(tbase + lo, (hi - lo) / 64, row,
+                                         tile_ws + ((size_t)rank * (S - 1) + r) * blk + (size_t)(lo / 4) * 128);
+                }
+                __threadfence();
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (threadIdx.x == 0) {
+                    st_release_gpu(p.flags + ((size_t)sg.t * S + q) * 2 + rank, p.epoch);
+                    // the other splits of this tile (same CTA rank), bounded wait each
+                    for (int s2 = 0; s2 < S; ++s2) {
+                        if (s2 == q) continue;
+                        const int32_t *f = p.flags + ((size_t)sg.t * S + s2) * 2 + rank;
+                        const long long t0 = clock64();
+                        while (ld_acquire_gpu(f) != p.epoch) {
+                            if (clock64() - t0 > p.wait_budget) {
+                                record_status(p.status, kDevTimeoutPartial);
+                                break;
+                            }
+                        }
+                    }
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                for (int s2 = 0; s2 < S; ++s2)  // each thread's own acquire of the partials it reads
+                    if (s2 != q) (void)ld_acquire_gpu(p.flags + ((size_t)sg.t * S + s2) * 2 + rank);
+                const int lo = split_col(q, S, BN), hi = split_col(q + 1, S, BN);
+                epilogue_chunks(tbase + lo, (hi - lo) / 64, stage + warp * 4096, lane, rvalid, off + lo,
+                                tcd.nb * BN + lo, g.Cg, dx, tile_ws + (size_t)rank * (S - 1) * blk + (size_t)(lo / 4) * 128,
+                                S - 1, blk, row);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);
+                continue;
+            }
+            if (!sg.owner) {
+                // stream-K contributor: park the fp32 partial, then raise this CTA's flag
+                store_partial_rows<BN>(tbase, row, p.partials + (size_t)(pair * 2 + rank) * slot_f4);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);
+                __threadfence();
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (threadIdx.x == 0) st_release_gpu(p.flags + pair * 2 + rank, p.epoch);
+                continue;
             }
             const int nparts = pair - sg.q_first;
             if (nparts > 0) {
@@ -291,37 +364,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);
+            if (threadIdx.x == 0) {
+                if (tc < 2) CBD_PHASE(pm, tc == 0 ? kPhEpi0Done : kPhEpi1Done);
+                CBD_PHASE(pm, kPhEpiLast);
+            }
         }
     }
 
     // no remote arrive or MMA may target a CTA that has left
     cluster_sync_all();
+    if (threadIdx.x == 0) CBD_PHASE(pm, kPhExit);
     if (warp == Cfg::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc2(tmem_base, Cfg::TMEM_COLS);
     }
 }
 
-template <int BN>
+template <int BN, bool PLAIN>
 static cudaError_t launch_tc2_bn(const TcParams &p, int grid, cudaStream_t s) {
     using Cfg = Tc2Cfg<BN>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(tc2_dgrad_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(tc2_dgrad_kernel<BN, PLAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    tc2_dgrad_kernel<BN><<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(p);
+    tc2_dgrad_kernel<BN, PLAIN><<<grid, Cfg::THREADS, Cfg::SMEM, s>>>(p);
     return cudaGetLastError();
+}
+
+template <bool PLAIN>
+static cudaError_t launch_tc2_a(const TcParams &p, int bn, int grid, cudaStream_t s) {
+    if (bn == 512) return launch_tc2_bn<512, PLAIN>(p, grid, s);
+    return bn == 256 ? launch_tc2_bn<256, PLAIN>(p, grid, s) : launch_tc2_bn<128, PLAIN>(p, grid, s);
 }
 
 cudaError_t launch_tc2(const TcParams &p, int bn, int grid, cudaStream_t s) {
     if (grid <= 0 || p.total_tiles <= 0) return cudaSuccess;
-    if (bn == 512) return launch_tc2_bn<512>(p, grid, s);
-    return bn == 256 ? launch_tc2_bn<256>(p, grid, s) : launch_tc2_bn<128>(p, grid, s);
+    return p.a_plain ? launch_tc2_a<true>(p, bn, grid, s) : launch_tc2_a<false>(p, bn, grid, s);
 }
 
 // SM pairs (clusters of two CTAs, one CTA per SM) that can be resident at once.
@@ -331,7 +414,7 @@ int tc2_max_pairs(int num_sms) {
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
     using Cfg = Tc2Cfg<256>;
-    cudaFuncSetAttribute(tc2_dgrad_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    cudaFuncSetAttribute(tc2_dgrad_kernel<256, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
@@ -344,7 +427,8 @@ int tc2_max_pairs(int num_sms) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, tc2_dgrad_kernel<256>, &cfg) != cudaSuccess || clusters <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, tc2_dgrad_kernel<256, false>, &cfg) != cudaSuccess ||
+        clusters <= 0) {
         cudaGetLastError();
         clusters = num_sms / 2;
     }

@@ -5,6 +5,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "device_util.cuh"
@@ -211,11 +212,11 @@ __device__ __forceinline__ void stage_half(const uint32_t (&v)[32], uint32_t sba
     }
 }
 
-template <int BN>
-__device__ __forceinline__ void epilogue_rows(uint32_t taddr, uint8_t *stage, int lane, bool rvalid, int64_t off,
-                                              int col0, int Cg, __nv_bfloat16 *dx, const float4 *parts = nullptr,
-                                              int nparts = 0, size_t pstride = 0, int prow = 0) {
-    constexpr int NC = BN / 64;
+// (NC 64-column chunks from taddr; epilogue_rows<BN> drains BN columns)
+__device__ __forceinline__ void epilogue_chunks(uint32_t taddr, int NC, uint8_t *stage, int lane, bool rvalid,
+                                                int64_t off, int col0, int Cg, __nv_bfloat16 *dx,
+                                                const float4 *parts = nullptr, int nparts = 0, size_t pstride = 0,
+                                                int prow = 0) {
     const uint32_t sbase = smem_u32(stage);
     int64_t roff[8];
     bool rok[8];
@@ -258,12 +259,19 @@ __device__ __forceinline__ void epilogue_rows(uint32_t taddr, uint8_t *stage, in
     }
 }
 
-// Park one warp's 32 accumulator rows as an fp32 partial tile (stream-K
-// contributor): column chunk c of 4 floats of row r at slot[c * 128 + r].
 template <int BN>
-__device__ __forceinline__ void store_partial_rows(uint32_t taddr, int prow, float4 *slot) {
+__device__ __forceinline__ void epilogue_rows(uint32_t taddr, uint8_t *stage, int lane, bool rvalid, int64_t off,
+                                              int col0, int Cg, __nv_bfloat16 *dx, const float4 *parts = nullptr,
+                                              int nparts = 0, size_t pstride = 0, int prow = 0) {
+    epilogue_chunks(taddr, BN / 64, stage, lane, rvalid, off, col0, Cg, dx, parts, nparts, pstride, prow);
+}
+
+// Park one warp's 32 accumulator rows (NC 64-column chunks from taddr) as an
+// fp32 partial tile (stream-K contributor, split-K scatter): column chunk c
+// of 4 floats of row r at slot[c * 128 + r].
+__device__ __forceinline__ void store_partial_chunks(uint32_t taddr, int NC, int prow, float4 *slot) {
 #pragma unroll 1
-    for (int cc = 0; cc < BN / 64; ++cc) {
+    for (int cc = 0; cc < NC; ++cc) {
         uint32_t v[64];
         tmem_ld64(taddr + cc * 64, v);
 #pragma unroll
@@ -272,6 +280,10 @@ __device__ __forceinline__ void store_partial_rows(uint32_t taddr, int prow, flo
                 make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
                             __uint_as_float(v[4 * i + 3]));
     }
+}
+template <int BN>
+__device__ __forceinline__ void store_partial_rows(uint32_t taddr, int prow, float4 *slot) {
+    store_partial_chunks(taddr, BN / 64, prow, slot);
 }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
@@ -346,6 +358,33 @@ __device__ __forceinline__ void tma_load_im2col_pair(uint32_t dst, const CUtenso
         : "memory");
 }
 
+// Pair-mode 2-D tile load (rows of a plain matrix): box at (c0 = column,
+// c1 = row), bytes completing on the pair leader's barrier.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Kernel parameters after the tensor maps, staged in shared memory at kernel
+// entry: every role then reads the class table and geometry from shared
+// memory instead of walking chains of dependent parameter-cache misses
+// (which held the first TMA issue back by ~1.8 us after the CTA had set up).
+// All threads copy; the returned view is valid after the kernel's next
+// CTA-wide barrier.  The tensor maps stay in parameter space (TMA reads them
+// there), so map addresses must still be taken from the kernel parameter.
+constexpr int kTcTailOffset = (int)offsetof(TcParams, dy);
+constexpr int kTcTailBytes = (int)sizeof(TcParams) - kTcTailOffset;
+static_assert(kTcTailOffset % 16 == 0 && kTcTailBytes % 16 == 0, "parameter tail must copy as 16-byte words");
+__device__ __forceinline__ const TcParams &stage_param_tail(const TcParams &pm, uint8_t *buf) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(&pm) + kTcTailOffset);
+    uint4 *dst = reinterpret_cast<uint4 *>(buf);
+    for (int i = threadIdx.x; i < kTcTailBytes / 16; i += blockDim.x) dst[i] = src[i];
+    return *reinterpret_cast<const TcParams *>(buf - kTcTailOffset);
+}
+
 // Zero the dx pixels that no residue class writes (bf16 NHWC, 16-byte
 // stores), spread over the CTAs of the launch: CTA b takes dx rows b,
 // b + gridDim.x, ...; a row no class writes is one contiguous run, a written
@@ -380,6 +419,7 @@ struct Segment {
     int t, kb0, kb1;
     bool owner;
     int q_first;
+    int split;  // split-K: this worker's index among the tile's splits
 };
 
 __device__ __forceinline__ int class_of_tile(const TcParams &p, int t) {
@@ -404,6 +444,22 @@ struct SegmentIter {
         return p.cls[ci].taps_y * p.cls[ci].taps_x * p.kb_per_tap;
     }
     __device__ __forceinline__ bool next(const TcParams &p, Segment &sg) {
+        if (p.splitk > 1) {
+            // split-K: worker w takes split w % S of tile w / S (one unit per
+            // worker, all units in one wave)
+            if (next_t < 0 || w >= p.total_tiles * p.splitk) return false;
+            const int S = p.splitk;
+            sg.t = w / S;
+            sg.split = w - sg.t * S;
+            const int n = nkb(p, class_of_tile(p, sg.t));
+            sg.kb0 = (int)((int64_t)sg.split * n / S);
+            sg.kb1 = (int)((int64_t)(sg.split + 1) * n / S);
+            sg.owner = true;
+            sg.q_first = w;
+            next_t = -1;
+            return true;
+        }
+        sg.split = 0;
         if (!p.streamk) {
             if (next_t >= p.total_tiles) return false;
             sg.t = next_t;

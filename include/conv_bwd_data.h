@@ -98,7 +98,9 @@ typedef struct conv_bwd_plan_s *conv_bwd_plan;
 typedef enum {
     CONV_BWD_PATH_TCGEN05 = 0, /* bf16: persistent tcgen05/TMEM implicit GEMM */
     CONV_BWD_PATH_SIMT = 1,    /* fp32 (or bf16 fallback): CUDA-core tiled implicit GEMM */
-    CONV_BWD_PATH_GROUPED = 2, /* bf16, C/G = K/G in {8, 16}, G % 8 == 0: memory-bound warp-MMA kernel */
+    CONV_BWD_PATH_GROUPED = 2, /* bf16 narrow groups, C/G = K/G: in {8, 16} with G % 8 == 0 the memory-bound
+                                  warp-MMA kernel; C/G = 32 (C % 64 == 0, <= 12 filter taps) the tcgen05
+                                  kernel with the groups of each 64-channel block in a block-diagonal B */
     CONV_BWD_PATH_TF32 = 3     /* fp32 NHWC/KYXC with >= 1e9 useful FLOP, K, C, C/G, K/G multiples of 4
                                   (K/G of 32 when G > 1): tcgen05 kind::tf32 with a three-term split */
 } conv_bwd_path;
@@ -121,6 +123,9 @@ typedef enum {
  *                                    tail split always / never
  *   CONVBWD_DEBUG_NO_WSPLIT=1        fp32 tensor-core plans behave as if the split filter could
  *                                    not be allocated (CUDA-core fallback)
+ *   CONVBWD_DEBUG_A=plain            plain-matrix A specialisation where it applies (see below)
+ *   CONVBWD_DEBUG_SPLITK=S           split-K over S SM pairs per tile where all units fit one wave
+ *   CONVBWD_DEBUG_GROUPED=tc         narrow groups on the tcgen05 block-diagonal kernel where it applies
  *   CONVBWD_DEBUG_RASTER_M=1         tiles walk m-blocks first
  *   CONVBWD_DEBUG_GRID=n             cap the 1-SM kernel's grid
  *   CONVBWD_DEBUG_L2PROMO=0|1       TMA L2 promotion none / 128 B (default 256 B)
@@ -194,6 +199,31 @@ conv_bwd_status conv_bwd_data_run_forward(conv_bwd_plan plan, const void *x, con
  * kernel, else 1).  The grouped kernel reports 0 x 0 (it has no tiles).  Any
  * output pointer may be NULL. */
 conv_bwd_status conv_bwd_data_tile(const conv_bwd_plan plan, int32_t *tile_m, int32_t *tile_n, int32_t *sms_per_tile);
+
+/* K splits of the plan's SM-pair tensor-core schedule: 1 = every 256-row tile
+ * computed whole by one SM pair; S > 1 = split-K with a reduce-scatter: each
+ * 256 x 512 (or x 256) tile is shared by S SM pairs, each accumulating 1/S of
+ * its k-blocks, which then exchange fp32 partials through a plan-owned
+ * workspace (allocated by create) so that each pair adds and stores 1/S of
+ * the tile's columns.  Used where the tiles alone cannot fill the GPU; all
+ * tiles then run in one wave.  Other paths report 1.  INVALID_ARG for NULL. */
+conv_bwd_status conv_bwd_data_k_splits(const conv_bwd_plan plan, int32_t *k_splits);
+
+/* How the plan's GEMM kernel loads its A operand (dy rows):
+ *   CONV_BWD_A_IM2COL  TMA im2col loads, one map per residue class (the dynamic
+ *                      kernel: any shape, the tap as the im2col offset);
+ *   CONV_BWD_A_PLAIN   2-D tiled TMA loads of dy as the matrix {N*Ho*Wo, K}: the
+ *                      SM-pair kernel's compile-time specialisation for plans whose
+ *                      every class has one tap and covers all of dy's pixels in
+ *                      order (1x1 filters, the 1x2 stride-(1,2) layer); selected
+ *                      by CONVBWD_DEBUG_A=plain at create.  It plays the "static"
+ *                      kernel against the dynamic one of "[igemm_dynamic] v4r1 bwd
+ *                      dynamic kernel" (dynamic within 10% of static);
+ *   CONV_BWD_A_GATHER  per-thread gathers (cp.async producers, CUDA cores, the
+ *                      narrow-group kernel).
+ * INVALID_ARG for a NULL argument. */
+typedef enum { CONV_BWD_A_IM2COL = 0, CONV_BWD_A_PLAIN = 1, CONV_BWD_A_GATHER = 2 } conv_bwd_a_mode;
+conv_bwd_status conv_bwd_data_a_operand(const conv_bwd_plan plan, int32_t *a_mode);
 
 /* Useful work: 2 * N * K * (C/G) * Th * Tw floating-point operations, where
  * Th = #{(ho, y): 0 <= ho*sh - ph + y*dh < Hi} counts only taps that land

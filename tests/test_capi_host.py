@@ -207,3 +207,23 @@ def test_status_strings(B):
     for s in range(7):
         assert B.status_string(s).startswith("CONV_BWD_")
     assert B.lib().conv_bwd_data_version() >= 100
+
+
+@pytest.mark.parametrize("name,eligible", [("bf16_16x1x512x2048", True), ("bf16_32x14x14_1024", True),
+                                           ("bf16_32x28x28x512", False), ("bf16_32x57x57x128", False)])
+def test_plain_matrix_specialisation_eligibility(B, monkeypatch, name, eligible):
+    """The plain-matrix A specialisation applies only where every class has one
+    tap and its rows are all of dy's pixels in order (checked here by
+    enumerating the classes); it is selected by the override, never by
+    default."""
+    c = wl.case(name)
+    p = B.Plan.from_case(c)
+    assert p.a_operand() == "im2col"
+    classes = [p.subgemm(i) for i in range(p.num_subgemms())]
+    # one tap per class and M = every dy pixel (a class with fewer rows would
+    # skip pixels; one tap with M = N*Ho*Wo means row m reads dy pixel m)
+    plain = all(k["taps_y"] == 1 and k["taps_x"] == 1 and k["M"] == c.N * p.Ho * p.Wo for k in classes)
+    assert plain == eligible
+    monkeypatch.setenv("CONVBWD_DEBUG_A", "plain")
+    q = B.Plan.from_case(c)
+    assert q.a_operand() == ("plain" if eligible else "im2col")

@@ -137,8 +137,12 @@ def test_tensor_core_path_full(B, c):
     check_full(c, got, g, dy, w)
 
 
-# Narrow-group path (C/G = K/G in {8, 16}, G % 32 == 0): every pixel written by
-# the kernel itself, including ones no tap reaches.
+# Narrow-group path (C/G = K/G in {8, 16, 32}): every pixel written by the
+# kernel itself, including ones no tap reaches.  Two kernels: the warp-level
+# MMA kernel (C/G in {8, 16}, G % 8 == 0; the default there), and tcgen05 with
+# the groups of each 64-channel block folded into a block-diagonal B (where
+# C % 64 == 0 and the filter has at most 12 taps: the only kernel for C/G = 32,
+# else selected by CONVBWD_DEBUG_GROUPED=tc).
 GROUPED_CASES = [
     _mk("grp_g32_cg8_3x3s2", N=2, C=256, K=256, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=32),
     _mk("grp_g32_cg8_s3_uncov", N=1, C=256, K=256, Hi=10, Wi=9, Y=2, X=2, pad=(0, 1), stride=(3, 3), groups=32),
@@ -149,14 +153,50 @@ GROUPED_CASES = [
     _mk("grp_g8_cg8", N=2, C=64, K=64, Hi=9, Wi=10, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=8),
     _mk("grp_g16_cg16_s4", N=2, C=256, K=256, Hi=11, Wi=9, Y=3, X=3, pad=(1, 1), stride=(4, 4), groups=16),
     _mk("grp_g32_cg8_5x3_s1x2", N=1, C=256, K=256, Hi=8, Wi=13, Y=5, X=3, pad=(2, 1), stride=(1, 2), groups=32),
+    _mk("grp_g8_cg8_3x3s2_many_tiles", N=4, C=64, K=64, Hi=30, Wi=29, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=8),
+]
+GROUPED_TC_ONLY = [
+    # 32 channels per group: only the tcgen05 kernel covers it
+    _mk("grp_g8_cg32_3x3s2", N=2, C=256, K=256, Hi=11, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=8),
+    # rows of one parity uncovered (stride 2, dilation 2, pad 2): the kernel's own fill
+    _mk("grp_g16_cg16_dil2_fill", N=2, C=256, K=256, Hi=13, Wi=10, Y=3, X=3, pad=(2, 2), stride=(2, 2), dil=(2, 2),
+        groups=16),
+    _mk("grp_g64_cg8_2x2_s2", N=3, C=512, K=512, Hi=9, Wi=8, Y=2, X=2, stride=(2, 2), groups=64),
 ]
 
 
+def _grouped_tc_eligible(c):
+    return c.C % 64 == 0 and c.Y * c.X <= 12
+
+
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
 @pytest.mark.parametrize("c", GROUPED_CASES, ids=lambda c: c.name)
-def test_grouped_path_full(B, c):
+def test_grouped_path_full(B, monkeypatch, c, kernel):
+    if kernel == "tc":
+        monkeypatch.setenv("CONVBWD_DEBUG_GROUPED", "tc")
     g, dy, w = inputs(c)
     got, plan = gpu_dgrad(B, c, dy, w)
     assert plan.path() == ("grouped", 1)
+    tc = kernel == "tc" and _grouped_tc_eligible(c)
+    assert plan.tile() == ((128, 64, 1) if tc else (0, 0, 1)), plan.tile()
+    check_full(c, got, g, dy, w)
+
+
+@pytest.mark.parametrize("c", GROUPED_TC_ONLY, ids=lambda c: c.name)
+def test_grouped_tensor_core_only_shapes(B, c):
+    g, dy, w = inputs(c)
+    got, plan = gpu_dgrad(B, c, dy, w)
+    assert plan.path() == ("grouped", 1) and plan.tile() == (128, 64, 1), (plan.path(), plan.tile())
+    check_full(c, got, g, dy, w)
+
+
+def test_grouped_layer_on_tensor_core_kernel(B, monkeypatch):
+    """The benchmark's grouped layer on the tcgen05 block-diagonal kernel (whole dx)."""
+    monkeypatch.setenv("CONVBWD_DEBUG_GROUPED", "tc")
+    c = wl.case("bf16_resnext")
+    g, dy, w = inputs(c)
+    got, plan = gpu_dgrad(B, c, dy, w)
+    assert plan.path() == ("grouped", 1) and plan.tile() == (128, 64, 1)
     check_full(c, got, g, dy, w)
 
 
@@ -309,6 +349,62 @@ def test_pair_tile_variants(B, monkeypatch, c, env):
         if "CONVBWD_DEBUG_BN" in env:
             assert tn == int(env["CONVBWD_DEBUG_BN"]), plan.tile()
         check_full(c, got, g, dy, w)
+
+
+# The plain-matrix specialisation of the SM-pair kernel (A = dy as the matrix
+# {N*Ho*Wo, K}, 2-D tiled loads): the 1x2 stride-(1,2) layer, 1x1 stride-2
+# layers, ragged M and N tails, 512- and 256-wide tiles, and the two benchmark
+# workloads it applies to (whole dx).
+PLAIN_CASES = [
+    _mk("plain_1x2_s1x2", N=2, C=256, K=256, Hi=1, Wi=64, Y=1, X=2, stride=(1, 2)),
+    _mk("plain_1x2_s1x2_w512", N=3, C=1024, K=192, Hi=1, Wi=90, Y=1, X=2, stride=(1, 2)),
+    _mk("plain_1x1_s2_ragged", N=3, C=384, K=200, Hi=13, Wi=13, Y=1, X=1, stride=(2, 2)),
+    _mk("plain_1x1_s1", N=2, C=512, K=128, Hi=9, Wi=7, Y=1, X=1),
+    wl.case("bf16_16x1x512x2048"),
+    wl.case("bf16_32x14x14_1024"),
+]
+
+
+@pytest.mark.parametrize("c", PLAIN_CASES, ids=lambda c: c.name)
+def test_plain_matrix_specialisation(B, monkeypatch, c):
+    monkeypatch.setenv("CONVBWD_DEBUG_A", "plain")
+    g, dy, w = inputs(c)
+    got, plan = gpu_dgrad(B, c, dy, w)
+    assert plan.a_operand() == "plain" and plan.tile()[2] == 2, (plan.a_operand(), plan.tile())
+    check_full(c, got, g, dy, w)
+
+
+# Split-K with a reduce-scatter on the SM-pair kernel: S pairs per tile, each
+# over 1/S of the k-blocks, exchanging fp32 partials so that each stores 1/S
+# of the columns.  Ragged M (a 256-row block whose second CTA has no rows),
+# ragged N (columns past C/G inside the last slice), 256- and 512-wide tiles,
+# several classes and the dilated stress layer at full size; each plan runs
+# twice (the second launch's flags carry a new epoch).
+SPLIT_CASES = [
+    (_mk("split2_deep", N=2, C=512, K=512, Hi=9, Wi=9, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)), 2),
+    (_mk("split3_ragged_m", N=1, C=512, K=320, Hi=11, Wi=10, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)), 3),
+    (_mk("split3_ragged_n", N=2, C=384, K=256, Hi=8, Wi=9, Y=3, X=3, pad=(1, 1)), 3),
+    (_mk("split4_cg256", N=2, C=256, K=512, Hi=7, Wi=7, Y=3, X=3, pad=(1, 1), stride=(2, 2)), 4),
+    # classes with 1 and 2 taps, rows of one residue uncovered (stride 3, 2 taps)
+    (_mk("split2_multiclass_fill", N=2, C=512, K=256, Hi=13, Wi=11, Y=2, X=3, pad=(0, 1), stride=(3, 2)), 2),
+    (wl.case("bf16_32x28x28x512"), 3),
+]
+
+
+@pytest.mark.parametrize("c,S", SPLIT_CASES, ids=[c.name + f"_S{S}" for c, S in SPLIT_CASES])
+def test_split_k_reduce_scatter(B, monkeypatch, c, S):
+    monkeypatch.setenv("CONVBWD_DEBUG_SPLITK", str(S))
+    g, dy, w = inputs(c)
+    plan = B.Plan.from_case(c)
+    assert plan.path()[0] == "tcgen05" and plan.k_splits() == S, (plan.path(), plan.k_splits())
+    dy_s, w_s, dx_s = plan.shapes()
+    dyd, wd = to_dev(dy, c.dtype), to_dev(w, c.dtype)
+    for _ in range(2):
+        dx = torch.full(dx_s, float("nan"), dtype=torch.bfloat16, device="cuda")
+        plan.run(dyd, wd, dx)
+        st, det = plan.status()
+        assert st == B.OK, (B.status_string(st), hex(det))
+        check_full(c, dx.float().cpu().numpy().astype(np.float64), g, dy, w)
 
 
 def test_deterministic_and_stream_ordered(B):
