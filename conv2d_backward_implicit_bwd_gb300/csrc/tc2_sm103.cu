@@ -77,11 +77,9 @@ struct Tc2Cfg {
 // kernel (PLAIN = false) serves every shape with the same tiles.
 template <int BN_, bool PLAIN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS, 1)
-    tc2_dgrad_kernel(const __grid_constant__ TcParams pm) {
+    tc2_dgrad_kernel(const __grid_constant__ TcParams p) {
     using Cfg = Tc2Cfg<BN_>;
     constexpr int S = Cfg::STAGES;
-    __shared__ __align__(16) uint8_t s_tail[kTcTailBytes];
-    const TcParams &p = stage_param_tail(pm, s_tail);  // read only after the cluster barrier below
     constexpr int BN = Cfg::BN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -101,7 +99,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
     const Geom &g = p.g;
     // scheduling unit: the pair (cluster of two CTAs)
     const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
-    if (threadIdx.x == 0) CBD_PHASE(pm, kPhEntry);
+    if (threadIdx.x == 0) CBD_PHASE(p, kPhEntry);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -121,15 +119,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
         tc_fence_before();
     }
     if (warp == 4 && lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pm.tmap_w)) : "memory");
-        for (int ci = 0; ci < pm.num_classes; ++ci)
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pm.tmap_a[ci])) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_w)) : "memory");
+        for (int ci = 0; ci < p.num_classes; ++ci)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_a[ci])) : "memory");
     }
     // barriers of both CTAs initialised and TMEM allocated before any remote operation
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    if (threadIdx.x == 0) CBD_PHASE(pm, kPhSetup);
+    if (threadIdx.x == 0) CBD_PHASE(p, kPhSetup);
     if (threadIdx.x == 0 && !leader) {
         // the pair's MMAs write this CTA's rows at the leader's TMEM address
         if (ld_shared_cluster_u32(mapa_shared(smem_u32(tmem_slot), pl)) != tmem_base)
@@ -146,7 +144,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
             const uint32_t full_leader0 = mapa_shared(full0, pl);
             uint32_t it = 0;
             bool ok = true, issued = false;
-            if (do_a) CBD_PHASE(pm, kPhProdStart);
+            if (do_a) CBD_PHASE(p, kPhProdStart);
             SegmentIter segs(p, pair, npairs);
             Segment sg;
             while (ok && segs.next(p, sg)) {
@@ -157,7 +155,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 const int n0 = m0 / HTWT, rem = m0 - n0 * HTWT;
                 const int bh = c.ht_lo + rem / c.WT - (c.taps_y - 1) * g.DH;
                 const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
-                const CUtensorMap *amap = &pm.tmap_a[tcd.ci];
+                const CUtensorMap *amap = &p.tmap_a[tcd.ci];
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const int tap = kb / p.kb_per_tap;
                     const int k0 = (kb - tap * p.kb_per_tap) * 64;
@@ -169,7 +167,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                         break;
                     }
                     const uint32_t bar = full_leader0 + 8 * s;
-                    if (do_a && it == 0) CBD_PHASE(pm, kPhProdWaited);
+                    if (do_a && it == 0) CBD_PHASE(p, kPhProdWaited);
                     // (B loads of a split producer may complete before this arrive:
                     // the transaction count dips below zero while the arrival is
                     // still pending, so the phase cannot complete early)
@@ -182,21 +180,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                             tma_load_im2col_pair(smem_u32(sA + s * Cfg::A_BYTES), amap, bar, tcd.gi * g.Kg + k0, bw,
                                                  bh, n0, (uint16_t)((c.taps_x - 1 - i) * g.DW),
                                                  (uint16_t)((c.taps_y - 1 - j) * g.DH));
-                        if (it == 0) CBD_PHASE(pm, kPhFirstIssue);
+                        if (it == 0) CBD_PHASE(p, kPhFirstIssue);
                     }
                     const uint32_t bdst = smem_u32(sB + s * Cfg::B_BYTES);
                     // box q feeds MMA q / QPM: this CTA's half of that MMA's columns
                     for (int cb = cb_lo; cb < cb_hi; ++cb) {
                         const int col = tcd.nb * BN + (cb / Cfg::QPM) * Cfg::MMA_N + (int)rank * (Cfg::MMA_N / 2) +
                                         (cb % Cfg::QPM) * 64;
-                        tma_load_5d_pair(bdst + cb * 8192, &pm.tmap_w, bar, col, c.tx + g.XT * i, c.ty + g.YT * j, k0,
+                        tma_load_5d_pair(bdst + cb * 8192, &p.tmap_w, bar, col, c.tx + g.XT * i, c.ty + g.YT * j, k0,
                                          tcd.gi);
                     }
-                    if (warp == Cfg::B_WARP && it == 0) CBD_PHASE(pm, kPhBFirst);
+                    if (warp == Cfg::B_WARP && it == 0) CBD_PHASE(p, kPhBFirst);
                     issued = true;
                 }
             }
-            if (do_a && issued) CBD_PHASE(pm, kPhLastIssue);
+            if (do_a && issued) CBD_PHASE(p, kPhLastIssue);
             if (!ok && issued) {
                 for (int q = 0; q < 100; ++q) __nanosleep(1000);
             }
@@ -220,7 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                     break;
                 }
                 tc_fence_after();
-                if (tc == 1) CBD_PHASE(pm, kPhMma1Start);
+                if (tc == 1) CBD_PHASE(p, kPhMma1Start);
                 const uint32_t d_tmem = tmem_base + b * BN;
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const uint32_t s = it % S, ph = (it / S) & 1;
@@ -230,7 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                         ok = false;
                         break;
                     }
-                    if (it == 0) CBD_PHASE(pm, kPhFirstFull);
+                    if (it == 0) CBD_PHASE(p, kPhFirstFull);
                     // descriptors: start address in 16-byte units in the low bits; k step of
                     // 16 elements = 32 bytes in A (K-major), 16 rows = 2048 bytes in B (MN-major)
                     const uint64_t ad0 = a_desc0 + (uint64_t)((s * Cfg::A_BYTES) >> 4);
@@ -248,8 +246,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 }
                 if (!ok) break;
                 tc_commit2_mc(tfull0 + 8 * b, (uint16_t)0x3);
-                if (tc == 0) CBD_PHASE(pm, kPhMma0Done);
-                CBD_PHASE(pm, kPhMmaLast);
+                if (tc == 0) CBD_PHASE(p, kPhMma0Done);
+                CBD_PHASE(p, kPhMmaLast);
             }
             if (!ok && issued) {
                 for (int q = 0; q < 100; ++q) __nanosleep(1000);
@@ -263,7 +261,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
         const uint32_t tempty_leader0 = mapa_shared(tempty0, pl);
         uint32_t tc = 0;
         if (p.fill) fill_uncovered(p, threadIdx.x, 128);  // threads 0..127 are the epilogue warps
-        if (threadIdx.x == 0) CBD_PHASE(pm, kPhFillDone);
+        if (threadIdx.x == 0) CBD_PHASE(p, kPhFillDone);
         SegmentIter segs(p, pair, npairs);
         Segment sg;
         const size_t slot_f4 = (size_t)(BN / 4) * 128;  // one CTA's 128 x BN fp32 partial, in float4
@@ -274,7 +272,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
             bool ok = mbar_wait_bounded(tfull0 + 8 * b, tph, p.wait_budget, abort_flag, p.status, kDevTimeoutEpilogue);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            if (threadIdx.x == 0 && tc < 2) CBD_PHASE(pm, tc == 0 ? kPhEpi0Start : kPhEpi1Start);
+            if (threadIdx.x == 0 && tc < 2) CBD_PHASE(p, tc == 0 ? kPhEpi0Start : kPhEpi1Start);
             const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + b * BN;
             const int m = tcd.mb * 256 + (int)rank * 128 + row;
             const bool rvalid = m < c.M;
@@ -365,15 +363,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);
             if (threadIdx.x == 0) {
-                if (tc < 2) CBD_PHASE(pm, tc == 0 ? kPhEpi0Done : kPhEpi1Done);
-                CBD_PHASE(pm, kPhEpiLast);
+                if (tc < 2) CBD_PHASE(p, tc == 0 ? kPhEpi0Done : kPhEpi1Done);
+                CBD_PHASE(p, kPhEpiLast);
             }
         }
     }
 
     // no remote arrive or MMA may target a CTA that has left
     cluster_sync_all();
-    if (threadIdx.x == 0) CBD_PHASE(pm, kPhExit);
+    if (threadIdx.x == 0) CBD_PHASE(p, kPhExit);
     if (warp == Cfg::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc2(tmem_base, Cfg::TMEM_COLS);

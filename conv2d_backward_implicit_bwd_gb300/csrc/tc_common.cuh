@@ -5,7 +5,6 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
-#include <stddef.h>
 #include <stdint.h>
 
 #include "device_util.cuh"
@@ -366,23 +365,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
-}
-
-// Kernel parameters after the tensor maps, staged in shared memory at kernel
-// entry: every role then reads the class table and geometry from shared
-// memory instead of walking chains of dependent parameter-cache misses
-// (which held the first TMA issue back by ~1.8 us after the CTA had set up).
-// All threads copy; the returned view is valid after the kernel's next
-// CTA-wide barrier.  The tensor maps stay in parameter space (TMA reads them
-// there), so map addresses must still be taken from the kernel parameter.
-constexpr int kTcTailOffset = (int)offsetof(TcParams, dy);
-constexpr int kTcTailBytes = (int)sizeof(TcParams) - kTcTailOffset;
-static_assert(kTcTailOffset % 16 == 0 && kTcTailBytes % 16 == 0, "parameter tail must copy as 16-byte words");
-__device__ __forceinline__ const TcParams &stage_param_tail(const TcParams &pm, uint8_t *buf) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(&pm) + kTcTailOffset);
-    uint4 *dst = reinterpret_cast<uint4 *>(buf);
-    for (int i = threadIdx.x; i < kTcTailBytes / 16; i += blockDim.x) dst[i] = src[i];
-    return *reinterpret_cast<const TcParams *>(buf - kTcTailOffset);
 }
 
 // Zero the dx pixels that no residue class writes (bf16 NHWC, 16-byte

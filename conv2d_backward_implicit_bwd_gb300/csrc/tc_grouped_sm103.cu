@@ -82,19 +82,16 @@ __device__ __forceinline__ void tg_tile(const TcParams &p, int u, int &ci, int &
     mb = u - p.cls[ci].tile_begin;
 }
 
-__global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(const __grid_constant__ TcParams pm) {
+__global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(const __grid_constant__ TcParams p) {
     using Cfg = TgCfg;
     constexpr int S = Cfg::STAGES;
-    __shared__ __align__(16) uint8_t s_tail[kTcTailBytes];
-    const TcParams &p = stage_param_tail(pm, s_tail);  // read only after the CTA barrier below
     extern __shared__ uint8_t smem_raw[];
-    const Geom &g = p.g;  // folded geometry: G = group blocks, Cg = Kg = 64 (read after the barrier)
-    const Geom &gm = pm.g;  // the same, from parameter space (before the barrier)
+    const Geom &g = p.g;  // folded geometry: G = group blocks, Cg = Kg = 64
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // [A stages | B tiles (taps x 8 KB) | epilogue staging | barriers], all 1024-aligned
     uint8_t *sA = smem;
     uint8_t *sB = sA + S * Cfg::A_BYTES;
-    uint8_t *stage = sB + gm.Y * gm.X * Cfg::B_TAP_BYTES;
+    uint8_t *stage = sB + g.Y * g.X * Cfg::B_TAP_BYTES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(stage + Cfg::STAGE_OUT_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
@@ -102,11 +99,11 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
     const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int gblocks = gm.G;
+    const int gblocks = g.G;
     const int gb = blockIdx.x % gblocks;            // this CTA's group block
     const int local = blockIdx.x / gblocks, nlocal = gridDim.x / gblocks;
-    const int units = pm.total_tiles / gblocks;     // tiles of one group block
-    if (threadIdx.x == 0) CBD_PHASE(pm, kPhEntry);
+    const int units = p.total_tiles / gblocks;     // tiles of one group block
+    if (threadIdx.x == 0) CBD_PHASE(p, kPhEntry);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -125,8 +122,8 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
         tc_fence_before();
     }
     if (warp == Cfg::PROD_WARP && lane == 0)
-        for (int ci = 0; ci < pm.num_classes; ++ci)
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pm.tmap_a[ci])) : "memory");
+        for (int ci = 0; ci < p.num_classes; ++ci)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_a[ci])) : "memory");
 
     // Block-diagonal B of this group block, one 64 (k) x 64 (c) tile per filter
     // tap, laid out as a 128-byte-swizzled MN-major operand (row k = 128 bytes
@@ -136,9 +133,9 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
         // One thread per (tap, k) row, four rows in flight per thread: the row's
         // cg / 8 nonzero chunks are loaded first (16-byte loads: cg and the
         // chunk offsets are multiples of 8), then all 8 chunks are written.
-        const int cg = pm.bd_cg, nzc = cg / 8;
-        const int ntap = gm.Y * gm.X, rows = ntap * 64;
-        const uint16_t *w = static_cast<const uint16_t *>(pm.w);
+        const int cg = p.bd_cg, nzc = cg / 8;
+        const int ntap = g.Y * g.X, rows = ntap * 64;
+        const uint16_t *w = static_cast<const uint16_t *>(p.w);
         const int64_t rowlen = (int64_t)ntap * cg;  // bf16 per filter row k (KYXC, C/G channels)
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
         for (int r0 = threadIdx.x; r0 < rows; r0 += 4 * Cfg::THREADS) {
@@ -173,7 +170,7 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    if (threadIdx.x == 0) CBD_PHASE(pm, kPhSetup);
+    if (threadIdx.x == 0) CBD_PHASE(p, kPhSetup);
 
     if (warp == Cfg::PROD_WARP) {
         // ------------------------------------------------------------ A producer
@@ -189,7 +186,7 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
                 const int n0 = m0 / HTWT, rem = m0 - n0 * HTWT;
                 const int bh = c.ht_lo + rem / c.WT - (c.taps_y - 1) * g.DH;
                 const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
-                const CUtensorMap *amap = &pm.tmap_a[ci];
+                const CUtensorMap *amap = &p.tmap_a[ci];
                 for (int j = 0; j < c.taps_y && ok; ++j)
                     for (int i = 0; i < c.taps_x; ++i, ++it) {
                         const uint32_t s = it % S, ph = (it / S) & 1;
@@ -201,11 +198,11 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
                         mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)Cfg::A_BYTES);
                         tma_load_im2col(smem_u32(sA + s * Cfg::A_BYTES), amap, full0 + 8 * s, gb * 64, bw, bh, n0,
                                         (uint16_t)((c.taps_x - 1 - i) * g.DW), (uint16_t)((c.taps_y - 1 - j) * g.DH));
-                        if (it == 0) CBD_PHASE(pm, kPhFirstIssue);
+                        if (it == 0) CBD_PHASE(p, kPhFirstIssue);
                         issued = true;
                     }
             }
-            if (issued) CBD_PHASE(pm, kPhLastIssue);
+            if (issued) CBD_PHASE(p, kPhLastIssue);
             if (!ok && issued) {
                 for (int q = 0; q < 100; ++q) __nanosleep(1000);
             }
@@ -229,7 +226,7 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
                     break;
                 }
                 tc_fence_after();
-                if (tc == 1) CBD_PHASE(pm, kPhMma1Start);
+                if (tc == 1) CBD_PHASE(p, kPhMma1Start);
                 const uint32_t d_tmem = tmem_base + b * Cfg::BN;
                 bool first = true;
                 for (int j = 0; j < c.taps_y && ok; ++j)
@@ -240,7 +237,7 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
                             ok = false;
                             break;
                         }
-                        if (it == 0) CBD_PHASE(pm, kPhFirstFull);
+                        if (it == 0) CBD_PHASE(p, kPhFirstFull);
                         tc_fence_after();
                         const int tap = (c.ty + g.YT * j) * g.X + c.tx + g.XT * i;
                         const uint32_t a_addr = smem_u32(sA + s * Cfg::A_BYTES);
@@ -257,8 +254,8 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
                     }
                 if (!ok) break;
                 tc_commit(tfull0 + 8 * b);
-                if (tc == 0) CBD_PHASE(pm, kPhMma0Done);
-                CBD_PHASE(pm, kPhMmaLast);
+                if (tc == 0) CBD_PHASE(p, kPhMma0Done);
+                CBD_PHASE(p, kPhMmaLast);
             }
             if (!ok && issued) {
                 for (int q = 0; q < 100; ++q) __nanosleep(1000);
@@ -271,7 +268,7 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
         const int row = (warp & 3) * 32 + lane;   // TMEM lane = tile row
         __nv_bfloat16 *dx = static_cast<__nv_bfloat16 *>(p.dx);
         if (p.fill) fill_uncovered(p, threadIdx.x, 32 * Cfg::EPI_WARPS);
-        if (threadIdx.x == 0) CBD_PHASE(pm, kPhFillDone);
+        if (threadIdx.x == 0) CBD_PHASE(p, kPhFillDone);
         uint32_t tc = 0;
         for (int u = local; u < units; u += nlocal, ++tc) {
             if ((int)(tc & 1) != e) continue;
@@ -282,7 +279,7 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
             bool ok = mbar_wait_bounded(tfull0 + 8 * e, tph, p.wait_budget, abort_flag, p.status, kDevTimeoutEpilogue);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            if (threadIdx.x == 0 && tc == 0) CBD_PHASE(pm, kPhEpi0Start);
+            if (threadIdx.x == 0 && tc == 0) CBD_PHASE(p, kPhEpi0Start);
             const int m = mb * 128 + row;
             const bool rvalid = m < c.M;
             int64_t off = 0;
@@ -298,13 +295,13 @@ __global__ void __launch_bounds__(TgCfg::THREADS, 1) tc_grouped_dgrad_kernel(con
             epilogue_rows<Cfg::BN>(tbase, stage + warp * 4096, lane, rvalid, off, 0, 64, dx);
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * e);
-            if (threadIdx.x == 0 && tc == 0) CBD_PHASE(pm, kPhEpi0Done);
-            if (lane == 0 && (warp & 3) == 0) CBD_PHASE(pm, kPhEpiLast);
+            if (threadIdx.x == 0 && tc == 0) CBD_PHASE(p, kPhEpi0Done);
+            if (lane == 0 && (warp & 3) == 0) CBD_PHASE(p, kPhEpiLast);
         }
     }
 
     __syncthreads();
-    if (threadIdx.x == 0) CBD_PHASE(pm, kPhExit);
+    if (threadIdx.x == 0) CBD_PHASE(p, kPhExit);
     if (warp == Cfg::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem_base, Cfg::TMEM_COLS);

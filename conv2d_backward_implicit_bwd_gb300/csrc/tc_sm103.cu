@@ -77,11 +77,9 @@ struct TcCfg {
 };
 
 template <int BN, bool IM2COL>
-__global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel(const __grid_constant__ TcParams pm) {
+__global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel(const __grid_constant__ TcParams p) {
     using Cfg = TcCfg<BN, IM2COL>;
     constexpr int S = Cfg::STAGES;
-    __shared__ __align__(16) uint8_t s_tail[kTcTailBytes];
-    const TcParams &p = stage_param_tail(pm, s_tail);  // read only after the CTA barrier below
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
@@ -96,7 +94,7 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
     const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const Geom &g = p.g;
-    if (threadIdx.x == 0) CBD_PHASE(pm, kPhEntry);
+    if (threadIdx.x == 0) CBD_PHASE(p, kPhEntry);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -117,15 +115,15 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
         tc_fence_before();
     }
     if (warp == 4 && lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pm.tmap_w)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_w)) : "memory");
         if (IM2COL)
-            for (int ci = 0; ci < pm.num_classes; ++ci)
-                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&pm.tmap_a[ci])) : "memory");
+            for (int ci = 0; ci < p.num_classes; ++ci)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_a[ci])) : "memory");
     }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    if (threadIdx.x == 0) CBD_PHASE(pm, kPhSetup);
+    if (threadIdx.x == 0) CBD_PHASE(p, kPhSetup);
 
     if (IM2COL && (warp == 4 || warp >= Cfg::B_WARP)) {
         // ------------------------------------------------------------ producers (TMA)
@@ -148,7 +146,7 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
                 const int n0 = m0 / HTWT, rem = m0 - n0 * HTWT;
                 const int bh = c.ht_lo + rem / c.WT - (c.taps_y - 1) * g.DH;
                 const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
-                const CUtensorMap *amap = &pm.tmap_a[tcd.ci];
+                const CUtensorMap *amap = &p.tmap_a[tcd.ci];
                 for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const int tap = kb / p.kb_per_tap;
                     const int k0 = (kb - tap * p.kb_per_tap) * 64;
@@ -168,16 +166,16 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
                         tma_load_im2col(smem_u32(sA + s * Cfg::A_BYTES), amap, full_s, tcd.gi * g.Kg + k0, bw, bh,
                                         n0, (uint16_t)((c.taps_x - 1 - i) * g.DW),
                                         (uint16_t)((c.taps_y - 1 - j) * g.DH));
-                        if (it == 0) CBD_PHASE(pm, kPhFirstIssue);
+                        if (it == 0) CBD_PHASE(p, kPhFirstIssue);
                     }
                     const uint32_t bdst = smem_u32(sB + s * Cfg::B_BYTES);
                     for (int cb = cb_lo; cb < cb_hi; ++cb)
-                        tma_load_5d(bdst + cb * 8192, &pm.tmap_w, full_s, tcd.nb * BN + cb * 64, c.tx + g.XT * i,
+                        tma_load_5d(bdst + cb * 8192, &p.tmap_w, full_s, tcd.nb * BN + cb * 64, c.tx + g.XT * i,
                                     c.ty + g.YT * j, k0, tcd.gi);
                     issued = true;
                 }
             }
-            if (do_a && issued) CBD_PHASE(pm, kPhLastIssue);
+            if (do_a && issued) CBD_PHASE(p, kPhLastIssue);
             if (!ok && issued) {
                 for (int q = 0; q < 100; ++q) __nanosleep(1000);
             }
@@ -240,7 +238,7 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
                     mbar_expect_tx(full_s, (uint32_t)Cfg::B_BYTES);
 #pragma unroll
                     for (int cb = 0; cb < BN / 64; ++cb)
-                        tma_load_5d(b_slot + cb * 8192, &pm.tmap_w, full_s, tcd.nb * BN + cb * 64, c.tx + g.XT * i,
+                        tma_load_5d(b_slot + cb * 8192, &p.tmap_w, full_s, tcd.nb * BN + cb * 64, c.tx + g.XT * i,
                                     c.ty + g.YT * j, k0, tcd.gi);
                     issued_tma = true;
                 }
@@ -288,7 +286,7 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
                     break;
                 }
                 tc_fence_after();
-                if (tc == 1) CBD_PHASE(pm, kPhMma1Start);
+                if (tc == 1) CBD_PHASE(p, kPhMma1Start);
                 const uint32_t d_tmem = tmem_base + b * BN;
                 for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const uint32_t s = it % S, ph = (it / S) & 1;
@@ -296,7 +294,7 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
                         ok = false;
                         break;
                     }
-                    if (it == 0) CBD_PHASE(pm, kPhFirstFull);
+                    if (it == 0) CBD_PHASE(p, kPhFirstFull);
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sA + s * Cfg::A_BYTES);
                     const uint32_t b_addr = smem_u32(sB + s * Cfg::B_BYTES);
@@ -311,8 +309,8 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
                 }
                 if (!ok) break;
                 tc_commit(tfull0 + 8 * b);
-                if (tc == 0) CBD_PHASE(pm, kPhMma0Done);
-                CBD_PHASE(pm, kPhMmaLast);
+                if (tc == 0) CBD_PHASE(p, kPhMma0Done);
+                CBD_PHASE(p, kPhMmaLast);
             }
             if (!ok && issued) {
                 for (int q = 0; q < 100; ++q) __nanosleep(1000);
@@ -325,7 +323,7 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
         __nv_bfloat16 *dx = static_cast<__nv_bfloat16 *>(p.dx);
         uint32_t tc = 0;
         if (p.fill) fill_uncovered(p, threadIdx.x, 128);  // threads 0..127 are the epilogue warps
-        if (threadIdx.x == 0) CBD_PHASE(pm, kPhFillDone);
+        if (threadIdx.x == 0) CBD_PHASE(p, kPhFillDone);
         for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++tc) {
             const TileCoord tcd = decode_tile(p, t);
             const ClassDesc &c = p.cls[tcd.ci];
@@ -333,7 +331,7 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
             bool ok = mbar_wait_bounded(tfull0 + 8 * b, tph, p.wait_budget, abort_flag, p.status, kDevTimeoutEpilogue);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            if (threadIdx.x == 0 && tc < 2) CBD_PHASE(pm, tc == 0 ? kPhEpi0Start : kPhEpi1Start);
+            if (threadIdx.x == 0 && tc < 2) CBD_PHASE(p, tc == 0 ? kPhEpi0Start : kPhEpi1Start);
             const int m = tcd.mb * 128 + row;
             const bool rvalid = m < c.M;
             int64_t off = 0;
@@ -350,14 +348,14 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * b);
             if (threadIdx.x == 0) {
-                if (tc < 2) CBD_PHASE(pm, tc == 0 ? kPhEpi0Done : kPhEpi1Done);
-                CBD_PHASE(pm, kPhEpiLast);
+                if (tc < 2) CBD_PHASE(p, tc == 0 ? kPhEpi0Done : kPhEpi1Done);
+                CBD_PHASE(p, kPhEpiLast);
             }
         }
     }
 
     __syncthreads();
-    if (threadIdx.x == 0) CBD_PHASE(pm, kPhExit);
+    if (threadIdx.x == 0) CBD_PHASE(p, kPhExit);
     if (warp == Cfg::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
