@@ -89,6 +89,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
     uint64_t *bars = reinterpret_cast<uint64_t *>(stage + Cfg::STAGE_OUT_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
+    const uint32_t gather_bar = smem_u32(bars + 2 * S + 5);  // split-K: partials landed in shared memory
 
     const uint32_t rank = cluster_ctarank();  // CTA within the pair: 0 = leader
     const uint32_t pl = 0;                    // cluster rank of the pair's leader
@@ -110,6 +111,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
             mbar_init(tfull0 + 8 * b, 1);   // one commit per tile
             mbar_init(tempty0 + 8 * b, 8);  // leader: 4 epilogue warps of each CTA
         }
+        mbar_init(gather_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async_smem();
@@ -304,6 +306,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 }
                 __threadfence();
                 asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (threadIdx.x == 0) CBD_PHASE(p, kPhEpi1Start);  // partials of the other slices written
+                const int lo = split_col(q, S, BN), hi = split_col(q + 1, S, BN);
+                // The other splits' partials of this slice: (S - 1) contiguous
+                // blocks of (hi - lo) x 512 bytes.  They land in the pipeline's
+                // shared memory (free: the tile's MMAs are done and this pair
+                // has no other segment) with one bulk copy each, so the sum below
+                // reads shared memory instead of waiting on L2 per 32 columns.
+                const uint32_t part_bytes = (uint32_t)(hi - lo) * 512u;
+                const bool land =
+                    (uint64_t)(S - 1) * part_bytes <= (uint64_t)Cfg::STAGES * (Cfg::A_BYTES + Cfg::B_BYTES);
+                const float4 *parts_g = tile_ws + (size_t)rank * (S - 1) * blk + (size_t)(lo / 4) * 128;
                 if (threadIdx.x == 0) {
                     st_release_gpu(p.flags + ((size_t)sg.t * S + q) * 2 + rank, p.epoch);
                     // the other splits of this tile (same CTA rank), bounded wait each
@@ -318,14 +331,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                             }
                         }
                     }
+                    CBD_PHASE(p, kPhMma1Start);  // (split-K: the other splits' flags acquired)
+                    if (land && part_bytes > 0) {
+                        fence_proxy_async_global();  // generic-proxy writes of the other SMs, read by the copy engine
+                        mbar_arrive_expect_tx(gather_bar, (uint32_t)(S - 1) * part_bytes);
+                        for (int r = 0; r < S - 1; ++r)
+                            bulk_load_g2s(smem_u32(sA) + (uint32_t)r * part_bytes, parts_g + (size_t)r * blk,
+                                          part_bytes, gather_bar);
+                    }
                 }
                 asm volatile("bar.sync 1, 128;" ::: "memory");
                 for (int s2 = 0; s2 < S; ++s2)  // each thread's own acquire of the partials it reads
                     if (s2 != q) (void)ld_acquire_gpu(p.flags + ((size_t)sg.t * S + s2) * 2 + rank);
-                const int lo = split_col(q, S, BN), hi = split_col(q + 1, S, BN);
+                const float4 *parts = parts_g;
+                size_t pstride = blk;
+                if (land && part_bytes > 0) {
+                    // on a timeout the status word is set and the sum reads whatever landed
+                    (void)mbar_wait_bounded(gather_bar, 0, p.wait_budget, abort_flag, p.status, kDevTimeoutPartial);
+                    parts = reinterpret_cast<const float4 *>(sA);
+                    pstride = part_bytes / 16;
+                }
+                if (threadIdx.x == 0) CBD_PHASE(p, kPhEpi1Done);  // partials landed
                 epilogue_chunks(tbase + lo, (hi - lo) / 64, stage + warp * 4096, lane, rvalid, off + lo,
-                                tcd.nb * BN + lo, g.Cg, dx, tile_ws + (size_t)rank * (S - 1) * blk + (size_t)(lo / 4) * 128,
-                                S - 1, blk, row);
+                                tcd.nb * BN + lo, g.Cg, dx, parts, S - 1, pstride, row);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);
