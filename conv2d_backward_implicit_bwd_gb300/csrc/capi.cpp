@@ -410,13 +410,32 @@ bool tf32_tail_split(const conv_bwd_plan_s *p, const ClassDesc *cls, size_t nc, 
 }
 
 // K splits of the SM-pair kernel's split-K schedule for this plan (1 = whole
-// tiles): CONVBWD_DEBUG_SPLITK=S forces S where the S * tiles units fit one
-// wave; otherwise none.
-int split_choice(const conv_bwd_plan_s *p) {
+// tiles).  CONVBWD_DEBUG_SPLITK=S forces S (where the S * tiles units fit one
+// wave).  By default: a layer whose 256 x 512 tiles number at most a third of
+// the SM pairs (so S >= 3 splits fill the GPU) and whose reduction is deep
+// enough for every split to keep >= 16 k-blocks: the 512-wide tiles need the
+// fewest operand bytes per multiply-add (the pair kernels are bound by operand
+// delivery) and the split gives them the whole GPU.  Measured on the dilated
+// 3x3 stride-2 layer (C = K = 512, 72 k-blocks, 25 tiles): 35.5-36.9 us with 3
+// splits against 37.3-37.6 us for 256-wide whole tiles on 50 pairs; 2 splits
+// (39 us) and the 1x1 layer's 32 k-blocks (27-30 us against 21-23 us) lose.
+int split_choice(const conv_bwd_plan_s *p, int max_pairs) {
     if (const char *f = env("CONVBWD_DEBUG_SPLITK")) {
         const int S = std::atoi(f);
         return S >= 2 && S <= 8 ? S : 1;
     }
+    const Geom &g = p->g;
+    if (g.Cg < 512 || max_pairs <= 0) return 1;
+    int64_t tiles = 0;
+    int min_kb = 1 << 30;
+    const int kbt = (g.Kg + 63) / 64;
+    for (const ClassDesc &c : p->classes) {
+        tiles += (int64_t)g.G * ((c.M + 255) / 256) * ((g.Cg + 511) / 512);
+        min_kb = std::min(min_kb, c.taps_y * c.taps_x * kbt);
+    }
+    if (tiles <= 0) return 1;
+    for (int S = (int)std::min<int64_t>(4, max_pairs / tiles); S >= 3; --S)
+        if (min_kb / S >= 16) return S;
     return 1;
 }
 
@@ -736,7 +755,7 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                 // The widest tile needs the fewest operand bytes per multiply-add (the
                 // SM pairs are bound by operand delivery), and the split gives a deep,
                 // short layer enough such tiles to fill the GPU.
-                int S = split_choice(p);
+                int S = split_choice(p, tc2_max_pairs(p->num_sms));
                 const int kbt = (g.Kg + 63) / 64;
                 for (const ClassDesc &c : p->classes)  // every split keeps at least two k-blocks
                     if (c.taps_y * c.taps_x * kbt < 2 * S) S = 1;

@@ -22,7 +22,15 @@
 //     leader's accumulator-empty barrier (remote arrive from the peer).
 // Per SM and per 128x256x64 step this moves 32 KB of operands into shared
 // memory instead of 48 KB (each SM loads only half of B); a 512-wide tile
-// moves 24 KB per 128x256x64 of work.
+// moves 24 KB per 128x256x64 of work.  Every CTA fetches its own operands
+// from L2 (no multicast); the pairs are bound by that operand delivery
+// (~40 bytes per SM clock measured), which is why the widest tile runs
+// closest to the MMA rate.
+// Schedules: whole tiles in LPT class order over the persistent pairs; or
+// (SegmentIter) split-K, where S pairs share each 256 x 512 tile over 1/S of
+// its k-blocks and exchange fp32 partials through a workspace so that each
+// pair adds and stores 1/S of the columns (the epilogue's reduce-scatter); or
+// the opt-in stream-K.  PLAIN instantiations read A as a plain matrix.
 // Every barrier wait is bounded; both CTAs meet in a cluster barrier before
 // deallocating TMEM and exiting.
 #include <cuda.h>
@@ -59,15 +67,18 @@ struct Tc2Cfg {
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + STAGE_OUT_BYTES + BAR_BYTES;
     static constexpr int MMA_WARP = 5;
-    // TMA issue is serialised per issuing thread (~70 SM clocks per tile-mode
-    // load, more for an im2col load), so the loads of a stage are spread over
-    // warps on different SM sub-partitions: warp 4 issues A, warps 6.. the
-    // 64-column B boxes (one or two each)
+    // TMA issue is serialised per issuing thread, so the loads of a stage are
+    // spread over warps on different SM sub-partitions: warps 6.. issue the
+    // 64-column B boxes (one or two each), warp 4 the A loads -- on tiles
+    // narrower than 512 (a stage every 256 or 512 MMA clocks) alternating with
+    // warp A2_WARP (odd stages), which took the 1x1 stride-2 layer's main loop
+    // from 13.3 to 11.7 us.
     static constexpr int B_WARP = 6;
     static constexpr int BOXES = BNH / 64;
     static constexpr int B_WARPS = BOXES < 2 ? BOXES : 2;
     static constexpr int BOXES_PER_WARP = BOXES / B_WARPS;
-    static constexpr int THREADS = 32 * (B_WARP + B_WARPS);
+    static constexpr int A2_WARP = BN < 512 ? B_WARP + B_WARPS : -1;
+    static constexpr int THREADS = 32 * (B_WARP + B_WARPS + (BN < 512 ? 1 : 0));
 };
 
 // PLAIN: the specialisation for plans whose every class reads dy as a plain
@@ -138,7 +149,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
 
     if (warp == 4 || warp >= Cfg::B_WARP) {
         // ------------------------------------------------------------ producers
-        const bool do_a = warp == 4;  // A loads + the stage's byte count
+        const bool do_a = warp == 4 || warp == Cfg::A2_WARP;  // A loads + the stage's byte count
+        const uint32_t a_par = warp == Cfg::A2_WARP ? 1u : 0u;  // the A issuers split the stages by parity
         // B boxes of this warp
         const int cb_lo = do_a ? 0 : (warp - Cfg::B_WARP) * Cfg::BOXES_PER_WARP;
         const int cb_hi = do_a ? 0 : cb_lo + Cfg::BOXES_PER_WARP;
@@ -159,6 +171,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
                 const CUtensorMap *amap = &p.tmap_a[tcd.ci];
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
+                    if (Cfg::A2_WARP >= 0 && do_a && (it & 1u) != a_par) continue;  // the other A issuer's stage
                     const int tap = kb / p.kb_per_tap;
                     const int k0 = (kb - tap * p.kb_per_tap) * 64;
                     const int j = tap / c.taps_x, i = tap - j * c.taps_x;

@@ -156,9 +156,9 @@ GROUPED_CASES = [
     _mk("grp_g8_cg8_3x3s2_many_tiles", N=4, C=64, K=64, Hi=30, Wi=29, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=8),
 ]
 GROUPED_TC_ONLY = [
-    # 32 channels per group: only the tcgen05 kernel covers it
+    # 32 channels per group: only the tcgen05 kernel covers it (the default there)
     _mk("grp_g8_cg32_3x3s2", N=2, C=256, K=256, Hi=11, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=8),
-    # rows of one parity uncovered (stride 2, dilation 2, pad 2): the kernel's own fill
+    # (tcgen05 kernel selected) rows of one parity uncovered (stride 2, dilation 2, pad 2): the kernel's own fill
     _mk("grp_g16_cg16_dil2_fill", N=2, C=256, K=256, Hi=13, Wi=10, Y=3, X=3, pad=(2, 2), stride=(2, 2), dil=(2, 2),
         groups=16),
     _mk("grp_g64_cg8_2x2_s2", N=3, C=512, K=512, Hi=9, Wi=8, Y=2, X=2, stride=(2, 2), groups=64),
@@ -183,7 +183,9 @@ def test_grouped_path_full(B, monkeypatch, c, kernel):
 
 
 @pytest.mark.parametrize("c", GROUPED_TC_ONLY, ids=lambda c: c.name)
-def test_grouped_tensor_core_only_shapes(B, c):
+def test_grouped_tensor_core_shapes(B, monkeypatch, c):
+    if c.C // c.groups != 32:
+        monkeypatch.setenv("CONVBWD_DEBUG_GROUPED", "tc")
     g, dy, w = inputs(c)
     got, plan = gpu_dgrad(B, c, dy, w)
     assert plan.path() == ("grouped", 1) and plan.tile() == (128, 64, 1), (plan.path(), plan.tile())
