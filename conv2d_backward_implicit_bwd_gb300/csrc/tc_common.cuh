@@ -404,6 +404,23 @@ __device__ __forceinline__ void fill_uncovered(const TcParams &p, int tid, int n
     }
 }
 
+// Tiles of worker b of G in snake order: round k takes tile k*G + b for even k
+// and k*G + G-1-b for odd k, so that the descending-cost (LPT) tile order of a
+// launch spreads evenly over the workers (on the 5x5 stride-3 layer the
+// busiest CTA's k-blocks drop from 34 to 32 against a mean of 29.9).
+struct SnakeTiles {
+    int b, G, total, k;
+    __device__ __forceinline__ SnakeTiles(int b_, int G_, int total_) : b(b_), G(G_), total(total_), k(0) {}
+    __device__ __forceinline__ bool next(int &t) {
+        while ((int64_t)k * G < total) {
+            t = k * G + ((k & 1) ? G - 1 - b : b);
+            ++k;
+            if (t < total) return true;
+        }
+        return false;
+    }
+};
+
 // A stretch [kb0, kb1) of the k-blocks of tile t handled by one worker (CTA or
 // SM pair).  `owner`: the stretch ends the tile, so this worker stores the
 // tile, first adding the partial tiles of workers q_first .. self-1 (stream-K).
@@ -428,7 +445,9 @@ __device__ __forceinline__ int class_of_tile(const TcParams &p, int t) {
 // stretch it owns after earlier workers' partials comes last.
 struct SegmentIter {
     int w, nw, next_t, u, u_lo;
-    __device__ __forceinline__ SegmentIter(const TcParams &p, int w_, int nw_) : w(w_), nw(nw_), next_t(w_) {
+    SnakeTiles whole;  // whole-tile schedule
+    __device__ __forceinline__ SegmentIter(const TcParams &p, int w_, int nw_)
+        : w(w_), nw(nw_), next_t(w_), whole(w_, nw_, p.total_tiles) {
         u_lo = (int)((int64_t)w * p.units_total / nw);
         u = (int)((int64_t)(w + 1) * p.units_total / nw);
     }
@@ -453,13 +472,11 @@ struct SegmentIter {
         }
         sg.split = 0;
         if (!p.streamk) {
-            if (next_t >= p.total_tiles) return false;
-            sg.t = next_t;
+            if (!whole.next(sg.t)) return false;
             sg.kb0 = 0;
-            sg.kb1 = nkb(p, class_of_tile(p, next_t));
+            sg.kb1 = nkb(p, class_of_tile(p, sg.t));
             sg.owner = true;
             sg.q_first = w;
-            next_t += nw;
             return true;
         }
         if (u <= u_lo) return false;

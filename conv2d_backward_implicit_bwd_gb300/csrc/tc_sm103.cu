@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true, issued = false;
-            for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            SnakeTiles tiles(blockIdx.x, gridDim.x, p.total_tiles);
+            for (int t; ok && tiles.next(t);) {
                 const TileCoord tcd = decode_tile(p, t);
                 const ClassDesc &c = p.cls[tcd.ci];
                 const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
@@ -193,7 +194,8 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
         const uint32_t b_slot = smem_u32(sB + pw * Cfg::B_BYTES);
         uint32_t it = 0;   // global stage counter of this CTA (all slots)
         bool ok = true, issued_tma = false;
-        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        SnakeTiles tiles(blockIdx.x, gridDim.x, p.total_tiles);
+        for (int t; ok && tiles.next(t);) {
             const TileCoord tcd = decode_tile(p, t);
             const ClassDesc &c = p.cls[tcd.ci];
             const uint32_t num_kb = (uint32_t)(c.taps_y * c.taps_x * p.kb_per_tap);
@@ -275,7 +277,8 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
             constexpr uint32_t idesc = idesc_bf16<BN>();
             uint32_t it = 0, tc = 0;
             bool ok = true, issued = false;
-            for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++tc) {
+            SnakeTiles tiles(blockIdx.x, gridDim.x, p.total_tiles);
+            for (int t; ok && tiles.next(t); ++tc) {
                 const TileCoord tcd = decode_tile(p, t);
                 const ClassDesc &c = p.cls[tcd.ci];
                 const int num_kb = c.taps_y * c.taps_x * p.kb_per_tap;
@@ -324,7 +327,8 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
         uint32_t tc = 0;
         if (p.fill) fill_uncovered(p, threadIdx.x, 128);  // threads 0..127 are the epilogue warps
         if (threadIdx.x == 0) CBD_PHASE(p, kPhFillDone);
-        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++tc) {
+        SnakeTiles tiles(blockIdx.x, gridDim.x, p.total_tiles);
+        for (int t; tiles.next(t); ++tc) {
             const TileCoord tcd = decode_tile(p, t);
             const ClassDesc &c = p.cls[tcd.ci];
             const uint32_t b = tc & 1, tph = (tc >> 1) & 1;
