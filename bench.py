@@ -44,13 +44,13 @@ TF32_PER_BF16 = 1.1 / 2.25  # NOMINAL dense TF32 / bf16 tensor rates of the part
 TC2_SOURCES = ("tc_common.cuh", "tc2_sm103.cu", "internal.h")
 GROUPED_SOURCES = ("tc_common.cuh", "grouped.cu", "internal.h")
 TRAFFIC = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, tc2_dgrad_kernel<512, 1>, one launch on the
-    # 16x1x512x2048 shape: 33.64 MB + 0.56 MB
-    "bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "tile": (256, 512, 2), "sha": "5f8d1699c7352864",
-                                    "bytes": 34.193e6},
-    # grouped_dgrad_kernel<8> on the 64x56x56x256 G=32 layer: 25.76 MB + 42.64 MB
-    "bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": GROUPED_SOURCES, "tile": (0, 0, 1), "sha": "d32b3a7c89beda60",
-                                             "bytes": 68.403e6},
+    # ncu --set full, tc2_dgrad_kernel<512, false>, one launch on the 16x1x512x2048 shape (after an L2 flush):
+    # dram__bytes_read.sum 33.67 MB + dram__bytes_write.sum 1.31 MB (dx stays in L2 at kernel end)
+    "bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "tile": (256, 512, 2), "sha": "f5989c50d22f818a",
+                                    "bytes": 34.983e6},
+    # grouped_dgrad_kernel<8> on the 64x56x56x256 G=32 layer: 25.76 MB + 42.02 MB
+    "bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": GROUPED_SOURCES, "tile": (0, 0, 1), "sha": "afeb7cf6418850ea",
+                                             "bytes": 67.786e6},
 }
 
 
@@ -360,6 +360,9 @@ def measure_workload(B, case, steps, warmup, flush, stream, peaks, num_sms, env=
     roof = roofline_of(path, case, useful, algo_bytes, kms, peaks, num_sms=num_sms)
     roof["kernel"] = kernel_label(path, plan, case)
     roof["kernel_ms"] = kms
+    tr = TRAFFIC.get(case.name)
+    roof["traffic"] = (tr["bytes"] if tr and tr["sha"] == kernel_sha(tr["files"]) and tuple(plan.tile()) == tr["tile"]
+                       else None)
     return {"ms_per_step": ms, "tflops": useful / (ms * 1e-3) / 1e12, "gbs": algo_bytes / (ms * 1e-3) / 1e9,
             "dtype": case.dtype, "path": path, "launches_per_step": launches, "tile": list(plan.tile()),
             "a_operand": plan.a_operand(), "k_splits": plan.k_splits(),

@@ -127,6 +127,9 @@ enum : int {
     kPhProdStart = 15,  // A producer about to decode its first tile
     kPhProdWaited = 16, // A producer passed its first empty-slot wait
     kPhBFirst = 17,     // first B producer issued its first load
+    kPhProdSeg = 18,    // A producer: first segment of its schedule known
+    kPhProdTile = 19,   // A producer: first tile decoded
+    kPhProdPreWait = 20,// A producer: about to wait for its first free stage
 };
 #endif
 

@@ -162,6 +162,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
             SegmentIter segs(p, pair, npairs);
             Segment sg;
             while (ok && segs.next(p, sg)) {
+                if (do_a && it == 0) CBD_PHASE(p, kPhProdSeg);
                 const TileCoord tcd = decode_tile(p, sg.t);
                 const ClassDesc &c = p.cls[tcd.ci];
                 const int HTWT = c.HT * c.WT;
@@ -170,12 +171,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 const int bh = c.ht_lo + rem / c.WT - (c.taps_y - 1) * g.DH;
                 const int bw = c.wt_lo + rem % c.WT - (c.taps_x - 1) * g.DW;
                 const CUtensorMap *amap = &p.tmap_a[tcd.ci];
+                if (do_a && it == 0) CBD_PHASE(p, kPhProdTile);
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     if (Cfg::A2_WARP >= 0 && do_a && (it & 1u) != a_par) continue;  // the other A issuer's stage
                     const int tap = kb / p.kb_per_tap;
                     const int k0 = (kb - tap * p.kb_per_tap) * 64;
                     const int j = tap / c.taps_x, i = tap - j * c.taps_x;
                     const uint32_t s = it % S, ph = (it / S) & 1;
+                    if (do_a && it == 0) CBD_PHASE(p, kPhProdPreWait);
                     if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, p.wait_budget, abort_flag, p.status,
                                            kDevTimeoutProducer)) {
                         ok = false;
