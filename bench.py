@@ -241,7 +241,8 @@ FP32_FFMA_PER_SM_CLK = 128  # fp32 lanes per SM (one FFMA = 2 FLOP per lane per 
 def kernel_label(path, plan, case):
     tm, tn, tsms = plan.tile()
     return {"tcgen05": (f"tc2_dgrad_kernel<{tn}>" if tsms >= 2 else f"tc_dgrad_kernel<{tn}>"),
-            "grouped": ("tc_grouped_dgrad_kernel" if tn else f"grouped_dgrad_kernel<{case.C // case.groups}>"),
+            "grouped": {"band": "tc_band_dgrad_kernel", "tc": "tc_grouped_dgrad_kernel"}.get(
+                plan.grouped_kernel(), f"grouped_dgrad_kernel<{case.C // case.groups}>"),
             "simt": "simt_dgrad_kernel", "tf32": "tf32_dgrad_kernel"}[path]
 
 

@@ -25,7 +25,7 @@ EXPORTED = [
     "conv_bwd_data_run", "conv_bwd_data_run_host", "conv_bwd_data_get_status", "conv_bwd_data_set_timing",
     "conv_bwd_data_last_timing", "conv_bwd_data_selftest_wait_timeout", "conv_bwd_status_string",
     "conv_bwd_data_version", "conv_bwd_data_run_noalloc", "conv_bwd_data_run_forward", "conv_bwd_data_a_operand",
-    "conv_bwd_data_k_splits",
+    "conv_bwd_data_k_splits", "conv_bwd_data_grouped_kernel",
 ]
 
 
@@ -61,6 +61,7 @@ def _load():
         "conv_bwd_data_work": [vp, P(ctypes.c_double), P(ctypes.c_double)],
         "conv_bwd_data_a_operand": [vp, P(i32)],
         "conv_bwd_data_k_splits": [vp, P(i32)],
+        "conv_bwd_data_grouped_kernel": [vp, P(i32)],
         "conv_bwd_data_run": [vp, vp, vp, vp, vp],
         "conv_bwd_data_run_forward": [vp, vp, vp, vp, vp],
         "conv_bwd_data_run_host": [vp, vp, vp, vp, vp, vp, vp, vp],
@@ -178,10 +179,17 @@ class Plan:
 
     def a_operand(self) -> str:
         """How the GEMM kernel loads dy: "im2col", "plain" (2-D tiles of dy as a
-        matrix; the specialised kernel) or "gather"."""
+        matrix; the specialised kernel), "gather" or "band" (tiled loads of a
+        band of dy rows read by every tap)."""
         m = ctypes.c_int32()
         _check(_lib.conv_bwd_data_a_operand(self._h, ctypes.byref(m)), "a_operand")
-        return {0: "im2col", 1: "plain", 2: "gather"}[m.value]
+        return {0: "im2col", 1: "plain", 2: "gather", 3: "band"}[m.value]
+
+    def grouped_kernel(self) -> str:
+        """Narrow-group kernel of the plan: "band", "mma", "tc" or "" (another path)."""
+        m = ctypes.c_int32()
+        _check(_lib.conv_bwd_data_grouped_kernel(self._h, ctypes.byref(m)), "grouped_kernel")
+        return {0: "", 1: "mma", 2: "tc", 3: "band"}[m.value]
 
     def k_splits(self) -> int:
         """SM pairs that share each tile of the split-K schedule (1: whole tiles)."""

@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libconv_bwd_data.so")
 SOURCES = ["capi.cpp", "simt.cu", "tc_sm103.cu", "tc2_sm103.cu", "tc_fwd_sm103.cu", "tf32_sm103.cu", "grouped.cu",
-           "tc_grouped_sm103.cu", "noalloc.cu"]
+           "tc_grouped_sm103.cu", "tc_band_sm103.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -58,6 +58,8 @@ struct conv_bwd_plan_s {
     bool two_sm = false;                  // 256x256 tiles on SM pairs (cta_group::2)
     bool a_plain = false;                 // SM-pair kernel specialised for dy read as a plain matrix
     bool grouped_tc = false;              // narrow groups on tcgen05 (block-diagonal B), else warp-level MMA
+    bool grouped_band = false;            // narrow groups on tcgen05 with dy staged once per band (band params)
+    BandParams band;                      // its geometry (pointers and the dy map filled by run)
     int max_pairs = 0;                    // co-resident SM pairs of the 2-SM kernel
     float4 *d_partials = nullptr;         // stream-K workspace: per pair and CTA, one 128x256 fp32 tile
     int32_t *d_flags = nullptr;           // stream-K flags, tagged with the launch epoch
@@ -286,6 +288,22 @@ bool encode_a_maps(conv_bwd_plan_s *p, const void *dy) {
     return true;
 }
 
+// Banded narrow-group kernel: dy as {K, Wo, Ho, N}, box {64 channels, 32
+// pixels, rows, 1 image}, 128-byte swizzle; coordinates outside dy (negative
+// ones included) read as zero.
+bool encode_band_map(conv_bwd_plan_s *p, const void *dy) {
+    PFN_encodeTiled enc = get_encode_tiled();
+    if (!enc) return false;
+    const Geom &g = p->g;
+    cuuint64_t dims[4] = {(cuuint64_t)g.K, (cuuint64_t)g.Wo, (cuuint64_t)g.Ho, (cuuint64_t)g.N};
+    cuuint64_t strides[3] = {(cuuint64_t)g.K * 2, (cuuint64_t)g.Wo * g.K * 2, (cuuint64_t)g.Ho * g.Wo * g.K * 2};
+    cuuint32_t box[4] = {64, 32, (cuuint32_t)p->band.rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(&p->band.tmap_dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(dy), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2_promotion(),
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp32 tensor-core path: the split filter (w_hi, w_lo, [G][Cg][Y][X][Kg]) as
 // 5-D {Kg, X, Y, Cg, G}; a box {32, 1, 1, 128, 1} is 128 c rows of 32 k
 // (128 bytes, 128-byte swizzle: B K-major).  k past Kg and c past Cg read as
@@ -379,6 +397,78 @@ conv_bwd_status validate(const conv_bwd_desc *d) {
     if (eh < 0 || ew < 0) return CONV_BWD_ERR_INVALID_ARG;
     if (d->stride_h > 64 || d->stride_w > 64) return CONV_BWD_ERR_UNSUPPORTED;
     return CONV_BWD_OK;
+}
+
+// Banded narrow-group kernel: output classes (a, b) = (hi % sh, wi % sw) with
+// strides <= 2; tap (y, x) reaches class (a, b) iff a + ph - y*dh and
+// b + pw - x*dw are multiples of the strides, and reads dy at row offset
+// oy = (a + ph - y*dh) / sh and column offset ox = (b + pw - x*dw) / sw from
+// the class's output index (i, j).  Fills the geometry of `bp` and returns
+// whether the kernel applies (shared memory for at least two A stages).
+bool plan_band(const conv_bwd_desc &d, const Geom &g, BandParams &bp) {
+    if (d.dtype != CONV_BWD_BF16 || d.layout != CONV_BWD_NHWC_KYXC || g.Cg != g.Kg) return false;
+    if (!(g.Cg == 8 || g.Cg == 16 || g.Cg == 32) || g.C % 64 != 0) return false;
+    if (g.sh > 2 || g.sw > 2 || g.Y * g.X > kBandMaxTaps) return false;
+    if (g.Hi >= (1 << 20) || g.Wi >= (1 << 20)) return false;
+    std::memset(&bp, 0, sizeof(bp));
+    bp.N = g.N; bp.C = g.C; bp.Hi = g.Hi; bp.Wi = g.Wi; bp.sh = g.sh; bp.sw = g.sw;
+    bp.cg = g.Cg; bp.ntaps = g.Y * g.X; bp.ncls = g.sh * g.sw; bp.cblocks = g.C / 64;
+    // per residue: taps and their offsets
+    std::vector<std::pair<int, int>> rt[2], ct[2];  // (filter index, offset)
+    int oy_min = 1 << 30, oy_max = -(1 << 30), ox_min = 1 << 30, ox_max = -(1 << 30);
+    for (int a = 0; a < g.sh; ++a)
+        for (int y = 0; y < g.Y; ++y) {
+            const int64_t num = (int64_t)a + g.ph - (int64_t)y * g.dh;
+            if (((num % g.sh) + g.sh) % g.sh) continue;
+            const int o = (int)(num / g.sh);
+            rt[a].push_back({y, o});
+            oy_min = std::min(oy_min, o); oy_max = std::max(oy_max, o);
+        }
+    for (int b = 0; b < g.sw; ++b)
+        for (int x = 0; x < g.X; ++x) {
+            const int64_t num = (int64_t)b + g.pw - (int64_t)x * g.dw;
+            if (((num % g.sw) + g.sw) % g.sw) continue;
+            const int o = (int)(num / g.sw);
+            ct[b].push_back({x, o});
+            ox_min = std::min(ox_min, o); ox_max = std::max(ox_max, o);
+        }
+    if (oy_min > oy_max || ox_min > ox_max) return false;
+    bp.oy_min = oy_min; bp.ox_min = ox_min;
+    bp.rows = 4 + oy_max - oy_min;
+    bp.copies = ox_max - ox_min + 1;
+    if (bp.rows > 64 || bp.copies > 16) return false;
+    // windows: one per distinct (copy, row offset); each class reads a window
+    // with at most one tap (its row offset fixes y, its column offset x)
+    std::memset(bp.win_tap, -1, sizeof(bp.win_tap));
+    for (int a = 0; a < g.sh; ++a)
+        for (int b = 0; b < g.sw; ++b) {
+            const int c = a * g.sw + b;
+            for (const auto &ry : rt[a])
+                for (const auto &cx : ct[b]) {
+                    const int cpy = cx.second - ox_min, dr = ry.second - oy_min;
+                    const int key = cpy | (dr << 8);
+                    int wi = 0;
+                    while (wi < bp.nwin && bp.win[wi] != key) ++wi;
+                    if (wi == bp.nwin) bp.win[bp.nwin++] = key;
+                    bp.win_tap[wi][c] = (int8_t)(ry.first * g.X + cx.first);
+                    bp.copy_mask |= 1u << cpy;
+                }
+        }
+    bp.copies_loaded = __builtin_popcount(bp.copy_mask);
+    for (int a = 0; a < g.sh; ++a) bp.hc[a] = g.Hi > a ? (g.Hi - a + g.sh - 1) / g.sh : 0;
+    for (int b = 0; b < g.sw; ++b) bp.wc[b] = g.Wi > b ? (g.Wi - b + g.sw - 1) / g.sw : 0;
+    bp.bands = (bp.hc[0] + 3) / 4;
+    bp.segs = (bp.wc[0] + 31) / 32;
+    const int64_t units = (int64_t)g.N * bp.bands * bp.segs;
+    if (units <= 0 || units * bp.cblocks >= (1LL << 31)) return false;
+    bp.units = (int)units;
+    const int stage_bytes = bp.copies * bp.rows * 32 * 128;
+    bp.stages = 0;
+    for (int st = 4; st >= 2 && !bp.stages; --st)
+        if (tc_band_smem_bytes(g.Cg, bp.ncls, bp.nwin, stage_bytes, st) <= 227 * 1024) bp.stages = st;
+    if (!bp.stages) return false;
+    bp.tmem_cols = 2 * bp.ncls * 64 <= 128 ? 128 : (2 * bp.ncls * 64 <= 256 ? 256 : 512);
+    return true;
 }
 
 }  // namespace
@@ -586,13 +676,22 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
             if (lo[q] < -128 || lo[q] > 127 || hi[q] < -128 || hi[q] > 127) grouped_tc = false;
         if ((c.taps_x - 1) * g.DW > 127 || (c.taps_y - 1) * g.DH > 127) grouped_tc = false;
     }
-    // The warp-level MMA kernel stages each dy row once per item and reuses it
-    // for every tap; the tcgen05 kernel re-reads dy per tap from L2 and measured
-    // slower on the ResNeXt layer (78 vs 51 us), so it runs only where the
-    // warp-level kernel does not apply (C/G = 32) or when CONVBWD_DEBUG_GROUPED=tc.
-    const char *gk = env("CONVBWD_DEBUG_GROUPED");
-    if (grouped_ok && !(gk && !std::strcmp(gk, "tc"))) grouped_tc = false;
-    grouped_ok = grouped_ok || grouped_tc;
+    // narrow groups on tcgen05 with each band of dy staged once and read by
+    // every tap (strides <= 2, C % 64 == 0)
+    BandParams band;
+    const bool band_ok = plan_band(d, g, band);
+    // Default order: the banded kernel; then the warp-level MMA kernel, which
+    // stages each dy row once per item and reuses it for every tap; then the
+    // per-tap tcgen05 kernel, which re-reads dy per tap from L2 (78 vs 51 us
+    // for the warp-level kernel on the ResNeXt layer).  CONVBWD_DEBUG_GROUPED
+    // = band | mma | tc selects one where it applies.
+    int gkind = band_ok ? 3 : (grouped_ok ? 1 : (grouped_tc ? 2 : 0));
+    if (const char *gk = env("CONVBWD_DEBUG_GROUPED")) {
+        if (!std::strcmp(gk, "tc") && grouped_tc) gkind = 2;
+        if (!std::strcmp(gk, "mma") && grouped_ok) gkind = 1;
+        if (!std::strcmp(gk, "band") && band_ok) gkind = 3;
+    }
+    grouped_ok = gkind != 0;
     // fp32 on the tensor cores (three-term TF32 split) for problems large
     // enough to pay for the filter split launch; NHWC/KYXC, 32-channel TMA
     // im2col blocks that stay inside a group, 16-byte pixel strides
@@ -612,7 +711,9 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                     : (grouped_ok ? CONV_BWD_PATH_GROUPED
                                   : (tf32_ok && tf32_big ? CONV_BWD_PATH_TF32 : CONV_BWD_PATH_SIMT));
     if (force && !std::strcmp(force, "simt")) p->path = CONV_BWD_PATH_SIMT;
-    p->grouped_tc = p->path == CONV_BWD_PATH_GROUPED && grouped_tc;
+    p->grouped_tc = p->path == CONV_BWD_PATH_GROUPED && gkind == 2;
+    p->grouped_band = p->path == CONV_BWD_PATH_GROUPED && gkind == 3;
+    if (p->grouped_band) p->band = band;
     p->bn = (p->path == CONV_BWD_PATH_TCGEN05) ? (g.Cg >= 256 ? 256 : 128)
                                                : (p->path == CONV_BWD_PATH_TF32 ? kTf32BN : 64);
     if (const char *f = env("CONVBWD_DEBUG_BN"))
@@ -968,9 +1069,10 @@ conv_bwd_status conv_bwd_data_tile(const conv_bwd_plan p, int32_t *tile_m, int32
     if (!p) return CONV_BWD_ERR_INVALID_ARG;
     if (p->nhwc_plan) return conv_bwd_data_tile(p->nhwc_plan, tile_m, tile_n, sms);
     const bool tc = p->path == CONV_BWD_PATH_TCGEN05, grouped = p->path == CONV_BWD_PATH_GROUPED;
-    if (tile_m) *tile_m = grouped ? (p->grouped_tc ? 128 : 0) : tc ? (p->two_sm ? 256 : 128)
+    const bool gtc = p->grouped_tc || p->grouped_band;
+    if (tile_m) *tile_m = grouped ? (gtc ? 128 : 0) : tc ? (p->two_sm ? 256 : 128)
                                                                    : p->path == CONV_BWD_PATH_TF32 ? 128 : 64;
-    if (tile_n) *tile_n = grouped ? (p->grouped_tc ? 64 : 0) : p->bn;
+    if (tile_n) *tile_n = grouped ? (gtc ? 64 : 0) : p->bn;
     if (sms) *sms = tc && p->two_sm ? 2 : 1;
     return CONV_BWD_OK;
 }
@@ -986,9 +1088,20 @@ conv_bwd_status conv_bwd_data_a_operand(const conv_bwd_plan p, int32_t *a_mode) 
     if (!p || !a_mode) return CONV_BWD_ERR_INVALID_ARG;
     if (p->nhwc_plan) return conv_bwd_data_a_operand(p->nhwc_plan, a_mode);
     const bool tc = p->path == CONV_BWD_PATH_TCGEN05 || p->path == CONV_BWD_PATH_TF32 || p->grouped_tc;
-    *a_mode = !tc ? CONV_BWD_A_GATHER
+    *a_mode = p->grouped_band ? CONV_BWD_A_BAND
+            : !tc ? CONV_BWD_A_GATHER
                   : (p->a_plain ? CONV_BWD_A_PLAIN
                                 : (p->im2col || p->path != CONV_BWD_PATH_TCGEN05 ? CONV_BWD_A_IM2COL : CONV_BWD_A_GATHER));
+    return CONV_BWD_OK;
+}
+
+conv_bwd_status conv_bwd_data_grouped_kernel(const conv_bwd_plan p, int32_t *kind) {
+    if (!p || !kind) return CONV_BWD_ERR_INVALID_ARG;
+    if (p->nhwc_plan) return conv_bwd_data_grouped_kernel(p->nhwc_plan, kind);
+    *kind = p->path != CONV_BWD_PATH_GROUPED ? CONV_BWD_GROUPED_NONE
+          : p->grouped_band                  ? CONV_BWD_GROUPED_TC_BAND
+          : p->grouped_tc                    ? CONV_BWD_GROUPED_TC_TAPS
+                                             : CONV_BWD_GROUPED_WARP_MMA;
     return CONV_BWD_OK;
 }
 
@@ -1041,6 +1154,29 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
     }
     p->fill_ran = false;
     const uint64_t all_w = g.sw >= 64 ? ~0ull : ((1ull << g.sw) - 1);
+    if (p->path == CONV_BWD_PATH_GROUPED && p->grouped_band) {
+        // every dx pixel is written by the kernel (classes without taps as zero)
+        if (p->tmap_a_ptr != dy) {
+            if (!encode_band_map(p, dy)) return CONV_BWD_ERR_CUDA;
+            p->tmap_a_ptr = dy;
+        }
+        BandParams bp = p->band;
+        bp.w = w; bp.dx = dx;
+        bp.status = p->d_status; bp.wait_budget = p->wait_budget;
+#ifdef CBD_PHASE_TIMES
+        bp.phase_log = nullptr;
+        if (p->d_phase &&
+            cudaMemsetAsync(p->d_phase, 0, kPhaseLogCtas * kPhaseSlots * sizeof(unsigned long long), s) == cudaSuccess)
+            bp.phase_log = p->d_phase;
+#endif
+        // each CTA keeps one 64-channel block; as many CTAs per block as fill the SMs
+        const int nsm = std::max(1, p->num_sms);
+        const int64_t per_cb = std::max<int64_t>(1, std::min<int64_t>(bp.units, nsm / bp.cblocks));
+        if (p->timing) cudaEventRecord(p->ev[2], s);
+        if (launch_tc_band(bp, (int)(per_cb * bp.cblocks), s) != cudaSuccess) return CONV_BWD_ERR_CUDA;
+        if (p->timing) cudaEventRecord(p->ev[3], s);
+        return CONV_BWD_OK;
+    }
     if (p->path == CONV_BWD_PATH_GROUPED && p->grouped_tc && !p->classes.empty()) {
         // 64-channel group blocks: the kernel sees G' = C / 64 groups of 64
         // channels and builds each block's block-diagonal B from w itself

@@ -98,9 +98,8 @@ typedef struct conv_bwd_plan_s *conv_bwd_plan;
 typedef enum {
     CONV_BWD_PATH_TCGEN05 = 0, /* bf16: persistent tcgen05/TMEM implicit GEMM */
     CONV_BWD_PATH_SIMT = 1,    /* fp32 (or bf16 fallback): CUDA-core tiled implicit GEMM */
-    CONV_BWD_PATH_GROUPED = 2, /* bf16 narrow groups, C/G = K/G: in {8, 16} with G % 8 == 0 the memory-bound
-                                  warp-MMA kernel; C/G = 32 (C % 64 == 0, <= 12 filter taps) the tcgen05
-                                  kernel with the groups of each 64-channel block in a block-diagonal B */
+    CONV_BWD_PATH_GROUPED = 2, /* bf16 narrow groups, C/G = K/G in {8, 16, 32}: one of three memory-bound
+                                  kernels, see conv_bwd_data_grouped_kernel */
     CONV_BWD_PATH_TF32 = 3     /* fp32 NHWC/KYXC with >= 1e9 useful FLOP, K, C, C/G, K/G multiples of 4
                                   (K/G of 32 when G > 1): tcgen05 kind::tf32 with a three-term split */
 } conv_bwd_path;
@@ -125,7 +124,8 @@ typedef enum {
  *                                    not be allocated (CUDA-core fallback)
  *   CONVBWD_DEBUG_A=plain            plain-matrix A specialisation where it applies (see below)
  *   CONVBWD_DEBUG_SPLITK=S           split-K over S SM pairs per tile where all units fit one wave
- *   CONVBWD_DEBUG_GROUPED=tc         narrow groups on the tcgen05 block-diagonal kernel where it applies
+ *   CONVBWD_DEBUG_GROUPED=band|mma|tc  narrow-group kernel (see conv_bwd_data_grouped_kernel) where
+ *                                    it applies
  *   CONVBWD_DEBUG_RASTER_M=1         tiles walk m-blocks first
  *   CONVBWD_DEBUG_GRID=n             cap the 1-SM kernel's grid
  *   CONVBWD_DEBUG_L2PROMO=0|1       TMA L2 promotion none / 128 B (default 256 B)
@@ -196,8 +196,9 @@ conv_bwd_status conv_bwd_data_run_forward(conv_bwd_plan plan, const void *x, con
 
 /* Output tile of the plan's GEMM kernel: rows (M) and columns (C/G) per tile,
  * and the number of SMs that share one tile (2 for the SM-pair tensor-core
- * kernel, else 1).  The grouped kernel reports 0 x 0 (it has no tiles).  Any
- * output pointer may be NULL. */
+ * kernel, else 1).  The narrow-group tcgen05 kernels report 128 x 64 (one
+ * 64-channel block), the warp-MMA one 0 x 0 (it has no tiles).  Any output
+ * pointer may be NULL. */
 conv_bwd_status conv_bwd_data_tile(const conv_bwd_plan plan, int32_t *tile_m, int32_t *tile_n, int32_t *sms_per_tile);
 
 /* K splits of the plan's SM-pair tensor-core schedule: 1 = every 256-row tile
@@ -220,10 +221,38 @@ conv_bwd_status conv_bwd_data_k_splits(const conv_bwd_plan plan, int32_t *k_spli
  *                      kernel against the dynamic one of "[igemm_dynamic] v4r1 bwd
  *                      dynamic kernel" (dynamic within 10% of static);
  *   CONV_BWD_A_GATHER  per-thread gathers (cp.async producers, CUDA cores, the
- *                      narrow-group kernel).
+ *                      warp-MMA narrow-group kernel);
+ *   CONV_BWD_A_BAND    tiled TMA loads of a band of dy rows (4 output rows plus
+ *                      the filter's row reach, 32 pixels, 64 channels), one per
+ *                      distinct column offset of the taps, read by every tap
+ *                      (the banded narrow-group kernel).
  * INVALID_ARG for a NULL argument. */
-typedef enum { CONV_BWD_A_IM2COL = 0, CONV_BWD_A_PLAIN = 1, CONV_BWD_A_GATHER = 2 } conv_bwd_a_mode;
+typedef enum { CONV_BWD_A_IM2COL = 0, CONV_BWD_A_PLAIN = 1, CONV_BWD_A_GATHER = 2, CONV_BWD_A_BAND = 3 } conv_bwd_a_mode;
 conv_bwd_status conv_bwd_data_a_operand(const conv_bwd_plan plan, int32_t *a_mode);
+
+/* Which narrow-group kernel a CONV_BWD_PATH_GROUPED plan runs (bf16 NHWC/KYXC,
+ * C/G = K/G; each writes every dx pixel itself, one launch):
+ *   CONV_BWD_GROUPED_TC_BAND   (default where it applies: C/G in {8, 16, 32},
+ *                              C % 64 == 0, strides 1 or 2, at most 32 filter
+ *                              taps, the staged band within shared memory)
+ *                              tcgen05 with the groups of each 64-channel block
+ *                              folded into a block-diagonal B whose all-zero
+ *                              16 x 16 blocks are skipped; each band of dy (4
+ *                              output rows x 32 columns of every residue
+ *                              class) is staged once and read by every tap;
+ *   CONV_BWD_GROUPED_WARP_MMA  (C/G in {8, 16}, G % 8 == 0) warp-level MMA on
+ *                              CUDA-core-staged dy rows;
+ *   CONV_BWD_GROUPED_TC_TAPS   (C/G in {8, 16, 32}, C % 64 == 0, <= 12 taps)
+ *                              tcgen05 with one TMA im2col load of dy per tap;
+ *   CONV_BWD_GROUPED_NONE      the plan is not on the narrow-group path.
+ * INVALID_ARG for a NULL argument. */
+typedef enum {
+    CONV_BWD_GROUPED_NONE = 0,
+    CONV_BWD_GROUPED_WARP_MMA = 1,
+    CONV_BWD_GROUPED_TC_TAPS = 2,
+    CONV_BWD_GROUPED_TC_BAND = 3
+} conv_bwd_grouped_kernel_kind;
+conv_bwd_status conv_bwd_data_grouped_kernel(const conv_bwd_plan plan, int32_t *kind);
 
 /* Useful work: 2 * N * K * (C/G) * Th * Tw floating-point operations, where
  * Th = #{(ho, y): 0 <= ho*sh - ph + y*dh < Hi} counts only taps that land

@@ -47,6 +47,15 @@ def fuzz_cases(kind, count, seed):
             Cg = int(rng.choice([64, 128, 192, 256, 320]))
             Kg = 8 * int(rng.integers(1, 25))
             dtype, layout = wl.BF16, wl.NHWC
+        elif kind == "band":      # bf16 NHWC, C/G = K/G in {8, 16, 32}, C % 64 == 0, strides <= 2
+            sh, sw = int(rng.integers(1, 3)), int(rng.integers(1, 3))
+            dh, dw = int(rng.integers(1, 3)), int(rng.integers(1, 3))
+            Y, X = int(rng.integers(1, 5)), int(rng.integers(1, 5))
+            Cg = int(rng.choice([8, 16, 32]))
+            Kg = Cg
+            G = (64 // Cg) * int(rng.integers(1, 4))
+            Wi = int(rng.integers(3, 80))
+            dtype, layout = wl.BF16, wl.NHWC
         elif kind == "grouped":   # bf16 NHWC, C/G = K/G in {8, 16}
             Cg = int(rng.choice([8, 16]))
             Kg = Cg
@@ -60,16 +69,30 @@ def fuzz_cases(kind, count, seed):
         c = wl.Case(name=f"{kind}{len(out)}", N=N, C=G * Cg, K=G * Kg, Hi=Hi, Wi=Wi, Y=Y, X=X, pad=(ph, pw),
                     stride=(sh, sw), dil=(dh, dw), groups=G, dtype=dtype, layout=layout,
                     dist="uniform" if dtype == wl.F32 else "normal", sigma=0.5, seed=seed * 1000 + len(out))
-        if _ok(c):
+        if _ok(c) and (kind != "band" or _band_stage_bytes(c) <= 80 * 1024):
             out.append(c)
     return out
 
 
-FUZZ = fuzz_cases("tc", 24, 71) + fuzz_cases("grouped", 10, 72) + fuzz_cases("simt", 10, 73)
+def _band_stage_bytes(c):
+    """Shared memory of one staged band of the banded narrow-group kernel: one
+    copy per distinct column offset of the taps, 4 output rows plus the row
+    offsets' span, 32 pixels x 128 bytes per row."""
+    def offsets(s, p, d, F):
+        return [(r + p - f * d) // s for r in range(s) for f in range(F) if (r + p - f * d) % s == 0]
+    oy = offsets(c.stride[0], c.pad[0], c.dil[0], c.Y)
+    ox = offsets(c.stride[1], c.pad[1], c.dil[1], c.X)
+    return (max(ox) - min(ox) + 1) * (4 + max(oy) - min(oy)) * 32 * 128
+
+
+FUZZ = (fuzz_cases("tc", 24, 71) + fuzz_cases("grouped", 10, 72) + fuzz_cases("band", 12, 74) +
+        fuzz_cases("simt", 10, 73))
 
 
 @pytest.mark.parametrize("c", FUZZ, ids=lambda c: c.name)
 def test_fuzz_against_oracle(B, c):
     g, dy, w = inputs(c)
     got, plan = gpu_dgrad(B, c, dy, w)
+    if c.name.startswith("band"):
+        assert plan.grouped_kernel() == "band", (plan.path(), plan.grouped_kernel())
     check_full(c, got, g, dy, w)

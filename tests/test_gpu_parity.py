@@ -138,11 +138,12 @@ def test_tensor_core_path_full(B, c):
 
 
 # Narrow-group path (C/G = K/G in {8, 16, 32}): every pixel written by the
-# kernel itself, including ones no tap reaches.  Two kernels: the warp-level
-# MMA kernel (C/G in {8, 16}, G % 8 == 0; the default there), and tcgen05 with
-# the groups of each 64-channel block folded into a block-diagonal B (where
-# C % 64 == 0 and the filter has at most 12 taps: the only kernel for C/G = 32,
-# else selected by CONVBWD_DEBUG_GROUPED=tc).
+# kernel itself, including ones no tap reaches.  Three kernels:
+#   band  tcgen05, each band of dy staged once and read by every tap (C % 64 == 0,
+#         strides <= 2, <= 32 taps): the default where it applies;
+#   mma   warp-level MMA (C/G in {8, 16}, G % 8 == 0);
+#   tc    tcgen05 with one im2col load of dy per tap (C % 64 == 0, <= 12 taps).
+# CONVBWD_DEBUG_GROUPED selects one where it applies.
 GROUPED_CASES = [
     _mk("grp_g32_cg8_3x3s2", N=2, C=256, K=256, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=32),
     _mk("grp_g32_cg8_s3_uncov", N=1, C=256, K=256, Hi=10, Wi=9, Y=2, X=2, pad=(0, 1), stride=(3, 3), groups=32),
@@ -156,50 +157,101 @@ GROUPED_CASES = [
     _mk("grp_g8_cg8_3x3s2_many_tiles", N=4, C=64, K=64, Hi=30, Wi=29, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=8),
 ]
 GROUPED_TC_ONLY = [
-    # 32 channels per group: only the tcgen05 kernel covers it (the default there)
+    # 32 channels per group: the tcgen05 kernels cover it
     _mk("grp_g8_cg32_3x3s2", N=2, C=256, K=256, Hi=11, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=8),
-    # (tcgen05 kernel selected) rows of one parity uncovered (stride 2, dilation 2, pad 2): the kernel's own fill
+    # rows of one parity uncovered (stride 2, dilation 2, pad 2): written as zero by the kernel itself
     _mk("grp_g16_cg16_dil2_fill", N=2, C=256, K=256, Hi=13, Wi=10, Y=3, X=3, pad=(2, 2), stride=(2, 2), dil=(2, 2),
         groups=16),
     _mk("grp_g64_cg8_2x2_s2", N=3, C=512, K=512, Hi=9, Wi=8, Y=2, X=2, stride=(2, 2), groups=64),
 ]
+# Banded kernel: several column segments, stride 1 (three column copies),
+# mixed strides, 32-channel groups at stride 1, a 1x1 stride-2 filter (classes
+# without taps), output rows not a multiple of the band, more 64-channel
+# blocks than SMs (a second wave of CTAs), and a full-size stride-1 ResNeXt
+# layer (many units per CTA: every stage and accumulator buffer reused).
+BAND_CASES = [
+    _mk("band_cg8_s2_segs", N=2, C=128, K=128, Hi=9, Wi=130, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=16),
+    _mk("band_cg8_s1_segs", N=2, C=64, K=64, Hi=7, Wi=70, Y=3, X=3, pad=(1, 1), stride=(1, 1), groups=8),
+    _mk("band_cg16_s2x1", N=3, C=128, K=128, Hi=10, Wi=21, Y=3, X=3, pad=(1, 1), stride=(2, 1), groups=8),
+    _mk("band_cg32_s1", N=2, C=256, K=256, Hi=14, Wi=15, Y=3, X=3, pad=(1, 1), stride=(1, 1), groups=8),
+    _mk("band_cg8_1x1_s2", N=2, C=256, K=256, Hi=11, Wi=9, Y=1, X=1, stride=(2, 2), groups=32),
+    _mk("band_cg8_4x4_s2_p1x2", N=1, C=128, K=128, Hi=9, Wi=11, Y=4, X=4, pad=(1, 2), stride=(2, 2), groups=16),
+    _mk("band_cg8_2x3_s2_p0", N=2, C=64, K=64, Hi=13, Wi=17, Y=2, X=3, pad=(0, 0), stride=(2, 2), groups=8),
+    _mk("band_cg8_160_blocks", N=1, C=10240, K=10240, Hi=5, Wi=5, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=1280),
+    _mk("band_resnext_s1_32x56x56x256", N=32, C=256, K=256, Hi=56, Wi=56, Y=3, X=3, pad=(1, 1), stride=(1, 1),
+        groups=32, sigma=0.05),
+]
 
 
-def _grouped_tc_eligible(c):
-    return c.C % 64 == 0 and c.Y * c.X <= 12
+def _band_smem_two_stages(c):
+    """Shared memory of the banded kernel with two A stages: per stage one copy
+    of the band per distinct column offset of the taps (4 output rows plus the
+    row offsets' span, 32 pixels x 128 bytes per row); per window (distinct
+    row and column offset pair) a B tile of classes x max(16, C/G) rows of 128
+    bytes; 32 KB epilogue staging; alignment and barriers."""
+    def taps(s, p, d, F):
+        return [(r, (r + p - f * d) // s) for r in range(s) for f in range(F) if (r + p - f * d) % s == 0]
+    ty = taps(c.stride[0], c.pad[0], c.dil[0], c.Y)
+    tx = taps(c.stride[1], c.pad[1], c.dil[1], c.X)
+    oy, ox = [o for _, o in ty], [o for _, o in tx]
+    windows = {(a[1], b[1]) for a in ty for b in tx}
+    stage = (max(ox) - min(ox) + 1) * (4 + max(oy) - min(oy)) * 32 * 128
+    btile = c.stride[0] * c.stride[1] * max(16, c.C // c.groups) * 128
+    return 1024 + 2 * stage + len(windows) * btile + 32768 + 256
 
 
-@pytest.mark.parametrize("kernel", ["tc", "mma"])
-@pytest.mark.parametrize("c", GROUPED_CASES, ids=lambda c: c.name)
-def test_grouped_path_full(B, monkeypatch, c, kernel):
+def _grouped_eligible(c, kernel):
+    cg, taps = c.C // c.groups, c.Y * c.X
+    if kernel == "band":
+        return (cg in (8, 16, 32) and c.C % 64 == 0 and max(c.stride) <= 2 and taps <= 32 and
+                _band_smem_two_stages(c) <= 227 * 1024)
     if kernel == "tc":
-        monkeypatch.setenv("CONVBWD_DEBUG_GROUPED", "tc")
+        return cg in (8, 16, 32) and c.C % 64 == 0 and taps <= 12
+    return cg in (8, 16) and c.groups % 8 == 0
+
+
+def _expected_kernel(c, kernel):
+    if _grouped_eligible(c, kernel):
+        return kernel
+    for k in ("band", "mma", "tc"):
+        if _grouped_eligible(c, k):
+            return k
+    raise AssertionError("no narrow-group kernel applies")
+
+
+def _run_grouped(B, monkeypatch, c, kernel):
+    monkeypatch.setenv("CONVBWD_DEBUG_GROUPED", kernel)
     g, dy, w = inputs(c)
     got, plan = gpu_dgrad(B, c, dy, w)
     assert plan.path() == ("grouped", 1)
-    tc = kernel == "tc" and _grouped_tc_eligible(c)
-    assert plan.tile() == ((128, 64, 1) if tc else (0, 0, 1)), plan.tile()
+    k = _expected_kernel(c, kernel)
+    assert plan.grouped_kernel() == k, (plan.grouped_kernel(), k)
+    assert plan.tile() == ((0, 0, 1) if k == "mma" else (128, 64, 1)), plan.tile()
+    assert plan.a_operand() == {"band": "band", "tc": "im2col", "mma": "gather"}[k]
     check_full(c, got, g, dy, w)
 
 
+@pytest.mark.parametrize("kernel", ["band", "tc", "mma"])
+@pytest.mark.parametrize("c", GROUPED_CASES, ids=lambda c: c.name)
+def test_grouped_path_full(B, monkeypatch, c, kernel):
+    _run_grouped(B, monkeypatch, c, kernel)
+
+
+@pytest.mark.parametrize("kernel", ["band", "tc"])
 @pytest.mark.parametrize("c", GROUPED_TC_ONLY, ids=lambda c: c.name)
-def test_grouped_tensor_core_shapes(B, monkeypatch, c):
-    if c.C // c.groups != 32:
-        monkeypatch.setenv("CONVBWD_DEBUG_GROUPED", "tc")
-    g, dy, w = inputs(c)
-    got, plan = gpu_dgrad(B, c, dy, w)
-    assert plan.path() == ("grouped", 1) and plan.tile() == (128, 64, 1), (plan.path(), plan.tile())
-    check_full(c, got, g, dy, w)
+def test_grouped_tensor_core_shapes(B, monkeypatch, c, kernel):
+    _run_grouped(B, monkeypatch, c, kernel)
 
 
-def test_grouped_layer_on_tensor_core_kernel(B, monkeypatch):
-    """The benchmark's grouped layer on the tcgen05 block-diagonal kernel (whole dx)."""
-    monkeypatch.setenv("CONVBWD_DEBUG_GROUPED", "tc")
-    c = wl.case("bf16_resnext")
-    g, dy, w = inputs(c)
-    got, plan = gpu_dgrad(B, c, dy, w)
-    assert plan.path() == ("grouped", 1) and plan.tile() == (128, 64, 1)
-    check_full(c, got, g, dy, w)
+@pytest.mark.parametrize("c", BAND_CASES, ids=lambda c: c.name)
+def test_grouped_band_kernel(B, monkeypatch, c):
+    _run_grouped(B, monkeypatch, c, "band")
+
+
+@pytest.mark.parametrize("kernel", ["tc", "mma"])
+def test_grouped_layer_on_other_kernels(B, monkeypatch, kernel):
+    """The benchmark's grouped layer (whole dx) on the two non-default kernels."""
+    _run_grouped(B, monkeypatch, wl.case("bf16_resnext"), kernel)
 
 
 # CUDA-core path: fp32 in both layouts, bf16 fallbacks (small channel
