@@ -23,6 +23,7 @@
 
 #include "../../include/conv_bwd_data.h"
 #include "internal.h"
+#include "band.h"
 #include "tf32.h"
 
 using namespace cbd;
@@ -404,7 +405,8 @@ conv_bwd_status validate(const conv_bwd_desc *d) {
 // b + pw - x*dw are multiples of the strides, and reads dy at row offset
 // oy = (a + ph - y*dh) / sh and column offset ox = (b + pw - x*dw) / sw from
 // the class's output index (i, j).  Fills the geometry of `bp` and returns
-// whether the kernel applies (shared memory for at least two A stages).
+// whether the kernel applies (shared memory for at least two A stages, at
+// least 16 output columns per 32-pixel staged row).
 bool plan_band(const conv_bwd_desc &d, const Geom &g, BandParams &bp) {
     if (d.dtype != CONV_BWD_BF16 || d.layout != CONV_BWD_NHWC_KYXC || g.Cg != g.Kg) return false;
     if (!(g.Cg == 8 || g.Cg == 16 || g.Cg == 32) || g.C % 64 != 0) return false;
@@ -435,36 +437,34 @@ bool plan_band(const conv_bwd_desc &d, const Geom &g, BandParams &bp) {
     if (oy_min > oy_max || ox_min > ox_max) return false;
     bp.oy_min = oy_min; bp.ox_min = ox_min;
     bp.rows = 4 + oy_max - oy_min;
-    bp.copies = ox_max - ox_min + 1;
-    if (bp.rows > 64 || bp.copies > 16) return false;
-    // windows: one per distinct (copy, row offset); each class reads a window
-    // with at most one tap (its row offset fixes y, its column offset x)
+    bp.segw = 32 - (ox_max - ox_min);
+    if (bp.rows > 64 || bp.segw < 16) return false;
+    // windows: one per distinct (column shift, row offset); each class reads a
+    // window with at most one tap (its row offset fixes y, its column offset x)
     std::memset(bp.win_tap, -1, sizeof(bp.win_tap));
     for (int a = 0; a < g.sh; ++a)
         for (int b = 0; b < g.sw; ++b) {
             const int c = a * g.sw + b;
             for (const auto &ry : rt[a])
                 for (const auto &cx : ct[b]) {
-                    const int cpy = cx.second - ox_min, dr = ry.second - oy_min;
-                    const int key = cpy | (dr << 8);
+                    const int cs = cx.second - ox_min, dr = ry.second - oy_min;
+                    const int key = cs | (dr << 8);
                     int wi = 0;
                     while (wi < bp.nwin && bp.win[wi] != key) ++wi;
                     if (wi == bp.nwin) bp.win[bp.nwin++] = key;
                     bp.win_tap[wi][c] = (int8_t)(ry.first * g.X + cx.first);
-                    bp.copy_mask |= 1u << cpy;
                 }
         }
-    bp.copies_loaded = __builtin_popcount(bp.copy_mask);
     for (int a = 0; a < g.sh; ++a) bp.hc[a] = g.Hi > a ? (g.Hi - a + g.sh - 1) / g.sh : 0;
     for (int b = 0; b < g.sw; ++b) bp.wc[b] = g.Wi > b ? (g.Wi - b + g.sw - 1) / g.sw : 0;
     bp.bands = (bp.hc[0] + 3) / 4;
-    bp.segs = (bp.wc[0] + 31) / 32;
+    bp.segs = (bp.wc[0] + bp.segw - 1) / bp.segw;
     const int64_t units = (int64_t)g.N * bp.bands * bp.segs;
     if (units <= 0 || units * bp.cblocks >= (1LL << 31)) return false;
     bp.units = (int)units;
-    const int stage_bytes = bp.copies * bp.rows * 32 * 128;
+    const int stage_bytes = bp.rows * 32 * 128;
     bp.stages = 0;
-    for (int st = 4; st >= 2 && !bp.stages; --st)
+    for (int st = 6; st >= 2 && !bp.stages; --st)
         if (tc_band_smem_bytes(g.Cg, bp.ncls, bp.nwin, stage_bytes, st) <= 227 * 1024) bp.stages = st;
     if (!bp.stages) return false;
     bp.tmem_cols = 2 * bp.ncls * 64 <= 128 ? 128 : (2 * bp.ncls * 64 <= 256 ? 256 : 512);

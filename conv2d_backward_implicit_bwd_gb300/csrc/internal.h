@@ -167,43 +167,6 @@ struct GroupedParams {
     int32_t step_wc, step_hi, step_n;  // the item stride (CTAs per group block) as (chunk, row, image)
 };
 
-// Banded narrow-group tcgen05 kernel parameters (C/G = K/G in {8, 16, 32},
-// C % 64 == 0, strides 1 or 2): output classes (a, b) = (hi % sh, wi % sw),
-// class index a * sw + b; a work unit is (image, band of 4 output rows,
-// segment of 32 output columns) of one 64-channel block; a window is a
-// (column copy, staged-row offset) position of the 128 GEMM rows in the
-// staged band, read by the taps of one or more classes.
-constexpr int kBandMaxTaps = 32;
-struct BandParams {
-    CUtensorMap tmap_dy;  // dy as {K, Wo, Ho, N}, box {64, 32, rows, 1}, 128B swizzle, zero outside dy
-    const void *w;        // filter (KYXC), read to build the block-diagonal B
-    void *dx;
-    int32_t *status;
-    int64_t wait_budget;
-    int32_t N, C, Hi, Wi;
-    int32_t sh, sw;
-    int32_t cg;           // channels per group
-    int32_t ntaps;        // Y * X
-    int32_t ncls;         // sh * sw
-    int32_t rows;         // staged dy rows per unit: 4 + (max - min row offset)
-    int32_t copies;       // column-shifted copies of the band: max - min column offset + 1
-    uint32_t copy_mask;   // copies some tap reads (only those are loaded)
-    int32_t copies_loaded;
-    int32_t oy_min, ox_min;
-    int32_t stages;       // A stages (2..4)
-    int32_t tmem_cols;    // TMEM allocation: two buffers of ncls x 64 columns, rounded up to a power of 2
-    int32_t bands, segs;  // per image: ceil(rows of class a = 0 / 4), ceil(columns of class b = 0 / 32)
-    int32_t units;        // units of one 64-channel block: N * bands * segs
-    int32_t cblocks;      // C / 64
-    int32_t hc[2], wc[2]; // output rows i / columns j of each row / column residue
-    int32_t nwin;         // dy windows (copy, staged-row offset) that some class's tap reads
-    int32_t win[kBandMaxTaps];         // window: copy | staged-row offset << 8
-    int8_t win_tap[kBandMaxTaps][4];   // per window and class: the filter tap (y*X + x) reading it, or -1
-#ifdef CBD_PHASE_TIMES
-    unsigned long long *phase_log;
-#endif
-};
-
 struct GroupedLayout {
     int32_t wch, span, wfrag_bytes, buf_bytes, smem;
 };
@@ -229,9 +192,6 @@ cudaError_t launch_fwd(const FwdParams &p, int bn, int grid, cudaStream_t s);
 // narrow groups on tcgen05: 64-channel group blocks, block-diagonal B resident per CTA
 cudaError_t launch_tc_grouped(const TcParams &p, int grid, cudaStream_t s);
 size_t tc_grouped_smem_bytes(int taps);
-// narrow groups on tcgen05, dy staged once per band and reused by every tap
-cudaError_t launch_tc_band(const BandParams &p, int grid, cudaStream_t s);
-size_t tc_band_smem_bytes(int cg, int ncls, int nwin, int stage_bytes, int stages);
 // out[b][c][r] = in[b][r][c] for bf16 elements (layout changes of NCHW/GKCYX problems)
 cudaError_t launch_transpose_b16(const void *in, void *out, int64_t batch, int64_t R, int64_t Cc, int num_sms,
                                  cudaStream_t s);

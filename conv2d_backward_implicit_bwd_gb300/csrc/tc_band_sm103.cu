@@ -10,16 +10,21 @@
 //   dy[n, i + oy, j + ox, k],  oy = (a + ph - y*dh) / sh,  ox = (b + pw - x*dw) / sw
 // (zero outside dy).  So every tap of every class reads the same dy window,
 // shifted by a few rows (oy) and columns (ox).  A work unit is one image n,
-// one band of four output rows i, one segment of 32 output columns j and one
-// 64-channel block.  Its A operand is a band of dy: rows i0 + oy_min ..
-// i0 + 3 + oy_max, 32 pixels each, 64 channels (128 bytes) per pixel, loaded
-// by TMA with 128-byte swizzle, pixels outside dy zero-filled.  The 128 GEMM
-// rows m = 32 * (i - i0) + (j - j0) of a class then read, for a tap, 128
-// consecutive staged pixels starting at staged row (oy - oy_min): the tap's
-// A is the staged band at a 4 KB-aligned offset.  The column shift ox cannot
-// be expressed that way (one pixel is 128 bytes, inside a swizzle atom), so
-// the band is staged once per distinct ox (a "copy" loaded at column origin
-// j0 + ox): two copies for a 3x3 stride-2 filter, three for stride 1.
+// one band of four output rows i, one segment of segw = 32 - (max ox - min ox)
+// output columns j and one 64-channel block.  Its A operand is a band of dy:
+// rows i0 + min oy .. i0 + 3 + max oy, 32 pixels from column j0 + min ox, 64
+// channels (128 bytes) per pixel, loaded by one TMA box with 128-byte swizzle,
+// pixels outside dy zero-filled.  The 128 GEMM rows m = 32 * (i - i0) +
+// (j - j0) of a class then read, for a tap, 128 consecutive staged pixels
+// starting at staged row oy - min oy, pixel ox - min ox: the tap's A is the
+// staged band at a (4 KB * row + 128 B * pixel) offset.  The tensor core's
+// 128-byte swizzle follows the absolute shared-memory address bits (the
+// same property that lets a K-major descriptor advance 32 bytes per k
+// slice), so a window may start at any pixel: measured on this kernel's
+// parity tests, which fail at every shifted window when the descriptor's
+// base-offset field is set to the shift instead of 0.  Rows j - j0 >= segw
+// read past their staged row (into the next row, or past the stage) and are
+// never stored.
 //
 // The groups of a 64-channel block are folded into one GEMM with a
 // block-diagonal B, but the MMAs skip the all-zero blocks: the 16-deep k
@@ -45,7 +50,7 @@
 //               i0 + w % 4) of the classes c with c % 2 == w / 4, rounding to
 //               bf16 and storing through swizzled shared memory so that each
 //               store instruction writes four whole 128-byte pixel segments;
-//   warp 8      producer: one lane issues the TMA loads of each unit's copies;
+//   warp 8      producer: one lane issues each unit's band load;
 //   warp 9      TMEM allocation and the single-thread tcgen05.mma issue.
 // Every dx pixel belongs to exactly one (unit, class, row, column), so the
 // kernel writes all of dx and needs no separate fill.  Each CTA keeps one
@@ -53,13 +58,14 @@
 // with a stride of the CTAs sharing it, so neighbouring bands are loaded at
 // about the same time and their shared halo rows come from L2.  Every barrier
 // wait is bounded; on a timeout the kernel records the status word, lets its
-// copies land and returns.
+// loads land and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
 
 #include "device_util.cuh"
 #include "internal.h"
+#include "band.h"
 #include "tc_common.cuh"
 
 namespace cbd {
@@ -79,6 +85,9 @@ struct BandCfg {
 
 __host__ __device__ __forceinline__ int band_nb(int cg) { return cg < 16 ? 16 : cg; }
 
+// [A stages | B tiles | staging | barriers]: a window's last rows read up to
+// (32 - segw) * 128 <= 2 KB past its stage, which stays inside the next stage
+// or the B tiles (one window's tile is at least 16 rows x 128 B).
 size_t tc_band_smem_bytes(int cg, int ncls, int nwin, int stage_bytes, int stages) {
     const size_t btile = (size_t)ncls * band_nb(cg) * 128;  // one window's B: classes x NB rows of 128 B
     size_t s = 1024 + (size_t)stages * stage_bytes + (size_t)nwin * btile + BandCfg::STAGE_OUT_BYTES +
@@ -170,7 +179,7 @@ __device__ __forceinline__ BandUnit band_unit(const BandParams &p, int u) {
     const int band = t % p.bands;
     r.n = t / p.bands;
     r.i0 = band * 4;
-    r.j0 = seg * 32;
+    r.j0 = seg * p.segw;
     return r;
 }
 
@@ -182,15 +191,14 @@ __global__ void __launch_bounds__(BandCfg::THREADS, 1) tc_band_dgrad_kernel(cons
     const int nb = band_nb(p.cg);
     const uint32_t ncol = (uint32_t)(p.ncls * nb);            // MMA N: every class's NB channels
     const uint32_t btile = ncol * 128;                         // one window's B tile
-    const uint32_t copy_bytes = (uint32_t)p.rows * Cfg::ROW_BYTES;
-    const uint32_t stage_bytes = (uint32_t)p.copies * copy_bytes;
+    const uint32_t stage_bytes = (uint32_t)p.rows * Cfg::ROW_BYTES;
     // [A stages | B tiles | epilogue staging | barriers], all 1024-aligned
     uint8_t *sA = smem;
     uint8_t *sB = sA + (size_t)S * stage_bytes;
     uint8_t *stage = sB + (size_t)p.nwin * btile;
     uint64_t *bars = reinterpret_cast<uint64_t *>(stage + Cfg::STAGE_OUT_BYTES);
-    // bars: full[0..S) | empty[0..S) | tfull[2] | tempty[2]   (S <= 4)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * 4 + 4);
+    // bars: full[0..S) | empty[0..S) | tfull[2] | tempty[2]   (S <= 6)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * 6 + 4);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
     const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
@@ -296,11 +304,8 @@ __global__ void __launch_bounds__(BandCfg::THREADS, 1) tc_band_dgrad_kernel(cons
             }
             const BandUnit un = band_unit(p, pu);
             const uint32_t dst = smem_u32(sA) + s * stage_bytes;
-            mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)p.copies_loaded * copy_bytes);
-            for (int cpy = 0; cpy < p.copies; ++cpy)
-                if ((p.copy_mask >> cpy) & 1u)
-                    tma_load_4d(dst + (uint32_t)cpy * copy_bytes, &p.tmap_dy, full0 + 8 * s, cb * 64,
-                                un.j0 + p.ox_min + cpy, un.i0 + p.oy_min, un.n);
+            mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
+            tma_load_4d(dst, &p.tmap_dy, full0 + 8 * s, cb * 64, un.j0 + p.ox_min, un.i0 + p.oy_min, un.n);
             if (pit == 0) CBD_PHASE(p, kPhFirstIssue);
         }
     };
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(BandCfg::THREADS, 1) tc_band_dgrad_kernel(cons
                 for (int wi = 0; wi < kBandMaxTaps; ++wi) {
                     if (wi >= p.nwin) break;
                     const int win = p.win[wi];
-                    const uint64_t ad = a_stage + ((((uint32_t)(win & 0xff)) * copy_bytes +
+                    const uint64_t ad = a_stage + ((((uint32_t)(win & 0xff)) * 128u +
                                                     ((uint32_t)(win >> 8)) * Cfg::ROW_BYTES) >> 4);
                     const uint64_t bd = bdesc0 + ((wi * btile) >> 4);
 #pragma unroll
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(BandCfg::THREADS, 1) tc_band_dgrad_kernel(cons
             const int i = un.i0 + qr, j = un.j0 + lane;
             for (int c = half; c < p.ncls; c += 2) {
                 const int a = c / p.sw, bb = c - a * p.sw;
-                const bool valid = i < p.hc[a] && j < p.wc[bb];
+                const bool valid = i < p.hc[a] && j < p.wc[bb] && lane < p.segw;
                 int64_t off = 0;
                 if (valid)
                     off = (((int64_t)un.n * p.Hi + (int64_t)p.sh * i + a) * p.Wi + (int64_t)p.sw * j + bb) * p.C +
@@ -431,7 +436,7 @@ __global__ void __launch_bounds__(BandCfg::THREADS, 1) tc_band_dgrad_kernel(cons
 
 cudaError_t launch_tc_band(const BandParams &p, int grid, cudaStream_t s) {
     if (grid <= 0 || p.units <= 0) return cudaSuccess;
-    const size_t smem = tc_band_smem_bytes(p.cg, p.ncls, p.nwin, p.copies * p.rows * BandCfg::ROW_BYTES, p.stages);
+    const size_t smem = tc_band_smem_bytes(p.cg, p.ncls, p.nwin, p.rows * BandCfg::ROW_BYTES, p.stages);
     cudaError_t e = cudaFuncSetAttribute(tc_band_dgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     tc_band_dgrad_kernel<<<grid, BandCfg::THREADS, smem, s>>>(p);

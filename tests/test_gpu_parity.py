@@ -183,28 +183,29 @@ BAND_CASES = [
 ]
 
 
-def _band_smem_two_stages(c):
-    """Shared memory of the banded kernel with two A stages: per stage one copy
-    of the band per distinct column offset of the taps (4 output rows plus the
-    row offsets' span, 32 pixels x 128 bytes per row); per window (distinct
-    row and column offset pair) a B tile of classes x max(16, C/G) rows of 128
-    bytes; 32 KB epilogue staging; alignment and barriers."""
+def _band_fits(c):
+    """The banded kernel's shared-memory and segment rules: two A stages of one
+    staged band each (4 output rows plus the row offsets' span, 32 pixels x 128
+    bytes per row), per window (distinct row and column offset pair) a B tile
+    of classes x max(16, C/G) rows of 128 bytes, 32 KB epilogue staging,
+    alignment and barriers within 227 KB; at least 16 output columns per
+    32-pixel staged row."""
     def taps(s, p, d, F):
         return [(r, (r + p - f * d) // s) for r in range(s) for f in range(F) if (r + p - f * d) % s == 0]
     ty = taps(c.stride[0], c.pad[0], c.dil[0], c.Y)
     tx = taps(c.stride[1], c.pad[1], c.dil[1], c.X)
     oy, ox = [o for _, o in ty], [o for _, o in tx]
     windows = {(a[1], b[1]) for a in ty for b in tx}
-    stage = (max(ox) - min(ox) + 1) * (4 + max(oy) - min(oy)) * 32 * 128
+    stage = (4 + max(oy) - min(oy)) * 32 * 128
     btile = c.stride[0] * c.stride[1] * max(16, c.C // c.groups) * 128
-    return 1024 + 2 * stage + len(windows) * btile + 32768 + 256
+    smem = 1024 + 2 * stage + len(windows) * btile + 32768 + 256
+    return smem <= 227 * 1024 and 32 - (max(ox) - min(ox)) >= 16 and 4 + max(oy) - min(oy) <= 64
 
 
 def _grouped_eligible(c, kernel):
     cg, taps = c.C // c.groups, c.Y * c.X
     if kernel == "band":
-        return (cg in (8, 16, 32) and c.C % 64 == 0 and max(c.stride) <= 2 and taps <= 32 and
-                _band_smem_two_stages(c) <= 227 * 1024)
+        return cg in (8, 16, 32) and c.C % 64 == 0 and max(c.stride) <= 2 and taps <= 32 and _band_fits(c)
     if kernel == "tc":
         return cg in (8, 16, 32) and c.C % 64 == 0 and taps <= 12
     return cg in (8, 16) and c.groups % 8 == 0
