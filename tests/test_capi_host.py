@@ -151,6 +151,40 @@ def test_paths(B):
     assert B.Plan(1, 4, 4, 9, 9, 1, 1, stride=(2, 2)).path() == ("simt", 2)
 
 
+def test_narrow_group_kernel_selection(B, monkeypatch):
+    """bf16 NHWC narrow groups: the banded tcgen05 kernel where C % 64 == 0,
+    strides <= 2 and its staged band fits (every pixel written by one launch);
+    otherwise the warp-MMA kernel (C/G in {8, 16}, G % 8 == 0) or the per-tap
+    tcgen05 kernel (C/G = 32, <= 12 taps); the override picks one where it
+    applies and falls back to the default order where it does not."""
+    def kernel(*a, **kw):
+        p = B.Plan(*a, layout="nhwc", dtype="bf16", **kw)
+        return p.path(), p.grouped_kernel(), p.a_operand(), p.tile()
+    band = (("grouped", 1), "band", "band", (128, 64, 1))
+    assert kernel(64, 256, 256, 56, 56, 3, 3, pad=(1, 1), stride=(2, 2), groups=32) == band   # the ResNeXt layer
+    assert kernel(2, 256, 256, 56, 56, 3, 3, pad=(1, 1), groups=32) == band                   # stride 1
+    assert kernel(2, 512, 512, 9, 9, 3, 3, pad=(1, 1), stride=(2, 1), groups=32) == band      # C/G = 16, strides 2x1
+    assert kernel(2, 256, 256, 9, 9, 3, 3, pad=(1, 1), stride=(2, 2), groups=8) == band       # C/G = 32
+    # stride 3: warp MMA for C/G = 8, the per-tap tcgen05 kernel for C/G = 32
+    assert kernel(2, 256, 256, 10, 9, 2, 2, pad=(0, 1), stride=(3, 3), groups=32)[1:3] == ("mma", "gather")
+    assert kernel(2, 256, 256, 10, 9, 3, 3, pad=(1, 1), stride=(3, 3), groups=8)[1:3] == ("tc", "im2col")
+    # 5x5 stride 1 (8 staged rows, 25 windows) fits; 7x7 (49 taps) is past the window table: warp MMA
+    assert kernel(2, 256, 256, 9, 9, 5, 5, pad=(2, 2), groups=32) == band
+    assert kernel(2, 256, 256, 9, 9, 7, 7, pad=(3, 3), groups=32)[1] == "mma"
+    # one 64-channel block; C % 64 != 0 with G % 8 != 0 has no narrow-group kernel (CUDA cores)
+    assert kernel(2, 64, 64, 9, 9, 3, 3, pad=(1, 1), stride=(2, 2), groups=8) == band
+    assert kernel(2, 96, 96, 9, 9, 3, 3, pad=(1, 1), stride=(2, 2), groups=12)[0][0] == "simt"
+    # overrides
+    monkeypatch.setenv("CONVBWD_DEBUG_GROUPED", "mma")
+    assert kernel(2, 256, 256, 9, 9, 3, 3, pad=(1, 1), stride=(2, 2), groups=32)[1:4] == ("mma", "gather", (0, 0, 1))
+    assert kernel(2, 256, 256, 9, 9, 3, 3, pad=(1, 1), stride=(2, 2), groups=8)[1] == "band"  # C/G = 32: no mma
+    monkeypatch.setenv("CONVBWD_DEBUG_GROUPED", "tc")
+    assert kernel(2, 256, 256, 9, 9, 3, 3, pad=(1, 1), stride=(2, 2), groups=32)[1:4] == ("tc", "im2col", (128, 64, 1))
+    # not on the narrow-group path
+    monkeypatch.delenv("CONVBWD_DEBUG_GROUPED")
+    assert B.Plan.from_case(wl.case("bf16_16x1x512x2048")).grouped_kernel() == ""
+
+
 def test_fp32_tensor_core_path_selection(B, monkeypatch):
     """fp32 NHWC problems above 1e9 useful FLOP take the three-term TF32
     tensor-core path (filter split + one kernel, which zeroes uncovered pixels

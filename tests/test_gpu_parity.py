@@ -164,9 +164,10 @@ GROUPED_TC_ONLY = [
         groups=16),
     _mk("grp_g64_cg8_2x2_s2", N=3, C=512, K=512, Hi=9, Wi=8, Y=2, X=2, stride=(2, 2), groups=64),
 ]
-# Banded kernel: several column segments, stride 1 (three column copies),
-# mixed strides, 32-channel groups at stride 1, a 1x1 stride-2 filter (classes
-# without taps), output rows not a multiple of the band, more 64-channel
+# Banded kernel: several column segments, stride 1 (windows shifted by -1, 0
+# and +1 pixel), mixed strides, 32-channel groups at stride 1, a 1x1 stride-2
+# filter (classes without taps), a 4x4 and a 5x5 filter (16 and 25 windows,
+# 28-column segments), output rows not a multiple of the band, more 64-channel
 # blocks than SMs (a second wave of CTAs), and a full-size stride-1 ResNeXt
 # layer (many units per CTA: every stage and accumulator buffer reused).
 BAND_CASES = [
@@ -176,6 +177,7 @@ BAND_CASES = [
     _mk("band_cg32_s1", N=2, C=256, K=256, Hi=14, Wi=15, Y=3, X=3, pad=(1, 1), stride=(1, 1), groups=8),
     _mk("band_cg8_1x1_s2", N=2, C=256, K=256, Hi=11, Wi=9, Y=1, X=1, stride=(2, 2), groups=32),
     _mk("band_cg8_4x4_s2_p1x2", N=1, C=128, K=128, Hi=9, Wi=11, Y=4, X=4, pad=(1, 2), stride=(2, 2), groups=16),
+    _mk("band_cg8_5x5_s1_p2", N=2, C=128, K=128, Hi=9, Wi=40, Y=5, X=5, pad=(2, 2), stride=(1, 1), groups=16),
     _mk("band_cg8_2x3_s2_p0", N=2, C=64, K=64, Hi=13, Wi=17, Y=2, X=3, pad=(0, 0), stride=(2, 2), groups=8),
     _mk("band_cg8_160_blocks", N=1, C=10240, K=10240, Hi=5, Wi=5, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=1280),
     _mk("band_resnext_s1_32x56x56x256", N=32, C=256, K=256, Hi=56, Wi=56, Y=3, X=3, pad=(1, 1), stride=(1, 1),
