@@ -83,7 +83,7 @@ def _band_stage_bytes(c):
     return (4 + max(oy) - min(oy)) * 32 * 128
 
 
-FUZZ = (fuzz_cases("tc", 24, 71) + fuzz_cases("grouped", 10, 72) + fuzz_cases("band", 12, 74) +
+FUZZ = (fuzz_cases("tc", 24, 71) + fuzz_cases("grouped", 10, 72) + fuzz_cases("band", 30, 74) +
         fuzz_cases("simt", 10, 73))
 
 
