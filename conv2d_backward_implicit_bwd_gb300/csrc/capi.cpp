@@ -59,6 +59,7 @@ struct conv_bwd_plan_s {
     bool two_sm = false;                  // 256x256 tiles on SM pairs (cta_group::2)
     bool a_plain = false;                 // SM-pair kernel specialised for dy read as a plain matrix
     bool grouped_tc = false;              // narrow groups on tcgen05 (block-diagonal B), else warp-level MMA
+    bool fuse = false;                    // 1-SM tiles of 256 columns computing two classes (C/G <= 128) at once
     bool grouped_band = false;            // narrow groups on tcgen05 with dy staged once per band (band params)
     BandParams band;                      // its geometry (pointers and the dy map filled by run)
     int max_pairs = 0;                    // co-resident SM pairs of the 2-SM kernel
@@ -400,6 +401,39 @@ conv_bwd_status validate(const conv_bwd_desc *d) {
     return CONV_BWD_OK;
 }
 
+// Two classes can share a 1-SM tile: same rows and tap counts.
+bool fusable_classes(const ClassDesc &a, const ClassDesc &b) {
+    return a.taps_y == b.taps_y && a.taps_x == b.taps_x && a.ht_lo == b.ht_lo && a.HT == b.HT && a.wt_lo == b.wt_lo &&
+           a.WT == b.WT;
+}
+
+// The classes of the tensor-core launches, in schedule order: with class
+// pairing on, each class takes the first later class it can share tiles with
+// (its residues become the entry's pty, ptx).  `map` gets each entry's class
+// index (its im2col map).
+void launch_classes(const conv_bwd_plan_s *p, std::vector<ClassDesc> &out, std::vector<int> &map) {
+    out.clear();
+    map.clear();
+    std::vector<char> used(p->classes.size(), 0);
+    for (size_t a = 0; a < p->sched.size(); ++a) {
+        const int idx = p->sched[a];
+        if (used[(size_t)idx]) continue;
+        used[(size_t)idx] = 1;
+        ClassDesc c = p->classes[(size_t)idx];
+        if (p->fuse)
+            for (size_t b = a + 1; b < p->sched.size(); ++b) {
+                const int j = p->sched[b];
+                if (used[(size_t)j] || !fusable_classes(c, p->classes[(size_t)j])) continue;
+                c.pty = p->classes[(size_t)j].ty;
+                c.ptx = p->classes[(size_t)j].tx;
+                used[(size_t)j] = 1;
+                break;
+            }
+        out.push_back(c);
+        map.push_back(idx);
+    }
+}
+
 // Banded narrow-group kernel: output classes (a, b) = (hi % sh, wi % sw) with
 // strides <= 2; tap (y, x) reaches class (a, b) iff a + ph - y*dh and
 // b + pw - x*dw are multiples of the strides, and reads dy at row offset
@@ -634,6 +668,7 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
             int64_t M = d.N * (int64_t)a.cnt * b.cnt;
             c.M = (int)M;
             c.gemm_id = (int)p->classes.size();
+            c.pty = c.ptx = -1;
             p->classes.push_back(c);
         }
     if ((int)p->classes.size() > kMaxClasses) {
@@ -781,6 +816,21 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                     c.WT == g.Wo;
         const char *f = env("CONVBWD_DEBUG_A");
         p->a_plain = plain && f && !std::strcmp(f, "plain");
+    }
+    // Class pairs on the 1-SM kernel (C/G <= 128): two classes with the same
+    // rows (ht, wt ranges) and tap counts read the same dy rows for every tap
+    // (tap (j, i) reads ho = ht - j*DH, wo = wt - i*DW in any class), so one
+    // 128 x 256 tile computes both -- one A load and one N = 256 MMA per k
+    // slice where two N = 128 tiles would load A twice and issue twice as many
+    // MMAs (an N = 256 MMA measured ~200 SM clocks in this kernel against ~175
+    // for N = 128).  CONVBWD_DEBUG_FUSE=0 keeps one class per tile.
+    if (p->path == CONV_BWD_PATH_TCGEN05 && !p->two_sm && p->im2col && !p->a_plain && g.Cg <= 128) {
+        for (size_t a = 0; a < p->classes.size() && !p->fuse; ++a)
+            for (size_t b = a + 1; b < p->classes.size() && !p->fuse; ++b)
+                p->fuse = fusable_classes(p->classes[a], p->classes[b]);
+        if (const char *f = env("CONVBWD_DEBUG_FUSE"))
+            if (f[0] == '0') p->fuse = false;
+        if (p->fuse) p->bn = 256;
     }
 
     // Schedule: classes with the longest reduction first (LPT), tiles of one
@@ -1035,7 +1085,12 @@ conv_bwd_status conv_bwd_data_path(const conv_bwd_plan p, int32_t *path, int32_t
     }
     if (path) *path = p->path;
     int gemm_launches = p->classes.empty() ? 0 : 1;
-    if (p->path == CONV_BWD_PATH_TCGEN05) gemm_launches = (int)((p->classes.size() + kMaxTcClasses - 1) / kMaxTcClasses);
+    if (p->path == CONV_BWD_PATH_TCGEN05) {
+        std::vector<ClassDesc> lcls;
+        std::vector<int> lmap;
+        launch_classes(p, lcls, lmap);
+        gemm_launches = (int)((lcls.size() + kMaxTcClasses - 1) / kMaxTcClasses);
+    }
     // the warp-MMA narrow-group kernel writes every pixel; the tensor-core
     // kernels zero uncovered pixels themselves; without any class the fill
     // kernel alone runs
@@ -1332,8 +1387,11 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             p->tmap_a_ptr = dy;
         }
         if (p->timing) cudaEventRecord(p->ev[2], s);
+        std::vector<ClassDesc> lcls;
+        std::vector<int> lmap;
+        launch_classes(p, lcls, lmap);
         // at most kMaxTcClasses sub-GEMMs per launch (their maps travel as kernel parameters)
-        for (size_t c0 = 0; c0 < p->sched.size(); c0 += kMaxTcClasses) {
+        for (size_t c0 = 0; c0 < lcls.size(); c0 += kMaxTcClasses) {
             TcParams tp;
             std::memset(&tp, 0, sizeof(tp));
             tp.tmap_w = p->tmap_w;
@@ -1353,13 +1411,13 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
             if (const char *f = env("CONVBWD_DEBUG_RASTER_M")) tp.raster_m = f[0] == '1' ? 1 : 0;
             tp.cov_h = p->cov_h;
             tp.cov_w = p->cov_w == all_w ? ~0ull : p->cov_w;
-            const size_t nc = std::min<size_t>(kMaxTcClasses, p->sched.size() - c0);
+            const size_t nc = std::min<size_t>(kMaxTcClasses, lcls.size() - c0);
             tp.num_classes = (int)nc;
             int64_t total = 0;
             int64_t units = 0;
             for (size_t i = 0; i < nc; ++i) {
-                const int idx = p->sched[c0 + i];
-                tp.cls[i] = p->classes[(size_t)idx];
+                const int idx = lmap[c0 + i];
+                tp.cls[i] = lcls[c0 + i];
                 tp.cls[i].tile_begin = (int)total;
                 tp.cls[i].unit_begin = (int)units;
                 const int64_t tiles_c = (int64_t)g.G * tp.cls[i].m_tiles * tp.n_tiles;

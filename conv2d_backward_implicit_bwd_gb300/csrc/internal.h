@@ -30,6 +30,8 @@ struct ClassDesc {
     int32_t tile_begin;      // first tile of this class in the launch's schedule
     int32_t gemm_id;         // consecutive id of the sub-GEMM
     int32_t unit_begin;      // first (tile, k-block) unit of this class in the launch (stream-K)
+    int32_t pty, ptx;        // 1-SM kernel, 256-wide tiles of C/G <= 128: residues of a second class with the
+                             // same rows and tap counts, computed in the tile's upper 128 columns (else -1)
 };
 
 struct Geom {

@@ -16,7 +16,12 @@
 // writes only rows of the class that exist in dx (the "OOB write" point).
 //
 // Tile: 128 (m) x BN (c) with BN in {128, 256}, K step 64 (one 128-byte
-// swizzled row per operand row), S pipeline slots.  Roles (one CTA per SM):
+// swizzled row per operand row), S pipeline slots.  With C/G <= 128 a
+// 256-wide tile may hold a class pair: two classes with the same rows and tap
+// counts read the same dy rows for every tap (ho = ht - j*DH), so one A load
+// and one N = 256 MMA per k slice serve both; columns 128-255 then belong to
+// the second class (residues pty, ptx: its own filter taps and dx pixels).
+// Roles (one CTA per SM):
 //   warps 0-3      epilogue: tcgen05.ld of the fp32 accumulator (warp q reads
 //                  TMEM lanes 32q..32q+31 = tile rows), RNE to bf16, 16-byte
 //                  stores to the class's strided dx pixels;
@@ -170,9 +175,14 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
                         if (it == 0) CBD_PHASE(p, kPhFirstIssue);
                     }
                     const uint32_t bdst = smem_u32(sB + s * Cfg::B_BYTES);
-                    for (int cb = cb_lo; cb < cb_hi; ++cb)
-                        tma_load_5d(bdst + cb * 8192, &p.tmap_w, full_s, tcd.nb * BN + cb * 64, c.tx + g.XT * i,
-                                    c.ty + g.YT * j, k0, tcd.gi);
+                    for (int cb = cb_lo; cb < cb_hi; ++cb) {
+                        // a class pair's tile: boxes 2, 3 are the second class's filter tap (its 128 columns)
+                        const bool second = BN == 256 && c.pty >= 0 && cb >= 2;
+                        const int col = second ? (cb - 2) * 64 : tcd.nb * BN + cb * 64;
+                        const int ty = second ? c.pty : c.ty, tx = second ? c.ptx : c.tx;
+                        tma_load_5d(bdst + cb * 8192, &p.tmap_w, full_s, col, tx + g.XT * i, ty + g.YT * j, k0,
+                                    tcd.gi);
+                    }
                     issued = true;
                 }
             }
@@ -348,7 +358,22 @@ __global__ void __launch_bounds__(TcCfg<BN, IM2COL>::THREADS, 1) tc_dgrad_kernel
                 off = (((int64_t)n * g.Hi + hi) * g.Wi + wi) * g.C + (int64_t)tcd.gi * g.Cg + (int64_t)tcd.nb * BN;
             }
             const uint32_t tbase = tmem_base + ((uint32_t)(warp * 32) << 16) + b * BN;
-            epilogue_rows<BN>(tbase, stage + warp * 4096, lane, rvalid, off, tcd.nb * BN, g.Cg, dx);
+            if (BN == 256 && c.pty >= 0) {
+                // class pair: columns 0-127 are this class's dx pixel, 128-255 the second class's
+                int64_t off2 = 0;
+                if (rvalid) {
+                    const int HTWT = c.HT * c.WT;
+                    const int n = m / HTWT;
+                    const int rem = m - n * HTWT;
+                    const int hi = (c.ht_lo + rem / c.WT) * g.sh + c.pty * g.dh - g.ph;
+                    const int wi = (c.wt_lo + rem % c.WT) * g.sw + c.ptx * g.dw - g.pw;
+                    off2 = (((int64_t)n * g.Hi + hi) * g.Wi + wi) * g.C + (int64_t)tcd.gi * g.Cg;
+                }
+                epilogue_chunks(tbase, 2, stage + warp * 4096, lane, rvalid, off, 0, g.Cg, dx);
+                epilogue_chunks(tbase + 128, 2, stage + warp * 4096, lane, rvalid, off2, 0, g.Cg, dx);
+            } else {
+                epilogue_rows<BN>(tbase, stage + warp * 4096, lane, rvalid, off, tcd.nb * BN, g.Cg, dx);
+            }
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * b);
             if (threadIdx.x == 0) {

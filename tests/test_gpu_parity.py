@@ -137,6 +137,33 @@ def test_tensor_core_path_full(B, c):
     check_full(c, got, g, dy, w)
 
 
+# Class pairs on the 1-SM kernel (C/G <= 128): two classes with the same rows
+# and tap counts share a 128 x 256 tile (one A load, N = 256 MMAs, the upper
+# 128 columns being the second class's channels and dx pixels): the 5x5
+# stride-3 geometry (two pairs of 4-tap classes, two of 2-tap classes, one
+# class alone), a 2x2 stride-2 filter with ragged C and K (columns past C/G and
+# k past K zero), groups, and a pair mixed with unpaired classes in one launch;
+# each also with pairing off (CONVBWD_DEBUG_FUSE=0, 128-wide tiles).
+FUSE_CASES = [
+    _mk("pair_tiles_5x5_s3", N=2, C=128, K=128, Hi=20, Wi=19, Y=5, X=5, pad=(2, 2), stride=(3, 3)),
+    _mk("pair_tiles_2x2_s2_c96_k72", N=3, C=96, K=72, Hi=14, Wi=12, Y=2, X=2, stride=(2, 2)),
+    _mk("pair_tiles_groups2", N=2, C=256, K=256, Hi=10, Wi=12, Y=2, X=2, stride=(2, 2), groups=2),
+    _mk("pair_tiles_3x3_s3_uneven", N=2, C=64, K=136, Hi=13, Wi=11, Y=3, X=3, pad=(1, 1), stride=(3, 3)),
+]
+
+
+@pytest.mark.parametrize("paired", [True, False])
+@pytest.mark.parametrize("c", FUSE_CASES + [wl.case("bf16_32x57x57x128")], ids=lambda c: c.name)
+def test_class_pair_tiles(B, monkeypatch, c, paired):
+    if not paired:
+        monkeypatch.setenv("CONVBWD_DEBUG_FUSE", "0")
+    g, dy, w = inputs(c)
+    got, plan = gpu_dgrad(B, c, dy, w)
+    assert plan.path()[0] == "tcgen05"
+    assert plan.tile() == ((128, 256, 1) if paired else (128, 128, 1)), plan.tile()
+    check_full(c, got, g, dy, w)
+
+
 # Narrow-group path (C/G = K/G in {8, 16, 32}): every pixel written by the
 # kernel itself, including ones no tap reaches.  Three kernels:
 #   band  tcgen05, each band of dy staged once and read by every tap (C % 64 == 0,
