@@ -42,17 +42,22 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 # sources are unchanged (hash below) and the plan launches the same tile shape.
 TF32_PER_BF16 = 1.1 / 2.25  # NOMINAL dense TF32 / bf16 tensor rates of the part (no measured TF32 peak)
 TC2_SOURCES = ("tc_common.cuh", "tc2_sm103.cu", "internal.h")
+TC_SOURCES = ("tc_common.cuh", "tc_sm103.cu", "internal.h")
 BAND_SOURCES = ("tc_common.cuh", "tc_band_sm103.cu", "band.h", "internal.h")
 TRAFFIC = {
     # ncu --set full, tc2_dgrad_kernel<512, false>, one launch on the 16x1x512x2048 shape (after an L2 flush):
-    # dram__bytes_read.sum 33.68 MB + dram__bytes_write.sum 1.42 MB (dx stays in L2 at kernel end)
+    # dram__bytes_read.sum 33.68 MB + dram__bytes_write.sum 1.41 MB (dx stays in L2 at kernel end)
     "bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "tile": (256, 512, 2), "kernel": "tc2_dgrad_kernel<512>",
-                                    "sha": "550337f3087fa1c5", "bytes": 35.097e6},
-    # ncu --set full, tc_band_dgrad_kernel on the 64x56x56x256 G=32 layer: 25.80 MB + 41.46 MB (the rest of
+                                    "sha": "b8af692f9d2b3a18", "bytes": 35.084e6},
+    # ncu --set full, tc_band_dgrad_kernel on the 64x56x56x256 G=32 layer: 25.80 MB + 41.59 MB (the rest of
     # dx stays in L2 at kernel end)
     "bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": BAND_SOURCES, "tile": (128, 64, 1),
-                                             "kernel": "tc_band_dgrad_kernel", "sha": "09e9dcfec29cb128",
-                                             "bytes": 67.263e6},
+                                             "kernel": "tc_band_dgrad_kernel", "sha": "98461057f31d4556",
+                                             "bytes": 67.386e6},
+    # ncu --set full, tc_dgrad_kernel<256, true> (class pairs) on the 32x57x57x128 5x5 stride-3 layer:
+    # 3.83 MB read (dy + w) + 0 written (dx stays in L2 at kernel end)
+    "bf16_32x57x57x128_5x5_s3_p2": {"files": TC_SOURCES, "tile": (128, 256, 1), "kernel": "tc_dgrad_kernel<256>",
+                                    "sha": "94e867b677661af2", "bytes": 3.829e6},
 }
 
 
