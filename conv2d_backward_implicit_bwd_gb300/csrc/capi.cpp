@@ -797,6 +797,27 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                 p->bn = widths[i];
             }
         }
+        // A layer whose 128 x 128 tiles all fit in one round of 1-SM CTAs runs
+        // faster on them than on SM pairs: the pair kernel's main loop moves
+        // 24-32 KB per SM per k-block in ~810-850 SM clocks, the 1-SM kernel
+        // 32 KB in ~710, and it reaches its first landed stage ~1.3 us sooner.
+        // Measured on eight such layers (1x1 and 3x3, C/G 256..1024, up to 64
+        // k-blocks per tile): 1-SM 128 x 128 tiles 0-22 % faster, never slower.
+        // Deeper tiles keep the pairs, whose split-K reaches ~90 % of the MMA
+        // rate in the main loop.  Any SM-pair override (tile width, split-K,
+        // stream-K, A operand, CONVBWD_DEBUG_2SM=1) keeps the pairs.
+        const bool pinned = env("CONVBWD_DEBUG_2SM") || env("CONVBWD_DEBUG_BN") || env("CONVBWD_DEBUG_SPLITK") ||
+                            env("CONVBWD_DEBUG_STREAMK") || env("CONVBWD_DEBUG_A");
+        int64_t t1 = 0, kb_max = 0;
+        const int64_t kbt = (g.Kg + 63) / 64;
+        for (const ClassDesc &c : p->classes) {
+            t1 += (int64_t)g.G * ((c.M + 127) / 128) * ((g.Cg + 127) / 128);
+            kb_max = std::max(kb_max, (int64_t)c.taps_y * c.taps_x * kbt);
+        }
+        if (!pinned && t1 <= 2 * pairs && kb_max <= 64) {
+            p->two_sm = false;
+            p->bn = 128;
+        }
     }
     if (const char *f = env("CONVBWD_DEBUG_BN")) {
         if (p->path == CONV_BWD_PATH_TCGEN05 && (!std::strcmp(f, "128") || !std::strcmp(f, "256"))) p->bn = std::atoi(f);

@@ -243,6 +243,24 @@ def test_status_strings(B):
     assert B.lib().conv_bwd_data_version() >= 100
 
 
+def test_one_round_layers_take_1sm_tiles(B, monkeypatch):
+    """C/G >= 256: 1-SM 128 x 128 tiles where they all fit in one round (the
+    device's SMs; 148 when planning without one) and a tile has at most 64 k-blocks;
+    SM pairs otherwise, or under any SM-pair override."""
+    assert B.Plan.from_case(wl.case("bf16_32x14x14_1024")).tile() == (128, 128, 1)   # 13 x 8 tiles, 32 k-blocks
+    assert B.Plan.from_case(wl.case("bf16_16x1x512x2048")).tile()[2] == 2          # 2 x 32 x 16 tiles
+    assert B.Plan.from_case(wl.case("bf16_32x28x28x512")).tile()[2] == 2           # 72 k-blocks per tile
+    one = dict(layout="nhwc", dtype="bf16", stride=(2, 2))
+    assert B.Plan(32, 1024, 4096, 14, 14, 1, 1, **one).tile() == (128, 128, 1)    # 64 k-blocks
+    assert B.Plan(32, 1024, 4160, 14, 14, 1, 1, **one).tile()[2] == 2             # 65 k-blocks
+    assert B.Plan(46, 1024, 2048, 14, 14, 1, 1, **one).tile() == (128, 128, 1)    # 18 x 8 = 144 tiles
+    assert B.Plan(64, 1024, 2048, 14, 14, 1, 1, **one).tile()[2] == 2             # 25 x 8 = 200 tiles
+    for k, v in (("CONVBWD_DEBUG_2SM", "1"), ("CONVBWD_DEBUG_BN", "256"), ("CONVBWD_DEBUG_A", "plain")):
+        monkeypatch.setenv(k, v)
+        assert B.Plan.from_case(wl.case("bf16_32x14x14_1024")).tile()[2] == 2, k
+        monkeypatch.delenv(k)
+
+
 @pytest.mark.parametrize("name,eligible", [("bf16_16x1x512x2048", True), ("bf16_32x14x14_1024", True),
                                            ("bf16_32x28x28x512", False), ("bf16_32x57x57x128", False)])
 def test_plain_matrix_specialisation_eligibility(B, monkeypatch, name, eligible):

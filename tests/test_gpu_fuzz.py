@@ -94,3 +94,19 @@ def test_fuzz_against_oracle(B, c):
     if c.name.startswith("band"):
         assert plan.grouped_kernel() == "band", (plan.path(), plan.grouped_kernel())
     check_full(c, got, g, dy, w)
+
+
+# The C/G >= 256 draws fit one round of 1-SM tiles, which the planner prefers:
+# run them again on SM pairs (those with im2col A loads: K/G a multiple of 64
+# when G > 1).
+FUZZ_PAIRS = [c for c in FUZZ if c.name.startswith("tc") and c.C // c.groups >= 256 and
+              (c.groups == 1 or (c.K // c.groups) % 64 == 0)]
+
+
+@pytest.mark.parametrize("c", FUZZ_PAIRS, ids=lambda c: c.name + "_pairs")
+def test_fuzz_on_sm_pairs(B, monkeypatch, c):
+    monkeypatch.setenv("CONVBWD_DEBUG_2SM", "1")
+    g, dy, w = inputs(c)
+    got, plan = gpu_dgrad(B, c, dy, w)
+    assert plan.tile()[2] == 2, plan.tile()
+    check_full(c, got, g, dy, w)
