@@ -797,26 +797,64 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                 p->bn = widths[i];
             }
         }
-        // A layer whose 128 x 128 tiles all fit in one round of 1-SM CTAs runs
-        // faster on them than on SM pairs: the pair kernel's main loop moves
-        // 24-32 KB per SM per k-block in ~810-850 SM clocks, the 1-SM kernel
-        // 32 KB in ~710, and it reaches its first landed stage ~1.3 us sooner.
-        // Measured on eight such layers (1x1 and 3x3, C/G 256..1024, up to 64
-        // k-blocks per tile): 1-SM 128 x 128 tiles 0-22 % faster, never slower.
-        // Deeper tiles keep the pairs, whose split-K reaches ~90 % of the MMA
-        // rate in the main loop.  Any SM-pair override (tile width, split-K,
-        // stream-K, A operand, CONVBWD_DEBUG_2SM=1) keeps the pairs.
+        // SM pairs or 1-SM 128 x 128 tiles: a makespan estimate of both in SM
+        // clocks.  Tiles are dealt to workers (pairs, or SMs) in the kernels'
+        // snake order, classes with the most taps first; a tile costs its
+        // k-blocks times the measured main-loop clocks per k-block of its kind
+        // (1-SM 128 wide 710; pairs 128 wide 845, 256 wide 808, 512 wide 1100)
+        // and its epilogue, from the per-tile rate of layers whose epilogues set
+        // the pace (1-SM 128 x 128: 2400 clocks; pairs: 7100 per 256 columns):
+        // added after every 512-wide tile (single-buffered accumulator);
+        // otherwise overlapped with the next tile's MMAs (a tile costs the
+        // larger of the two) and added once after the last tile.  The 1-SM tiles win on
+        // layers with few tiles (one round, or a second round of cheap classes)
+        // and on shallow ones whose epilogues set the pace.  Measured on 22
+        // layers (1x1 and 3x3, C/G 256..2048, 1..72 k-blocks): 1-SM tiles 0-30 %
+        // faster where chosen; where pairs are kept they are faster, or the
+        // 1-SM tiles at most 4 % faster.  Tiles deeper than 64 k-blocks keep the
+        // pairs, whose split-K reaches ~90 % of the MMA rate.  Any SM-pair
+        // override (CONVBWD_DEBUG_2SM=1, tile width, split-K, stream-K, A
+        // operand) keeps the pairs.
         const bool pinned = env("CONVBWD_DEBUG_2SM") || env("CONVBWD_DEBUG_BN") || env("CONVBWD_DEBUG_SPLITK") ||
                             env("CONVBWD_DEBUG_STREAMK") || env("CONVBWD_DEBUG_A");
-        int64_t t1 = 0, kb_max = 0;
         const int64_t kbt = (g.Kg + 63) / 64;
+        int64_t t1 = 0, kb_max = 0;
         for (const ClassDesc &c : p->classes) {
             t1 += (int64_t)g.G * ((c.M + 127) / 128) * ((g.Cg + 127) / 128);
             kb_max = std::max(kb_max, (int64_t)c.taps_y * c.taps_x * kbt);
         }
-        if (!pinned && t1 <= 2 * pairs && kb_max <= 64) {
-            p->two_sm = false;
-            p->bn = 128;
+        if (!pinned && kb_max <= 64 && t1 <= 64 * 2 * pairs) {
+            std::vector<const ClassDesc *> order;
+            for (const ClassDesc &c : p->classes) order.push_back(&c);
+            std::stable_sort(order.begin(), order.end(), [](const ClassDesc *a, const ClassDesc *b) {
+                return a->taps_y * a->taps_x > b->taps_y * b->taps_x;
+            });
+            // snake makespan of `workers` over tiles of `rows` x `bn` whose
+            // epilogues take `epi` clocks
+            auto makespan = [&](int64_t workers, int rows, int bn, double per_kb, double epi, bool epi_each) {
+                int64_t n = 0;
+                for (const ClassDesc *c : order) n += (int64_t)g.G * ((c->M + rows - 1) / rows) * ((g.Cg + bn - 1) / bn);
+                const int64_t W = std::max<int64_t>(1, std::min(workers, n));
+                std::vector<double> load((size_t)W, 0.0);
+                int64_t t = 0;
+                for (const ClassDesc *c : order) {
+                    const int64_t nt = (int64_t)g.G * ((c->M + rows - 1) / rows) * ((g.Cg + bn - 1) / bn);
+                    const double mma = (double)(c->taps_y * c->taps_x * kbt) * per_kb;
+                    const double cost = epi_each ? mma + epi : std::max(mma, epi);
+                    for (int64_t q = 0; q < nt; ++q, ++t) {
+                        const int64_t k = t / W, r = t - k * W;
+                        load[(size_t)((k & 1) ? W - 1 - r : r)] += cost;
+                    }
+                }
+                return *std::max_element(load.begin(), load.end()) + (epi_each ? 0.0 : epi);
+            };
+            const double pair_kb = p->bn == 512 ? 1100.0 : (p->bn == 256 ? 808.0 : 845.0);
+            const double t_pair = makespan(pairs, 256, p->bn, pair_kb, 7100.0 * p->bn / 256, p->bn == 512);
+            const double t_one = makespan(2 * pairs, 128, 128, 710.0, 2400.0, false);
+            if (t_one < t_pair) {
+                p->two_sm = false;
+                p->bn = 128;
+            }
         }
     }
     if (const char *f = env("CONVBWD_DEBUG_BN")) {

@@ -115,8 +115,8 @@ typedef enum {
  *   CONVBWD_DEBUG_PATH=simt          CUDA-core path for every plan
  *   CONVBWD_DEBUG_PATH=tf32          fp32 tensor-core path whatever the problem size
  *   CONVBWD_DEBUG_NOIM2COL=1         cp.async A producer instead of TMA im2col
- *   CONVBWD_DEBUG_2SM=1 / _NO2SM=1   SM-pair kernel for C/G >= 128, also where 1-SM 128 x 128
- *                                    tiles would fit one round / never
+ *   CONVBWD_DEBUG_2SM=1 / _NO2SM=1   SM-pair kernel for C/G >= 128, also where the planner's
+ *                                    estimate would pick 1-SM 128 x 128 tiles / never
  *   CONVBWD_DEBUG_BN=128|256|512     tile width
  *   CONVBWD_DEBUG_STREAMK=1|0        stream-K schedule on the SM-pair kernel (its scratch is
  *                                    allocated only then); on the fp32 tensor-core path, the

@@ -243,10 +243,12 @@ def test_status_strings(B):
     assert B.lib().conv_bwd_data_version() >= 100
 
 
-def test_one_round_layers_take_1sm_tiles(B, monkeypatch):
-    """C/G >= 256: 1-SM 128 x 128 tiles where they all fit in one round (the
-    device's SMs; 148 when planning without one) and a tile has at most 64 k-blocks;
-    SM pairs otherwise, or under any SM-pair override."""
+def test_few_tile_layers_take_1sm_tiles(B, monkeypatch):
+    """C/G >= 256: 1-SM 128 x 128 tiles where the planner's makespan estimate
+    (tiles dealt in snake order to the SMs, or the SM pairs, at the measured
+    clocks per k-block and per epilogue) favours them and a tile has at most
+    64 k-blocks; SM pairs otherwise, or under any SM-pair override.  Planning
+    without a device assumes 148 SMs."""
     assert B.Plan.from_case(wl.case("bf16_32x14x14_1024")).tile() == (128, 128, 1)   # 13 x 8 tiles, 32 k-blocks
     assert B.Plan.from_case(wl.case("bf16_16x1x512x2048")).tile()[2] == 2          # 2 x 32 x 16 tiles
     assert B.Plan.from_case(wl.case("bf16_32x28x28x512")).tile()[2] == 2           # 72 k-blocks per tile
@@ -254,7 +256,16 @@ def test_one_round_layers_take_1sm_tiles(B, monkeypatch):
     assert B.Plan(32, 1024, 4096, 14, 14, 1, 1, **one).tile() == (128, 128, 1)    # 64 k-blocks
     assert B.Plan(32, 1024, 4160, 14, 14, 1, 1, **one).tile()[2] == 2             # 65 k-blocks
     assert B.Plan(46, 1024, 2048, 14, 14, 1, 1, **one).tile() == (128, 128, 1)    # 18 x 8 = 144 tiles
-    assert B.Plan(64, 1024, 2048, 14, 14, 1, 1, **one).tile()[2] == 2             # 25 x 8 = 200 tiles
+    assert B.Plan(64, 1024, 2048, 14, 14, 1, 1, **one).tile()[2] == 2             # 25 x 8 tiles: two rounds
+    # 3x3 stride 2: four classes of 32, 16, 16 and 8 k-blocks; the second
+    # round of 1-SM tiles holds only the cheapest class
+    assert B.Plan(32, 512, 512, 14, 14, 3, 3, pad=(1, 1), **one).tile() == (128, 128, 1)
+    # a 1x1 layer of one k-block per tile runs at its epilogues' pace, where the
+    # 1-SM tiles are faster; with 16 k-blocks per tile the pairs' wider tiles win
+    plain = dict(layout="nhwc", dtype="bf16")
+    assert B.Plan(64, 256, 64, 56, 56, 1, 1, **plain).tile() == (128, 128, 1)
+    assert B.Plan(64, 256, 1024, 56, 56, 1, 1, **plain).tile()[2] == 2
+    assert B.Plan(32, 256, 256, 28, 28, 3, 3, pad=(1, 1), **plain).tile()[2] == 2   # 36 k-blocks, 2 rounds
     for k, v in (("CONVBWD_DEBUG_2SM", "1"), ("CONVBWD_DEBUG_BN", "256"), ("CONVBWD_DEBUG_A", "plain")):
         monkeypatch.setenv(k, v)
         assert B.Plan.from_case(wl.case("bf16_32x14x14_1024")).tile()[2] == 2, k

@@ -96,9 +96,9 @@ def test_fuzz_against_oracle(B, c):
     check_full(c, got, g, dy, w)
 
 
-# The C/G >= 256 draws fit one round of 1-SM tiles, which the planner prefers:
-# run them again on SM pairs (those with im2col A loads: K/G a multiple of 64
-# when G > 1).
+# The C/G >= 256 draws are small enough that the planner gives them 1-SM
+# tiles: run them again on SM pairs (those with im2col A loads: K/G a multiple
+# of 64 when G > 1).
 FUZZ_PAIRS = [c for c in FUZZ if c.name.startswith("tc") and c.C // c.groups >= 256 and
               (c.groups == 1 or (c.K // c.groups) % 64 == 0)]
 

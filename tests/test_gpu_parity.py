@@ -435,22 +435,26 @@ def test_pair_tile_variants(B, monkeypatch, c, env):
         check_full(c, got, g, dy, w)
 
 
-# C/G >= 256 layers whose 128 x 128 tiles fit in one round of 1-SM CTAs (and at
-# most 64 k-blocks per tile): 1-SM tiles by default, SM pairs under
+# C/G >= 256 layers where the planner's makespan estimate picks 1-SM 128 x 128
+# tiles (at most 64 k-blocks per tile): 1-SM tiles by default, SM pairs under
 # CONVBWD_DEBUG_2SM=1; both against the oracle.  Ragged M and N tails, several
-# classes, a 64-k-block tile, and the 1x1 stride-2 benchmark layer.
-ONE_ROUND_CASES = [
+# classes, a 64-k-block tile, a layer whose 1-SM tiles take two rounds (208
+# tiles of four classes), a shallow 1x1 layer of 784 one-k-block tiles, and the
+# 1x1 stride-2 benchmark layer.
+ONE_SM_CASES = [
     _mk("one_round_1x1s2", N=4, C=512, K=384, Hi=14, Wi=14, Y=1, X=1, stride=(2, 2)),
     _mk("one_round_3x3_cg320", N=2, C=320, K=96, Hi=9, Wi=9, Y=3, X=3, pad=(1, 1)),
     _mk("one_round_3x3s2_classes", N=3, C=256, K=200, Hi=11, Wi=13, Y=3, X=3, pad=(1, 1), stride=(2, 2)),
     _mk("one_round_64_kblocks", N=1, C=384, K=4096, Hi=10, Wi=10, Y=1, X=1, stride=(2, 2)),
+    _mk("two_rounds_3x3s2_32x14x14_512", N=32, C=512, K=512, Hi=14, Wi=14, Y=3, X=3, pad=(1, 1), stride=(2, 2)),
+    _mk("shallow_1x1_16x56x56_c256_k64", N=16, C=256, K=64, Hi=56, Wi=56, Y=1, X=1),
     wl.case("bf16_32x14x14_1024"),
 ]
 
 
 @pytest.mark.parametrize("pairs", [False, True])
-@pytest.mark.parametrize("c", ONE_ROUND_CASES, ids=lambda c: c.name)
-def test_one_round_layers(B, monkeypatch, c, pairs):
+@pytest.mark.parametrize("c", ONE_SM_CASES, ids=lambda c: c.name)
+def test_one_sm_tile_layers(B, monkeypatch, c, pairs):
     if pairs:
         monkeypatch.setenv("CONVBWD_DEBUG_2SM", "1")
     g, dy, w = inputs(c)
