@@ -16,6 +16,11 @@ namespace cbd {
 constexpr int kBandMaxTaps = 32;
 struct BandParams {
     CUtensorMap tmap_dy;  // dy as {K, Wo, Ho, N}, box {64, 32, rows, 1}, 128B swizzle, zero outside dy
+    // dx pixels of class (a, b) = a * sw + b as {C, wc[b], hc[a], N} (pixel
+    // (sh*i + a, sw*j + b)), box {64, segw, 1, 1}, 128B swizzle: the epilogue's
+    // TMA stores; encoded only for classes with pixels (bit c of dx_maps)
+    CUtensorMap tmap_dx[4];
+    int32_t dx_maps;
     const void *w;        // filter (KYXC), read to build the block-diagonal B
     void *dx;
     int32_t *status;

@@ -54,6 +54,7 @@ struct conv_bwd_plan_s {
     const void *tmap_w_ptr = nullptr;
     CUtensorMap tmap_w, tmap_w_half;
     const void *tmap_a_ptr = nullptr;     // dy pointer the per-class im2col maps were encoded for
+    const void *tmap_dx_ptr = nullptr;    // dx pointer the banded kernel's store maps were encoded for
     std::vector<CUtensorMap> tmap_a;      // per class (gemm_id order)
     bool im2col = false;                  // A rows by TMA im2col loads (else cp.async gather)
     bool two_sm = false;                  // 256x256 tiles on SM pairs (cta_group::2)
@@ -293,6 +294,34 @@ bool encode_a_maps(conv_bwd_plan_s *p, const void *dy) {
 // Banded narrow-group kernel: dy as {K, Wo, Ho, N}, box {64 channels, 32
 // pixels, rows, 1 image}, 128-byte swizzle; coordinates outside dy (negative
 // ones included) read as zero.
+// Banded kernel's dx stores: the pixels (sh*i + a, sw*j + b) of class (a, b)
+// as {C, wc[b], hc[a], N}, one box = 64 channels of segw consecutive j of one
+// output row; rows and columns past the class's last are clipped by the map.
+bool encode_band_dx_maps(conv_bwd_plan_s *p, void *dx) {
+    PFN_encodeTiled enc = get_encode_tiled();
+    if (!enc) return false;
+    const Geom &g = p->g;
+    BandParams &b = p->band;
+    b.dx_maps = 0;
+    for (int a = 0; a < b.sh; ++a)
+        for (int c = 0; c < b.sw; ++c) {
+            if (b.hc[a] <= 0 || b.wc[c] <= 0) continue;
+            const int ci = a * b.sw + c;
+            uint16_t *base = static_cast<uint16_t *>(dx) + ((int64_t)a * g.Wi + c) * g.C;  // bf16 elements
+            cuuint64_t dims[4] = {(cuuint64_t)g.C, (cuuint64_t)b.wc[c], (cuuint64_t)b.hc[a], (cuuint64_t)g.N};
+            cuuint64_t strides[3] = {(cuuint64_t)b.sw * g.C * 2, (cuuint64_t)b.sh * g.Wi * g.C * 2,
+                                     (cuuint64_t)g.Hi * g.Wi * g.C * 2};
+            cuuint32_t box[4] = {64, (cuuint32_t)b.segw, 1, 1};
+            cuuint32_t estr[4] = {1, 1, 1, 1};
+            if (enc(&b.tmap_dx[ci], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return false;
+            b.dx_maps |= 1 << ci;
+        }
+    return true;
+}
+
 bool encode_band_map(conv_bwd_plan_s *p, const void *dy) {
     PFN_encodeTiled enc = get_encode_tiled();
     if (!enc) return false;
@@ -1273,6 +1302,10 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
         if (p->tmap_a_ptr != dy) {
             if (!encode_band_map(p, dy)) return CONV_BWD_ERR_CUDA;
             p->tmap_a_ptr = dy;
+        }
+        if (p->tmap_dx_ptr != dx) {
+            if (!encode_band_dx_maps(p, dx)) return CONV_BWD_ERR_CUDA;
+            p->tmap_dx_ptr = dx;
         }
         BandParams bp = p->band;
         bp.w = w; bp.dx = dx;

@@ -48,8 +48,9 @@
 // MMAs of the next.  Roles (320 threads):
 //   warps 0-7   epilogue: warp w drains TMEM lanes 32*(w % 4) .. (output row
 //               i0 + w % 4) of the classes c with c % 2 == w / 4, rounding to
-//               bf16 and storing through swizzled shared memory so that each
-//               store instruction writes four whole 128-byte pixel segments;
+//               bf16 into swizzled shared memory, from where one TMA tensor
+//               store per class writes the row's segw pixels (the class's dx
+//               map clips rows and columns past its last);
 //   warp 8      producer: one lane issues each unit's band load;
 //   warp 9      TMEM allocation and the single-thread tcgen05.mma issue.
 // Every dx pixel belongs to exactly one (unit, class, row, column), so the
@@ -123,15 +124,31 @@ __device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&v)[32
         : "memory");
 }
 
+// TMA tensor store of one staged box (4-D map) from shared memory, in this
+// thread's bulk async-group
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the bulk stores of this thread have finished reading shared memory
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// the bulk stores of this thread are complete (written to global memory)
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Drain one class of one warp's 32 accumulator rows (TMEM lane = GEMM row =
 // output column j0 + lane of output row i0 + warp % 4): its 64 channels sit in
 // 64 / NB blocks of NB columns, `stride` columns apart.  Rounded to bf16
-// (RNE), staged by rows with 16-byte chunks XOR-swizzled by row, and stored
-// by 8 lanes per row so that each store instruction writes four whole
-// 128-byte pixel segments.  `off` is the dx element offset of this thread's
-// pixel at the block's first channel; rows with `valid` false are not stored.
+// (RNE) and staged by rows (pixel = lane) with 16-byte chunks XOR-swizzled by
+// row: the 128-byte swizzle of the class's dx store map, whose box (64
+// channels x segw pixels of this output row) lane 0 then stores with one TMA
+// tensor store when `store` is set.  The map clips rows and columns past the
+// class's last; lanes >= segw lie outside the box.  Lane 0 first waits until
+// its previous store has read the staging buffer.
 __device__ __forceinline__ void band_epilogue(uint32_t taddr, int nb, uint32_t stride, uint8_t *stage, int lane,
-                                              bool valid, int64_t off, __nv_bfloat16 *dx) {
+                                              bool store, const CUtensorMap *map, int c0, int j0, int i, int n) {
     const uint32_t sbase = smem_u32(stage);
     uint32_t va[32], vb[32];
     // channel 16q .. 16q+15 at column (16q / nb) * stride + 16q % nb
@@ -139,34 +156,15 @@ __device__ __forceinline__ void band_epilogue(uint32_t taddr, int nb, uint32_t s
     tmem_ld16_issue<16>(taddr + (uint32_t)(16 / nb) * stride + (16 % nb), va);
     tmem_ld16_issue<0>(taddr + (uint32_t)(32 / nb) * stride + (32 % nb), vb);
     tmem_ld16_issue<16>(taddr + (uint32_t)(48 / nb) * stride + (48 % nb), vb);
-    int64_t roff[8];
-    bool rok[8];
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int row = it * 4 + (lane >> 3);
-        const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)(uint64_t)off, row);
-        const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)((uint64_t)off >> 32), row);
-        roff[it] = (int64_t)(((uint64_t)hi << 32) | lo);
-        rok[it] = __shfl_sync(0xffffffffu, valid ? 1 : 0, row) != 0;
-    }
+    if (lane == 0) tma_store_wait_read();
+    __syncwarp();
     tmem_wait_ld(va);
     tmem_wait_ld(vb);
     stage_half(va, sbase, lane, 0);
     stage_half(vb, sbase, lane, 1);
+    fence_proxy_async_smem();  // the staged rows, visible to the store's async proxy
     __syncwarp();
-    const int ch = lane & 7;
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int row = it * 4 + (lane >> 3);
-        const uint32_t a = sbase + (uint32_t)row * 128u + ((uint32_t)(ch ^ (row & 7)) << 4);
-        uint4 val;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                     : "r"(a)
-                     : "memory");
-        if (rok[it]) *reinterpret_cast<uint4 *>(dx + roff[it] + ch * 8) = val;
-    }
-    __syncwarp();
+    if (lane == 0 && store) tma_store_4d(map, sbase, c0, j0, i, n);
 }
 
 struct BandUnit {
@@ -397,7 +395,6 @@ __global__ void __launch_bounds__(BandCfg::THREADS, 1) tc_band_dgrad_kernel(cons
     } else {
         // ------------------------------------------------------------ epilogue
         const int qr = warp & 3, half = warp >> 2;
-        __nv_bfloat16 *dx = static_cast<__nv_bfloat16 *>(p.dx);
         uint32_t it = 0;
         for (int u = local; u < p.units; u += nlocal, ++it) {
             const uint32_t b = it & 1, tph = (it >> 1) & 1;
@@ -407,16 +404,12 @@ __global__ void __launch_bounds__(BandCfg::THREADS, 1) tc_band_dgrad_kernel(cons
             if (threadIdx.x == 0 && it == 0) CBD_PHASE(p, kPhEpi0Start);
             if (threadIdx.x == 0 && it == 1) CBD_PHASE(p, kPhEpi1Start);
             const BandUnit un = band_unit(p, u);
-            const int i = un.i0 + qr, j = un.j0 + lane;
+            const int i = un.i0 + qr;
             for (int c = half; c < p.ncls; c += 2) {
                 const int a = c / p.sw, bb = c - a * p.sw;
-                const bool valid = i < p.hc[a] && j < p.wc[bb] && lane < p.segw;
-                int64_t off = 0;
-                if (valid)
-                    off = (((int64_t)un.n * p.Hi + (int64_t)p.sh * i + a) * p.Wi + (int64_t)p.sw * j + bb) * p.C +
-                          (int64_t)cb * 64;
+                const bool store = i < p.hc[a] && un.j0 < p.wc[bb] && ((p.dx_maps >> c) & 1);
                 const uint32_t tb = tmem_base + ((uint32_t)(qr * 32) << 16) + b * tcols + (uint32_t)(c * nb);
-                band_epilogue(tb, nb, ncol, stage + warp * 4096, lane, valid, off, dx);
+                band_epilogue(tb, nb, ncol, stage + warp * 4096, lane, store, &p.tmap_dx[c], cb * 64, un.j0, i, un.n);
             }
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * b);
@@ -424,6 +417,7 @@ __global__ void __launch_bounds__(BandCfg::THREADS, 1) tc_band_dgrad_kernel(cons
             if (threadIdx.x == 0 && it == 1) CBD_PHASE(p, kPhEpi1Done);
             if (lane == 0 && qr == 0) CBD_PHASE(p, kPhEpiLast);
         }
+        if (lane == 0) tma_store_wait_all();
     }
 
     __syncthreads();
