@@ -778,8 +778,10 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
     p->grouped_tc = p->path == CONV_BWD_PATH_GROUPED && gkind == 2;
     p->grouped_band = p->path == CONV_BWD_PATH_GROUPED && gkind == 3;
     if (p->grouped_band) p->band = band;
+    // CUDA-core tiles: 64 x 64, or 64 x 32 for fp32 with C/G <= 32 (no idle columns)
+    const int simt_bn = d.dtype == CONV_BWD_F32 && g.Cg <= 32 ? 32 : 64;
     p->bn = (p->path == CONV_BWD_PATH_TCGEN05) ? (g.Cg >= 256 ? 256 : 128)
-                                               : (p->path == CONV_BWD_PATH_TF32 ? kTf32BN : 64);
+                                               : (p->path == CONV_BWD_PATH_TF32 ? kTf32BN : simt_bn);
     if (const char *f = env("CONVBWD_DEBUG_BN"))
         if (p->path == CONV_BWD_PATH_TCGEN05 && (!std::strcmp(f, "128") || !std::strcmp(f, "256"))) p->bn = std::atoi(f);
     // im2col loads read 64 channels past k0 of dy's flat K axis, exact only
@@ -1028,13 +1030,13 @@ static conv_bwd_status create_impl(const conv_bwd_desc *desc, conv_bwd_plan *out
                     cudaMalloc(&p->w_lo, nsplit) == cudaSuccess) {
                     p->owns_wsplit = true;
                 } else {
-                    // no room for the split filter: CUDA-core path, rescheduled for its 64x64 tiles
+                    // no room for the split filter: CUDA-core path, rescheduled for its 64-row tiles
                     cudaGetLastError();
                     cudaFree(p->w_hi);
                     cudaFree(p->w_lo);
                     p->w_hi = p->w_lo = nullptr;
                     p->path = CONV_BWD_PATH_SIMT;
-                    p->bn = 64;
+                    p->bn = simt_bn;
                     if (schedule(64) > lim) {
                         conv_bwd_data_destroy(p);
                         return CONV_BWD_ERR_CUDA;
@@ -1563,7 +1565,8 @@ conv_bwd_status conv_bwd_data_run(conv_bwd_plan p, const void *dy, const void *w
     std::memset(&sp, 0, sizeof(sp));
     sp.g = g; sp.st = p->st; sp.dy = dy; sp.w = w; sp.dx = dx;
     sp.num_classes = (int)p->sched.size();
-    sp.n_tiles = (g.Cg + 63) / 64;
+    sp.bn = p->bn;
+    sp.n_tiles = (g.Cg + sp.bn - 1) / sp.bn;
     int64_t total = 0;
     for (size_t i = 0; i < p->sched.size(); ++i) {
         sp.cls[i] = p->classes[(size_t)p->sched[i]];

@@ -55,7 +55,8 @@ struct SimtParams {
     const void *w;
     void *dx;
     int32_t num_classes;
-    int32_t n_tiles;      // ceil(Cg / 64)
+    int32_t bn;           // tile width: 64, or 32 (fp32 kernel, C/G <= 32)
+    int32_t n_tiles;      // ceil(Cg / bn)
     int32_t total_tiles;  // sum over classes of G * m_tiles * n_tiles
     ClassDesc cls[kMaxClasses];
 };

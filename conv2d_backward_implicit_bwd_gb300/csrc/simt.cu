@@ -215,19 +215,28 @@ __global__ void __launch_bounds__(256) simt_dgrad_kernel(const __grid_constant__
     }
 }
 
-// fp32 variant of the same tiles with a 4-stage cp.async pipeline: each thread
-// gathers its 4 A and 4 B elements of a 16-deep slice with 4-byte copies
-// (zero-filled outside dy, past the class's reduction or past C/G) while the
-// FMAs run on the slices already in shared memory, so the reduction pays one
-// memory latency instead of one per slice.
+// fp32 variant: 64 x BN tiles (BN = 64, or 32 where C/G <= 32) with a 4-stage
+// cp.async pipeline of 16-deep slices -- each thread gathers its A and B
+// elements of a slice with 4-byte copies (zero-filled outside dy, past the
+// class's reduction or past C/G) while the FMAs run on the slices already in
+// shared memory, so the reduction pays one memory latency instead of one per
+// slice.  The 16 k of a slice are split over four groups of 64 threads:
+// thread (kg, lt) accumulates an 8 x BN/8 micro-tile over k = 4kg .. 4kg+3 of
+// every slice (8 + BN/8 shared-memory reads per 8 x BN/8 FMAs), and the four
+// partial tiles are summed at the end in a fixed order ((0 + 2) + (1 + 3)).
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
+template <int BN>
 __global__ void __launch_bounds__(256) simt_dgrad_f32_kernel(const __grid_constant__ SimtParams p) {
-    constexpr int BM = 64, BN = 64, BK = 16, S = 4;
-    __shared__ float As[S][BK][BM + 4];
-    __shared__ float Bs[S][BK][BN + 4];
+    constexpr int BM = 64, BK = 16, S = 4, TM = 8, TN = BN / 8;
+    constexpr int A_LD = BM + 4, B_LD = BN + 4;  // row pitch (floats): 16-byte aligned rows
+    constexpr int AQ = BM * BK / 256, BQ = BN * BK / 256;  // elements per thread and slice
+    __shared__ __align__(16) float smem[S * BK * (A_LD + B_LD)];
+    static_assert(2 * BM * BN <= S * BK * (A_LD + B_LD), "reduction buffer");
+    float(*As)[BK][A_LD] = reinterpret_cast<float(*)[BK][A_LD]>(smem);
+    float(*Bs)[BK][B_LD] = reinterpret_cast<float(*)[BK][B_LD]>(smem + S * BK * A_LD);
     const Geom &g = p.g;
     const Strides &st = p.st;
     const float *dy = static_cast<const float *>(p.dy);
@@ -265,96 +274,191 @@ __global__ void __launch_bounds__(256) simt_dgrad_f32_kernel(const __grid_consta
     const float *dy_n = dy + (an >= 0 ? (int64_t)an * st.dy_n : 0) + (int64_t)gi * g.Kg * st.dy_k;
     const float *w_g = w + (int64_t)gi * g.Kg * st.w_k + (int64_t)(bc < g.Cg ? bc : 0) * st.w_c;
 
-    // the reduction index r = tap*Kg + k of this thread's 4 elements in the next
-    // slice to issue, kept as (k, i, j) counters advanced by BK per slice (no
-    // divisions in the loop)
-    int qk[4], qi[4], qj[4], qr[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int r = tid / BM + 4 * q;
+    // reduction index r = tap*Kg + k of each element this thread issues next,
+    // kept as (r, k, i, j) counters advanced by BK per slice (no divisions in
+    // the loop); A element q sits at slice row tid / BM + (256 / BM) q, B
+    // element q at tid / BN + (256 / BN) q
+    struct Ctr {
+        int r, k, i, j;
+    };
+    auto start = [&](int r) {
+        Ctr q;
         const int tap = r / g.Kg;
-        qk[q] = r - tap * g.Kg;
-        qj[q] = tap / c.taps_x;
-        qi[q] = tap - qj[q] * c.taps_x;
-        qr[q] = r;
-    }
+        q.r = r;
+        q.k = r - tap * g.Kg;
+        q.j = tap / c.taps_x;
+        q.i = tap - q.j * c.taps_x;
+        return q;
+    };
+    auto advance = [&](Ctr &q) {
+        q.r += BK;
+        q.k += BK;
+        while (q.k >= g.Kg) {
+            q.k -= g.Kg;
+            if (++q.i == c.taps_x) {
+                q.i = 0;
+                ++q.j;
+            }
+        }
+    };
+    Ctr qa[AQ], qb[BQ];
+#pragma unroll
+    for (int q = 0; q < AQ; ++q) qa[q] = start(tid / BM + (256 / BM) * q);
+#pragma unroll
+    for (int q = 0; q < BQ; ++q) qb[q] = start(tid / BN + (256 / BN) * q);
     auto issue = [&](int slice) {
         const int sb = slice % S;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int kk = tid / BM + 4 * q;
-            const float *sa = dy, *sbp = w;
-            bool va = false, vb = false;
-            if (qr[q] < Kred) {
-                const int ho = aht - qj[q] * g.DH, wo = awt - qi[q] * g.DW;
-                va = an >= 0 && ho >= 0 && ho < g.Ho && wo >= 0 && wo < g.Wo;
-                if (va) sa = dy_n + (int64_t)qk[q] * st.dy_k + (int64_t)ho * st.dy_h + (int64_t)wo * st.dy_w;
-                vb = bc < g.Cg;
-                if (vb)
-                    sbp = w_g + (int64_t)qk[q] * st.w_k + (int64_t)(c.ty + g.YT * qj[q]) * st.w_y +
-                          (int64_t)(c.tx + g.XT * qi[q]) * st.w_x;
+        for (int q = 0; q < AQ; ++q) {
+            const int kk = tid / BM + (256 / BM) * q;
+            const float *src = dy;
+            bool v = false;
+            if (qa[q].r < Kred && an >= 0) {
+                const int ho = aht - qa[q].j * g.DH, wo = awt - qa[q].i * g.DW;
+                v = ho >= 0 && ho < g.Ho && wo >= 0 && wo < g.Wo;
+                if (v) src = dy_n + (int64_t)qa[q].k * st.dy_k + (int64_t)ho * st.dy_h + (int64_t)wo * st.dy_w;
             }
-            cp_async_4(smem_u32(&As[sb][kk][arow]), sa, va ? 4u : 0u);
-            cp_async_4(smem_u32(&Bs[sb][kk][bcol]), sbp, vb ? 4u : 0u);
-            // advance to the next slice: r += BK
-            qr[q] += BK;
-            qk[q] += BK;
-            while (qk[q] >= g.Kg) {
-                qk[q] -= g.Kg;
-                if (++qi[q] == c.taps_x) {
-                    qi[q] = 0;
-                    ++qj[q];
-                }
+            cp_async_4(smem_u32(&As[sb][kk][arow]), src, v ? 4u : 0u);
+            advance(qa[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < BQ; ++q) {
+            const int kk = tid / BN + (256 / BN) * q;
+            const float *src = w;
+            const bool v = qb[q].r < Kred && bc < g.Cg;
+            if (v)
+                src = w_g + (int64_t)qb[q].k * st.w_k + (int64_t)(c.ty + g.YT * qb[q].j) * st.w_y +
+                      (int64_t)(c.tx + g.XT * qb[q].i) * st.w_x;
+            cp_async_4(smem_u32(&Bs[sb][kk][bcol]), src, v ? 4u : 0u);
+            advance(qb[q]);
+        }
+    };
+
+    // Kg a multiple of BK: every slice lies within one tap, so a thread's
+    // elements of a slice share the tap's bounds check and base address and
+    // step by whole rows of k (counters (k0, i, j) of the next slice to issue)
+    const bool tap_slices = g.Kg % BK == 0;
+    int fk = 0, fi = 0, fj = 0;
+    auto issue_tap = [&](int slice) {
+        const int sb = slice % S;
+        const int ho = aht - fj * g.DH, wo = awt - fi * g.DW;
+        const bool va = an >= 0 && ho >= 0 && ho < g.Ho && wo >= 0 && wo < g.Wo;
+        const float *pa = va ? dy_n + (int64_t)(fk + tid / BM) * st.dy_k + (int64_t)ho * st.dy_h + (int64_t)wo * st.dy_w
+                             : dy;
+        const int64_t da = va ? (int64_t)(256 / BM) * st.dy_k : 0;
+#pragma unroll
+        for (int q = 0; q < AQ; ++q)
+            cp_async_4(smem_u32(&As[sb][tid / BM + (256 / BM) * q][arow]), pa + q * da, va ? 4u : 0u);
+        const bool vb = bc < g.Cg;
+        const float *pb = vb ? w_g + (int64_t)(fk + tid / BN) * st.w_k + (int64_t)(c.ty + g.YT * fj) * st.w_y +
+                                   (int64_t)(c.tx + g.XT * fi) * st.w_x
+                             : w;
+        const int64_t db = vb ? (int64_t)(256 / BN) * st.w_k : 0;
+#pragma unroll
+        for (int q = 0; q < BQ; ++q)
+            cp_async_4(smem_u32(&Bs[sb][tid / BN + (256 / BN) * q][bcol]), pb + q * db, vb ? 4u : 0u);
+        fk += BK;
+        if (fk == g.Kg) {
+            fk = 0;
+            if (++fi == c.taps_x) {
+                fi = 0;
+                ++fj;
             }
         }
     };
 
-    float acc[4][4];
+    const int kg = tid >> 6, lt = tid & 63, tr = lt >> 3, tc = lt & 7;
+    float acc[TM][TN];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
     for (int sl = 0; sl < S - 1; ++sl) {
-        if (sl < nslices) issue(sl);
+        if (sl < nslices) {
+            if (tap_slices)
+                issue_tap(sl);
+            else
+                issue(sl);
+        }
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    const int tr = tid / 16, tc = tid % 16;
     for (int sl = 0; sl < nslices; ++sl) {
         asm volatile("cp.async.wait_group %0;" ::"n"(S - 2) : "memory");  // slice sl has landed
         __syncthreads();
-        if (sl + S - 1 < nslices) issue(sl + S - 1);  // refills the buffer read in iteration sl - 1
+        if (sl + S - 1 < nslices) {  // refills the buffer read in iteration sl - 1
+            if (tap_slices)
+                issue_tap(sl + S - 1);
+            else
+                issue(sl + S - 1);
+        }
         asm volatile("cp.async.commit_group;" ::: "memory");
         const int sb = sl % S;
 #pragma unroll
-        for (int kk = 0; kk < BK; ++kk) {
-            float a[4], b[4];
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = kg * 4 + k4;
+            float a[TM], b[TN];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = As[sb][kk][tr * 4 + i];
+            for (int i = 0; i < TM; i += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(&As[sb][kk][tr * TM + i]);
+                a[i] = v.x, a[i + 1] = v.y, a[i + 2] = v.z, a[i + 3] = v.w;
+            }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = Bs[sb][kk][tc * 4 + j];
+            for (int j = 0; j < TN; j += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(&Bs[sb][kk][tc * TN + j]);
+                b[j] = v.x, b[j + 1] = v.y, b[j + 2] = v.z, b[j + 3] = v.w;
+            }
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < TM; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
 
+    // sum the four k groups' partial tiles: (0 + 2) + (1 + 3), then the final
+    // tile in red[BM*BN ..)
+    float *red = smem;
+    auto put = [&](float *dst) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int m = mb * BM + tr * 4 + i;
-        if (m >= c.M) continue;
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) dst[(tr * TM + i) * BN + tc * TN + j] = acc[i][j];
+    };
+    auto add = [&](const float *src) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] += src[(tr * TM + i) * BN + tc * TN + j];
+    };
+    if (kg >= 2) put(red + (kg - 2) * BM * BN);
+    __syncthreads();
+    if (kg < 2) add(red + kg * BM * BN);
+    __syncthreads();
+    if (kg == 1) put(red);
+    __syncthreads();
+    if (kg == 0) {
+        add(red);
+        put(red + BM * BN);
+    }
+    __syncthreads();
+
+    // store the tile, consecutive threads on dx's contiguous index (channels
+    // for NHWC, pixels for NCHW)
+    const float *fin = red + BM * BN;
+    const bool chan_inner = st.dx_c == 1;
+#pragma unroll 4
+    for (int e = tid; e < BM * BN; e += 256) {
+        const int row = chan_inner ? e / BN : e % BM;
+        const int col = chan_inner ? e % BN : e / BM;
+        const int m = mb * BM + row, cc = nb * BN + col;
+        if (m >= c.M || cc >= g.Cg) continue;
         const int n = m / HTWT;
         const int rem = m - n * HTWT;
         const int hi = (c.ht_lo + rem / c.WT) * g.sh + c.ty * g.dh - g.ph;
         const int wi = (c.wt_lo + rem % c.WT) * g.sw + c.tx * g.dw - g.pw;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int cc = nb * BN + tc * 4 + j;
-            if (cc >= g.Cg) continue;
-            dx[n * st.dx_n + (int64_t)(gi * g.Cg + cc) * st.dx_c + hi * st.dx_h + wi * st.dx_w] = acc[i][j];
-        }
+        dx[n * st.dx_n + (int64_t)(gi * g.Cg + cc) * st.dx_c + hi * st.dx_h + wi * st.dx_w] = fin[row * BN + col];
     }
 }
 
@@ -362,8 +466,10 @@ cudaError_t launch_simt(const SimtParams &p, int dtype, cudaStream_t s) {
     if (p.total_tiles <= 0) return cudaSuccess;
     if (dtype == 1)
         simt_dgrad_kernel<__nv_bfloat16><<<p.total_tiles, 256, 0, s>>>(p);
+    else if (p.bn == 32)
+        simt_dgrad_f32_kernel<32><<<p.total_tiles, 256, 0, s>>>(p);
     else
-        simt_dgrad_f32_kernel<<<p.total_tiles, 256, 0, s>>>(p);
+        simt_dgrad_f32_kernel<64><<<p.total_tiles, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

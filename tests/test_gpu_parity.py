@@ -209,6 +209,12 @@ BAND_CASES = [
     _mk("band_cg8_160_blocks", N=1, C=10240, K=10240, Hi=5, Wi=5, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=1280),
     _mk("band_resnext_s1_32x56x56x256", N=32, C=256, K=256, Hi=56, Wi=56, Y=3, X=3, pad=(1, 1), stride=(1, 1),
         groups=32, sigma=0.05),
+    # classes without pixels (one dx row / column: its odd residue is empty, so
+    # the class has no store map) and odd sizes (the odd residue has one row /
+    # column fewer, clipped by its map; segments starting past its last column)
+    _mk("band_cg8_hi1_s2", N=3, C=64, K=64, Hi=1, Wi=20, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=8),
+    _mk("band_cg8_wi1_s2", N=2, C=128, K=128, Hi=9, Wi=1, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=16),
+    _mk("band_cg16_odd_s2", N=2, C=128, K=128, Hi=7, Wi=63, Y=3, X=3, pad=(1, 1), stride=(2, 2), groups=8),
 ]
 
 
