@@ -49,11 +49,11 @@ TRAFFIC = {
     # dram__bytes_read.sum 33.68 MB + dram__bytes_write.sum 1.41 MB (dx stays in L2 at kernel end)
     "bf16_16x1x512x2048_1x2_s1x2": {"files": TC2_SOURCES, "tile": (256, 512, 2), "kernel": "tc2_dgrad_kernel<512>",
                                     "sha": "b8af692f9d2b3a18", "bytes": 35.084e6},
-    # ncu --set full, tc_band_dgrad_kernel on the 64x56x56x256 G=32 layer: 25.80 MB + 41.59 MB (the rest of
+    # ncu --set full, tc_band_dgrad_kernel on the 64x56x56x256 G=32 layer: 25.81 MB + 41.42 MB (the rest of
     # dx stays in L2 at kernel end)
     "bf16_resnext_64x56x56x256_g32_3x3_s2": {"files": BAND_SOURCES, "tile": (128, 64, 1),
-                                             "kernel": "tc_band_dgrad_kernel", "sha": "98461057f31d4556",
-                                             "bytes": 67.386e6},
+                                             "kernel": "tc_band_dgrad_kernel", "sha": "17f1d15c09232dd0",
+                                             "bytes": 67.227e6},
     # ncu --set full, tc_dgrad_kernel<256, true> (class pairs) on the 32x57x57x128 5x5 stride-3 layer:
     # 3.83 MB read (dy + w) + 0 written (dx stays in L2 at kernel end)
     "bf16_32x57x57x128_5x5_s3_p2": {"files": TC_SOURCES, "tile": (128, 256, 1), "kernel": "tc_dgrad_kernel<256>",
