@@ -47,6 +47,19 @@ namespace cbd {
 // (multiples of 64 columns; slice S - 1 ends at BN).
 __device__ __forceinline__ int split_col(int s, int S, int BN) { return (s * BN / S) / 64 * 64; }
 
+// one non-blocking test of an mbarrier phase
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 template <int BN_>
 struct Tc2Cfg {
     static constexpr int BN = BN_;          // tile width of the pair: 128, 256 or 512
@@ -111,6 +124,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
     const Geom &g = p.g;
     // scheduling unit: the pair (cluster of two CTAs)
     const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
+    // 512-wide whole tiles: the epilogue releases the accumulator by 256-column
+    // halves (tempty[0], tempty[1]), so the next tile's MMAs into the first half
+    // start while the second is drained
+    const bool half_release = BN == 512 && p.splitk <= 1 && !p.streamk;
     if (threadIdx.x == 0) CBD_PHASE(p, kPhEntry);
 
     if (threadIdx.x == 0) {
@@ -238,6 +255,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 tc_fence_after();
                 if (tc == 1) CBD_PHASE(p, kPhMma1Start);
                 const uint32_t d_tmem = tmem_base + b * BN;
+                if (half_release) {
+                    // 512-wide whole tiles: columns [0, 256) are free (tempty[0]);
+                    // the N = 256 MMAs into [256, 512) wait for tempty[1], so the
+                    // stages they need are held (at most S) until the epilogue has
+                    // drained that half.  Each column's k order is unchanged.
+                    bool h1 = mbar_test_wait(tempty0 + 8, tph ^ 1);
+                    if (h1) tc_fence_after();
+                    int pend = sg.kb0;            // first k-block whose upper-half MMAs are pending
+                    const uint32_t it0 = it;      // stage counter at k-block kb0
+                    auto upper = [&](int q) {
+                        const uint32_t sq = (it0 + (uint32_t)(q - sg.kb0)) % S;
+                        const uint64_t ad0 = a_desc0 + (uint64_t)((sq * Cfg::A_BYTES) >> 4);
+                        const uint64_t bd0 = b_desc0 + (uint64_t)((sq * Cfg::B_BYTES) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma2(d_tmem + Cfg::MMA_N, ad0 + (uint64_t)(2 * kk),
+                                    bd0 + (uint64_t)(128 * kk + ((Cfg::QPM * 8192) >> 4)), idesc,
+                                    (q != sg.kb0 || kk != 0) ? 1u : 0u);
+                        tc_commit2_mc(empty0 + 8 * sq, (uint16_t)0x3);
+                    };
+                    for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
+                        const uint32_t s = it % S, ph = (it / S) & 1;
+                        if (!mbar_wait_bounded(full0 + 8 * s, ph, p.wait_budget, abort_flag, p.status,
+                                               kDevTimeoutMma)) {
+                            ok = false;
+                            break;
+                        }
+                        if (it == 0) CBD_PHASE(p, kPhFirstFull);
+                        const uint64_t ad0 = a_desc0 + (uint64_t)((s * Cfg::A_BYTES) >> 4);
+                        const uint64_t bd0 = b_desc0 + (uint64_t)((s * Cfg::B_BYTES) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma2(d_tmem, ad0 + (uint64_t)(2 * kk), bd0 + (uint64_t)(128 * kk), idesc,
+                                    (kb != sg.kb0 || kk != 0) ? 1u : 0u);
+                        issued = true;
+                        if (!h1) {
+                            h1 = mbar_test_wait(tempty0 + 8, tph ^ 1);
+                            if (!h1 && kb + 1 - pend >= S) {  // every stage held: wait for the upper half
+                                if (!mbar_wait_bounded(tempty0 + 8, tph ^ 1, p.wait_budget, abort_flag, p.status,
+                                                       kDevTimeoutMma)) {
+                                    ok = false;
+                                    break;
+                                }
+                                h1 = true;
+                            }
+                            if (h1) tc_fence_after();
+                        }
+                        if (h1) {
+                            for (; pend <= kb; ++pend) upper(pend);
+                        }
+                    }
+                    if (ok && pend < sg.kb1) {
+                        if (!mbar_wait_bounded(tempty0 + 8, tph ^ 1, p.wait_budget, abort_flag, p.status,
+                                               kDevTimeoutMma)) {
+                            ok = false;
+                        } else {
+                            tc_fence_after();
+                            for (; pend < sg.kb1; ++pend) upper(pend);
+                        }
+                    }
+                    if (!ok) break;
+                    tc_commit2_mc(tfull0 + 8 * b, (uint16_t)0x3);
+                    if (tc == 0) CBD_PHASE(p, kPhMma0Done);
+                    CBD_PHASE(p, kPhMmaLast);
+                    continue;
+                }
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const uint32_t s = it % S, ph = (it / S) & 1;
                     // the stage barrier orders the TMA writes of both CTAs before the MMA
@@ -401,11 +484,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Tc2Cfg<BN_>::THREADS
                 }
             }
             const float4 *parts = nparts > 0 ? p.partials + (size_t)(sg.q_first * 2 + rank) * slot_f4 : nullptr;
-            epilogue_rows<BN>(tbase, stage + warp * 4096, lane, rvalid, off, tcd.nb * BN, g.Cg, dx, parts, nparts,
-                              2 * slot_f4, row);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);
+            if (half_release) {
+                // columns [0, 256), then release that half; then [256, 512)
+                epilogue_chunks(tbase, 4, stage + warp * 4096, lane, rvalid, off, tcd.nb * BN, g.Cg, dx);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(tempty_leader0);
+                epilogue_chunks(tbase + 256, 4, stage + warp * 4096, lane, rvalid, off + 256, tcd.nb * BN + 256, g.Cg,
+                                dx);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8);
+            } else {
+                epilogue_rows<BN>(tbase, stage + warp * 4096, lane, rvalid, off, tcd.nb * BN, g.Cg, dx, parts, nparts,
+                                  2 * slot_f4, row);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(tempty_leader0 + 8 * b);
+            }
             if (threadIdx.x == 0) {
                 if (tc < 2) CBD_PHASE(p, tc == 0 ? kPhEpi0Done : kPhEpi1Done);
                 CBD_PHASE(p, kPhEpiLast);
