@@ -423,6 +423,10 @@ PAIR_CASES = [
     (_mk("pair_dil2_fill", N=4, C=256, K=256, Hi=12, Wi=12, Y=3, X=3, pad=(1, 1), stride=(2, 2), dil=(2, 2)), W256),
     (_mk("w512_short_last_block", N=3, C=1024, K=128, Hi=11, Wi=9, Y=3, X=3, pad=(1, 1), stride=(2, 2)), W512),
     (_mk("w512_one_block", N=1, C=512, K=64, Hi=8, Wi=8, Y=1, X=1), W512),
+    # 144 tiles on 76 pairs: the accumulator released by 256-column halves
+    # between a pair's tiles, with C/G = 1000 leaving the last tile's upper
+    # half partly past C/G
+    (_mk("w512_two_tiles_per_pair", N=8, C=1000, K=64, Hi=48, Wi=48, Y=1, X=1), W512),
 ]
 
 
