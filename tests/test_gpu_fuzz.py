@@ -62,6 +62,10 @@ def fuzz_cases(kind, count, seed):
             G = 8 * int(rng.integers(1, 5))
             Y, X = int(rng.integers(1, 5)), int(rng.integers(1, 5))
             dtype, layout = wl.BF16, wl.NHWC
+        elif kind == "simt_tap":  # fp32 CUDA-core kernel, K/G a multiple of 16 (slices within one tap)
+            G = int(rng.integers(1, 4))
+            Cg, Kg = int(rng.integers(1, 80)), 16 * int(rng.integers(1, 4))
+            dtype, layout = wl.F32, (wl.NCHW if rng.integers(2) else wl.NHWC)
         else:                     # fp32 CUDA-core kernel, either layout
             G = int(rng.integers(1, 4))
             Cg, Kg = int(rng.integers(1, 40)), int(rng.integers(1, 40))
@@ -84,7 +88,7 @@ def _band_stage_bytes(c):
 
 
 FUZZ = (fuzz_cases("tc", 24, 71) + fuzz_cases("grouped", 10, 72) + fuzz_cases("band", 30, 74) +
-        fuzz_cases("simt", 10, 73))
+        fuzz_cases("simt", 10, 73) + fuzz_cases("simt_tap", 12, 75))
 
 
 @pytest.mark.parametrize("c", FUZZ, ids=lambda c: c.name)
